@@ -1,0 +1,140 @@
+"""ctypes wrapper around the plain CPU oracle (``oracle/oracle.c``).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product package
+(``kv_cache_decode_append_gb300``) never imports it and shares no code with it.
+
+Arrays are numpy: fp32 data as ``float32``, bf16 data as ``uint16`` holding the
+raw bf16 bits.  Outputs of the attention routines are ``float64``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+F32, BF16 = 0, 1
+_DTYPES = {"f32": F32, "bf16": BF16}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_library(src: str = _SRC, out: str = LIB_PATH, extra_flags=()) -> str:
+    """Compile ``src`` with gcc into the shared library ``out`` and return its path."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", *extra_flags,
+           "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def build() -> str:
+    """Build ``liboracle.so`` if it is missing or older than ``oracle.c``."""
+    if (not os.path.exists(LIB_PATH)
+            or os.path.getmtime(LIB_PATH) < os.path.getmtime(_SRC)):
+        compile_library()
+    return LIB_PATH
+
+
+class Oracle:
+    """Typed entry points of one compiled oracle library (the real one or a test mutant)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        vp, i32p, dp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_double)
+        ci, cd, cll = ctypes.c_int, ctypes.c_double, ctypes.c_longlong
+        lib.oracle_cache_bytes.restype = ctypes.c_ulonglong
+        lib.oracle_cache_bytes.argtypes = [cll] * 6
+        lib.oracle_max_threads.restype = ci
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_set_threads.restype = None
+        lib.oracle_set_threads.argtypes = [ci]
+        lib.oracle_append.restype = ci
+        lib.oracle_append.argtypes = [vp, vp, vp, vp, i32p, ci, ci, ci, ci, ci, ci]
+        lib.oracle_decode_attention.restype = ci
+        lib.oracle_decode_attention.argtypes = [vp, vp, vp, dp, i32p, ci, ci, ci, ci, ci, ci, cd, ci]
+        lib.oracle_full_causal_attention.restype = ci
+        lib.oracle_full_causal_attention.argtypes = [dp, dp, dp, dp, ci, ci, cd]
+        self.lib = lib
+        self.path = path
+
+    # -- helpers ---------------------------------------------------------------
+    @staticmethod
+    def _check(arr: np.ndarray, dtype: str, name: str) -> None:
+        want = np.float32 if dtype == "f32" else np.uint16
+        if arr.dtype != want:
+            raise TypeError(f"{name}: expected {np.dtype(want)} for {dtype}, got {arr.dtype}")
+        if not arr.flags.c_contiguous:
+            raise ValueError(f"{name} must be C-contiguous")
+
+    # -- entry points --------------------------------------------------------------
+    def cache_bytes(self, L, B, H_kv, D, T, bytes_per_elem) -> int:
+        return int(self.lib.oracle_cache_bytes(L, B, H_kv, D, T, bytes_per_elem))
+
+    def max_threads(self) -> int:
+        return int(self.lib.oracle_max_threads())
+
+    def set_threads(self, n: int) -> None:
+        self.lib.oracle_set_threads(int(n))
+
+    def append(self, k_cache, v_cache, k_new, v_new, past_len, dtype: str) -> int:
+        """In place on ``k_cache``/``v_cache`` ([B,H_kv,T_max,D]); returns the status."""
+        for a, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"), (v_new, "v_new")):
+            self._check(a, dtype, n)
+        past_len = np.ascontiguousarray(past_len, dtype=np.int32)
+        B, H_kv, T_max, D = k_cache.shape
+        N = k_new.shape[2]
+        if v_cache.shape != k_cache.shape or k_new.shape != (B, H_kv, N, D) or v_new.shape != k_new.shape:
+            raise ValueError("shape mismatch")
+        return int(self.lib.oracle_append(
+            k_cache.ctypes.data, v_cache.ctypes.data, k_new.ctypes.data, v_new.ctypes.data,
+            past_len.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            B, H_kv, T_max, D, N, _DTYPES[dtype]))
+
+    def decode_attention(self, q, k_cache, v_cache, past_len, dtype: str, scale=None):
+        """Returns ``(out float64 [B,H_q,N,D], status)`` for an already-appended cache."""
+        for a, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+            self._check(a, dtype, n)
+        past_len = np.ascontiguousarray(past_len, dtype=np.int32)
+        B, H_q, N, D = q.shape
+        _, H_kv, T_max, _ = k_cache.shape
+        if scale is None:
+            scale = 1.0 / np.sqrt(D)
+        out = np.empty((B, H_q, N, D), dtype=np.float64)
+        st = self.lib.oracle_decode_attention(
+            q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
+            out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+            past_len.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            B, H_q, H_kv, T_max, D, N, float(scale), _DTYPES[dtype])
+        return out, int(st)
+
+    def full_causal_attention(self, qf, kf, vf, scale):
+        """Causal self-attention of one head: float64 [T,D] inputs, float64 [T,D] output."""
+        qf, kf, vf = (np.ascontiguousarray(x, dtype=np.float64) for x in (qf, kf, vf))
+        T, D = qf.shape
+        out = np.empty((T, D), dtype=np.float64)
+        dp = ctypes.POINTER(ctypes.c_double)
+        st = self.lib.oracle_full_causal_attention(
+            qf.ctypes.data_as(dp), kf.ctypes.data_as(dp), vf.ctypes.data_as(dp),
+            out.ctypes.data_as(dp), T, D, float(scale))
+        if st != 0:
+            raise ValueError("oracle_full_causal_attention rejected its arguments")
+        return out
+
+
+def load() -> Oracle:
+    """The oracle built from ``oracle.c`` (compiled on first use)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = Oracle(build())
+        return _lib

@@ -1,0 +1,286 @@
+"""Pins for the CPU oracle: facts fixed by the pages and by mathematics.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when the
+oracle disagrees with something other than itself:
+
+* printed values   -- the KV-cache size table (golden file);
+* library routines -- ``torch.cat`` for the cache update, and
+  ``torch.nn.functional.scaled_dot_product_attention`` (float64, square causal
+  mask, ``enable_gqa``) for the uncached full-recompute route;
+* closed forms     -- one visible key gives exactly its value row; identical
+  keys give the mean of the visible value rows; a dominant key gives its value
+  row;
+* invariants       -- the pages' trap: with one new token a joint permutation
+  of cached (K, V) pairs leaves the output unchanged, with several new tokens a
+  reversed old/new order changes it.
+
+``test_oracle_pins.py`` runs them on the real oracle and on mutants of it with
+one planted mistake each, to show that every plausible mistake fails a pin.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+_UNITS = {"B": 1, "KiB": 1024, "MiB": 1024 ** 2}
+
+
+# ---------------------------------------------------------------------------------
+# helpers (no attention arithmetic here: inputs and conversions only)
+def _rand(shape, seed, dtype):
+    g = torch.Generator("cpu").manual_seed(seed)
+    t = torch.randn(shape, generator=g, dtype=torch.float32)
+    return t.to(torch.bfloat16) if dtype == "bf16" else t
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    """Oracle representation: float32, or uint16 raw bits for bf16."""
+    t = t.contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def to_f64(t: torch.Tensor) -> torch.Tensor:
+    return t.to(torch.float64)
+
+
+def _appended(k_cache, v_cache, k_new, v_new, past_len):
+    """Caches after the update, built with torch.cat on the sequence axis."""
+    kc, vc = k_cache.clone(), v_cache.clone()
+    N = k_new.shape[2]
+    for b, P in enumerate(past_len.tolist()):
+        kc[b, :, : P + N] = torch.cat([k_cache[b, :, :P], k_new[b]], dim=1)
+        vc[b, :, : P + N] = torch.cat([v_cache[b, :, :P], v_new[b]], dim=1)
+    return kc, vc
+
+
+def _problem(B, H_q, H_kv, D, N, T_max, past, dtype, seed):
+    q = _rand((B, H_q, N, D), seed, dtype)
+    k_new = _rand((B, H_kv, N, D), seed + 1, dtype)
+    v_new = _rand((B, H_kv, N, D), seed + 2, dtype)
+    k_cache = _rand((B, H_kv, T_max, D), seed + 3, dtype)
+    v_cache = _rand((B, H_kv, T_max, D), seed + 4, dtype)
+    past_len = torch.tensor(past, dtype=torch.int32)
+    for b, P in enumerate(past):  # slots past the history hold NaN
+        k_cache[b, :, P:] = float("nan")
+        v_cache[b, :, P:] = float("nan")
+    return q, k_new, v_new, k_cache, v_cache, past_len
+
+
+def _oracle_decode(orc, q, k_cache, v_cache, past_len, dtype, scale=None):
+    out, st = orc.decode_attention(to_np(q), to_np(k_cache), to_np(v_cache),
+                                   past_len.numpy(), dtype, scale)
+    assert st == 0, f"oracle status {st}"
+    return torch.from_numpy(out)
+
+
+def _max_rel(a: torch.Tensor, b: torch.Tensor) -> float:
+    """Row-normwise relative error of ``a`` against ``b`` over the last axis."""
+    num = (a - b).abs().amax(dim=-1)
+    den = b.abs().amax(dim=-1).clamp_min(1e-300)
+    return float((num / den).max())
+
+
+# ---------------------------------------------------------------------------------
+def pin_cache_bytes(orc):
+    """The size formula reproduces every value the page prints."""
+    with open(os.path.join(GOLDEN, "kv_cache_bytes.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 9
+    for L, B, H, D, T, s, expected, unit, match in rows:
+        got = orc.cache_bytes(int(L), int(B), int(H), int(D), int(T), int(s)) / _UNITS[unit]
+        if match == "exact":
+            assert got == float(expected), (L, B, H, D, T, s, got, expected)
+        else:
+            decimals = len(expected.split(".")[1])
+            assert round(got, decimals) == float(expected), (got, expected)
+
+
+def pin_append_is_concat(orc):
+    """Cache update = concat of history and new tokens on the sequence axis, in place."""
+    for dtype in ("f32", "bf16"):
+        B, H, T_max, D, N = 3, 2, 11, 8, 3
+        past = [4, 0, T_max - N]
+        _, k_new, v_new, k_cache, v_cache, past_len = _problem(B, H, H, D, N, T_max, past, dtype, 7)
+        # sentinel: slots past P+N keep arbitrary recognisable values
+        k_cache[:, :, :] = torch.where(torch.isnan(k_cache), torch.full_like(k_cache, -3.25), k_cache)
+        v_cache[:, :, :] = torch.where(torch.isnan(v_cache), torch.full_like(v_cache, 5.5), v_cache)
+        exp_k, exp_v = _appended(k_cache, v_cache, k_new, v_new, past_len)
+        kc, vc = to_np(k_cache), to_np(v_cache)
+        st = orc.append(kc, vc, to_np(k_new), to_np(v_new), past_len.numpy(), dtype)
+        assert st == 0
+        assert np.array_equal(kc.view(np.uint8), to_np(exp_k).view(np.uint8))
+        assert np.array_equal(vc.view(np.uint8), to_np(exp_v).view(np.uint8))
+        # capacity: P + N > T_max must leave that sequence untouched and report it
+        bad = torch.tensor([T_max - N + 1, 0, 2], dtype=torch.int32)
+        kc2, vc2 = to_np(k_cache), to_np(v_cache)
+        st = orc.append(kc2, vc2, to_np(k_new), to_np(v_new), bad.numpy(), dtype)
+        assert st == 2
+        assert np.array_equal(kc2[0], to_np(k_cache)[0])
+        assert np.array_equal(vc2[0], to_np(v_cache)[0])
+        assert not np.array_equal(kc2[1], to_np(k_cache)[1])
+
+
+def pin_single_visible_key(orc):
+    """Empty history, one new token: the only visible key has weight 1, out = v_new.
+
+    Runs over every bf16 bit pattern as a value, so the bf16 widening is pinned
+    against torch's own conversion (NaN stays NaN, infinities stay infinite).
+    """
+    D = 1 << 16
+    v_bits = torch.arange(D, dtype=torch.int32).to(torch.int16).view(1, 1, 1, D)
+    v_new = v_bits.view(torch.bfloat16).clone()
+    q = torch.zeros((1, 1, 1, D), dtype=torch.bfloat16)
+    k_new = torch.zeros_like(q)
+    k_cache = torch.zeros((1, 1, 2, D), dtype=torch.bfloat16)
+    v_cache = torch.zeros_like(k_cache)
+    past_len = torch.tensor([0], dtype=torch.int32)
+    kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
+    out = _oracle_decode(orc, q, kc, vc, past_len, "bf16")
+    want = to_f64(v_new)
+    assert torch.equal(torch.isnan(out), torch.isnan(want))
+    fin = ~torch.isnan(want)
+    assert torch.equal(out[fin], want[fin])
+    for dtype in ("f32", "bf16"):
+        q, k_new, v_new, k_cache, v_cache, past_len = _problem(2, 4, 2, 16, 1, 5, [0, 0], dtype, 11)
+        kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
+        out = _oracle_decode(orc, q, kc, vc, past_len, dtype)
+        want = to_f64(v_new).repeat_interleave(2, dim=1)
+        assert torch.equal(out, want)
+
+
+def pin_identical_keys_mean(orc):
+    """All keys equal: equal weights, so row i is the mean of the P+i+1 visible value rows."""
+    for dtype in ("f32", "bf16"):
+        B, H_q, H_kv, D, N, T_max = 2, 4, 2, 8, 4, 16
+        past = [5, 9]
+        q, k_new, v_new, k_cache, v_cache, past_len = _problem(B, H_q, H_kv, D, N, T_max, past, dtype, 21)
+        key = _rand((D,), 99, dtype)
+        k_cache[:] = key
+        k_new[:] = key
+        kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
+        out = _oracle_decode(orc, q, kc, vc, past_len, dtype)
+        vf = to_f64(vc)
+        for b, P in enumerate(past):
+            for hq in range(H_q):
+                for i in range(N):
+                    want = vf[b, hq // (H_q // H_kv), : P + i + 1].mean(dim=0)
+                    assert _max_rel(out[b, hq, i], want) < 1e-13
+
+
+def pin_dominant_key(orc):
+    """One key aligned with q far above the rest: softmax puts all weight on it."""
+    D, T_max = 16, 12
+    for dtype in ("f32", "bf16"):
+        q, k_new, v_new, k_cache, v_cache, past_len = _problem(1, 2, 1, D, 2, T_max, [7], dtype, 31)
+        q[:] = _rand((D,), 5, dtype)
+        for j in (0, 3, 6):  # history positions, visible to both new rows
+            kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
+            kc[0, 0, :9] = 0.01 * _rand((9, D), 40 + j, "f32").to(kc.dtype)
+            kc[0, 0, j] = (q[0, 0, 0].float() * 64.0).to(kc.dtype)  # score ~ 64*|q|^2/4
+            out = _oracle_decode(orc, q, kc, vc, past_len, dtype)
+            want = to_f64(vc[0, 0, j])
+            for hq in range(2):
+                for i in range(2):
+                    assert _max_rel(out[0, hq, i], want) < 1e-9, (dtype, j, hq, i)
+
+
+def _route_b_sdpa(q, k_new, v_new, k_cache, v_cache, past_len, scale, seed):
+    """Uncached route: full causal attention over the concatenated sequence, last N rows.
+
+    The first P query rows are random and discarded; keys/values are
+    ``torch.cat([history, new])``; the square causal mask comes from SDPA.
+    """
+    B, H_q, N, D = q.shape
+    H_kv = k_new.shape[1]
+    outs = []
+    for b, P in enumerate(past_len.tolist()):
+        qf = torch.cat([to_f64(_rand((H_q, P, D), seed + b, "f32")), to_f64(q[b])], dim=1)
+        kf = torch.cat([to_f64(k_cache[b, :, :P]), to_f64(k_new[b])], dim=1)
+        vf = torch.cat([to_f64(v_cache[b, :, :P]), to_f64(v_new[b])], dim=1)
+        o = F.scaled_dot_product_attention(qf[None], kf[None], vf[None], is_causal=True,
+                                           scale=scale, enable_gqa=H_q != H_kv)[0]
+        outs.append(o[:, P:])
+    return torch.stack(outs)
+
+
+_ROUTE_CASES = [
+    # B, H_q, H_kv, D, N, T_max, past, dtype, scale
+    (1, 12, 12, 64, 1, 64, [16], "f32", None),
+    (2, 4, 4, 64, 4, 40, [0, 13], "f32", None),
+    (2, 8, 2, 128, 3, 33, [30, 7], "bf16", None),
+    (3, 8, 1, 64, 16, 48, [32, 0, 5], "bf16", 0.3),
+    (1, 6, 3, 128, 5, 21, [16], "f32", 1.7),
+]
+
+
+def pin_route_b_sdpa(orc):
+    """Cached chunked decode = last N rows of uncached full causal attention (library SDPA)."""
+    for n, (B, H_q, H_kv, D, N, T_max, past, dtype, scale) in enumerate(_ROUTE_CASES):
+        q, k_new, v_new, k_cache, v_cache, past_len = _problem(B, H_q, H_kv, D, N, T_max, past, dtype, 100 + n)
+        kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
+        out = _oracle_decode(orc, q, kc, vc, past_len, dtype, scale)
+        want = _route_b_sdpa(q, k_new, v_new, k_cache, v_cache, past_len,
+                             scale if scale is not None else 1.0 / D ** 0.5, 500 + n)
+        assert _max_rel(out, want) < 1e-12, (n, _max_rel(out, want))
+
+
+def pin_full_causal_sdpa(orc):
+    """The oracle's own uncached route agrees with library causal attention."""
+    for T, D, scale in ((1, 8, 0.5), (17, 64, 0.125), (40, 128, 1.0 / 128 ** 0.5)):
+        qf, kf, vf = (to_f64(_rand((T, D), 600 + s, "f32")) for s in range(3))
+        got = torch.from_numpy(orc.full_causal_attention(qf.numpy(), kf.numpy(), vf.numpy(), scale))
+        want = F.scaled_dot_product_attention(qf[None], kf[None], vf[None], is_causal=True, scale=scale)[0]
+        assert _max_rel(got, want) < 1e-12
+
+
+def pin_permutation_single_token(orc):
+    """N = 1: jointly permuting the (K, V) pairs of all visible slots changes nothing."""
+    for dtype in ("f32", "bf16"):
+        P, D = 23, 64
+        q, k_new, v_new, k_cache, v_cache, past_len = _problem(1, 4, 2, D, 1, 32, [P], dtype, 41)
+        kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
+        base = _oracle_decode(orc, q, kc, vc, past_len, dtype)
+        perm = torch.randperm(P + 1, generator=torch.Generator().manual_seed(3))
+        kp, vp = kc.clone(), vc.clone()
+        kp[:, :, : P + 1] = kc[:, :, perm]
+        vp[:, :, : P + 1] = vc[:, :, perm]
+        out = _oracle_decode(orc, q, kp, vp, past_len, dtype)
+        assert _max_rel(out, base) < 1e-13
+
+
+def pin_reversed_order_trap(orc):
+    """The concat-order trap: new||old hides for N = 1 and shows for N > 1."""
+    for dtype in ("f32", "bf16"):
+        for N, must_differ in ((1, False), (4, True)):
+            P, D = 12, 64
+            q, k_new, v_new, k_cache, v_cache, past_len = _problem(1, 2, 2, D, N, 24, [P], dtype, 51)
+            kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
+            good = _oracle_decode(orc, q, kc, vc, past_len, dtype)
+            kr, vr = kc.clone(), vc.clone()
+            kr[0, :, : P + N] = torch.cat([k_new[0], k_cache[0, :, :P]], dim=1)
+            vr[0, :, : P + N] = torch.cat([v_new[0], v_cache[0, :, :P]], dim=1)
+            rev = _oracle_decode(orc, q, kr, vr, past_len, dtype)
+            err = _max_rel(rev, good)
+            if must_differ:
+                assert err > 1e-2, err
+            else:
+                assert err < 1e-13, err
+
+
+ALL_PINS = [
+    pin_cache_bytes,
+    pin_append_is_concat,
+    pin_single_visible_key,
+    pin_identical_keys_mean,
+    pin_dominant_key,
+    pin_route_b_sdpa,
+    pin_full_causal_sdpa,
+    pin_permutation_single_token,
+    pin_reversed_order_trap,
+]
