@@ -1,0 +1,146 @@
+/*
+ * kvd.h -- C ABI of the GB300 (sm_103a) KV-cache decode step.
+ *
+ * One decode step of GPT-style attention for one layer:
+ *   1. kvd_append            writes the K/V of N new tokens in place into a
+ *                            preallocated [B, H_kv, T_max, D] cache;
+ *   2. kvd_decode_attention  attends the N new query rows over the whole
+ *                            cached history (scaled q.K^T, softmax, .V) with
+ *                            the history-offset causal mask and GQA grouping.
+ *
+ * Sources (page title and section):
+ *   - The cache holds the K/V of past tokens, which do not change; decode feeds
+ *     only the new tokens and appends their K/V: gitcode.csdn.net
+ *     miniONNXRuntime article, section "KV Cache 原理"; shapes [1,H,T,D] +
+ *     [1,H,1,D] -> [1,H,T+1,D] on the time axis: section "Decode Shape 示例".
+ *   - Real engines write new K/V in place into preallocated slots rather than
+ *     concatenating: jennyma11.github.io/infra/ch07-01 "7.1 自回归生成过程",
+ *     section "Decode 阶段", note under code 1-2; openai-hub.com/news/2435
+ *     "GPT-2缓存实测：千倍计算只快6倍", section "显存测量最容易被分配器误导".
+ *   - Decode attention q.K^T/sqrt(D), softmax, .V with H_q query heads and
+ *     H_kv KV heads: "7.1 自回归生成过程", code 1-2.
+ *   - With P cached and N new tokens, new row i sees P+i+1 keys:
+ *     "GPT-2缓存实测", section "一个很容易漏掉的错误".
+ *   - Cache size 2 x layers x KV heads x head dim x tokens x batch x bytes:
+ *     "GPT-2缓存实测", section "GPT-2缓存要占多少显存".
+ *
+ * Conventions for every entry point
+ *   - Layouts are dense row-major: caches [B, H_kv, T_max, D]; q and out
+ *     [B, H_q, N, D]; k_new and v_new [B, H_kv, N, D].  One dtype (fp32 or
+ *     bf16) covers q, caches, new K/V and out; arithmetic accumulates in fp32.
+ *   - Pointers named as device pointers must be CUDA device memory of the
+ *     current device and 16-byte aligned.  Every buffer is owned by the caller;
+ *     the library allocates nothing, keeps no pointer after the call returns,
+ *     and never synchronises the host with the device.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All device work of a call is enqueued on it, in order.
+ *   - Argument errors are found on the host before anything is launched and are
+ *     returned as a status; nothing is written then.  A launch failure returns
+ *     KVD_ERR_CUDA.
+ *   - past_len lives in device memory, so per-sequence violations are detected
+ *     on the device: a sequence b with past_len[b] < 0, past_len[b] >
+ *     max_past_len or past_len[b] + N > T_max is skipped (nothing of it is
+ *     written) and KVD_DEVERR_PAST_LEN is OR-ed into *err_word when err_word is
+ *     not NULL.  The kernels never trap and every wait they contain is bounded.
+ *   - GQA: query head hq reads KV head hq / (H_q / H_kv).
+ */
+#ifndef KVD_H
+#define KVD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvd_status {
+    KVD_OK = 0,
+    KVD_ERR_INVALID_ARG = 1, /* null pointer, bad size, H_q % H_kv != 0, N < 1, misalignment */
+    KVD_ERR_CAPACITY = 2,    /* max_past_len + N > T_max, or max_past_len < 0 */
+    KVD_ERR_UNSUPPORTED = 3, /* D not in {64, 128}, unknown dtype, too many query rows */
+    KVD_ERR_WORKSPACE = 4,   /* workspace missing, misaligned or smaller than required */
+    KVD_ERR_CUDA = 5         /* a CUDA call or launch failed */
+} kvd_status;
+
+typedef enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1 } kvd_dtype;
+
+/* Bits OR-ed into the device error word. */
+#define KVD_DEVERR_PAST_LEN 1u /* a sequence had an out-of-range past_len and was skipped */
+#define KVD_DEVERR_TIMEOUT 2u  /* a bounded shared-memory pipeline wait gave up */
+
+/*
+ * kvd_append -- in-place cache update (step 1 of a decode step).
+ *
+ * For every sequence b < B, KV head h < H_kv and new token i < N:
+ *   k_cache[b, h, past_len[b] + i, :] = k_new[b, h, i, :]   (bit copy)
+ *   v_cache[b, h, past_len[b] + i, :] = v_new[b, h, i, :]
+ * No other slot is touched; nothing is reallocated or concatenated.
+ *
+ *   k_cache, v_cache  device, [B, H_kv, T_max, D], modified in place
+ *   k_new, v_new      device, [B, H_kv, N, D]
+ *   past_len          device int32[B]: tokens cached BEFORE this append
+ *   max_past_len      host bound on every past_len[b] (checked on the device)
+ *   err_word          device uint32 or NULL (see conventions)
+ * Returns KVD_OK, KVD_ERR_INVALID_ARG, KVD_ERR_CAPACITY, KVD_ERR_UNSUPPORTED or
+ * KVD_ERR_CUDA.  D may be any positive multiple of 8 (bf16) or 4 (fp32).
+ */
+kvd_status kvd_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                      const int32_t *past_len, int B, int H_kv, int T_max, int D, int N,
+                      int max_past_len, kvd_dtype dtype, uint32_t *err_word, void *stream);
+
+/*
+ * kvd_decode_workspace_bytes -- scratch size for kvd_decode_attention with the
+ * same shape arguments on the current device (0 when the arguments are
+ * invalid).  The split-T plan depends on the shapes and on the device's SM
+ * count, so query it on the device that will run the call.
+ */
+size_t kvd_decode_workspace_bytes(int B, int H_q, int H_kv, int D, int N, int max_past_len,
+                                  kvd_dtype dtype);
+
+/*
+ * kvd_decode_attention -- split-T attention of the new rows (step 2).
+ *
+ * Call after kvd_append with the SAME (pre-append) past_len.  For b < B,
+ * query head hq < H_q, new row i < N, with h = hq / (H_q / H_kv) and
+ * P = past_len[b]:
+ *   s_j = scale * q[b,hq,i,:] . k_cache[b,h,j,:]     for j = 0 .. P+i
+ *   out[b,hq,i,:] = sum_j softmax(s)_j * v_cache[b,h,j,:]
+ * Slots j > P+i (including any stale or NaN slot past P+N-1) are never read.
+ *
+ *   q, out            device, [B, H_q, N, D]; out gets the input dtype
+ *                     (bf16 rounded to nearest even from the fp32 result)
+ *   k_cache, v_cache  device, [B, H_kv, T_max, D], already appended
+ *   scale             softmax scale; <= 0 selects 1/sqrt(D)
+ *   workspace         device scratch of at least kvd_decode_workspace_bytes(...)
+ *                     bytes, 256-byte aligned, zero-filled before its first use
+ *                     (kvd_workspace_init); every call leaves it zero-filled
+ *                     again.  Calls that run concurrently need distinct
+ *                     workspaces.
+ * Supported: D in {64, 128}; dtype fp32 or bf16; H_q % H_kv == 0;
+ * (H_q / H_kv) * N <= 128.
+ * Returns KVD_OK or the first argument error found (see kvd_status).
+ */
+kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                void *out, const int32_t *past_len, int B, int H_q, int H_kv,
+                                int T_max, int D, int N, int max_past_len, float scale,
+                                kvd_dtype dtype, void *workspace, size_t workspace_bytes,
+                                uint32_t *err_word, void *stream);
+
+/* kvd_workspace_init -- zero-fill a workspace on `stream` (asynchronous). */
+kvd_status kvd_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * kvd_cache_bytes -- bytes of K and V caches for L layers:
+ *   2 * L * H_kv * D * T * B * (4 for fp32, 2 for bf16); 0 on invalid input.
+ */
+size_t kvd_cache_bytes(int L, int B, int H_kv, int D, int T, kvd_dtype dtype);
+
+/* kvd_status_string -- a static, human-readable name for a status code. */
+const char *kvd_status_string(kvd_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVD_H */

@@ -1,0 +1,332 @@
+// kvd_api.cu -- the C ABI (include/kvd.h): argument checks, the split-T plan,
+// launches, and the in-place append kernel.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kvd_attention.cuh"
+
+namespace kvd {
+
+// ---------------------------------------------------------------------------
+// kv_append: cache[b, h, P_b + i, :] = new[b, h, i, :] for i < N, K and V.
+// The cache is updated in place in its preallocated slots, as production
+// engines do instead of concatenating ("7.1 自回归生成过程", section "Decode
+// 阶段", the note under code 1-2).  One thread moves one 16-byte chunk of K and
+// the matching chunk of V; consecutive threads cover consecutive chunks of a
+// row, so loads and stores are fully coalesced 16-byte vector accesses.
+struct AppendArgs {
+    uint4 *k_cache;
+    uint4 *v_cache;
+    const uint4 *k_new;
+    const uint4 *v_new;
+    const int32_t *past_len;
+    uint32_t *err_word;
+    int H_kv, T_max, N, max_past_len;
+    int row_chunks;   // 16-byte chunks per row
+    long long total;  // B * H_kv * N * row_chunks
+};
+
+__global__ void __launch_bounds__(256) append_kernel(const AppendArgs a)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < a.total;
+         idx += stride) {
+        const int c = (int)(idx % a.row_chunks);
+        const long long row = idx / a.row_chunks;  // (bh, i)
+        const int i = (int)(row % a.N);
+        const long long bh = row / a.N;
+        const int b = (int)(bh / a.H_kv);
+        const int P = __ldg(a.past_len + b);
+        if (!past_len_ok(P, a.N, a.T_max, a.max_past_len)) {
+            if (c == 0 && i == 0 && bh % a.H_kv == 0) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
+            continue;
+        }
+        const long long dst = (bh * a.T_max + P + i) * a.row_chunks + c;
+        stg128(a.k_cache + dst, ldg128_nc(a.k_new + idx));
+        stg128(a.v_cache + dst, ldg128_nc(a.v_new + idx));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Per-device facts, queried once.
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxRows = 128;  // (H_q / H_kv) * N supported per (b, h)
+
+std::mutex g_mu;
+int g_sm_count[kMaxDevices];
+
+struct OccEntry {
+    int device;
+    const void *fn;
+    int ctas_per_sm;
+};
+OccEntry g_occ[256];
+int g_occ_n = 0;
+
+kvd_status current_device(int *dev)
+{
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return KVD_ERR_CUDA;
+    return KVD_OK;
+}
+
+kvd_status sm_count(int dev, int *n)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            return KVD_ERR_CUDA;
+        g_sm_count[dev] = v;
+    }
+    *n = g_sm_count[dev];
+    return KVD_OK;
+}
+
+// Opt the kernel into its dynamic shared memory and return its occupancy.
+kvd_status prepare_kernel(int dev, const AttnVariant &v, int *ctas_per_sm)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int k = 0; k < g_occ_n; ++k) {
+        if (g_occ[k].device == dev && g_occ[k].fn == v.split_fn) {
+            *ctas_per_sm = g_occ[k].ctas_per_sm;
+            return KVD_OK;
+        }
+    }
+    if (cudaFuncSetAttribute(v.split_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem_bytes) !=
+        cudaSuccess)
+        return KVD_ERR_CUDA;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.split_fn, v.threads, v.smem_bytes) !=
+            cudaSuccess ||
+        occ <= 0)
+        return KVD_ERR_CUDA;
+    if (g_occ_n < 256) g_occ[g_occ_n++] = OccEntry{dev, v.split_fn, occ};
+    *ctas_per_sm = occ;
+    return KVD_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int elem_bytes(kvd_dtype dt) { return dt == KVD_F32 ? 4 : (dt == KVD_BF16 ? 2 : 0); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The split-T plan of one decode_attention call.
+struct Plan {
+    AttnVariant v;
+    int rows, rb, n_rowblocks, rows_pad;
+    int split_keys, n_splits;
+    long long grid;
+    size_t part_o_off, part_ml_off, ws_bytes;
+};
+
+kvd_status check_shapes(int B, int H_q, int H_kv, int D, int N, int max_past_len, kvd_dtype dtype)
+{
+    if (B < 0 || H_q < 1 || H_kv < 1 || N < 1 || max_past_len < 0) return KVD_ERR_INVALID_ARG;
+    if (H_q % H_kv != 0) return KVD_ERR_INVALID_ARG;
+    if (elem_bytes(dtype) == 0) return KVD_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return KVD_ERR_UNSUPPORTED;
+    if ((long long)(H_q / H_kv) * N > kMaxRows) return KVD_ERR_UNSUPPORTED;
+    return KVD_OK;
+}
+
+kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, kvd_dtype dtype,
+                     Plan *pl)
+{
+    kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
+    if (st != KVD_OK) return st;
+    pl->rows = (H_q / H_kv) * N;
+    pl->rb = pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : pl->rows <= 4 ? 4 : 8;
+    pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
+    pl->rows_pad = pl->n_rowblocks * pl->rb;
+    const bool ok = dtype == KVD_F32 ? attn_variant_f32(D, pl->rb, &pl->v)
+                                     : attn_variant_bf16(D, pl->rb, &pl->v);
+    if (!ok) return KVD_ERR_UNSUPPORTED;
+
+    int dev = 0, sms = 0, occ = 0;
+    if ((st = current_device(&dev)) != KVD_OK) return st;
+    if ((st = sm_count(dev, &sms)) != KVD_OK) return st;
+    if ((st = prepare_kernel(dev, pl->v, &occ)) != KVD_OK) return st;
+
+    // Split T so that the non-empty CTAs fill every SM about twice over; a
+    // split is never shorter than two tiles.
+    const long long tk = pl->v.tile_keys;
+    const long long t_hint = (long long)max_past_len + N;
+    const long long pairs = (long long)B * H_kv * pl->n_rowblocks;
+    const long long target = 2LL * sms * occ;
+    long long sk = pairs > 0 ? (t_hint * pairs + target - 1) / target : t_hint;
+    sk = (sk + tk - 1) / tk * tk;
+    if (sk < 2 * tk) sk = 2 * tk;
+    const long long t_cover = (t_hint + tk - 1) / tk * tk;
+    if (sk > t_cover) sk = t_cover;
+    pl->split_keys = (int)sk;
+    pl->n_splits = (int)((t_hint + sk - 1) / sk);
+    pl->grid = pairs * pl->n_splits;
+
+    if (pl->n_splits == 1) {
+        pl->part_o_off = pl->part_ml_off = pl->ws_bytes = 0;
+    } else {
+        const size_t parts = (size_t)B * H_kv * pl->n_splits * pl->rows_pad;
+        pl->part_o_off = 0;
+        pl->part_ml_off = round_up(parts * D * sizeof(float), 256);
+        pl->ws_bytes = pl->part_ml_off + round_up(parts * 2 * sizeof(float), 256);
+    }
+    return KVD_OK;
+}
+
+}  // namespace
+}  // namespace kvd
+
+using namespace kvd;
+
+extern "C" {
+
+kvd_status kvd_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                      const int32_t *past_len, int B, int H_kv, int T_max, int D, int N,
+                      int max_past_len, kvd_dtype dtype, uint32_t *err_word, void *stream)
+{
+    const int s = elem_bytes(dtype);
+    if (s == 0) return KVD_ERR_UNSUPPORTED;
+    if (!k_cache || !v_cache || !k_new || !v_new || !past_len) return KVD_ERR_INVALID_ARG;
+    if (B < 0 || H_kv < 1 || T_max < 1 || D < 1 || N < 1 || max_past_len < 0)
+        return KVD_ERR_INVALID_ARG;
+    if (((long long)D * s) % 16 != 0) return KVD_ERR_UNSUPPORTED;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+        return KVD_ERR_INVALID_ARG;
+    if ((long long)max_past_len + N > T_max) return KVD_ERR_CAPACITY;
+    if (B == 0) return KVD_OK;
+
+    int dev = 0, sms = 0;
+    kvd_status st;
+    if ((st = current_device(&dev)) != KVD_OK) return st;
+    if ((st = sm_count(dev, &sms)) != KVD_OK) return st;
+
+    AppendArgs a;
+    a.k_cache = static_cast<uint4 *>(k_cache);
+    a.v_cache = static_cast<uint4 *>(v_cache);
+    a.k_new = static_cast<const uint4 *>(k_new);
+    a.v_new = static_cast<const uint4 *>(v_new);
+    a.past_len = past_len;
+    a.err_word = err_word;
+    a.H_kv = H_kv;
+    a.T_max = T_max;
+    a.N = N;
+    a.max_past_len = max_past_len;
+    a.row_chunks = (int)(((long long)D * s) / 16);
+    a.total = (long long)B * H_kv * N * a.row_chunks;
+    const int threads = 256;
+    long long blocks = (a.total + threads - 1) / threads;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    void *args[] = {&a};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(&append_kernel), dim3((unsigned)blocks),
+                            dim3(threads), args, 0, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+size_t kvd_decode_workspace_bytes(int B, int H_q, int H_kv, int D, int N, int max_past_len,
+                                  kvd_dtype dtype)
+{
+    Plan pl;
+    if (make_plan(B, H_q, H_kv, D, N, max_past_len, dtype, &pl) != KVD_OK) return 0;
+    return pl.ws_bytes;
+}
+
+kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                void *out, const int32_t *past_len, int B, int H_q, int H_kv,
+                                int T_max, int D, int N, int max_past_len, float scale,
+                                kvd_dtype dtype, void *workspace, size_t workspace_bytes,
+                                uint32_t *err_word, void *stream)
+{
+    if (!q || !k_cache || !v_cache || !out || !past_len) return KVD_ERR_INVALID_ARG;
+    kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
+    if (st != KVD_OK) return st;
+    if (T_max < 1) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return KVD_ERR_INVALID_ARG;
+    if ((long long)max_past_len + N > T_max) return KVD_ERR_CAPACITY;
+    if (B == 0) return KVD_OK;
+
+    Plan pl;
+    if ((st = make_plan(B, H_q, H_kv, D, N, max_past_len, dtype, &pl)) != KVD_OK) return st;
+    if (pl.ws_bytes > 0) {
+        if (workspace == nullptr || workspace_bytes < pl.ws_bytes ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return KVD_ERR_WORKSPACE;
+    }
+
+    AttnArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.out = out;
+    a.past_len = past_len;
+    a.part_o = pl.ws_bytes ? reinterpret_cast<float *>(static_cast<char *>(workspace) + pl.part_o_off)
+                           : nullptr;
+    a.part_ml = pl.ws_bytes
+                    ? reinterpret_cast<float *>(static_cast<char *>(workspace) + pl.part_ml_off)
+                    : nullptr;
+    a.err_word = err_word;
+    a.B = B;
+    a.H_kv = H_kv;
+    a.T_max = T_max;
+    a.N = N;
+    a.max_past_len = max_past_len;
+    a.rows = pl.rows;
+    a.rows_pad = pl.rows_pad;
+    a.n_rowblocks = pl.n_rowblocks;
+    a.n_splits = pl.n_splits;
+    a.split_keys = pl.split_keys;
+    const float sc = (scale > 0.f) ? scale : 1.0f / sqrtf((float)D);
+    a.qscale = sc * kLog2e;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *args[] = {&a};
+    if (cudaLaunchKernel(pl.v.split_fn, dim3((unsigned)pl.grid), dim3(pl.v.threads), args,
+                         (size_t)pl.v.smem_bytes, s) != cudaSuccess)
+        return KVD_ERR_CUDA;
+    if (pl.n_splits > 1) {
+        const long long warps = (long long)B * H_kv * pl.rows;
+        const long long blocks = (warps * 32 + 127) / 128;
+        if (cudaLaunchKernel(pl.v.merge_fn, dim3((unsigned)blocks), dim3(128), args, 0, s) !=
+            cudaSuccess)
+            return KVD_ERR_CUDA;
+    }
+    return KVD_OK;
+}
+
+kvd_status kvd_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (workspace_bytes == 0) return KVD_OK;
+    if (workspace == nullptr) return KVD_ERR_WORKSPACE;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+size_t kvd_cache_bytes(int L, int B, int H_kv, int D, int T, kvd_dtype dtype)
+{
+    const int s = elem_bytes(dtype);
+    if (s == 0 || L < 0 || B < 0 || H_kv < 0 || D < 0 || T < 0) return 0;
+    return (size_t)2 * (size_t)L * (size_t)H_kv * (size_t)D * (size_t)T * (size_t)B * (size_t)s;
+}
+
+const char *kvd_status_string(kvd_status status)
+{
+    switch (status) {
+    case KVD_OK: return "KVD_OK";
+    case KVD_ERR_INVALID_ARG: return "KVD_ERR_INVALID_ARG";
+    case KVD_ERR_CAPACITY: return "KVD_ERR_CAPACITY";
+    case KVD_ERR_UNSUPPORTED: return "KVD_ERR_UNSUPPORTED";
+    case KVD_ERR_WORKSPACE: return "KVD_ERR_WORKSPACE";
+    case KVD_ERR_CUDA: return "KVD_ERR_CUDA";
+    default: return "KVD_UNKNOWN_STATUS";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,171 @@
+// kvd_device.cuh -- device helpers shared by the decode-step kernels (sm_103a).
+//
+// Inline PTX for the Blackwell bulk-copy (TMA) engine and shared-memory
+// mbarriers, bf16 widening, and the bounded wait used by every pipeline.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvd.h"
+
+namespace kvd {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// A pipeline wait gives up after this long (ns of %globaltimer), sets
+// KVD_DEVERR_TIMEOUT and lets the kernel wind down.  A healthy wait ends in
+// microseconds; the bound only exists so that no kernel can spin forever.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make the mbarrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        "  .reg .pred p;\n"
+        "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "  selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait until phase `parity` of `bar` has completed.  Bounded: returns false
+// after kWaitLimitNs without completion.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// L2 policy for data that is read exactly once (K/V streams).
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// One bulk (TMA) copy global -> shared of `bytes` (multiple of 16, both
+// addresses 16-byte aligned), completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load_g2s(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg128_nc(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void stg128(void *p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Element type traits: how a 16-byte chunk widens to fp32.
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static constexpr int kBytes = 4;
+    static constexpr int kPerChunk = 4;
+    __device__ __forceinline__ static void widen(const uint4 &c, float *f)
+    {
+        f[0] = __uint_as_float(c.x);
+        f[1] = __uint_as_float(c.y);
+        f[2] = __uint_as_float(c.z);
+        f[3] = __uint_as_float(c.w);
+    }
+    __device__ __forceinline__ static void store(float *dst, float v) { *dst = v; }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+    static constexpr int kPerChunk = 8;
+    // A bf16 is the upper half of an fp32: element 2k sits in the low half of
+    // word k (little endian), element 2k+1 in the high half.
+    __device__ __forceinline__ static void widen(const uint4 &c, float *f)
+    {
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            f[2 * k] = __uint_as_float(w[k] << 16);
+            f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static void store(__nv_bfloat16 *dst, float v)
+    {
+        *dst = __float2bfloat16_rn(v);
+    }
+};
+
+__device__ __forceinline__ void raise_error(uint32_t *err_word, uint32_t bit)
+{
+    if (err_word != nullptr) atomicOr(err_word, bit);
+}
+
+__device__ __forceinline__ bool past_len_ok(int P, int N, int T_max, int max_past_len)
+{
+    return P >= 0 && P <= max_past_len && P + N <= T_max;
+}
+
+}  // namespace kvd

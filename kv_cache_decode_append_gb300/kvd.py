@@ -1,0 +1,205 @@
+"""Thin ctypes binding of ``include/kvd.h``.
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of ``libkvd.so``.  There is no fallback: when the library is missing
+or a call returns a non-OK status, these functions raise.
+
+Two layers, same names as the C ABI:
+
+* ``raw`` -- the C functions with integer pointers (``ctypes``), for callers
+  that manage their own memory;
+* the module-level functions -- take ``torch`` CUDA tensors, check dtype,
+  device and contiguity, derive the shape arguments, and pass the current
+  stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KVD_OK = 0
+KVD_ERR_INVALID_ARG = 1
+KVD_ERR_CAPACITY = 2
+KVD_ERR_UNSUPPORTED = 3
+KVD_ERR_WORKSPACE = 4
+KVD_ERR_CUDA = 5
+
+KVD_F32 = 0
+KVD_BF16 = 1
+
+KVD_DEVERR_PAST_LEN = 1
+KVD_DEVERR_TIMEOUT = 2
+
+_TORCH_DTYPE = {torch.float32: KVD_F32, torch.bfloat16: KVD_BF16}
+_NAME_DTYPE = {"f32": KVD_F32, "bf16": KVD_BF16}
+
+
+class KvdError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {raw.kvd_status_string(status).decode()} ({status})")
+
+
+class _Lib:
+    """The loaded ``libkvd.so`` with typed C signatures."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        vp, sz, ci, cf, u32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+        lib.kvd_append.restype = ci
+        lib.kvd_append.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, u32p, vp]
+        lib.kvd_decode_workspace_bytes.restype = sz
+        lib.kvd_decode_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci, ci]
+        lib.kvd_decode_attention.restype = ci
+        lib.kvd_decode_attention.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
+                                             vp, sz, u32p, vp]
+        lib.kvd_workspace_init.restype = ci
+        lib.kvd_workspace_init.argtypes = [vp, sz, vp]
+        lib.kvd_cache_bytes.restype = sz
+        lib.kvd_cache_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
+        lib.kvd_status_string.restype = ctypes.c_char_p
+        lib.kvd_status_string.argtypes = [ci]
+        self._lib = lib
+        self.path = path
+
+    def __getattr__(self, name):
+        return getattr(self._lib, name)
+
+
+_lock = threading.Lock()
+_loaded: Optional[_Lib] = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> _Lib:
+    """Load ``libkvd.so``; raises if it has not been built."""
+    global _loaded
+    with _lock:
+        if _loaded is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            _loaded = _Lib(path)
+        return _loaded
+
+
+class _Raw:
+    def __getattr__(self, name):
+        return getattr(load(), name)
+
+
+raw = _Raw()
+
+
+# ---------------------------------------------------------------------------------
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype=None) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _TORCH_DTYPE:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return _TORCH_DTYPE[t.dtype]
+
+
+def _check(fn: str, status: int) -> None:
+    if status != KVD_OK:
+        raise KvdError(fn, status)
+
+
+def kvd_append(k_cache, v_cache, k_new, v_new, past_len, max_past_len: int,
+               err_word=None, stream=None) -> None:
+    """Write ``k_new``/``v_new`` [B,H_kv,N,D] into slots ``past_len[b] + i`` of the caches."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new)):
+        _need_cuda(n, t, k_cache.dtype)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_kv, T_max, D = k_cache.shape
+    N = k_new.shape[2]
+    if v_cache.shape != k_cache.shape or tuple(k_new.shape) != (B, H_kv, N, D) or v_new.shape != k_new.shape:
+        raise ValueError("shape mismatch between caches and new K/V")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    st = raw.kvd_append(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                        past_len.data_ptr(), B, H_kv, T_max, D, N, int(max_past_len),
+                        _dtype_code(k_cache), _ptr(err_word), _stream_handle(stream))
+    _check("kvd_append", st)
+
+
+def kvd_decode_workspace_bytes(B: int, H_q: int, H_kv: int, D: int, N: int, max_past_len: int,
+                               dtype) -> int:
+    code = _NAME_DTYPE[dtype] if isinstance(dtype, str) else _TORCH_DTYPE[dtype]
+    return int(raw.kvd_decode_workspace_bytes(B, H_q, H_kv, D, N, int(max_past_len), code))
+
+
+def alloc_workspace(B, H_q, H_kv, D, N, max_past_len, dtype, device=None) -> Optional[torch.Tensor]:
+    """A zero-filled device workspace sized for these shapes (None when none is needed)."""
+    n = kvd_decode_workspace_bytes(B, H_q, H_kv, D, N, max_past_len, dtype)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def kvd_workspace_init(workspace: Optional[torch.Tensor], stream=None) -> None:
+    if workspace is None:
+        return
+    _check("kvd_workspace_init", raw.kvd_workspace_init(workspace.data_ptr(), workspace.numel(),
+                                                        _stream_handle(stream)))
+
+
+def kvd_decode_attention(q, k_cache, v_cache, out, past_len, max_past_len: int, scale: float = 0.0,
+                         workspace: Optional[torch.Tensor] = None, err_word=None, stream=None) -> None:
+    """Attention of the N new rows of ``q`` over the appended caches into ``out`` [B,H_q,N,D]."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        _need_cuda(n, t, q.dtype)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_q, N, D = q.shape
+    _, H_kv, T_max, _ = k_cache.shape
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError("shape mismatch between q, out and the caches")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = raw.kvd_decode_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                  past_len.data_ptr(), B, H_q, H_kv, T_max, D, N, int(max_past_len),
+                                  float(scale), _dtype_code(q), ws_ptr, ws_bytes, _ptr(err_word),
+                                  _stream_handle(stream))
+    _check("kvd_decode_attention", st)
+
+
+def kvd_cache_bytes(L: int, B: int, H_kv: int, D: int, T: int, dtype) -> int:
+    code = _NAME_DTYPE[dtype] if isinstance(dtype, str) else _TORCH_DTYPE[dtype]
+    return int(raw.kvd_cache_bytes(L, B, H_kv, D, T, code))
+
+
+def kvd_status_string(status: int) -> str:
+    return raw.kvd_status_string(int(status)).decode()

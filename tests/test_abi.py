@@ -1,0 +1,112 @@
+"""The C-ABI library loads and exports every declared entry point; host-side
+argument checks return their documented status before touching a GPU.  CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from helpers import *  # noqa: F401,F403
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvd.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "kv_cache_bytes.txt")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_decode_append_gb300 import build as kbuild
+    from kv_cache_decode_append_gb300 import kvd
+    kbuild.build()
+    return kvd.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvd_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("kvd_append", "kvd_decode_attention", "kvd_decode_workspace_bytes",
+              "kvd_workspace_init", "kvd_cache_bytes", "kvd_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(lib.path)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_cache_bytes_matches_the_pages_table(lib):
+    import kv_cache_decode_append_gb300 as kvd
+    units = {"B": 1, "KiB": 1024, "MiB": 1024 ** 2}
+    for line in open(GOLDEN):
+        if not line.strip() or line.startswith("#"):
+            continue
+        L, B, H, D, T, s, expected, unit, match = line.split()
+        got = kvd.kvd_cache_bytes(int(L), int(B), int(H), int(D), int(T), "f32" if s == "4" else "bf16")
+        got /= units[unit]
+        if match == "exact":
+            assert got == float(expected)
+        else:
+            assert round(got, len(expected.split(".")[1])) == float(expected)
+    assert kvd.kvd_cache_bytes(-1, 1, 1, 1, 1, "f32") == 0
+
+
+def test_status_strings(lib):
+    import kv_cache_decode_append_gb300 as kvd
+    assert kvd.kvd_status_string(0) == "KVD_OK"
+    assert kvd.kvd_status_string(4) == "KVD_ERR_WORKSPACE"
+    assert kvd.kvd_status_string(99) == "KVD_UNKNOWN_STATUS"
+
+
+# Fake, 256-byte aligned addresses: every call below must be rejected on the
+# host before any pointer is dereferenced or any CUDA call is made.
+A = 1 << 20
+
+
+def _attn(lib, q=A, k=A, v=A, out=A, past=A, B=1, H_q=4, H_kv=2, T_max=64, D=64, N=1,
+          max_past=10, dtype=1):
+    return lib.kvd_decode_attention(q, k, v, out, past, B, H_q, H_kv, T_max, D, N, max_past,
+                                    0.0, dtype, None, 0, None, None)
+
+
+def _append(lib, k=A, v=A, kn=A, vn=A, past=A, B=1, H_kv=2, T_max=64, D=64, N=1, max_past=10, dtype=1):
+    return lib.kvd_append(k, v, kn, vn, past, B, H_kv, T_max, D, N, max_past, dtype, None, None)
+
+
+def test_attention_argument_errors(lib):
+    assert _attn(lib, q=0) == 1
+    assert _attn(lib, past=0) == 1
+    assert _attn(lib, H_q=3, H_kv=2) == 1
+    assert _attn(lib, N=0) == 1
+    assert _attn(lib, B=-1) == 1
+    assert _attn(lib, max_past=-1) == 1
+    assert _attn(lib, D=96) == 3
+    assert _attn(lib, dtype=7) == 3
+    assert _attn(lib, H_q=16, H_kv=1, N=9) == 3      # 144 query rows per KV head
+    assert _attn(lib, q=A + 8) == 1                   # misaligned
+    assert _attn(lib, out=A + 4) == 1
+    assert _attn(lib, max_past=64, N=1, T_max=64) == 2  # P + N > T_max
+    assert _attn(lib, B=0) == 0                       # empty batch: nothing to do
+
+
+def test_append_argument_errors(lib):
+    assert _append(lib, k=0) == 1
+    assert _append(lib, vn=0) == 1
+    assert _append(lib, N=0) == 1
+    assert _append(lib, T_max=0) == 1
+    assert _append(lib, dtype=9) == 3
+    assert _append(lib, D=3, dtype=1) == 3            # 6-byte rows are not whole 16-byte chunks
+    assert _append(lib, kn=A + 2) == 1
+    assert _append(lib, max_past=60, N=5, T_max=64) == 2
+    assert _append(lib, B=0) == 0
+
+
+def test_workspace_query_rejects_bad_shapes(lib):
+    assert lib.kvd_decode_workspace_bytes(1, 3, 2, 64, 1, 10, 1) == 0
+    assert lib.kvd_decode_workspace_bytes(1, 4, 2, 80, 1, 10, 1) == 0
+    assert lib.kvd_decode_workspace_bytes(1, 4, 2, 64, 0, 10, 1) == 0
