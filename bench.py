@@ -1,0 +1,459 @@
+"""Benchmark of the KV-cache decode step on GB300.
+
+One step = one decode step of the whole layer stack: for every layer,
+kvd_append (new K/V into the preallocated cache) then kvd_decode_attention
+(split-T attention + log-sum-exp merge), on one stream.  The default workload
+is the grouped-query long-context case (32 layers, B=32, 32 query / 8 KV
+heads, D=128, per-sequence history U[1024, 8192], N=1, bf16); the K/V read
+per step (19 GB) is far larger than L2, so no flush is needed between steps.
+
+Metric: achieved HBM GB/s of algorithmic bytes (K/V read over P+N keys, Q
+read, O written, append read+write; workspace traffic excluded) and
+microseconds per layer-step.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+``--impl reference`` times the CPU oracle (double precision, all host cores)
+on the same workload, one layer-step per step.  Under torchrun with N > 1 each
+rank runs an independent replica (the path shards by sequence and head with no
+exchange): weak scaling, the max time over ranks, no data-path collective.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kv_cache_decode_append_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "decode attention: achieved HBM GB/s (% of GB300 peak) and μs per layer-step"
+DEFAULT_WORKLOAD = "gqa_longctx_b32_bf16"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_attention_gqa_longctx_b32.md")
+
+
+# ---------------------------------------------------------------------------------
+# algorithmic bytes (the roofline's per-unit figures)
+def attn_bytes(w: wl.Workload, past) -> int:
+    """K/V read over P_b + N keys of every (b, h_kv), plus Q read and O written."""
+    s = w.elem_bytes
+    keys = sum(int(p) + w.N for p in past)
+    return 2 * w.H_kv * w.D * s * keys + 2 * w.B * w.H_q * w.N * w.D * s
+
+
+def append_bytes(w: wl.Workload) -> int:
+    """New K and V read, and the same bytes written into the cache."""
+    return 4 * w.B * w.H_kv * w.N * w.D * w.elem_bytes
+
+
+def layer_bytes(w, past) -> int:
+    return attn_bytes(w, past) + append_bytes(w)
+
+
+# ---------------------------------------------------------------------------------
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "kv_cache_decode_append_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            text = f.read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(fields["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def gpu_smi_id(dev) -> str:
+    """An nvidia-smi --id for this torch device (PCI bus id, else UUID, else index)."""
+    props = torch.cuda.get_device_properties(dev)
+    try:
+        return f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    except AttributeError:
+        pass
+    try:
+        u = str(props.uuid)
+        return u if u.startswith("GPU-") else f"GPU-{u}"
+    except AttributeError:
+        return str(dev.index or 0)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str):
+        self.index = index
+        self.samples = []  # (time, sm_mhz, max_mhz, reasons)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, mx, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        used = inside if inside else [s for s in self.samples if t0 - 0.5 <= s[0] <= t1 + 0.5]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({r for s in used for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in used), "sm_max_mhz": max(s[2] for s in used),
+                "reasons": reasons, "samples": len(used),
+                "window": "timed region" if inside else "timed region +-0.5 s"}
+
+
+# ---------------------------------------------------------------------------------
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Host-side aggregation of the timed region (not part of the data path)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda") if torch.cuda.is_available() and dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_layer_step(orc, host, past_np, dtype):
+    st = orc.append(host["k_cache"], host["v_cache"], host["k_new"], host["v_new"], past_np, dtype)
+    out, st2 = orc.decode_attention(host["q"], host["k_cache"], host["v_cache"], past_np, dtype)
+    if st != 0 or st2 != 0:
+        raise RuntimeError("oracle rejected the workload")
+    return out
+
+
+def to_host_np(t: torch.Tensor):
+    import numpy as np
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def time_oracle(w, host, past, budget_s: float = 10.0, max_reps: int = 64):
+    """Repeat the oracle's layer-step on one layer's host data for about budget_s."""
+    import oracle
+    orc = oracle.load()
+    past_np = past.numpy()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_layer_step(orc, host, past_np, w.dtype)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    return reps, el, orc.max_threads()
+
+
+# ---------------------------------------------------------------------------------
+def run_reference(args, w, rank, world):
+    """The reference arm: the CPU oracle, as it stands, one layer-step per step."""
+    if rank != 0:
+        return
+    import oracle
+    orc = oracle.load()
+    past = wl.past_lens(w)
+    t = wl.layer_inputs(w, 0, past, device="cpu", tail_fill="zero")
+    host = {k: to_host_np(v) for k, v in t.items()}
+    past_np = past.numpy()
+    for _ in range(args.warmup):
+        oracle_layer_step(orc, host, past_np, w.dtype)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_layer_step(orc, host, past_np, w.dtype)
+    el = time.perf_counter() - t0
+    per_step = el / args.steps
+    gbs = layer_bytes(w, past.tolist()) / per_step / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "describe": w.describe(),
+                   "step": "one layer-step (append + decode attention) of the workload"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": orc.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"one layer of {w.name} (all {w.B} sequences) per step"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, w, rank, world, local):
+    import kv_cache_decode_append_gb300 as kvd
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    past = wl.past_lens(w)
+    max_past = int(past.max())
+    past_d = past.to(dev)
+    layers = [wl.layer_inputs(w, l, past, device=dev, tail_fill="zero") for l in range(w.L)]
+    outs = [torch.empty_like(x["q"]) for x in layers]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, w.torch_dtype, dev)
+    merge = ws is not None
+    launches_per_layer = 2 + (1 if merge else 0)
+
+    def layer_step(l):
+        x = layers[l]
+        kvd.kvd_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past, err, stream)
+        kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past, 0.0, ws,
+                                 err, stream)
+
+    def step():
+        for l in range(w.L):
+            layer_step(l)
+
+    # warm-up (also builds nothing: the library is loaded on the first call)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())}")
+
+    sampler = ClockSampler(gpu_smi_id(dev))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.2)
+
+    # timed region: K steps, events around every attention call for the roofline
+    ev_a = [[torch.cuda.Event(enable_timing=True) for _ in range(w.L)] for _ in range(args.steps)]
+    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(w.L)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for k in range(args.steps):
+        for l in range(w.L):
+            x = layers[l]
+            kvd.kvd_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past, err, stream)
+            ev_a[k][l].record(stream)
+            kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past, 0.0,
+                                     ws, err, stream)
+            ev_b[k][l].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    elapsed = start.elapsed_time(end) / 1e3
+    attn_s = sum(a.elapsed_time(b) for ra, rb in zip(ev_a, ev_b) for a, b in zip(ra, rb)) / 1e3
+    attn_per_launch = attn_s / (args.steps * w.L)
+    elapsed_max = max_over_ranks(elapsed, world)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())}")
+
+    # end to end: inputs from pinned host memory each step, result read back each step
+    host_in = [{k: layers[l][k].cpu().pin_memory() for k in ("q", "k_new", "v_new")} for l in range(w.L)]
+    host_out = [torch.empty(outs[l].shape, dtype=outs[l].dtype).pin_memory() for l in range(w.L)]
+    past_h = past.pin_memory()
+    h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values()) + past_h.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        past_d.copy_(past_h, non_blocking=True)
+        for l in range(w.L):
+            for key in ("q", "k_new", "v_new"):
+                layers[l][key].copy_(host_in[l][key], non_blocking=True)
+            layer_step(l)
+            host_out[l].copy_(outs[l], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    barrier(world)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(1, args.steps // 2)
+    e_start.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_el = max_over_ranks(e_start.elapsed_time(e_end) / 1e3, world)
+    if rank == 0:
+        sampler.stop()
+
+    if rank != 0:
+        return
+    bytes_step = w.L * layer_bytes(w, past.tolist())
+    gbs = world * bytes_step * args.steps / elapsed_max / 1e9
+    ms_step = elapsed_max / args.steps * 1e3
+    peak, peak_kind = measured_peak()
+    a_bytes = attn_bytes(w, past.tolist())
+    achieved = a_bytes / attn_per_launch / 1e9
+
+    # CPU baseline: the oracle on layer 0's data, all host cores, ~10 s
+    host = {k: to_host_np(v) for k, v in layers[0].items()}
+    reps, cpu_el, cores = time_oracle(w, host, past, budget_s=args.cpu_seconds)
+    cpu_gbs = reps * layer_bytes(w, past.tolist()) / cpu_el / 1e9
+
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "describe": w.describe(), "layers": w.L, "B": w.B, "H_q": w.H_q,
+            "H_kv": w.H_kv, "D": w.D, "N": w.N, "T_max": w.T_max,
+            "P": (w.P if w.P is not None else f"U[{w.P_range[0]},{w.P_range[1]}] seeded, sum {int(past.sum())}"),
+            "step": f"{w.L} x (kvd_append + kvd_decode_attention) on one stream",
+            "l2": f"no flush: inputs larger than L2 ({bytes_step / 1e9:.1f} GB per step)"
+            if bytes_step > 2 * 126e6 else "warm L2 (inputs smaller than L2)",
+            "parallelism": f"replicas x{world}",
+        },
+        "us_per_layer_step": round(ms_step * 1e3 / w.L, 3),
+        "frac_of_peak": round(gbs / world / peak, 4),
+        "attn_us_per_layer": round(attn_per_launch * 1e6, 3),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "kvd_decode_attention (split-T kernel + LSE merge)" if merge else "kvd_decode_attention",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy burst)" if peak_kind == "measured" else "fallback",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "algorithmic_bytes_per_launch": a_bytes,
+            "traffic": profiled_traffic(),
+        },
+        "cpu_baseline": {
+            "value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"layer 0 of {w.name} (all {w.B} sequences, append + attention, fp64), "
+                      f"repeated {reps}x in {cpu_el:.1f} s",
+        },
+        "e2e": {
+            "value": round(world * bytes_step * e_steps / e2e_el / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(e2e_el / e_steps * 1e3, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": args.steps * w.L * launches_per_layer,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--n-new", type=int, default=None, help="override N (chunked decode sweep)")
+    ap.add_argument("--impl", default="kvd", choices=["kvd", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = wl.WORKLOADS[args.workload]
+    if args.n_new is not None:
+        w = wl.with_n(w, args.n_new)
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+    else:
+        run_gpu(args, w, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
