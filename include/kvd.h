@@ -113,10 +113,8 @@ size_t kvd_decode_workspace_bytes(int B, int H_q, int H_kv, int D, int N, int ma
  *   k_cache, v_cache  device, [B, H_kv, T_max, D], already appended
  *   scale             softmax scale; <= 0 selects 1/sqrt(D)
  *   workspace         device scratch of at least kvd_decode_workspace_bytes(...)
- *                     bytes, 256-byte aligned, zero-filled before its first use
- *                     (kvd_workspace_init); every call leaves it zero-filled
- *                     again.  Calls that run concurrently need distinct
- *                     workspaces.
+ *                     bytes, 256-byte aligned; no initial contents are needed.
+ *                     Calls that run concurrently need distinct workspaces.
  * Supported: D in {64, 128}; dtype fp32 or bf16; H_q % H_kv == 0;
  * (H_q / H_kv) * N <= 128.
  * Returns KVD_OK or the first argument error found (see kvd_status).
@@ -127,7 +125,30 @@ kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *
                                 kvd_dtype dtype, void *workspace, size_t workspace_bytes,
                                 uint32_t *err_word, void *stream);
 
-/* kvd_workspace_init -- zero-fill a workspace on `stream` (asynchronous). */
+/*
+ * kvd_decode_plan -- how kvd_decode_attention would run these shapes on the
+ * current device, without launching anything: keys per tile, the most tiles
+ * one sequence-head can have (from max_past_len + N), the persistent grid
+ * (one CTA per resident slot; each CTA streams an equal share of all tiles)
+ * and block, dynamic shared memory, kernels launched per call (2 when a
+ * sequence-head can span CTAs and the merge pass runs, else 1) and the
+ * workspace size.  Returns the same argument errors as kvd_decode_attention.
+ */
+typedef struct kvd_plan_info {
+    int tile_keys;
+    int max_tiles;
+    int grid;
+    int threads;
+    int smem_bytes;
+    int launches;
+    size_t workspace_bytes;
+} kvd_plan_info;
+
+kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len,
+                           kvd_dtype dtype, kvd_plan_info *info);
+
+/* kvd_workspace_init -- zero-fill a workspace on `stream` (asynchronous); optional,
+ * kvd_decode_attention needs no particular initial contents. */
 kvd_status kvd_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /*

@@ -62,10 +62,13 @@ int g_sm_count[kMaxDevices];
 struct OccEntry {
     int device;
     const void *fn;
+    int smem;
     int ctas_per_sm;
 };
 OccEntry g_occ[256];
 int g_occ_n = 0;
+
+constexpr int kMaxSmemPerCta = 227 * 1024;
 
 kvd_status current_device(int *dev)
 {
@@ -86,25 +89,28 @@ kvd_status sm_count(int dev, int *n)
     return KVD_OK;
 }
 
-// Opt the kernel into its dynamic shared memory and return its occupancy.
-kvd_status prepare_kernel(int dev, const AttnVariant &v, int *ctas_per_sm)
+// Resident CTAs per SM of `fn` with `smem` bytes of dynamic shared memory
+// (the kernel is opted into the full 227 KB the first time it is seen).
+kvd_status occupancy(int dev, const void *fn, int threads, int smem, int *ctas_per_sm)
 {
     std::lock_guard<std::mutex> lk(g_mu);
+    bool opted = false;
     for (int k = 0; k < g_occ_n; ++k) {
-        if (g_occ[k].device == dev && g_occ[k].fn == v.split_fn) {
-            *ctas_per_sm = g_occ[k].ctas_per_sm;
-            return KVD_OK;
+        if (g_occ[k].device == dev && g_occ[k].fn == fn) {
+            opted = true;
+            if (g_occ[k].smem == smem) {
+                *ctas_per_sm = g_occ[k].ctas_per_sm;
+                return KVD_OK;
+            }
         }
     }
-    if (cudaFuncSetAttribute(v.split_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem_bytes) !=
-        cudaSuccess)
+    if (!opted && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMaxSmemPerCta) != cudaSuccess)
         return KVD_ERR_CUDA;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.split_fn, v.threads, v.smem_bytes) !=
-            cudaSuccess ||
-        occ <= 0)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, smem) != cudaSuccess || occ <= 0)
         return KVD_ERR_CUDA;
-    if (g_occ_n < 256) g_occ[g_occ_n++] = OccEntry{dev, v.split_fn, occ};
+    if (g_occ_n < 256) g_occ[g_occ_n++] = OccEntry{dev, fn, smem, occ};
     *ctas_per_sm = occ;
     return KVD_OK;
 }
@@ -118,10 +124,9 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // The split-T plan of one decode_attention call.
 struct Plan {
     AttnVariant v;
-    int rows, rb, n_rowblocks, rows_pad;
-    int split_keys, n_splits;
-    long long grid;
-    size_t part_o_off, part_ml_off, ws_bytes;
+    int rows, rb, n_rowblocks;
+    int grid, smem, launches, max_tiles;
+    size_t part_o_off, part_ml_off, seg_off, ws_bytes;
 };
 
 kvd_status check_shapes(int B, int H_q, int H_kv, int D, int N, int max_past_len, kvd_dtype dtype)
@@ -142,39 +147,37 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     pl->rows = (H_q / H_kv) * N;
     pl->rb = pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : pl->rows <= 4 ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
-    pl->rows_pad = pl->n_rowblocks * pl->rb;
     const bool ok = dtype == KVD_F32 ? attn_variant_f32(D, pl->rb, &pl->v)
                                      : attn_variant_bf16(D, pl->rb, &pl->v);
     if (!ok) return KVD_ERR_UNSUPPORTED;
 
+    // Shared memory holds the ring plus two per-sequence tables (B + 1 tile
+    // prefix sums, B history lengths).
+    const size_t smem = (size_t)pl->v.fixed_smem_bytes + (((size_t)2 * B + 1) * 4 + 15) / 16 * 16;
+    if (smem > (size_t)kMaxSmemPerCta) return KVD_ERR_UNSUPPORTED;
+    pl->smem = (int)smem;
+
     int dev = 0, sms = 0, occ = 0;
     if ((st = current_device(&dev)) != KVD_OK) return st;
     if ((st = sm_count(dev, &sms)) != KVD_OK) return st;
-    if ((st = prepare_kernel(dev, pl->v, &occ)) != KVD_OK) return st;
+    if ((st = occupancy(dev, pl->v.fn, pl->v.threads, pl->smem, &occ)) != KVD_OK) return st;
 
-    // Split T so that the non-empty CTAs fill every SM about twice over; a
-    // split is never shorter than two tiles.
-    const long long tk = pl->v.tile_keys;
+    // One CTA per resident slot; each takes an equal share of all tiles.  A
+    // sequence-head longer than one tile may span CTAs, so the merge runs.
+    pl->grid = sms * occ;
     const long long t_hint = (long long)max_past_len + N;
-    const long long pairs = (long long)B * H_kv * pl->n_rowblocks;
-    const long long target = 2LL * sms * occ;
-    long long sk = pairs > 0 ? (t_hint * pairs + target - 1) / target : t_hint;
-    sk = (sk + tk - 1) / tk * tk;
-    if (sk < 2 * tk) sk = 2 * tk;
-    const long long t_cover = (t_hint + tk - 1) / tk * tk;
-    if (sk > t_cover) sk = t_cover;
-    pl->split_keys = (int)sk;
-    pl->n_splits = (int)((t_hint + sk - 1) / sk);
-    pl->grid = pairs * pl->n_splits;
+    pl->max_tiles = (int)((t_hint + pl->v.tile_keys - 1) / pl->v.tile_keys);
+    pl->launches = pl->max_tiles > 1 ? 2 : 1;
 
-    if (pl->n_splits == 1) {
-        pl->part_o_off = pl->part_ml_off = pl->ws_bytes = 0;
-    } else {
-        const size_t parts = (size_t)B * H_kv * pl->n_splits * pl->rows_pad;
-        pl->part_o_off = 0;
-        pl->part_ml_off = round_up(parts * D * sizeof(float), 256);
-        pl->ws_bytes = pl->part_ml_off + round_up(parts * 2 * sizeof(float), 256);
-    }
+    const size_t pieces = (size_t)pl->grid * 2 * pl->rb;
+    size_t off = 0;
+    pl->part_o_off = off;
+    off += round_up(pieces * D * sizeof(float), 256);
+    pl->part_ml_off = off;
+    off += round_up(pieces * 2 * sizeof(float), 256);
+    pl->seg_off = off;
+    off += round_up((size_t)B * H_kv * pl->n_rowblocks * 2 * sizeof(int), 256);
+    pl->ws_bytes = off;
     return KVD_OK;
 }
 
@@ -236,6 +239,23 @@ size_t kvd_decode_workspace_bytes(int B, int H_q, int H_kv, int D, int N, int ma
     return pl.ws_bytes;
 }
 
+kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len,
+                           kvd_dtype dtype, kvd_plan_info *info)
+{
+    if (info == nullptr) return KVD_ERR_INVALID_ARG;
+    Plan pl;
+    const kvd_status st = make_plan(B, H_q, H_kv, D, N, max_past_len, dtype, &pl);
+    if (st != KVD_OK) return st;
+    info->tile_keys = pl.v.tile_keys;
+    info->max_tiles = pl.max_tiles;
+    info->grid = pl.grid;
+    info->threads = pl.v.threads;
+    info->smem_bytes = pl.smem;
+    info->launches = pl.launches;
+    info->workspace_bytes = pl.ws_bytes;
+    return KVD_OK;
+}
+
 kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *v_cache,
                                 void *out, const int32_t *past_len, int B, int H_q, int H_kv,
                                 int T_max, int D, int N, int max_past_len, float scale,
@@ -253,23 +273,20 @@ kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *
 
     Plan pl;
     if ((st = make_plan(B, H_q, H_kv, D, N, max_past_len, dtype, &pl)) != KVD_OK) return st;
-    if (pl.ws_bytes > 0) {
-        if (workspace == nullptr || workspace_bytes < pl.ws_bytes ||
-            (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-            return KVD_ERR_WORKSPACE;
-    }
+    if (workspace == nullptr || workspace_bytes < pl.ws_bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KVD_ERR_WORKSPACE;
 
+    char *ws = static_cast<char *>(workspace);
     AttnArgs a;
     a.q = q;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.out = out;
     a.past_len = past_len;
-    a.part_o = pl.ws_bytes ? reinterpret_cast<float *>(static_cast<char *>(workspace) + pl.part_o_off)
-                           : nullptr;
-    a.part_ml = pl.ws_bytes
-                    ? reinterpret_cast<float *>(static_cast<char *>(workspace) + pl.part_ml_off)
-                    : nullptr;
+    a.part_o = reinterpret_cast<float *>(ws + pl.part_o_off);
+    a.part_ml = reinterpret_cast<float *>(ws + pl.part_ml_off);
+    a.seg = reinterpret_cast<int2 *>(ws + pl.seg_off);
     a.err_word = err_word;
     a.B = B;
     a.H_kv = H_kv;
@@ -277,24 +294,32 @@ kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *
     a.N = N;
     a.max_past_len = max_past_len;
     a.rows = pl.rows;
-    a.rows_pad = pl.rows_pad;
     a.n_rowblocks = pl.n_rowblocks;
-    a.n_splits = pl.n_splits;
-    a.split_keys = pl.split_keys;
     const float sc = (scale > 0.f) ? scale : 1.0f / sqrtf((float)D);
     a.qscale = sc * kLog2e;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Both kernels are programmatic dependents of whatever precedes them on
+    // the stream: they start early and wait (griddepcontrol.wait) before
+    // touching any input, which hides their launch latency.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     void *args[] = {&a};
-    if (cudaLaunchKernel(pl.v.split_fn, dim3((unsigned)pl.grid), dim3(pl.v.threads), args,
-                         (size_t)pl.v.smem_bytes, s) != cudaSuccess)
-        return KVD_ERR_CUDA;
-    if (pl.n_splits > 1) {
-        const long long warps = (long long)B * H_kv * pl.rows;
-        const long long blocks = (warps * 32 + 127) / 128;
-        if (cudaLaunchKernel(pl.v.merge_fn, dim3((unsigned)blocks), dim3(128), args, 0, s) !=
-            cudaSuccess)
-            return KVD_ERR_CUDA;
+
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(pl.v.threads);
+    cfg.dynamicSmemBytes = (size_t)pl.smem;
+    if (cudaLaunchKernelExC(&cfg, pl.v.fn, args) != cudaSuccess) return KVD_ERR_CUDA;
+    if (pl.launches == 2) {
+        const long long warps = (long long)B * H_kv * pl.n_rowblocks * pl.rb;
+        cfg.gridDim = dim3((unsigned)((warps * 32 + 127) / 128));
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        if (cudaLaunchKernelExC(&cfg, pl.v.merge_fn, args) != cudaSuccess) return KVD_ERR_CUDA;
     }
     return KVD_OK;
 }

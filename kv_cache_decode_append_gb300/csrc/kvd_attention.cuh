@@ -8,29 +8,42 @@
 // once per group: same page, section "GPT-2缓存要占多少显存").
 //
 // Decode is bound by reading K/V from HBM ("7.1", the bullets under code 1-2),
-// so the kernel is a streaming reduction on the CUDA cores, not a GEMM:
+// so the kernel is a streaming reduction on the CUDA cores, not a GEMM.
 //
-//   * one CTA = one (sequence b, KV head h, block of RB query rows, T-split);
-//   * one elected thread streams [TK, D] K and V tiles of the split, which are
-//     contiguous in the [B, H_kv, T_max, D] cache, through a STAGES-deep ring
-//     of shared-memory buffers with 1-D bulk (TMA) copies completing on
-//     mbarriers, L2 evict-first;
-//   * each warp splits into key groups of L lanes; a group owns whole keys,
-//     each lane owns E = D / L head-dim elements of q (in registers,
-//     pre-scaled by scale*log2 e) and of the output accumulators for all RB
-//     rows; a dot product is E FMAs per lane plus a log2(L)-step xor-shuffle
-//     reduction inside the group;
-//   * every group keeps its own online softmax (running max m, sum l, output
-//     o) in registers; the running max is only moved when a tile's max
+// Work decomposition (flash-decoding split over T, balanced statically):
+//   * a "sequence-head" u is one (sequence b, KV head h, block of RB query
+//     rows); its query rows are g*N rows (g query heads of the group x N new
+//     tokens), contiguous in q and out; its keys 0..P_b+N-1 form
+//     ceil((P_b+N)/TK) tiles of TK keys;
+//   * every CTA reads past_len, forms the prefix sum of tiles over all
+//     sequence-heads, and takes an equal contiguous range of that flattened
+//     tile list (the grid is SMs x resident CTAs; with fewer tiles than CTAs
+//     only the first n_tiles CTAs work): every CTA streams the same number
+//     of tiles whatever the mix of sequence lengths, with no atomics and a
+//     split that depends only on the inputs;
+//   * thread 0 walks the range and streams each tile's [TK, D] K and V rows
+//     (contiguous in the [B, H_kv, T_max, D] cache), plus the q rows at the
+//     start of each sequence-head, into a STAGES-deep shared-memory ring with
+//     1-D bulk (TMA) copies completing on mbarriers (L2 evict-first); it
+//     refills a slot right after the one CTA barrier of each tile;
+//   * the warps split into key groups of L lanes; a group owns whole keys,
+//     each lane owns E = D / L head-dim elements of q (registers, pre-scaled
+//     by scale*log2 e) and of the output accumulators for all RB rows; a dot
+//     product is E FMAs per lane plus a log2(L)-step xor-shuffle reduction
+//     inside the group; every group keeps its own online softmax (running
+//     max m, sum l, output o); the running max only moves when a tile's max
 //     exceeds it by more than 2^8, which keeps exp2 arguments <= 8 and makes
-//     the rescale of o rare; o/l is unchanged by that choice;
-//   * at the end the CTA merges its groups through shared memory by
-//     log-sum-exp and writes either the final output (the sequence fits one
-//     split) or a partial (o, m, l) for attn_merge_kernel.
+//     the rescale of o rare (o/l is unchanged by that choice);
+//   * where the range leaves a sequence-head the warps merge their groups by
+//     log-sum-exp (shuffles) and, after the tile barrier, across warps
+//     (shared memory): the output is written directly when the sequence-head
+//     lies inside one CTA's range, else the piece goes to a partial slot
+//     (a CTA holds at most two: the head it continues and the head it
+//     starts) and attn_merge_kernel combines the pieces.
 //
-// Masked slots (past P+i for row i, or past the split) never feed the
-// arithmetic: their scores are forced to -inf and value rows past the end of
-// the sequence are replaced by zeros before the weighted sum.
+// Masked slots (past P+i for row i, or past the end of the sequence) never
+// feed the arithmetic: their scores are forced to -inf and value rows past
+// the end of the sequence are replaced by zeros before the weighted sum.
 #pragma once
 
 #include "kvd_device.cuh"
@@ -43,21 +56,20 @@ struct AttnArgs {
     const void *v_cache;     // [B, H_kv, T_max, D]
     void *out;               // [B, H_q, N, D]
     const int32_t *past_len; // [B]
-    float *part_o;           // [B*H_kv][n_splits][rows_pad][D]   (unnormalised)
-    float *part_ml;          // [B*H_kv][n_splits][rows_pad][2]   (max in log2 units, sum)
+    float *part_o;           // [grid][2][RB][D]  piece partials (unnormalised)
+    float *part_ml;          // [grid][2][RB][2]  (max in log2 units, sum)
+    int2 *seg;               // [B*H_kv*n_rowblocks]: (first CTA, CTAs) of each sequence-head
     uint32_t *err_word;
     int B, H_kv, T_max, N, max_past_len;
-    int rows;        // query rows per (b, h): (H_q / H_kv) * N, contiguous in q and out
-    int rows_pad;    // n_rowblocks * RB
-    int n_rowblocks;
-    int n_splits;    // T-splits per (b, h, row block)
-    int split_keys;  // keys per split, a multiple of the tile
-    float qscale;    // softmax scale * log2(e)
+    int rows;         // query rows per (b, h): (H_q / H_kv) * N, contiguous in q and out
+    int n_rowblocks;  // ceil(rows / RB)
+    float qscale;     // softmax scale * log2(e)
 };
 
 // Compile-time shape of one kernel variant.
 template <typename T, int D, int RB> struct AttnShape {
     using Ty = Elem<T>;
+    static constexpr int kRB = RB;
     static constexpr int kRowBytes = D * Ty::kBytes;
     static constexpr int kRowChunks = kRowBytes / 16;
     // Lanes per key: 8 keeps each 8-lane shared-memory phase on one 128-byte
@@ -73,18 +85,39 @@ template <typename T, int D, int RB> struct AttnShape {
     static constexpr int kKpw = kGpw * kKpg;           // keys per warp per tile
     static constexpr int kTileBytes = kTK * kRowBytes; // one of K or V
     static constexpr int kStages = (2 * kTileBytes <= 16384) ? 4 : 3;
-    static constexpr int kPipeBytes = kStages * 2 * kTileBytes;
-    static constexpr int kParts = kNW * kGpw;          // partial softmax states per CTA
-    static constexpr int kEpiFloats = kParts * RB * (D + 3) + RB;
-    static constexpr int kEpiBytes = kEpiFloats * 4;
-    static constexpr int kBarOffset = ((kPipeBytes > kEpiBytes ? kPipeBytes : kEpiBytes) + 127) / 128 * 128;
-    static constexpr int kSmemBytes = kBarOffset + kStages * 8;
+    static constexpr int kQSlotBytes = RB * kRowBytes;
+
+    // shared memory layout (bytes); the per-sequence tables follow kFixedBytes
+    static constexpr int kRingOff = 0;
+    static constexpr int kQOff = kRingOff + kStages * 2 * kTileBytes;
+    static constexpr int kEpiOff = kQOff + kStages * kQSlotBytes;
+    static constexpr int kEpiFloats = ((kNW * RB * (D + 2) + 3) / 4) * 4;  // o, m, l per warp
+    static constexpr int kEpiBytes = (kEpiFloats > kThreads ? kEpiFloats : kThreads) * 4;
+    static constexpr int kMetaOff = kEpiOff + kEpiBytes;
+    static constexpr int kBarOff = kMetaOff + kStages * 32;
+    static constexpr int kFixedBytes = kBarOff + kStages * 8;
 
     static_assert(kRowBytes % 16 == 0, "rows must be whole 16-byte chunks");
     static_assert(kCpl >= 1 && kRowChunks % kL == 0, "lane mapping");
     static_assert(kNW >= 1 && kTK % kKpw == 0, "tile mapping");
-    static_assert(kParts * RB <= kThreads, "epilogue mapping");
+    static_assert(kQOff % 128 == 0 && kEpiOff % 16 == 0 && kBarOff % 8 == 0, "alignment");
 };
+
+// Shared-memory bytes of a launch with B sequences: fixed part + tile prefix
+// sums (B + 1 ints) + history lengths (B ints).
+template <typename S> constexpr size_t attn_smem_bytes(int B)
+{
+    return (size_t)S::kFixedBytes + (((size_t)(2 * B + 1) * 4 + 15) / 16) * 16;
+}
+
+// Per-stage description written by thread 0, read by every thread.
+struct TileMeta {
+    int bh, rb, tile_k0, nk;      // pair, row block, global key index of tile row 0, rows loaded
+    int P, flags, n_chunks, slot; // history, kMeta*, CTAs sharing the head, partial slot
+};
+constexpr int kMetaFirst = 1;  // first tile of a piece: the stage also carries the q rows
+constexpr int kMetaLast = 2;   // last tile of a piece
+constexpr int kMetaEnd = 4;    // no more work
 
 template <typename T, int D, int RB, bool kMasked>
 __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigned char *Vs,
@@ -173,7 +206,7 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
 #pragma unroll
         for (int c = 0; c < S::kCpl; ++c) Ty::widen(raw[u][c], vf + c * Ty::kPerChunk);
         if constexpr (kMasked) {
-            // Rows past the end of the split were not loaded: stale shared memory.
+            // Rows past the end of the chunk were not loaded: stale shared memory.
             if (tile_k0 + warp * S::kKpw + u * S::kGpw + grp >= k_end) {
 #pragma unroll
                 for (int e = 0; e < S::kE; ++e) vf[e] = 0.f;
@@ -186,226 +219,369 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
     }
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ float safe_weight(float m, float M)
+{
+    return (m == __int_as_float(0xff800000)) ? 0.f : exp2f(m - M);
+}
+
+// CTA whose range [c*n/G, (c+1)*n/G) holds flattened tile t.  With G <= n
+// every range is non-empty, so the CTAs holding a head's tiles are consecutive.
+__device__ __forceinline__ int owner_cta(long long t, long long n, long long G)
+{
+    return (int)(((t + 1) * G + n - 1) / n) - 1;
+}
+
+// Thread 0's walk over the CTA's tile range.
+template <typename S> struct RangeWalk {
+    long long t, hi, n, G;  // next tile, end of range, tiles in total, working CTAs
+    int b, hr, tin, tb;  // sequence, head x row block, tile within the head, its tiles
+    int HR;              // H_kv * n_rowblocks
+    bool ended;
+    bool piece_start;    // the next tile starts a piece (the head's first tile, or the range's)
+    uint64_t policy;
+
+    __device__ __forceinline__ void start(const AttnArgs &a, const int *pre, long long lo, long long hi_,
+                                          long long n_, long long G_)
+    {
+        policy = l2_evict_first_policy();
+        HR = a.H_kv * a.n_rowblocks;
+        t = lo;
+        hi = hi_;
+        n = n_;
+        G = G_;
+        ended = false;
+        piece_start = true;
+        if (t >= hi) return;
+        int lo_b = 0, hi_b = a.B - 1;  // last b with pre[b] * HR <= t
+        while (lo_b < hi_b) {
+            const int mid = (lo_b + hi_b + 1) / 2;
+            if ((long long)pre[mid] * HR <= t) lo_b = mid; else hi_b = mid - 1;
+        }
+        b = lo_b;
+        tb = pre[b + 1] - pre[b];
+        const long long local = t - (long long)pre[b] * HR;
+        hr = (int)(local / tb);
+        tin = (int)(local % tb);
+    }
+
+    __device__ __forceinline__ void fill(const AttnArgs &a, const int *pre, const int *pl,
+                                         unsigned char *smem, TileMeta *meta, uint64_t *full, int s)
+    {
+        if (ended) return;
+        if (t >= hi) {
+            meta[s].flags = kMetaEnd;
+            mbar_arrive(&full[s]);
+            ended = true;
+            return;
+        }
+        const int h = hr / a.n_rowblocks, rb = hr % a.n_rowblocks;
+        const int bh = b * a.H_kv + h;
+        const int P = pl[b];
+        const long long ts = t - tin;  // first tile of this sequence-head
+        const int c_first = owner_cta(ts, n, G);
+        const int n_chunks = owner_cta(ts + tb - 1, n, G) - c_first + 1;
+        TileMeta mt;
+        mt.bh = bh;
+        mt.rb = rb;
+        mt.tile_k0 = tin * S::kTK;
+        mt.nk = min(S::kTK, P + a.N - mt.tile_k0);
+        mt.P = P;
+        mt.flags = (piece_start ? kMetaFirst : 0) | ((tin == tb - 1 || t == hi - 1) ? kMetaLast : 0);
+        mt.n_chunks = n_chunks;
+        mt.slot = ((int)blockIdx.x == c_first) ? 1 : 0;
+        meta[s] = mt;
+        if (tin == 0) a.seg[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
+
+        const size_t row = (size_t)bh * a.T_max + mt.tile_k0;
+        const uint32_t bytes = (uint32_t)mt.nk * S::kRowBytes;
+        const int q_rows = min(S::kRB, a.rows - rb * S::kRB);
+        const uint32_t qbytes = piece_start ? (uint32_t)q_rows * S::kRowBytes : 0u;
+        unsigned char *dst = smem + S::kRingOff + s * 2 * S::kTileBytes;
+        mbar_arrive_expect_tx(&full[s], 2u * bytes + qbytes);
+        bulk_load_g2s(dst, static_cast<const unsigned char *>(a.k_cache) + row * S::kRowBytes, bytes,
+                      &full[s], policy);
+        bulk_load_g2s(dst + S::kTileBytes, static_cast<const unsigned char *>(a.v_cache) + row * S::kRowBytes,
+                      bytes, &full[s], policy);
+        if (qbytes) {
+            const unsigned char *qg = static_cast<const unsigned char *>(a.q) +
+                                      ((size_t)bh * a.rows + rb * S::kRB) * S::kRowBytes;
+            bulk_load_g2s(smem + S::kQOff + s * S::kQSlotBytes, qg, qbytes, &full[s], policy);
+        }
+
+        // advance to the next tile of the flattened list
+        ++t;
+        piece_start = false;
+        if (++tin == tb) {
+            tin = 0;
+            piece_start = true;
+            if (++hr == HR) {
+                hr = 0;
+                do {
+                    ++b;
+                } while (b < a.B && pre[b + 1] == pre[b]);
+                if (b < a.B) tb = pre[b + 1] - pre[b];
+            }
+        }
+    }
+};
+
 template <typename T, int D, int RB>
 __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
-    attn_split_kernel(const AttnArgs a)
+    attn_balanced_kernel(const AttnArgs a)
 {
     using S = AttnShape<T, D, RB>;
     using Ty = Elem<T>;
     const float kNegInf = __int_as_float(0xff800000);
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBarOffset);
-
-    const int split = blockIdx.x % a.n_splits;
-    const int rest = blockIdx.x / a.n_splits;
-    const int rb = rest % a.n_rowblocks;
-    const int bh = rest / a.n_rowblocks;
-    const int b = bh / a.H_kv;
-
-    const int P = __ldg(a.past_len + b);
-    if (!past_len_ok(P, a.N, a.T_max, a.max_past_len)) {
-        if (split == 0 && rb == 0 && bh % a.H_kv == 0 && threadIdx.x == 0)
-            raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
-        return;
-    }
-    const int T_b = P + a.N;
-    const int k0 = split * a.split_keys;
-    if (k0 >= T_b) return;  // this split lies past the end of a shorter sequence
-    const int k1 = min(T_b, k0 + a.split_keys);
-    const int n_valid_splits = (T_b + a.split_keys - 1) / a.split_keys;
-    const int n_tiles = (k1 - k0 + S::kTK - 1) / S::kTK;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBarOff);
+    TileMeta *meta = reinterpret_cast<TileMeta *>(smem + S::kMetaOff);
+    int *pre = reinterpret_cast<int *>(smem + S::kFixedBytes);  // [B + 1] tile prefix per head
+    int *pl = pre + a.B + 1;                                     // [B] history lengths
 
     const int tid = threadIdx.x;
     const int warp = tid / 32, lane = tid % 32;
     const int grp = lane / S::kL, j = lane % S::kL;
 
-    const size_t row0 = (size_t)bh * a.T_max + k0;
-    const unsigned char *kg = static_cast<const unsigned char *>(a.k_cache) + row0 * S::kRowBytes;
-    const unsigned char *vg = static_cast<const unsigned char *>(a.v_cache) + row0 * S::kRowBytes;
-
-    uint64_t policy = 0;
-    auto issue = [&](int t) {
-        const int s = t % S::kStages;
-        const int nk = min(S::kTK, k1 - k0 - t * S::kTK);
-        const uint32_t bytes = (uint32_t)nk * S::kRowBytes;
-        unsigned char *dst = smem + s * 2 * S::kTileBytes;
-        mbar_arrive_expect_tx(&bars[s], 2u * bytes);
-        bulk_load_g2s(dst, kg + (size_t)t * S::kTileBytes, bytes, &bars[s], policy);
-        bulk_load_g2s(dst + S::kTileBytes, vg + (size_t)t * S::kTileBytes, bytes, &bars[s], policy);
-    };
-
     if (tid == 0) {
 #pragma unroll
-        for (int s = 0; s < S::kStages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < S::kStages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
-        policy = l2_evict_first_policy();
-        for (int t = 0; t < min(n_tiles, S::kStages); ++t) issue(t);
     }
-    int issued = min(n_tiles, S::kStages);  // meaningful in thread 0 only
+    // Every input may come from the previous kernel on the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // q rows of this block, pre-scaled into log2 units; padding rows are 0.
-    float qv[RB][S::kE];
-    int lim[RB];
-#pragma unroll
-    for (int r = 0; r < RB; ++r) {
-        const int rg = rb * RB + r;
-        lim[r] = P + 1 + (rg % a.N);
-        if (rg < a.rows) {
-            const unsigned char *qrow =
-                static_cast<const unsigned char *>(a.q) + ((size_t)bh * a.rows + rg) * S::kRowBytes;
-#pragma unroll
-            for (int c = 0; c < S::kCpl; ++c) {
-                Ty::widen(ldg128_nc(qrow + (c * S::kL + j) * 16), &qv[r][c * Ty::kPerChunk]);
+    // ---- tiles per sequence and their prefix sum (block-wide scan) ----
+    {
+        int *scan = reinterpret_cast<int *>(smem + S::kEpiOff);
+        const int per = (a.B + S::kThreads - 1) / S::kThreads;
+        const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
+        int local = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int P = __ldg(a.past_len + b);
+            const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
+            if (!ok && blockIdx.x == 0) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
+            const int tiles = ok ? (P + a.N + S::kTK - 1) / S::kTK : 0;
+            pl[b] = P;
+            pre[b + 1] = tiles;
+            local += tiles;
+        }
+        scan[tid] = local;
+        __syncthreads();
+        if (tid == 0) {
+            int run = 0;
+            for (int i = 0; i < S::kThreads; ++i) {
+                const int v = scan[i];
+                scan[i] = run;
+                run += v;
             }
-#pragma unroll
-            for (int e = 0; e < S::kE; ++e) qv[r][e] *= a.qscale;
-        } else {
-#pragma unroll
-            for (int e = 0; e < S::kE; ++e) qv[r][e] = 0.f;
+            pre[0] = 0;
         }
-    }
-
-    float o[RB][S::kE];
-    float m_run[RB], l_run[RB];
-#pragma unroll
-    for (int r = 0; r < RB; ++r) {
-        m_run[r] = kNegInf;
-        l_run[r] = 0.f;
-#pragma unroll
-        for (int e = 0; e < S::kE; ++e) o[r][e] = 0.f;
-    }
-
-    __syncthreads();  // barrier initialisation visible to every thread
-
-    bool timed_out = false;
-    int first_unwaited = n_tiles;  // first tile whose wait this thread gave up on
-    for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % S::kStages;
-        const uint32_t parity = (uint32_t)(t / S::kStages) & 1u;
-        if (!timed_out && !mbar_wait_bounded(&bars[s], parity)) {
-            timed_out = true;
-            first_unwaited = t;
-        }
-        const unsigned char *Ks = smem + s * 2 * S::kTileBytes;
-        const unsigned char *Vs = Ks + S::kTileBytes;
-        const int tile_k0 = k0 + t * S::kTK;
-        if (tile_k0 + S::kTK <= P + 1) {
-            attn_tile<T, D, RB, false>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, tile_k0, lim, k1);
-        } else {
-            attn_tile<T, D, RB, true>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, tile_k0, lim, k1);
-        }
-        __syncthreads();  // every warp is done with stage s
-        if (tid == 0 && !timed_out && t + S::kStages < n_tiles) {
-            issue(t + S::kStages);
-            issued = t + S::kStages + 1;
-        }
-    }
-    if (__syncthreads_or(timed_out)) {  // uniform: every thread takes this branch or none
-        if (timed_out) raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
-        // Copies still in flight must land before the CTA reuses or releases
-        // its shared memory: wait for them under one overall deadline.  Only
-        // thread 0 can have copies outstanding that it did not see complete.
-        if (tid == 0 && timed_out) {
-            const uint64_t t0 = global_timer_ns();
-            for (int t = first_unwaited; t < issued; ++t) {
-                const uint32_t parity = (uint32_t)(t / S::kStages) & 1u;
-                while (!mbar_try_wait(&bars[t % S::kStages], parity) &&
-                       global_timer_ns() - t0 < kWaitLimitNs) {
-                }
-            }
+        __syncthreads();
+        int run = scan[tid];
+        for (int b = b0; b < b1; ++b) {
+            run += pre[b + 1];
+            pre[b + 1] = run;
         }
         __syncthreads();
     }
+    const int HR = a.H_kv * a.n_rowblocks;
+    const long long n_total = (long long)pre[a.B] * HR;
+    const long long G = min((long long)gridDim.x, n_total);  // CTAs that get work
+    const long long lo = blockIdx.x < G ? n_total * blockIdx.x / G : 0;
+    const long long hi = blockIdx.x < G ? n_total * (blockIdx.x + 1) / G : 0;
 
-    // ---- merge the CTA's key groups (shared memory aliases the ring) ----
-    // ep_o first: every (part, row) slice starts on a 16-byte boundary.
-    float *ep_o = reinterpret_cast<float *>(smem);
-    float *ep_m = ep_o + S::kParts * RB * D;
-    float *ep_l = ep_m + S::kParts * RB;
-    float *ep_w = ep_l + S::kParts * RB;
-    float *ep_M = ep_w + S::kParts * RB;
-    const int part = warp * S::kGpw + grp;
-    if (j == 0) {
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            ep_m[part * RB + r] = m_run[r];
-            ep_l[part * RB + r] = l_run[r];
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < RB; ++r) {
-        float *dst = ep_o + (part * RB + r) * D;
-#pragma unroll
-        for (int c = 0; c < S::kCpl; ++c) {
-            const int d0 = (c * S::kL + j) * Ty::kPerChunk;
-#pragma unroll
-            for (int e = 0; e < Ty::kPerChunk; e += 4)
-                *reinterpret_cast<float4 *>(dst + d0 + e) =
-                    make_float4(o[r][c * Ty::kPerChunk + e], o[r][c * Ty::kPerChunk + e + 1],
-                                o[r][c * Ty::kPerChunk + e + 2], o[r][c * Ty::kPerChunk + e + 3]);
-        }
-    }
-    __syncthreads();
-    if (tid < S::kParts * RB) {
-        const int r = tid % RB;
-        float M = kNegInf;
-#pragma unroll
-        for (int pp = 0; pp < S::kParts; ++pp) M = fmaxf(M, ep_m[pp * RB + r]);
-        const float mp = ep_m[tid];
-        ep_w[tid] = (mp == kNegInf) ? 0.f : exp2f(mp - M);
-        if (tid < RB) ep_M[r] = M;
+    RangeWalk<S> walk;  // used by thread 0 only
+    if (tid == 0) {
+        walk.start(a, pre, lo, hi, n_total, G);
+        for (int s = 0; s < S::kStages; ++s) walk.fill(a, pre, pl, smem, meta, full, s);
     }
     __syncthreads();
 
-    const bool single = (n_valid_splits == 1);
-    for (int idx = tid; idx < RB * D; idx += S::kThreads) {
-        const int r = idx / D, d = idx % D;
-        const int rg = rb * RB + r;
-        if (rg >= a.rows) continue;
-        float num = 0.f, den = 0.f;
-#pragma unroll
-        for (int pp = 0; pp < S::kParts; ++pp) {
-            const float w = ep_w[pp * RB + r];
-            num = fmaf(w, ep_o[(pp * RB + r) * D + d], num);
-            den = fmaf(w, ep_l[pp * RB + r], den);
+    float qv[RB][S::kE];
+    float o[RB][S::kE];
+    float m_run[RB], l_run[RB];
+    int lim[RB];
+    bool prev_last = false;  // the previous tile ended a piece (uniform across the CTA)
+    bool timed_out = false;
+    int first_unwaited = -1;  // first ring position this thread gave up waiting for
+
+    for (int pos = 0; lo < hi; ++pos) {
+        const int s = pos % S::kStages;
+        const uint32_t ph = (uint32_t)(pos / S::kStages) & 1u;
+        if (!timed_out && !mbar_wait_bounded(&full[s], ph)) {
+            // Keep the same control flow as every other thread (the metadata is
+            // valid even if the data never landed); the result is flagged.
+            timed_out = true;
+            first_unwaited = pos;
+            raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
         }
-        if (single) {
-            T *out = static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + d;
-            Ty::store(out, num / den);
+        const TileMeta mt = meta[s];
+        if (mt.flags & kMetaEnd) break;
+        const unsigned char *Ks = smem + S::kRingOff + s * 2 * S::kTileBytes;
+        const unsigned char *Vs = Ks + S::kTileBytes;
+
+        if (mt.flags & kMetaFirst) {
+            const unsigned char *qs = smem + S::kQOff + s * S::kQSlotBytes;
+            const int q_rows = min(RB, a.rows - mt.rb * RB);
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const int rg = mt.rb * RB + r;
+                lim[r] = mt.P + 1 + (rg % a.N);
+                m_run[r] = kNegInf;
+                l_run[r] = 0.f;
+#pragma unroll
+                for (int e = 0; e < S::kE; ++e) o[r][e] = 0.f;
+                if (r < q_rows) {
+#pragma unroll
+                    for (int c = 0; c < S::kCpl; ++c)
+                        Ty::widen(lds128(qs + r * S::kRowBytes + (c * S::kL + j) * 16),
+                                  &qv[r][c * Ty::kPerChunk]);
+#pragma unroll
+                    for (int e = 0; e < S::kE; ++e) qv[r][e] *= a.qscale;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < S::kE; ++e) qv[r][e] = 0.f;
+                }
+            }
+        }
+
+        const int k_end = mt.tile_k0 + mt.nk;
+        if (mt.tile_k0 + S::kTK <= mt.P + 1) {
+            attn_tile<T, D, RB, false>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim, k_end);
         } else {
-            const size_t pidx = ((size_t)bh * a.n_splits + split) * a.rows_pad + rg;
-            a.part_o[pidx * D + d] = num;
-            if (d == 0) {
-                a.part_ml[pidx * 2 + 0] = ep_M[r];
-                a.part_ml[pidx * 2 + 1] = den;
+            attn_tile<T, D, RB, true>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim, k_end);
+        }
+
+        const bool last = (mt.flags & kMetaLast) != 0;
+        float *ep_o = reinterpret_cast<float *>(smem + S::kEpiOff);
+        float *ep_m = ep_o + S::kNW * RB * D;
+        float *ep_l = ep_m + S::kNW * RB;
+        if (last) {
+            // Merge the key groups of this warp (xor shuffles), then publish the
+            // warp's state for the cross-warp merge after the tile barrier.  If
+            // the previous tile also ended a piece, its readers may still be in
+            // the shared area: wait for them first.
+#pragma unroll
+            for (int off = S::kL; off < 32; off *= 2) {
+#pragma unroll
+                for (int r = 0; r < RB; ++r) {
+                    const float m_o = __shfl_xor_sync(0xffffffffu, m_run[r], off);
+                    const float l_o = __shfl_xor_sync(0xffffffffu, l_run[r], off);
+                    const float M = fmaxf(m_run[r], m_o);
+                    const float wa = safe_weight(m_run[r], M), wb = safe_weight(m_o, M);
+                    l_run[r] = l_run[r] * wa + l_o * wb;
+#pragma unroll
+                    for (int e = 0; e < S::kE; ++e)
+                        o[r][e] = o[r][e] * wa + __shfl_xor_sync(0xffffffffu, o[r][e], off) * wb;
+                    m_run[r] = M;
+                }
+            }
+            if (prev_last) __syncthreads();
+            if (grp == 0) {
+#pragma unroll
+                for (int r = 0; r < RB; ++r) {
+                    float *dst = ep_o + (warp * RB + r) * D;
+#pragma unroll
+                    for (int c = 0; c < S::kCpl; ++c) {
+                        const int d0 = (c * S::kL + j) * Ty::kPerChunk;
+#pragma unroll
+                        for (int e = 0; e < Ty::kPerChunk; e += 4)
+                            *reinterpret_cast<float4 *>(dst + d0 + e) =
+                                make_float4(o[r][c * Ty::kPerChunk + e], o[r][c * Ty::kPerChunk + e + 1],
+                                            o[r][c * Ty::kPerChunk + e + 2], o[r][c * Ty::kPerChunk + e + 3]);
+                    }
+                    if (j == 0) {
+                        ep_m[warp * RB + r] = m_run[r];
+                        ep_l[warp * RB + r] = l_run[r];
+                    }
+                }
+            }
+        }
+
+        __syncthreads();  // slot s is free; the warps' end-of-piece states are published
+        if (tid == 0) walk.fill(a, pre, pl, smem, meta, full, s);
+
+        if (last) {
+            const bool single = (mt.n_chunks == 1);
+            const size_t pbase = ((size_t)blockIdx.x * 2 + mt.slot) * RB;
+            for (int idx = tid; idx < RB * D; idx += S::kThreads) {
+                const int r = idx / D, d = idx % D;
+                const int rg = mt.rb * RB + r;
+                if (rg >= a.rows) continue;
+                float M = kNegInf;
+#pragma unroll
+                for (int w = 0; w < S::kNW; ++w) M = fmaxf(M, ep_m[w * RB + r]);
+                float num = 0.f, den = 0.f;
+#pragma unroll
+                for (int w = 0; w < S::kNW; ++w) {
+                    const float wt = safe_weight(ep_m[w * RB + r], M);
+                    num = fmaf(wt, ep_o[(w * RB + r) * D + d], num);
+                    den = fmaf(wt, ep_l[w * RB + r], den);
+                }
+                if (single) {
+                    Ty::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
+                } else {
+                    a.part_o[(pbase + r) * D + d] = num;
+                    if (d == 0) {
+                        a.part_ml[(pbase + r) * 2 + 0] = M;
+                        a.part_ml[(pbase + r) * 2 + 1] = den;
+                    }
+                }
+            }
+        }
+        prev_last = last;
+    }
+
+    if (tid == 0 && timed_out) {
+        // Copies that may still be in flight must land before the CTA exits:
+        // wait for every position from the first abandoned one, one deadline.
+        const uint64_t t0 = global_timer_ns();
+        for (int p = first_unwaited; p < first_unwaited + S::kStages; ++p) {
+            const uint32_t ph = (uint32_t)(p / S::kStages) & 1u;
+            while (!mbar_try_wait(&full[p % S::kStages], ph) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
     }
+    // Let the dependent merge launch; its griddepcontrol.wait still waits for
+    // this whole grid to finish and flush.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Second pass: log-sum-exp merge of the T-splits of one query row per warp.
-//   M = max_s m_s;  w_s = 2^(m_s - M);  out = sum_s w_s o_s / sum_s w_s l_s
-template <typename T, int D>
+// Second pass: log-sum-exp merge of the pieces of one query row per warp.
+//   M = max_c m_c;  w_c = 2^(m_c - M);  out = sum_c w_c o_c / sum_c w_c l_c
+template <typename T, int D, int RB>
 __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
 {
     using Ty = Elem<T>;
     const float kNegInf = __int_as_float(0xff800000);
     constexpr int kDpl = D / 32;
-    const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) / 32);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const int lane = threadIdx.x % 32;
-    if (gw >= a.B * a.H_kv * a.rows) return;
-    const int bh = gw / a.rows, rg = gw % a.rows;
-    const int b = bh / a.H_kv;
+    const int HR = a.H_kv * a.n_rowblocks;
+    if (gw >= (long long)a.B * HR * RB) return;
+    const int r = (int)(gw % RB);
+    const int u = (int)(gw / RB);
+    const int b = u / HR, hr = u % HR;
+    const int h = hr / a.n_rowblocks, rb = hr % a.n_rowblocks;
+    const int rg = rb * RB + r;
+    if (rg >= a.rows) return;
     const int P = __ldg(a.past_len + b);
     if (!past_len_ok(P, a.N, a.T_max, a.max_past_len)) return;  // reported by the split pass
-    const int T_b = P + a.N;
-    const int nv = (T_b + a.split_keys - 1) / a.split_keys;
-    if (nv <= 1) return;  // the split pass wrote this row directly
+    const int2 seg = a.seg[u];
+    if (seg.y <= 1) return;  // the split pass wrote this row directly
 
-    const size_t base = (size_t)bh * a.n_splits * a.rows_pad + rg;
-    const size_t stride = a.rows_pad;
     float M = kNegInf;
-    for (int s = lane; s < nv; s += 32) M = fmaxf(M, a.part_ml[(base + s * stride) * 2]);
+    for (int k = lane; k < seg.y; k += 32) {
+        const int c = seg.x + k;
+        M = fmaxf(M, a.part_ml[(((size_t)c * 2 + (k == 0)) * RB + r) * 2]);
+    }
 #pragma unroll
     for (int off = 16; off >= 1; off /= 2) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
@@ -413,10 +589,9 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
 #pragma unroll
     for (int k = 0; k < kDpl; ++k) acc[k] = 0.f;
     float den = 0.f;
-    for (int s = 0; s < nv; ++s) {
-        const size_t pidx = base + s * stride;
-        const float ms = a.part_ml[pidx * 2];
-        const float w = (ms == kNegInf) ? 0.f : exp2f(ms - M);
+    for (int k = 0; k < seg.y; ++k) {
+        const size_t pidx = ((size_t)(seg.x + k) * 2 + (k == 0)) * RB + r;
+        const float w = safe_weight(a.part_ml[pidx * 2], M);
         den = fmaf(w, a.part_ml[pidx * 2 + 1], den);
         const float *po = a.part_o + pidx * D + lane * kDpl;
         if constexpr (kDpl == 4) {
@@ -427,9 +602,10 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
             acc[3] = fmaf(w, v.w, acc[3]);
         } else {
 #pragma unroll
-            for (int k = 0; k < kDpl; ++k) acc[k] = fmaf(w, po[k], acc[k]);
+            for (int k2 = 0; k2 < kDpl; ++k2) acc[k2] = fmaf(w, po[k2], acc[k2]);
         }
     }
+    const int bh = b * a.H_kv + h;
     T *out = static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + lane * kDpl;
 #pragma unroll
     for (int k = 0; k < kDpl; ++k) Ty::store(out + k, acc[k] / den);
@@ -437,10 +613,10 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
 
 // Launch facts of one compiled variant, for the host planner.
 struct AttnVariant {
-    const void *split_fn;
+    const void *fn;
     const void *merge_fn;
     int threads;
-    int smem_bytes;
+    int fixed_smem_bytes;  // plus (2B + 1) ints, rounded to 16 bytes
     int tile_keys;
     int rows_per_block;
 };
@@ -449,10 +625,10 @@ template <typename T, int D, int RB> AttnVariant make_variant()
 {
     using S = AttnShape<T, D, RB>;
     AttnVariant v;
-    v.split_fn = reinterpret_cast<const void *>(&attn_split_kernel<T, D, RB>);
-    v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D>);
+    v.fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB>);
+    v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, RB>);
     v.threads = S::kThreads;
-    v.smem_bytes = S::kSmemBytes;
+    v.fixed_smem_bytes = S::kFixedBytes;
     v.tile_keys = S::kTK;
     v.rows_per_block = RB;
     return v;

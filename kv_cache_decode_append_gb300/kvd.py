@@ -46,6 +46,12 @@ class KvdError(RuntimeError):
         super().__init__(f"{fn} failed: {raw.kvd_status_string(status).decode()} ({status})")
 
 
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("tile_keys", ctypes.c_int), ("max_tiles", ctypes.c_int), ("grid", ctypes.c_int),
+                ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("launches", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
 class _Lib:
     """The loaded ``libkvd.so`` with typed C signatures."""
 
@@ -59,6 +65,8 @@ class _Lib:
         lib.kvd_decode_attention.restype = ci
         lib.kvd_decode_attention.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
                                              vp, sz, u32p, vp]
+        lib.kvd_decode_plan.restype = ci
+        lib.kvd_decode_plan.argtypes = [ci, ci, ci, ci, ci, ci, ci, ctypes.POINTER(PlanInfo)]
         lib.kvd_workspace_init.restype = ci
         lib.kvd_workspace_init.argtypes = [vp, sz, vp]
         lib.kvd_cache_bytes.restype = sz
@@ -159,12 +167,21 @@ def kvd_decode_workspace_bytes(B: int, H_q: int, H_kv: int, D: int, N: int, max_
     return int(raw.kvd_decode_workspace_bytes(B, H_q, H_kv, D, N, int(max_past_len), code))
 
 
+def kvd_decode_plan(B: int, H_q: int, H_kv: int, D: int, N: int, max_past_len: int, dtype) -> dict:
+    """The split-T plan kvd_decode_attention uses for these shapes on the current device."""
+    code = _NAME_DTYPE[dtype] if isinstance(dtype, str) else _TORCH_DTYPE[dtype]
+    info = PlanInfo()
+    _check("kvd_decode_plan", raw.kvd_decode_plan(B, H_q, H_kv, D, N, int(max_past_len), code,
+                                                  ctypes.byref(info)))
+    return {k: getattr(info, k) for k, _ in PlanInfo._fields_}
+
+
 def alloc_workspace(B, H_q, H_kv, D, N, max_past_len, dtype, device=None) -> Optional[torch.Tensor]:
-    """A zero-filled device workspace sized for these shapes (None when none is needed)."""
+    """A device workspace sized for these shapes (None when none is needed)."""
     n = kvd_decode_workspace_bytes(B, H_q, H_kv, D, N, max_past_len, dtype)
     if n == 0:
         return None
-    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
 
 
 def kvd_workspace_init(workspace: Optional[torch.Tensor], stream=None) -> None:

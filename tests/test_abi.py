@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("kvd_append", "kvd_decode_attention", "kvd_decode_workspace_bytes",
+    for n in ("kvd_append", "kvd_decode_attention", "kvd_decode_workspace_bytes", "kvd_decode_plan",
               "kvd_workspace_init", "kvd_cache_bytes", "kvd_status_string"):
         assert n in names
 
