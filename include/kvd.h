@@ -147,6 +147,36 @@ typedef struct kvd_plan_info {
 kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len,
                            kvd_dtype dtype, kvd_plan_info *info);
 
+/*
+ * kvd_decode_attention_noalloc -- kvd_decode_attention without a caller
+ * workspace, for callers that cannot allocate device memory.
+ *
+ * The source pages describe no such entry point; it exists for callers that
+ * may not allocate on their hot path, such as a plugin inside a host engine
+ * that owns all device memory through its own pool and offers no allocator,
+ * or a serving loop where cudaMalloc could block on the device or run out of
+ * memory mid-run.  Arguments, semantics and results are those of
+ * kvd_decode_attention, minus the workspace: the scratch is a 4 MiB array
+ * built into the library (every device that loads the library holds it
+ * until the process exits).  The function allocates nothing and calls no
+ * allocating routine.
+ *
+ *   - Shapes whose kvd_decode_workspace_bytes exceeds 4 MiB are rejected with
+ *     KVD_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up that device's scratch address
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before any stream capture on the device.
+ *   - All calls on a device share the one scratch array: calls whose GPU work
+ *     can overlap (unordered streams) race and give undefined results.
+ *   - The scratch keeps the previous call's contents; no call needs it to
+ *     start at zero.
+ */
+kvd_status kvd_decode_attention_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                        void *out, const int32_t *past_len, int B, int H_q,
+                                        int H_kv, int T_max, int D, int N, int max_past_len,
+                                        float scale, kvd_dtype dtype, uint32_t *err_word,
+                                        void *stream);
+
 /* kvd_workspace_init -- zero-fill a workspace on `stream` (asynchronous); optional,
  * kvd_decode_attention needs no particular initial contents. */
 kvd_status kvd_workspace_init(void *workspace, size_t workspace_bytes, void *stream);

@@ -1,0 +1,78 @@
+// kvd_noalloc.cu -- decode attention whose scratch memory is built into the
+// library, for callers that must not allocate device memory.
+//
+// Some callers cannot allocate device memory where they call us: a plugin
+// running inside a host engine that owns every device buffer through its own
+// pool and hands extensions no allocator; or a latency-critical serving loop
+// where cudaMalloc could block on the device or fail with out-of-memory in the
+// middle of a run.  kvd_decode_attention_noalloc serves them: its scratch is a
+// fixed array compiled into this file instead of a caller-provided workspace.
+//
+// Costs and rules of the built-in scratch:
+//   * every device that loads the library holds kNoAllocScratchBytes (4 MiB)
+//     of device memory for it until the process exits;
+//   * all calls on a device share that one array: calls whose GPU work can
+//     overlap (different streams without ordering between them) race on it;
+//   * the array keeps whatever the previous call left in it; nothing in it
+//     has to start at zero, because each call writes every scratch word it
+//     later reads;
+//   * shapes needing more than kNoAllocScratchBytes are rejected with
+//     KVD_ERR_WORKSPACE before anything is launched.
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "kvd.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+constexpr int kNoAllocMaxDevices = 64;
+
+// The scratch itself.  Host code must not use this name as an address: on the
+// host it is only a stand-in; the device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_dev_ptr[kNoAllocMaxDevices];  // device address of g_noalloc_scratch, per device
+
+// Device address of the scratch on the current device, looked up once per
+// device (with that device current) and remembered.
+kvd_status noalloc_scratch(void **ptr)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return KVD_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_dev_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return KVD_ERR_CUDA;
+        g_noalloc_dev_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_dev_ptr[dev];
+    return KVD_OK;
+}
+
+}  // namespace
+
+extern "C" kvd_status kvd_decode_attention_noalloc(const void *q, const void *k_cache,
+                                                   const void *v_cache, void *out,
+                                                   const int32_t *past_len, int B, int H_q,
+                                                   int H_kv, int T_max, int D, int N,
+                                                   int max_past_len, float scale, kvd_dtype dtype,
+                                                   uint32_t *err_word, void *stream)
+{
+    const size_t need = kvd_decode_workspace_bytes(B, H_q, H_kv, D, N, max_past_len, dtype);
+    if (need == 0) {
+        // Invalid shapes: let the regular entry point report which argument is wrong.
+        return kvd_decode_attention(q, k_cache, v_cache, out, past_len, B, H_q, H_kv, T_max, D, N,
+                                    max_past_len, scale, dtype, nullptr, 0, err_word, stream);
+    }
+    if (need > kNoAllocScratchBytes) return KVD_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    const kvd_status st = noalloc_scratch(&scratch);
+    if (st != KVD_OK) return st;
+    return kvd_decode_attention(q, k_cache, v_cache, out, past_len, B, H_q, H_kv, T_max, D, N,
+                                max_past_len, scale, dtype, scratch, kNoAllocScratchBytes, err_word,
+                                stream);
+}

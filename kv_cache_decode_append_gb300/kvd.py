@@ -65,6 +65,9 @@ class _Lib:
         lib.kvd_decode_attention.restype = ci
         lib.kvd_decode_attention.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
                                              vp, sz, u32p, vp]
+        lib.kvd_decode_attention_noalloc.restype = ci
+        lib.kvd_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
+                                                     ci, u32p, vp]
         lib.kvd_decode_plan.restype = ci
         lib.kvd_decode_plan.argtypes = [ci, ci, ci, ci, ci, ci, ci, ctypes.POINTER(PlanInfo)]
         lib.kvd_workspace_init.restype = ci
@@ -211,6 +214,31 @@ def kvd_decode_attention(q, k_cache, v_cache, out, past_len, max_past_len: int, 
                                   float(scale), _dtype_code(q), ws_ptr, ws_bytes, _ptr(err_word),
                                   _stream_handle(stream))
     _check("kvd_decode_attention", st)
+
+
+def kvd_decode_attention_noalloc(q, k_cache, v_cache, out, past_len, max_past_len: int,
+                                 scale: float = 0.0, err_word=None, stream=None) -> None:
+    """kvd_decode_attention with the library's built-in 4 MiB scratch instead of a workspace.
+
+    For callers that cannot allocate device memory where they call; calls whose
+    GPU work may overlap must not use it concurrently (they share the scratch).
+    """
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        _need_cuda(n, t, q.dtype)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_q, N, D = q.shape
+    _, H_kv, T_max, _ = k_cache.shape
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError("shape mismatch between q, out and the caches")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    st = raw.kvd_decode_attention_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                          out.data_ptr(), past_len.data_ptr(), B, H_q, H_kv, T_max, D, N,
+                                          int(max_past_len), float(scale), _dtype_code(q), _ptr(err_word),
+                                          _stream_handle(stream))
+    _check("kvd_decode_attention_noalloc", st)
 
 
 def kvd_cache_bytes(L: int, B: int, H_kv: int, D: int, T: int, dtype) -> int:
