@@ -24,8 +24,10 @@
 //   * thread 0 walks the range and streams each tile's [TK, D] K and V rows
 //     (contiguous in the [B, H_kv, T_max, D] cache), plus the q rows at the
 //     start of each sequence-head, into a STAGES-deep shared-memory ring with
-//     1-D bulk (TMA) copies completing on mbarriers (L2 evict-first); it
-//     refills a slot right after the one CTA barrier of each tile;
+//     1-D bulk (TMA) copies completing on "full" mbarriers (L2 evict-first);
+//     each warp releases a slot on its "empty" mbarrier when done with it, so
+//     warps drift independently and the CTA only synchronises where a piece
+//     ends;
 //   * the warps split into key groups of L lanes; a group owns whole keys,
 //     each lane owns E = D / L head-dim elements of q (registers, pre-scaled
 //     by scale*log2 e) and of the output accumulators for all RB rows; a dot
@@ -35,7 +37,7 @@
 //     exceeds it by more than 2^8, which keeps exp2 arguments <= 8 and makes
 //     the rescale of o rare (o/l is unchanged by that choice);
 //   * where the range leaves a sequence-head the warps merge their groups by
-//     log-sum-exp (shuffles) and, after the tile barrier, across warps
+//     log-sum-exp (shuffles) and then, between two CTA barriers, across warps
 //     (shared memory): the output is written directly when the sequence-head
 //     lies inside one CTA's range, else the piece goes to a partial slot
 //     (a CTA holds at most two: the head it continues and the head it
@@ -95,7 +97,7 @@ template <typename T, int D, int RB> struct AttnShape {
     static constexpr int kEpiBytes = (kEpiFloats > kThreads ? kEpiFloats : kThreads) * 4;
     static constexpr int kMetaOff = kEpiOff + kEpiBytes;
     static constexpr int kBarOff = kMetaOff + kStages * 32;
-    static constexpr int kFixedBytes = kBarOff + kStages * 8;
+    static constexpr int kFixedBytes = kBarOff + 2 * kStages * 8;  // full and empty barriers
 
     static_assert(kRowBytes % 16 == 0, "rows must be whole 16-byte chunks");
     static_assert(kCpl >= 1 && kRowChunks % kL == 0, "lane mapping");
@@ -236,17 +238,41 @@ __device__ __forceinline__ int owner_cta(long long t, long long n, long long G)
     return (int)(((t + 1) * G + n - 1) / n) - 1;
 }
 
-// Thread 0's walk over the CTA's tile range.
+// Thread 0's walk over the CTA's tile range.  Per-head values are computed
+// once when the walk enters a sequence-head; a tile only costs a few stores
+// and the bulk copies.
 template <typename S> struct RangeWalk {
     long long t, hi, n, G;  // next tile, end of range, tiles in total, working CTAs
-    int b, hr, tin, tb;  // sequence, head x row block, tile within the head, its tiles
-    int HR;              // H_kv * n_rowblocks
+    int b, hr, tin, tb;     // sequence, head x row block, tile within the head, its tiles
+    int HR;                 // H_kv * n_rowblocks
     bool ended;
-    bool piece_start;    // the next tile starts a piece (the head's first tile, or the range's)
+    bool piece_start;       // the next tile starts a piece (the head's first tile, or the range's)
+    // per-head values
+    int bh, rb, P, T_b, n_chunks, slot, q_bytes;
+    const unsigned char *kg, *vg, *qg;
     uint64_t policy;
 
-    __device__ __forceinline__ void start(const AttnArgs &a, const int *pre, long long lo, long long hi_,
-                                          long long n_, long long G_)
+    __device__ __forceinline__ void enter_head(const AttnArgs &a, const int *pl)
+    {
+        const int h = hr / a.n_rowblocks;
+        rb = hr % a.n_rowblocks;
+        bh = b * a.H_kv + h;
+        P = pl[b];
+        T_b = P + a.N;
+        const long long ts = t - tin;  // first tile of this head
+        const int c_first = owner_cta(ts, n, G);
+        n_chunks = owner_cta(ts + tb - 1, n, G) - c_first + 1;
+        slot = ((int)blockIdx.x == c_first) ? 1 : 0;
+        const size_t row = (size_t)bh * a.T_max;
+        kg = static_cast<const unsigned char *>(a.k_cache) + row * S::kRowBytes;
+        vg = static_cast<const unsigned char *>(a.v_cache) + row * S::kRowBytes;
+        qg = static_cast<const unsigned char *>(a.q) + ((size_t)bh * a.rows + rb * S::kRB) * S::kRowBytes;
+        q_bytes = min(S::kRB, a.rows - rb * S::kRB) * S::kRowBytes;
+        if (tin == 0) a.seg[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
+    }
+
+    __device__ __forceinline__ void start(const AttnArgs &a, const int *pre, const int *pl, long long lo,
+                                          long long hi_, long long n_, long long G_)
     {
         policy = l2_evict_first_policy();
         HR = a.H_kv * a.n_rowblocks;
@@ -267,8 +293,10 @@ template <typename S> struct RangeWalk {
         const long long local = t - (long long)pre[b] * HR;
         hr = (int)(local / tb);
         tin = (int)(local % tb);
+        enter_head(a, pl);
     }
 
+    // Describe and load the next tile into slot s, or mark the end of work.
     __device__ __forceinline__ void fill(const AttnArgs &a, const int *pre, const int *pl,
                                          unsigned char *smem, TileMeta *meta, uint64_t *full, int s)
     {
@@ -279,39 +307,25 @@ template <typename S> struct RangeWalk {
             ended = true;
             return;
         }
-        const int h = hr / a.n_rowblocks, rb = hr % a.n_rowblocks;
-        const int bh = b * a.H_kv + h;
-        const int P = pl[b];
-        const long long ts = t - tin;  // first tile of this sequence-head
-        const int c_first = owner_cta(ts, n, G);
-        const int n_chunks = owner_cta(ts + tb - 1, n, G) - c_first + 1;
         TileMeta mt;
         mt.bh = bh;
         mt.rb = rb;
         mt.tile_k0 = tin * S::kTK;
-        mt.nk = min(S::kTK, P + a.N - mt.tile_k0);
+        mt.nk = min(S::kTK, T_b - mt.tile_k0);
         mt.P = P;
         mt.flags = (piece_start ? kMetaFirst : 0) | ((tin == tb - 1 || t == hi - 1) ? kMetaLast : 0);
         mt.n_chunks = n_chunks;
-        mt.slot = ((int)blockIdx.x == c_first) ? 1 : 0;
+        mt.slot = slot;
         meta[s] = mt;
-        if (tin == 0) a.seg[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
 
-        const size_t row = (size_t)bh * a.T_max + mt.tile_k0;
         const uint32_t bytes = (uint32_t)mt.nk * S::kRowBytes;
-        const int q_rows = min(S::kRB, a.rows - rb * S::kRB);
-        const uint32_t qbytes = piece_start ? (uint32_t)q_rows * S::kRowBytes : 0u;
+        const uint32_t qbytes = piece_start ? (uint32_t)q_bytes : 0u;
+        const size_t off = (size_t)mt.tile_k0 * S::kRowBytes;
         unsigned char *dst = smem + S::kRingOff + s * 2 * S::kTileBytes;
         mbar_arrive_expect_tx(&full[s], 2u * bytes + qbytes);
-        bulk_load_g2s(dst, static_cast<const unsigned char *>(a.k_cache) + row * S::kRowBytes, bytes,
-                      &full[s], policy);
-        bulk_load_g2s(dst + S::kTileBytes, static_cast<const unsigned char *>(a.v_cache) + row * S::kRowBytes,
-                      bytes, &full[s], policy);
-        if (qbytes) {
-            const unsigned char *qg = static_cast<const unsigned char *>(a.q) +
-                                      ((size_t)bh * a.rows + rb * S::kRB) * S::kRowBytes;
-            bulk_load_g2s(smem + S::kQOff + s * S::kQSlotBytes, qg, qbytes, &full[s], policy);
-        }
+        bulk_load_g2s(dst, kg + off, bytes, &full[s], policy);
+        bulk_load_g2s(dst + S::kTileBytes, vg + off, bytes, &full[s], policy);
+        if (qbytes) bulk_load_g2s(smem + S::kQOff + s * S::kQSlotBytes, qg, qbytes, &full[s], policy);
 
         // advance to the next tile of the flattened list
         ++t;
@@ -326,6 +340,7 @@ template <typename S> struct RangeWalk {
                 } while (b < a.B && pre[b + 1] == pre[b]);
                 if (b < a.B) tb = pre[b + 1] - pre[b];
             }
+            if (t < hi) enter_head(a, pl);
         }
     }
 };
@@ -339,6 +354,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     const float kNegInf = __int_as_float(0xff800000);
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBarOff);
+    uint64_t *empty = full + S::kStages;
     TileMeta *meta = reinterpret_cast<TileMeta *>(smem + S::kMetaOff);
     int *pre = reinterpret_cast<int *>(smem + S::kFixedBytes);  // [B + 1] tile prefix per head
     int *pl = pre + a.B + 1;                                     // [B] history lengths
@@ -349,7 +365,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
 
     if (tid == 0) {
 #pragma unroll
-        for (int s = 0; s < S::kStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < S::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], S::kNW);
+        }
         fence_mbar_init();
     }
     // Every input may come from the previous kernel on the stream.
@@ -395,10 +414,13 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     const long long lo = blockIdx.x < G ? n_total * blockIdx.x / G : 0;
     const long long hi = blockIdx.x < G ? n_total * (blockIdx.x + 1) / G : 0;
 
+    // Thread 0 fills the ring; slot s of ring position p is free again once
+    // every warp has released position p - STAGES on empty[s].
     RangeWalk<S> walk;  // used by thread 0 only
+    int issued = 0;     // ring positions filled so far (thread 0)
     if (tid == 0) {
-        walk.start(a, pre, lo, hi, n_total, G);
-        for (int s = 0; s < S::kStages; ++s) walk.fill(a, pre, pl, smem, meta, full, s);
+        walk.start(a, pre, pl, lo, hi, n_total, G);
+        for (; issued < S::kStages; ++issued) walk.fill(a, pre, pl, smem, meta, full, issued);
     }
     __syncthreads();
 
@@ -406,13 +428,26 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     float o[RB][S::kE];
     float m_run[RB], l_run[RB];
     int lim[RB];
-    bool prev_last = false;  // the previous tile ended a piece (uniform across the CTA)
     bool timed_out = false;
     int first_unwaited = -1;  // first ring position this thread gave up waiting for
 
     for (int pos = 0; lo < hi; ++pos) {
         const int s = pos % S::kStages;
         const uint32_t ph = (uint32_t)(pos / S::kStages) & 1u;
+        if (tid == 0) {
+            // Position pos must have been issued before anyone waits for it; its
+            // slot frees as soon as the slower warps release pos - STAGES.
+            while (issued <= pos && !walk.ended) {
+                const int fs = issued % S::kStages;
+                const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
+                if (!timed_out && !mbar_wait_bounded(&empty[fs], fph)) {
+                    timed_out = true;
+                    raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+                }
+                walk.fill(a, pre, pl, smem, meta, full, fs);
+                ++issued;
+            }
+        }
         if (!timed_out && !mbar_wait_bounded(&full[s], ph)) {
             // Keep the same control flow as every other thread (the metadata is
             // valid even if the data never landed); the result is flagged.
@@ -456,92 +491,95 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
         } else {
             attn_tile<T, D, RB, true>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim, k_end);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with slot s
 
-        const bool last = (mt.flags & kMetaLast) != 0;
+        // Opportunistic refill: if every warp has released the slot, issue now.
+        if (tid == 0 && !walk.ended && issued < pos + 1 + S::kStages) {
+            const int fs = issued % S::kStages;
+            const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
+            if (mbar_test_wait(&empty[fs], fph)) {
+                walk.fill(a, pre, pl, smem, meta, full, fs);
+                ++issued;
+            }
+        }
+
+        if (!(mt.flags & kMetaLast)) continue;
+
+        // ---- end of a piece: merge the key groups of each warp (xor shuffles),
+        //      then the warps through shared memory ----
         float *ep_o = reinterpret_cast<float *>(smem + S::kEpiOff);
         float *ep_m = ep_o + S::kNW * RB * D;
         float *ep_l = ep_m + S::kNW * RB;
-        if (last) {
-            // Merge the key groups of this warp (xor shuffles), then publish the
-            // warp's state for the cross-warp merge after the tile barrier.  If
-            // the previous tile also ended a piece, its readers may still be in
-            // the shared area: wait for them first.
 #pragma unroll
-            for (int off = S::kL; off < 32; off *= 2) {
+        for (int off = S::kL; off < 32; off *= 2) {
 #pragma unroll
-                for (int r = 0; r < RB; ++r) {
-                    const float m_o = __shfl_xor_sync(0xffffffffu, m_run[r], off);
-                    const float l_o = __shfl_xor_sync(0xffffffffu, l_run[r], off);
-                    const float M = fmaxf(m_run[r], m_o);
-                    const float wa = safe_weight(m_run[r], M), wb = safe_weight(m_o, M);
-                    l_run[r] = l_run[r] * wa + l_o * wb;
+            for (int r = 0; r < RB; ++r) {
+                const float m_o = __shfl_xor_sync(0xffffffffu, m_run[r], off);
+                const float l_o = __shfl_xor_sync(0xffffffffu, l_run[r], off);
+                const float M = fmaxf(m_run[r], m_o);
+                const float wa = safe_weight(m_run[r], M), wb = safe_weight(m_o, M);
+                l_run[r] = l_run[r] * wa + l_o * wb;
 #pragma unroll
-                    for (int e = 0; e < S::kE; ++e)
-                        o[r][e] = o[r][e] * wa + __shfl_xor_sync(0xffffffffu, o[r][e], off) * wb;
-                    m_run[r] = M;
-                }
+                for (int e = 0; e < S::kE; ++e)
+                    o[r][e] = o[r][e] * wa + __shfl_xor_sync(0xffffffffu, o[r][e], off) * wb;
+                m_run[r] = M;
             }
-            if (prev_last) __syncthreads();
-            if (grp == 0) {
+        }
+        __syncthreads();  // the previous piece's readers are done with the shared area
+        if (grp == 0) {
 #pragma unroll
-                for (int r = 0; r < RB; ++r) {
-                    float *dst = ep_o + (warp * RB + r) * D;
+            for (int r = 0; r < RB; ++r) {
+                float *dst = ep_o + (warp * RB + r) * D;
 #pragma unroll
-                    for (int c = 0; c < S::kCpl; ++c) {
-                        const int d0 = (c * S::kL + j) * Ty::kPerChunk;
+                for (int c = 0; c < S::kCpl; ++c) {
+                    const int d0 = (c * S::kL + j) * Ty::kPerChunk;
 #pragma unroll
-                        for (int e = 0; e < Ty::kPerChunk; e += 4)
-                            *reinterpret_cast<float4 *>(dst + d0 + e) =
-                                make_float4(o[r][c * Ty::kPerChunk + e], o[r][c * Ty::kPerChunk + e + 1],
-                                            o[r][c * Ty::kPerChunk + e + 2], o[r][c * Ty::kPerChunk + e + 3]);
-                    }
-                    if (j == 0) {
-                        ep_m[warp * RB + r] = m_run[r];
-                        ep_l[warp * RB + r] = l_run[r];
-                    }
+                    for (int e = 0; e < Ty::kPerChunk; e += 4)
+                        *reinterpret_cast<float4 *>(dst + d0 + e) =
+                            make_float4(o[r][c * Ty::kPerChunk + e], o[r][c * Ty::kPerChunk + e + 1],
+                                        o[r][c * Ty::kPerChunk + e + 2], o[r][c * Ty::kPerChunk + e + 3]);
+                }
+                if (j == 0) {
+                    ep_m[warp * RB + r] = m_run[r];
+                    ep_l[warp * RB + r] = l_run[r];
                 }
             }
         }
-
-        __syncthreads();  // slot s is free; the warps' end-of-piece states are published
-        if (tid == 0) walk.fill(a, pre, pl, smem, meta, full, s);
-
-        if (last) {
-            const bool single = (mt.n_chunks == 1);
-            const size_t pbase = ((size_t)blockIdx.x * 2 + mt.slot) * RB;
-            for (int idx = tid; idx < RB * D; idx += S::kThreads) {
-                const int r = idx / D, d = idx % D;
-                const int rg = mt.rb * RB + r;
-                if (rg >= a.rows) continue;
-                float M = kNegInf;
+        __syncthreads();
+        const bool single = (mt.n_chunks == 1);
+        const size_t pbase = ((size_t)blockIdx.x * 2 + mt.slot) * RB;
+        for (int idx = tid; idx < RB * D; idx += S::kThreads) {
+            const int r = idx / D, d = idx % D;
+            const int rg = mt.rb * RB + r;
+            if (rg >= a.rows) continue;
+            float M = kNegInf;
 #pragma unroll
-                for (int w = 0; w < S::kNW; ++w) M = fmaxf(M, ep_m[w * RB + r]);
-                float num = 0.f, den = 0.f;
+            for (int w = 0; w < S::kNW; ++w) M = fmaxf(M, ep_m[w * RB + r]);
+            float num = 0.f, den = 0.f;
 #pragma unroll
-                for (int w = 0; w < S::kNW; ++w) {
-                    const float wt = safe_weight(ep_m[w * RB + r], M);
-                    num = fmaf(wt, ep_o[(w * RB + r) * D + d], num);
-                    den = fmaf(wt, ep_l[w * RB + r], den);
-                }
-                if (single) {
-                    Ty::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
-                } else {
-                    a.part_o[(pbase + r) * D + d] = num;
-                    if (d == 0) {
-                        a.part_ml[(pbase + r) * 2 + 0] = M;
-                        a.part_ml[(pbase + r) * 2 + 1] = den;
-                    }
+            for (int w = 0; w < S::kNW; ++w) {
+                const float wt = safe_weight(ep_m[w * RB + r], M);
+                num = fmaf(wt, ep_o[(w * RB + r) * D + d], num);
+                den = fmaf(wt, ep_l[w * RB + r], den);
+            }
+            if (single) {
+                Ty::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
+            } else {
+                a.part_o[(pbase + r) * D + d] = num;
+                if (d == 0) {
+                    a.part_ml[(pbase + r) * 2 + 0] = M;
+                    a.part_ml[(pbase + r) * 2 + 1] = den;
                 }
             }
         }
-        prev_last = last;
     }
 
-    if (tid == 0 && timed_out) {
+    if (tid == 0 && timed_out && first_unwaited >= 0) {
         // Copies that may still be in flight must land before the CTA exits:
-        // wait for every position from the first abandoned one, one deadline.
+        // wait for every issued position from the first abandoned one, one deadline.
         const uint64_t t0 = global_timer_ns();
-        for (int p = first_unwaited; p < first_unwaited + S::kStages; ++p) {
+        for (int p = first_unwaited; p < issued; ++p) {
             const uint32_t ph = (uint32_t)(p / S::kStages) & 1u;
             while (!mbar_try_wait(&full[p % S::kStages], ph) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
