@@ -204,6 +204,12 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def whole_job_gbs(bytes_per_step_per_rank: int, steps: int, elapsed_max_s: float, world: int) -> float:
+    """Weak scaling: every rank processes the same step; the job moves world x
+    the bytes of one rank in the slowest rank's time."""
+    return world * bytes_per_step_per_rank * steps / elapsed_max_s / 1e9
+
+
 def oracle_layer_step(orc, host, past_np, dtype):
     st = orc.append(host["k_cache"], host["v_cache"], host["k_new"], host["v_new"], past_np, dtype)
     out, st2 = orc.decode_attention(host["q"], host["k_cache"], host["v_cache"], past_np, dtype)
@@ -386,7 +392,7 @@ def run_gpu(args, w, rank, world, local):
     if rank != 0:
         return
     bytes_step = w.L * layer_bytes(w, past.tolist())
-    gbs = world * bytes_step * args.steps / elapsed_max / 1e9
+    gbs = whole_job_gbs(bytes_step, args.steps, elapsed_max, world)
     ms_step = elapsed_max / args.steps * 1e3
     peak, peak_kind = measured_peak()
     a_bytes = attn_bytes(w, past.tolist())
@@ -441,7 +447,7 @@ def run_gpu(args, w, rank, world, local):
                       f"repeated {reps}x in {cpu_el:.1f} s",
         },
         "e2e": {
-            "value": round(world * bytes_step * e_steps / e2e_el / 1e9, 2), "unit": "GB/s",
+            "value": round(whole_job_gbs(bytes_step, e_steps, e2e_el, world), 2), "unit": "GB/s",
             "ms_per_step": round(e2e_el / e_steps * 1e3, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
         },
