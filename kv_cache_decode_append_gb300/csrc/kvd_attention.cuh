@@ -30,9 +30,9 @@
 //     ends;
 //   * the warps split into key groups of L lanes; a group owns whole keys,
 //     each lane owns E = D / L head-dim elements of q (registers, pre-scaled
-//     by scale*log2 e) and of the output accumulators for all RB rows; a dot
-//     product is E FMAs per lane plus a log2(L)-step xor-shuffle reduction
-//     inside the group; every group keeps its own online softmax (running
+//     by scale*log2 e) and of the output accumulators for all RB rows, as
+//     fp32 pairs for the packed f32x2 FMA; a dot product is E/2 packed FMAs
+//     per lane plus a log2(L)-step xor-shuffle reduction inside the group; every group keeps its own online softmax (running
 //     max m, sum l, output o); the running max only moves when a tile's max
 //     exceeds it by more than 2^8, which keeps exp2 arguments <= 8 and makes
 //     the rescale of o rare (o/l is unchanged by that choice);
@@ -121,15 +121,21 @@ constexpr int kMetaFirst = 1;  // first tile of a piece: the stage also carries 
 constexpr int kMetaLast = 2;   // last tile of a piece
 constexpr int kMetaEnd = 4;    // no more work
 
+// One tile for one warp: keys warp*kKpw .. +kKpw of the tile, RB query rows.
+// q, K, V and the accumulators are held as fp32 pairs (E/2 per row) and
+// multiplied with packed f32x2 FMAs; a score is the sum of its even and odd
+// partial dot products.
 template <typename T, int D, int RB, bool kMasked>
 __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigned char *Vs,
-                                          const float (&qv)[RB][AttnShape<T, D, RB>::kE],
-                                          float (&o)[RB][AttnShape<T, D, RB>::kE], float (&m_run)[RB],
+                                          const f32x2 (&qv)[RB][AttnShape<T, D, RB>::kE / 2],
+                                          f32x2 (&o)[RB][AttnShape<T, D, RB>::kE / 2], float (&m_run)[RB],
                                           float (&l_run)[RB], int warp, int grp, int j,
                                           int tile_k0, const int (&lim)[RB], int k_end)
 {
     using S = AttnShape<T, D, RB>;
     using Ty = Elem<T>;
+    constexpr int E2 = S::kE / 2;
+    constexpr int P2 = Ty::kPerChunk / 2;  // pairs per 16-byte chunk
     const float kNegInf = __int_as_float(0xff800000);
     constexpr float kRescaleThreshold = 8.0f;
 
@@ -145,15 +151,17 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
     }
 #pragma unroll
     for (int u = 0; u < S::kKpg; ++u) {
-        float kf[S::kE];
+        f32x2 kf[E2];
 #pragma unroll
-        for (int c = 0; c < S::kCpl; ++c) Ty::widen(raw[u][c], kf + c * Ty::kPerChunk);
+        for (int c = 0; c < S::kCpl; ++c) Ty::widen2(raw[u][c], kf + c * P2);
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
-            float acc = 0.f;
+            f32x2 acc = fma2(qv[r][0], kf[0], 0ull);
 #pragma unroll
-            for (int e = 0; e < S::kE; ++e) acc = fmaf(qv[r][e], kf[e], acc);
-            sc[u][r] = acc;
+            for (int e = 1; e < E2; ++e) acc = fma2(qv[r][e], kf[e], acc);
+            float lo, hi;
+            unpack2(acc, lo, hi);
+            sc[u][r] = lo + hi;
         }
     }
 #pragma unroll
@@ -174,7 +182,7 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
     }
 
     // Online softmax, one state per key group.
-    float p[S::kKpg][RB];
+    f32x2 p2[S::kKpg][RB];
 #pragma unroll
     for (int r = 0; r < RB; ++r) {
         float mt = sc[0][r];
@@ -183,15 +191,17 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
         if (mt > m_run[r] + kRescaleThreshold) {
             const float alpha = exp2f(m_run[r] - mt);
             l_run[r] *= alpha;
+            const f32x2 alpha2 = pack2(alpha, alpha);
 #pragma unroll
-            for (int e = 0; e < S::kE; ++e) o[r][e] *= alpha;
+            for (int e = 0; e < E2; ++e) o[r][e] = mul2(o[r][e], alpha2);
             m_run[r] = mt;
         }
         const float mu = (m_run[r] == kNegInf) ? 0.f : m_run[r];
 #pragma unroll
         for (int u = 0; u < S::kKpg; ++u) {
-            p[u][r] = exp2f(sc[u][r] - mu);
-            l_run[r] += p[u][r];
+            const float p = exp2f(sc[u][r] - mu);
+            l_run[r] += p;
+            p2[u][r] = pack2(p, p);
         }
     }
 
@@ -204,20 +214,20 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
     }
 #pragma unroll
     for (int u = 0; u < S::kKpg; ++u) {
-        float vf[S::kE];
+        f32x2 vf[E2];
 #pragma unroll
-        for (int c = 0; c < S::kCpl; ++c) Ty::widen(raw[u][c], vf + c * Ty::kPerChunk);
+        for (int c = 0; c < S::kCpl; ++c) Ty::widen2(raw[u][c], vf + c * P2);
         if constexpr (kMasked) {
             // Rows past the end of the chunk were not loaded: stale shared memory.
             if (tile_k0 + warp * S::kKpw + u * S::kGpw + grp >= k_end) {
 #pragma unroll
-                for (int e = 0; e < S::kE; ++e) vf[e] = 0.f;
+                for (int e = 0; e < E2; ++e) vf[e] = 0ull;
             }
         }
 #pragma unroll
         for (int r = 0; r < RB; ++r)
 #pragma unroll
-            for (int e = 0; e < S::kE; ++e) o[r][e] = fmaf(p[u][r], vf[e], o[r][e]);
+            for (int e = 0; e < E2; ++e) o[r][e] = fma2(p2[u][r], vf[e], o[r][e]);
     }
 }
 
@@ -424,8 +434,8 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     }
     __syncthreads();
 
-    float qv[RB][S::kE];
-    float o[RB][S::kE];
+    f32x2 qv[RB][S::kE / 2];
+    f32x2 o[RB][S::kE / 2];
     float m_run[RB], l_run[RB];
     int lim[RB];
     bool timed_out = false;
@@ -470,17 +480,18 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
                 m_run[r] = kNegInf;
                 l_run[r] = 0.f;
 #pragma unroll
-                for (int e = 0; e < S::kE; ++e) o[r][e] = 0.f;
+                for (int e = 0; e < S::kE / 2; ++e) o[r][e] = 0ull;
                 if (r < q_rows) {
+                    const f32x2 qs2 = pack2(a.qscale, a.qscale);
 #pragma unroll
                     for (int c = 0; c < S::kCpl; ++c)
-                        Ty::widen(lds128(qs + r * S::kRowBytes + (c * S::kL + j) * 16),
-                                  &qv[r][c * Ty::kPerChunk]);
+                        Ty::widen2(lds128(qs + r * S::kRowBytes + (c * S::kL + j) * 16),
+                                   &qv[r][c * (Ty::kPerChunk / 2)]);
 #pragma unroll
-                    for (int e = 0; e < S::kE; ++e) qv[r][e] *= a.qscale;
+                    for (int e = 0; e < S::kE / 2; ++e) qv[r][e] = mul2(qv[r][e], qs2);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < S::kE; ++e) qv[r][e] = 0.f;
+                    for (int e = 0; e < S::kE / 2; ++e) qv[r][e] = 0ull;
                 }
             }
         }
@@ -521,8 +532,13 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
                 const float wa = safe_weight(m_run[r], M), wb = safe_weight(m_o, M);
                 l_run[r] = l_run[r] * wa + l_o * wb;
 #pragma unroll
-                for (int e = 0; e < S::kE; ++e)
-                    o[r][e] = o[r][e] * wa + __shfl_xor_sync(0xffffffffu, o[r][e], off) * wb;
+                for (int e = 0; e < S::kE / 2; ++e) {
+                    float lo, hi;
+                    unpack2(o[r][e], lo, hi);
+                    lo = lo * wa + __shfl_xor_sync(0xffffffffu, lo, off) * wb;
+                    hi = hi * wa + __shfl_xor_sync(0xffffffffu, hi, off) * wb;
+                    o[r][e] = pack2(lo, hi);
+                }
                 m_run[r] = M;
             }
         }
@@ -535,10 +551,12 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
                 for (int c = 0; c < S::kCpl; ++c) {
                     const int d0 = (c * S::kL + j) * Ty::kPerChunk;
 #pragma unroll
-                    for (int e = 0; e < Ty::kPerChunk; e += 4)
-                        *reinterpret_cast<float4 *>(dst + d0 + e) =
-                            make_float4(o[r][c * Ty::kPerChunk + e], o[r][c * Ty::kPerChunk + e + 1],
-                                        o[r][c * Ty::kPerChunk + e + 2], o[r][c * Ty::kPerChunk + e + 3]);
+                    for (int e = 0; e < Ty::kPerChunk; e += 4) {
+                        float4 v;
+                        unpack2(o[r][(c * Ty::kPerChunk + e) / 2], v.x, v.y);
+                        unpack2(o[r][(c * Ty::kPerChunk + e) / 2 + 1], v.z, v.w);
+                        *reinterpret_cast<float4 *>(dst + d0 + e) = v;
+                    }
                 }
                 if (j == 0) {
                     ep_m[warp * RB + r] = m_run[r];

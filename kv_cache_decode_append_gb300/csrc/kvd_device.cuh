@@ -138,6 +138,37 @@ __device__ __forceinline__ void stg128(void *p, uint4 v)
                  : "memory");
 }
 
+// Two fp32 values in one 64-bit register pair, for the packed fp32 pipe of
+// sm_100-class GPUs: one f32x2 instruction performs two IEEE fp32 operations
+// with the same rounding as two scalar ones.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi)
+{
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(f32x2 v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Element type traits: how a 16-byte chunk widens to fp32.
 template <typename T> struct Elem;
 
@@ -150,6 +181,12 @@ template <> struct Elem<float> {
         f[1] = __uint_as_float(c.y);
         f[2] = __uint_as_float(c.z);
         f[3] = __uint_as_float(c.w);
+    }
+    // the chunk as two fp32 pairs (elements 0,1 and 2,3)
+    __device__ __forceinline__ static void widen2(const uint4 &c, f32x2 *f)
+    {
+        f[0] = pack2(__uint_as_float(c.x), __uint_as_float(c.y));
+        f[1] = pack2(__uint_as_float(c.z), __uint_as_float(c.w));
     }
     __device__ __forceinline__ static void store(float *dst, float v) { *dst = v; }
 };
@@ -167,6 +204,14 @@ template <> struct Elem<__nv_bfloat16> {
             f[2 * k] = __uint_as_float(w[k] << 16);
             f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
         }
+    }
+    // the chunk as four fp32 pairs (elements 2k, 2k+1 of word k)
+    __device__ __forceinline__ static void widen2(const uint4 &c, f32x2 *f)
+    {
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            f[k] = pack2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
     }
     __device__ __forceinline__ static void store(__nv_bfloat16 *dst, float v)
     {
