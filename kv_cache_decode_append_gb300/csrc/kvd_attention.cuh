@@ -15,12 +15,13 @@
 //     rows); its query rows are g*N rows (g query heads of the group x N new
 //     tokens), contiguous in q and out; its keys 0..P_b+N-1 form
 //     ceil((P_b+N)/TK) tiles of TK keys;
-//   * every CTA reads past_len, forms the prefix sum of tiles over all
-//     sequence-heads, and takes an equal contiguous range of that flattened
-//     tile list (the grid is SMs x resident CTAs; with fewer tiles than CTAs
-//     only the first n_tiles CTAs work): every CTA streams the same number
-//     of tiles whatever the mix of sequence lengths, with no atomics and a
-//     split that depends only on the inputs;
+//   * every CTA reads past_len, forms the prefix sum over all sequence-heads
+//     of their cost in units (tiles plus a fixed overhead per head for the
+//     piece boundary), and takes an equal contiguous range of that flattened
+//     list (the grid is SMs x resident CTAs; with fewer units than CTAs only
+//     the first n_units CTAs work): every CTA gets the same work whatever the
+//     mix of sequence lengths, with no atomics and a split that depends only
+//     on the inputs;
 //   * thread 0 walks the range and streams each tile's [TK, D] K and V rows
 //     (contiguous in the [B, H_kv, T_max, D] cache), plus the q rows at the
 //     start of each sequence-head, into a STAGES-deep shared-memory ring with
@@ -88,6 +89,9 @@ template <typename T, int D, int RB> struct AttnShape {
     static constexpr int kTileBytes = kTK * kRowBytes; // one of K or V
     static constexpr int kStages = (2 * kTileBytes <= 16384) ? 4 : 3;
     static constexpr int kQSlotBytes = RB * kRowBytes;
+    // Cost of a piece boundary in tile units for the static split (measured:
+    // a boundary costs about as much as streaming 96 KB of K/V per CTA).
+    static constexpr int kPieceUnits = (96 * 1024 / (2 * kTileBytes)) > 1 ? (96 * 1024 / (2 * kTileBytes)) : 1;
 
     // shared memory layout (bytes); the per-sequence tables follow kFixedBytes
     static constexpr int kRingOff = 0;
@@ -241,18 +245,23 @@ __device__ __forceinline__ float safe_weight(float m, float M)
     return (m == __int_as_float(0xff800000)) ? 0.f : exp2f(m - M);
 }
 
-// CTA whose range [c*n/G, (c+1)*n/G) holds flattened tile t.  With G <= n
+// CTA whose range [c*n/G, (c+1)*n/G) holds flattened unit t.  With G <= n
 // every range is non-empty, so the CTAs holding a head's tiles are consecutive.
 __device__ __forceinline__ int owner_cta(long long t, long long n, long long G)
 {
-    return (int)(((t + 1) * G + n - 1) / n) - 1;
+    const unsigned long long num = (unsigned long long)(t + 1) * G + n - 1;
+    if (num < (1ull << 32)) return (int)((unsigned)num / (unsigned)n) - 1;  // common case: 32-bit divide
+    return (int)(num / (unsigned long long)n) - 1;
 }
 
-// Thread 0's walk over the CTA's tile range.  Per-head values are computed
-// once when the walk enters a sequence-head; a tile only costs a few stores
-// and the bulk copies.
+// Thread 0's walk over the CTA's range.  The range is counted in units: a
+// sequence-head with tb tiles is kPieceUnits overhead units (what a piece
+// boundary costs: merges, restarting the ring) followed by tb tile units, so
+// CTAs whose range crosses more head starts receive fewer tiles.  Per-head
+// values are computed once when the walk enters a head; a tile only costs a
+// few stores and the bulk copies.
 template <typename S> struct RangeWalk {
-    long long t, hi, n, G;  // next tile, end of range, tiles in total, working CTAs
+    long long t, hi, n, G;  // unit of the next tile, end of range, units in total, working CTAs
     int b, hr, tin, tb;     // sequence, head x row block, tile within the head, its tiles
     int HR;                 // H_kv * n_rowblocks
     bool ended;
@@ -269,7 +278,7 @@ template <typename S> struct RangeWalk {
         bh = b * a.H_kv + h;
         P = pl[b];
         T_b = P + a.N;
-        const long long ts = t - tin;  // first tile of this head
+        const long long ts = t - tin;  // unit of the head's first tile
         const int c_first = owner_cta(ts, n, G);
         n_chunks = owner_cta(ts + tb - 1, n, G) - c_first + 1;
         slot = ((int)blockIdx.x == c_first) ? 1 : 0;
@@ -281,29 +290,36 @@ template <typename S> struct RangeWalk {
         if (tin == 0) a.seg[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
     }
 
+    // pre[b] = units of sequences 0..b-1 per head (a head of sequence b has
+    // pre[b+1] - pre[b] units, kPieceUnits of them overhead, or 0 if empty).
     __device__ __forceinline__ void start(const AttnArgs &a, const int *pre, const int *pl, long long lo,
                                           long long hi_, long long n_, long long G_)
     {
         policy = l2_evict_first_policy();
         HR = a.H_kv * a.n_rowblocks;
-        t = lo;
         hi = hi_;
         n = n_;
         G = G_;
         ended = false;
         piece_start = true;
-        if (t >= hi) return;
-        int lo_b = 0, hi_b = a.B - 1;  // last b with pre[b] * HR <= t
+        if (lo >= hi) {
+            t = hi;
+            return;
+        }
+        int lo_b = 0, hi_b = a.B - 1;  // last b with pre[b] * HR <= lo
         while (lo_b < hi_b) {
             const int mid = (lo_b + hi_b + 1) / 2;
-            if ((long long)pre[mid] * HR <= t) lo_b = mid; else hi_b = mid - 1;
+            if ((long long)pre[mid] * HR <= lo) lo_b = mid; else hi_b = mid - 1;
         }
         b = lo_b;
-        tb = pre[b + 1] - pre[b];
-        const long long local = t - (long long)pre[b] * HR;
-        hr = (int)(local / tb);
-        tin = (int)(local % tb);
-        enter_head(a, pl);
+        const int ub = pre[b + 1] - pre[b];
+        tb = ub - S::kPieceUnits;
+        const long long local = lo - (long long)pre[b] * HR;
+        hr = (int)(local / ub);
+        const int off = (int)(local % ub);
+        tin = max(0, off - S::kPieceUnits);
+        t = (long long)pre[b] * HR + (long long)hr * ub + S::kPieceUnits + tin;
+        if (t < hi) enter_head(a, pl);
     }
 
     // Describe and load the next tile into slot s, or mark the end of work.
@@ -337,7 +353,8 @@ template <typename S> struct RangeWalk {
         bulk_load_g2s(dst + S::kTileBytes, vg + off, bytes, &full[s], policy);
         if (qbytes) bulk_load_g2s(smem + S::kQOff + s * S::kQSlotBytes, qg, qbytes, &full[s], policy);
 
-        // advance to the next tile of the flattened list
+        // advance to the next tile of the flattened list (skipping the next
+        // head's overhead units)
         ++t;
         piece_start = false;
         if (++tin == tb) {
@@ -348,8 +365,9 @@ template <typename S> struct RangeWalk {
                 do {
                     ++b;
                 } while (b < a.B && pre[b + 1] == pre[b]);
-                if (b < a.B) tb = pre[b + 1] - pre[b];
+                if (b < a.B) tb = pre[b + 1] - pre[b] - S::kPieceUnits;
             }
+            t += S::kPieceUnits;
             if (t < hi) enter_head(a, pl);
         }
     }
@@ -366,7 +384,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBarOff);
     uint64_t *empty = full + S::kStages;
     TileMeta *meta = reinterpret_cast<TileMeta *>(smem + S::kMetaOff);
-    int *pre = reinterpret_cast<int *>(smem + S::kFixedBytes);  // [B + 1] tile prefix per head
+    int *pre = reinterpret_cast<int *>(smem + S::kFixedBytes);  // [B + 1] unit prefix per head
     int *pl = pre + a.B + 1;                                     // [B] history lengths
 
     const int tid = threadIdx.x;
@@ -384,7 +402,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     // Every input may come from the previous kernel on the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // ---- tiles per sequence and their prefix sum (block-wide scan) ----
+    // ---- units per sequence-head and their prefix sum over sequences (block-wide scan) ----
     {
         int *scan = reinterpret_cast<int *>(smem + S::kEpiOff);
         const int per = (a.B + S::kThreads - 1) / S::kThreads;
@@ -394,10 +412,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
             const int P = __ldg(a.past_len + b);
             const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
             if (!ok && blockIdx.x == 0) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
-            const int tiles = ok ? (P + a.N + S::kTK - 1) / S::kTK : 0;
+            const int units = ok ? (P + a.N + S::kTK - 1) / S::kTK + S::kPieceUnits : 0;
             pl[b] = P;
-            pre[b + 1] = tiles;
-            local += tiles;
+            pre[b + 1] = units;
+            local += units;
         }
         scan[tid] = local;
         __syncthreads();
