@@ -290,14 +290,20 @@ def run_gpu(args, w, rank, world, local):
     ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, w.torch_dtype, dev)
     plan = kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, w.torch_dtype)
     merge = plan["launches"] == 2
-    launches_per_layer = 1 + plan["launches"]
+    launches_per_layer = plan["launches"] + (0 if args.path == "fused" else 1)
+
+    fused = args.path == "fused"
 
     def layer_step(l):
         x = layers[l]
         # the current stream: the capture stream inside torch.cuda.graph
-        kvd.kvd_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past, err)
-        kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past, 0.0, ws,
-                                 err)
+        if fused:
+            kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l], past_d,
+                                max_past, 0.0, ws, err)
+        else:
+            kvd.kvd_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past, err)
+            kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past, 0.0, ws,
+                                     err)
 
     def step():
         for l in range(w.L):
@@ -325,8 +331,12 @@ def run_gpu(args, w, rank, world, local):
     with torch.cuda.graph(attn_graph):
         for l in range(w.L):
             x = layers[l]
-            kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past, 0.0,
-                                     ws, err)
+            if fused:  # the dominant kernel is the fused step itself
+                kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l],
+                                    past_d, max_past, 0.0, ws, err)
+            else:
+                kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past, 0.0,
+                                         ws, err)
     graph_stream = torch.cuda.current_stream()
     for _ in range(2):
         step_graph.replay()
@@ -395,7 +405,7 @@ def run_gpu(args, w, rank, world, local):
     gbs = whole_job_gbs(bytes_step, args.steps, elapsed_max, world)
     ms_step = elapsed_max / args.steps * 1e3
     peak, peak_kind = measured_peak()
-    a_bytes = attn_bytes(w, past.tolist())
+    a_bytes = layer_bytes(w, past.tolist()) if fused else attn_bytes(w, past.tolist())
     achieved = a_bytes / attn_per_launch / 1e9
 
     # CPU baseline: the oracle on layer 0's data, all host cores, ~10 s
@@ -420,7 +430,8 @@ def run_gpu(args, w, rank, world, local):
             "workload": w.name, "describe": w.describe(), "layers": w.L, "B": w.B, "H_q": w.H_q,
             "H_kv": w.H_kv, "D": w.D, "N": w.N, "T_max": w.T_max,
             "P": (w.P if w.P is not None else f"U[{w.P_range[0]},{w.P_range[1]}] seeded, sum {int(past.sum())}"),
-            "step": f"{w.L} x (kvd_append + kvd_decode_attention) on one stream, one CUDA graph per step",
+            "step": (f"{w.L} x kvd_decode_step (append + attention in one launch)" if fused else
+                     f"{w.L} x (kvd_append + kvd_decode_attention)") + " on one stream, one CUDA graph per step",
             "l2": f"no flush: inputs larger than L2 ({bytes_step / 1e9:.1f} GB per step)"
             if bytes_step > 2 * 126e6 else "warm L2 (inputs smaller than L2)",
             "parallelism": f"replicas x{world}",
@@ -428,10 +439,12 @@ def run_gpu(args, w, rank, world, local):
         "us_per_layer_step": round(ms_step * 1e3 / w.L, 3),
         "frac_of_peak": round(gbs / world / peak, 4),
         "attn_us_per_layer": round(attn_per_launch * 1e6, 3),
+        "path": args.path,
         "roofline": {
             "bound": "hbm",
-            "kernel": "kvd_decode_attention (persistent split-T kernel + LSE merge)" if merge else "kvd_decode_attention",
-            "timing": "graph of the L attention calls replayed K times, CUDA events on its stream",
+            "kernel": ("kvd_decode_step (fused append + split-T attention" if fused else
+                       "kvd_decode_attention (split-T attention") + (" + LSE merge)" if merge else ")"),
+            "timing": "graph of the L calls replayed K times, CUDA events on its stream",
             "achieved": round(achieved, 2),
             "peak": peak,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy burst)" if peak_kind == "measured" else "fallback",
@@ -465,6 +478,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--n-new", type=int, default=None, help="override N (chunked decode sweep)")
     ap.add_argument("--impl", default="kvd", choices=["kvd", "reference"])
+    ap.add_argument("--path", default="fused", choices=["fused", "separate"],
+                    help="fused: kvd_decode_step per layer; separate: kvd_append + kvd_decode_attention")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -126,6 +126,27 @@ kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *
                                 uint32_t *err_word, void *stream);
 
 /*
+ * kvd_decode_step -- kvd_append followed by kvd_decode_attention, in one
+ * launch (the layer step of a decode iteration).
+ *
+ * Same result as calling kvd_append(k_cache, v_cache, k_new, v_new, past_len,
+ * ...) and then kvd_decode_attention(q, k_cache, v_cache, out, past_len, ...)
+ * with the same pre-append past_len: afterwards the cache slots P..P+N-1 of
+ * every valid sequence hold k_new / v_new and out holds the attention of the
+ * new rows.  The tile holding a sequence's new keys takes them from k_new /
+ * v_new directly and writes them to their cache slots from shared memory, so
+ * no separate append pass runs.  Arguments are those of the two calls;
+ * workspace as for kvd_decode_attention (kvd_decode_workspace_bytes).
+ * Sequences with an out-of-range past_len are skipped entirely (no cache write,
+ * no output) and flagged with KVD_DEVERR_PAST_LEN.
+ */
+kvd_status kvd_decode_step(const void *q, void *k_cache, void *v_cache, const void *k_new,
+                           const void *v_new, void *out, const int32_t *past_len, int B, int H_q,
+                           int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                           kvd_dtype dtype, void *workspace, size_t workspace_bytes,
+                           uint32_t *err_word, void *stream);
+
+/*
  * kvd_decode_plan -- how kvd_decode_attention would run these shapes on the
  * current device, without launching anything: keys per tile, the most tiles
  * one sequence-head can have (from max_past_len + N), the persistent grid

@@ -160,7 +160,12 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     int dev = 0, sms = 0, occ = 0;
     if ((st = current_device(&dev)) != KVD_OK) return st;
     if ((st = sm_count(dev, &sms)) != KVD_OK) return st;
+    // The attention and the fused-step kernels share the plan (and so the
+    // workspace layout): size the grid for the one with the lower occupancy.
+    int occ_fused = 0;
     if ((st = occupancy(dev, pl->v.fn, pl->v.threads, pl->smem, &occ)) != KVD_OK) return st;
+    if ((st = occupancy(dev, pl->v.fused_fn, pl->v.threads, pl->smem, &occ_fused)) != KVD_OK) return st;
+    if (occ_fused < occ) occ = occ_fused;
 
     // One CTA per resident slot; each takes an equal share of all tiles.  A
     // sequence-head longer than one tile may span CTAs, so the merge runs.
@@ -256,11 +261,15 @@ kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_
     return KVD_OK;
 }
 
-kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *v_cache,
-                                void *out, const int32_t *past_len, int B, int H_q, int H_kv,
-                                int T_max, int D, int N, int max_past_len, float scale,
-                                kvd_dtype dtype, void *workspace, size_t workspace_bytes,
-                                uint32_t *err_word, void *stream)
+}  // extern "C"
+
+namespace {
+
+// Attention (k_new == v_new == null) or the fused step (append inside).
+kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache, const void *k_new,
+                         const void *v_new, void *out, const int32_t *past_len, int B, int H_q, int H_kv,
+                         int T_max, int D, int N, int max_past_len, float scale, kvd_dtype dtype,
+                         void *workspace, size_t workspace_bytes, uint32_t *err_word, void *stream)
 {
     if (!q || !k_cache || !v_cache || !out || !past_len) return KVD_ERR_INVALID_ARG;
     kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
@@ -284,6 +293,8 @@ kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *
     a.v_cache = v_cache;
     a.out = out;
     a.past_len = past_len;
+    a.k_new = k_new;
+    a.v_new = v_new;
     a.part_o = reinterpret_cast<float *>(ws + pl.part_o_off);
     a.part_ml = reinterpret_cast<float *>(ws + pl.part_ml_off);
     a.seg = reinterpret_cast<int2 *>(ws + pl.seg_off);
@@ -313,7 +324,8 @@ kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *
     cfg.gridDim = dim3((unsigned)pl.grid);
     cfg.blockDim = dim3(pl.v.threads);
     cfg.dynamicSmemBytes = (size_t)pl.smem;
-    if (cudaLaunchKernelExC(&cfg, pl.v.fn, args) != cudaSuccess) return KVD_ERR_CUDA;
+    if (cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.fused_fn : pl.v.fn, args) != cudaSuccess)
+        return KVD_ERR_CUDA;
     if (pl.launches == 2) {
         const long long warps = (long long)B * H_kv * pl.n_rowblocks * pl.rb;
         cfg.gridDim = dim3((unsigned)((warps * 32 + 127) / 128));
@@ -322,6 +334,32 @@ kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *
         if (cudaLaunchKernelExC(&cfg, pl.v.merge_fn, args) != cudaSuccess) return KVD_ERR_CUDA;
     }
     return KVD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                void *out, const int32_t *past_len, int B, int H_q, int H_kv,
+                                int T_max, int D, int N, int max_past_len, float scale,
+                                kvd_dtype dtype, void *workspace, size_t workspace_bytes,
+                                uint32_t *err_word, void *stream)
+{
+    return decode_launch(q, k_cache, v_cache, nullptr, nullptr, out, past_len, B, H_q, H_kv, T_max, D, N,
+                         max_past_len, scale, dtype, workspace, workspace_bytes, err_word, stream);
+}
+
+kvd_status kvd_decode_step(const void *q, void *k_cache, void *v_cache, const void *k_new,
+                           const void *v_new, void *out, const int32_t *past_len, int B, int H_q,
+                           int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                           kvd_dtype dtype, void *workspace, size_t workspace_bytes,
+                           uint32_t *err_word, void *stream)
+{
+    if (!k_new || !v_new) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return KVD_ERR_INVALID_ARG;
+    return decode_launch(q, k_cache, v_cache, k_new, v_new, out, past_len, B, H_q, H_kv, T_max, D, N,
+                         max_past_len, scale, dtype, workspace, workspace_bytes, err_word, stream);
 }
 
 kvd_status kvd_workspace_init(void *workspace, size_t workspace_bytes, void *stream)

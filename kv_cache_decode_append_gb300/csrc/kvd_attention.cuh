@@ -59,6 +59,8 @@ struct AttnArgs {
     const void *v_cache;     // [B, H_kv, T_max, D]
     void *out;               // [B, H_q, N, D]
     const int32_t *past_len; // [B]
+    const void *k_new;       // [B, H_kv, N, D]: fused step only (append inside)
+    const void *v_new;       // [B, H_kv, N, D]: fused step only
     float *part_o;           // [grid][2][RB][D]  piece partials (unnormalised)
     float *part_ml;          // [grid][2][RB][2]  (max in log2 units, sum)
     int2 *seg;               // [B*H_kv*n_rowblocks]: (first CTA, CTAs) of each sequence-head
@@ -129,12 +131,18 @@ constexpr int kMetaEnd = 4;    // no more work
 // q, K, V and the accumulators are held as fp32 pairs (E/2 per row) and
 // multiplied with packed f32x2 FMAs; a score is the sum of its even and odd
 // partial dot products.
-template <typename T, int D, int RB, bool kMasked>
+// In a fused step (kFused) the new keys P..P+N-1 are not in the cache yet: in
+// the tiles that hold them (always on the masked path) their K/V rows are read
+// from k_new / v_new (kn, vn: the rows of this (b, h)) and, when kc / vc are
+// given, written to their cache slots by the lanes that read them.
+template <typename T, int D, int RB, bool kMasked, bool kFused>
 __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigned char *Vs,
                                           const f32x2 (&qv)[RB][AttnShape<T, D, RB>::kE / 2],
                                           f32x2 (&o)[RB][AttnShape<T, D, RB>::kE / 2], float (&m_run)[RB],
                                           float (&l_run)[RB], int warp, int grp, int j,
-                                          int tile_k0, const int (&lim)[RB], int k_end)
+                                          int tile_k0, const int (&lim)[RB], int k_end, int P,
+                                          const unsigned char *kn, const unsigned char *vn,
+                                          unsigned char *kc, unsigned char *vc)
 {
     using S = AttnShape<T, D, RB>;
     using Ty = Elem<T>;
@@ -149,6 +157,20 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
 #pragma unroll
     for (int u = 0; u < S::kKpg; ++u) {
         const int kk = warp * S::kKpw + u * S::kGpw + grp;
+        if constexpr (kMasked && kFused) {
+            const int key = tile_k0 + kk;
+            if (key >= P && key < k_end) {
+                const unsigned char *src = kn + (size_t)(key - P) * S::kRowBytes;
+#pragma unroll
+                for (int c = 0; c < S::kCpl; ++c) raw[u][c] = ldg128_nc(src + (c * S::kL + j) * 16);
+                if (kc != nullptr) {
+#pragma unroll
+                    for (int c = 0; c < S::kCpl; ++c)
+                        stg128(kc + (size_t)key * S::kRowBytes + (c * S::kL + j) * 16, raw[u][c]);
+                }
+                continue;
+            }
+        }
 #pragma unroll
         for (int c = 0; c < S::kCpl; ++c)
             raw[u][c] = lds128(Ks + kk * S::kRowBytes + (c * S::kL + j) * 16);
@@ -212,6 +234,20 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
 #pragma unroll
     for (int u = 0; u < S::kKpg; ++u) {
         const int kk = warp * S::kKpw + u * S::kGpw + grp;
+        if constexpr (kMasked && kFused) {
+            const int key = tile_k0 + kk;
+            if (key >= P && key < k_end) {
+                const unsigned char *src = vn + (size_t)(key - P) * S::kRowBytes;
+#pragma unroll
+                for (int c = 0; c < S::kCpl; ++c) raw[u][c] = ldg128_nc(src + (c * S::kL + j) * 16);
+                if (vc != nullptr) {
+#pragma unroll
+                    for (int c = 0; c < S::kCpl; ++c)
+                        stg128(vc + (size_t)key * S::kRowBytes + (c * S::kL + j) * 16, raw[u][c]);
+                }
+                continue;
+            }
+        }
 #pragma unroll
         for (int c = 0; c < S::kCpl; ++c)
             raw[u][c] = lds128(Vs + kk * S::kRowBytes + (c * S::kL + j) * 16);
@@ -373,7 +409,7 @@ template <typename S> struct RangeWalk {
     }
 };
 
-template <typename T, int D, int RB>
+template <typename T, int D, int RB, bool kFused>
 __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     attn_balanced_kernel(const AttnArgs a)
 {
@@ -515,10 +551,26 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
         }
 
         const int k_end = mt.tile_k0 + mt.nk;
-        if (mt.tile_k0 + S::kTK <= mt.P + 1) {
-            attn_tile<T, D, RB, false>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim, k_end);
+        // Tiles below every row's limit (and, in a fused step, below the new
+        // keys) take the unmasked path; the rest the masked one.
+        if (mt.tile_k0 + S::kTK <= mt.P + (kFused ? 0 : 1)) {
+            attn_tile<T, D, RB, false, kFused>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim, k_end,
+                                               mt.P, nullptr, nullptr, nullptr, nullptr);
         } else {
-            attn_tile<T, D, RB, true>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim, k_end);
+            const unsigned char *kn = nullptr, *vn = nullptr;
+            unsigned char *kc = nullptr, *vc = nullptr;
+            if constexpr (kFused) {
+                const size_t nrow = (size_t)mt.bh * a.N * S::kRowBytes;
+                kn = static_cast<const unsigned char *>(a.k_new) + nrow;
+                vn = static_cast<const unsigned char *>(a.v_new) + nrow;
+                if (mt.rb == 0) {  // one row block writes the new rows into the cache
+                    const size_t crow = (size_t)mt.bh * a.T_max * S::kRowBytes;
+                    kc = static_cast<unsigned char *>(const_cast<void *>(a.k_cache)) + crow;
+                    vc = static_cast<unsigned char *>(const_cast<void *>(a.v_cache)) + crow;
+                }
+            }
+            attn_tile<T, D, RB, true, kFused>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim, k_end,
+                                              mt.P, kn, vn, kc, vc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with slot s
@@ -687,7 +739,8 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
 
 // Launch facts of one compiled variant, for the host planner.
 struct AttnVariant {
-    const void *fn;
+    const void *fn;        // attention over an appended cache
+    const void *fused_fn;  // append + attention (kvd_decode_step)
     const void *merge_fn;
     int threads;
     int fixed_smem_bytes;  // plus (2B + 1) ints, rounded to 16 bytes
@@ -699,7 +752,8 @@ template <typename T, int D, int RB> AttnVariant make_variant()
 {
     using S = AttnShape<T, D, RB>;
     AttnVariant v;
-    v.fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB>);
+    v.fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false>);
+    v.fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true>);
     v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, RB>);
     v.threads = S::kThreads;
     v.fixed_smem_bytes = S::kFixedBytes;

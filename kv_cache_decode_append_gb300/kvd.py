@@ -65,6 +65,9 @@ class _Lib:
         lib.kvd_decode_attention.restype = ci
         lib.kvd_decode_attention.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
                                              vp, sz, u32p, vp]
+        lib.kvd_decode_step.restype = ci
+        lib.kvd_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
+                                        vp, sz, u32p, vp]
         lib.kvd_decode_attention_noalloc.restype = ci
         lib.kvd_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
                                                      ci, u32p, vp]
@@ -214,6 +217,31 @@ def kvd_decode_attention(q, k_cache, v_cache, out, past_len, max_past_len: int, 
                                   float(scale), _dtype_code(q), ws_ptr, ws_bytes, _ptr(err_word),
                                   _stream_handle(stream))
     _check("kvd_decode_attention", st)
+
+
+def kvd_decode_step(q, k_cache, v_cache, k_new, v_new, out, past_len, max_past_len: int,
+                    scale: float = 0.0, workspace: Optional[torch.Tensor] = None, err_word=None,
+                    stream=None) -> None:
+    """Append ``k_new``/``v_new`` and attend the new rows of ``q`` in one launch."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new),
+                 ("v_new", v_new), ("out", out)):
+        _need_cuda(n, t, q.dtype)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_q, N, D = q.shape
+    _, H_kv, T_max, _ = k_cache.shape
+    if (out.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B
+            or k_cache.shape[3] != D or tuple(k_new.shape) != (B, H_kv, N, D) or v_new.shape != k_new.shape):
+        raise ValueError("shape mismatch between q, out, the caches and the new K/V")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = raw.kvd_decode_step(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
+                             v_new.data_ptr(), out.data_ptr(), past_len.data_ptr(), B, H_q, H_kv, T_max, D,
+                             N, int(max_past_len), float(scale), _dtype_code(q), ws_ptr, ws_bytes,
+                             _ptr(err_word), _stream_handle(stream))
+    _check("kvd_decode_step", st)
 
 
 def kvd_decode_attention_noalloc(q, k_cache, v_cache, out, past_len, max_past_len: int,

@@ -2,7 +2,8 @@
 
     python -m kv_cache_decode_append_gb300.profile_case --workload gqa_longctx_b32_bf16 --launches 3
 
-Each launch is one kvd_append + kvd_decode_attention on the same layer, so a
+Each launch is one kvd_append + kvd_decode_attention (or, with --fused, one
+kvd_decode_step) on the same layer, so a
 profiler filtered on a kernel name sees ``--launches`` identical launches with
 the full-size per-layer working set (for the default workload 2 x 545 MB of
 cache, larger than L2) and nothing else on the device.
@@ -22,6 +23,7 @@ def main():
     ap.add_argument("--workload", default="gqa_longctx_b32_bf16", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--n-new", type=int, default=None)
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--fused", action="store_true", help="kvd_decode_step instead of append + attention")
     args = ap.parse_args()
     w = wl.WORKLOADS[args.workload]
     if args.n_new is not None:
@@ -35,8 +37,12 @@ def main():
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, w.torch_dtype, dev)
     for _ in range(args.launches):
-        kvd.kvd_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past, err)
-        kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], out, past_d, max_past, 0.0, ws, err)
+        if args.fused:
+            kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], out, past_d,
+                                max_past, 0.0, ws, err)
+        else:
+            kvd.kvd_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past, err)
+            kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], out, past_d, max_past, 0.0, ws, err)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise SystemExit(f"device error word {int(err.item())}")
