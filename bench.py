@@ -41,7 +41,7 @@ from kv_cache_decode_append_gb300 import workloads as wl  # noqa: E402
 METRIC = "decode attention: achieved HBM GB/s (% of GB300 peak) and μs per layer-step"
 DEFAULT_WORKLOAD = "gqa_longctx_b32_bf16"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_attention_gqa_longctx_b32.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_step_gqa_longctx_b32.md")
 
 
 # ---------------------------------------------------------------------------------
