@@ -215,7 +215,7 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
 #pragma unroll
         for (int u = 1; u < S::kKpg; ++u) mt = fmaxf(mt, sc[u][r]);
         if (mt > m_run[r] + kRescaleThreshold) {
-            const float alpha = exp2f(m_run[r] - mt);
+            const float alpha = fast_exp2(m_run[r] - mt);
             l_run[r] *= alpha;
             const f32x2 alpha2 = pack2(alpha, alpha);
 #pragma unroll
@@ -225,7 +225,7 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
         const float mu = (m_run[r] == kNegInf) ? 0.f : m_run[r];
 #pragma unroll
         for (int u = 0; u < S::kKpg; ++u) {
-            const float p = exp2f(sc[u][r] - mu);
+            const float p = fast_exp2(sc[u][r] - mu);
             l_run[r] += p;
             p2[u][r] = pack2(p, p);
         }

@@ -93,6 +93,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz.f32, one MUFU op).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // L2 policy for data that is read exactly once (K/V streams).
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
 {
