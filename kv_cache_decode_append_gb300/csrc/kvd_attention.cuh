@@ -91,9 +91,10 @@ template <typename T, int D, int RB> struct AttnShape {
     static constexpr int kTileBytes = kTK * kRowBytes; // one of K or V
     static constexpr int kStages = (2 * kTileBytes <= 16384) ? 4 : 3;
     static constexpr int kQSlotBytes = RB * kRowBytes;
-    // Cost of a piece boundary in tile units for the static split (measured:
-    // a boundary costs about as much as streaming 96 KB of K/V per CTA).
-    static constexpr int kPieceUnits = (96 * 1024 / (2 * kTileBytes)) > 1 ? (96 * 1024 / (2 * kTileBytes)) : 1;
+    // Cost of a piece boundary in tile units for the static split (a sweep
+    // over 0..8 on GB300 put the best at 2 for both the 32 KB tiles of D=128
+    // bf16 and the 16 KB tiles of D=64 bf16).
+    static constexpr int kPieceUnits = 2;
 
     // shared memory layout (bytes); the per-sequence tables follow kFixedBytes
     static constexpr int kRingOff = 0;
