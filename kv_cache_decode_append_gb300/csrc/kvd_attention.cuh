@@ -438,56 +438,48 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     }
     // Every input may come from the previous kernel on the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncthreads();  // barrier initialisation visible to every thread
 
-    // ---- units per sequence-head and their prefix sum over sequences (block-wide scan) ----
-    {
-        int *scan = reinterpret_cast<int *>(smem + S::kEpiOff);
-        const int per = (a.B + S::kThreads - 1) / S::kThreads;
-        const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
-        int local = 0;
-        for (int b = b0; b < b1; ++b) {
-            const int P = __ldg(a.past_len + b);
-            const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
-            if (!ok && blockIdx.x == 0) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
-            const int units = ok ? (P + a.N + S::kTK - 1) / S::kTK + S::kPieceUnits : 0;
-            pl[b] = P;
-            pre[b + 1] = units;
-            local += units;
-        }
-        scan[tid] = local;
-        __syncthreads();
-        if (tid == 0) {
-            int run = 0;
-            for (int i = 0; i < S::kThreads; ++i) {
-                const int v = scan[i];
-                scan[i] = run;
-                run += v;
-            }
-            pre[0] = 0;
-        }
-        __syncthreads();
-        int run = scan[tid];
-        for (int b = b0; b < b1; ++b) {
-            run += pre[b + 1];
-            pre[b + 1] = run;
-        }
-        __syncthreads();
-    }
-    const int HR = a.H_kv * a.n_rowblocks;
-    const long long n_total = (long long)pre[a.B] * HR;
-    const long long G = min((long long)gridDim.x, n_total);  // CTAs that get work
-    const long long lo = blockIdx.x < G ? n_total * blockIdx.x / G : 0;
-    const long long hi = blockIdx.x < G ? n_total * (blockIdx.x + 1) / G : 0;
-
-    // Thread 0 fills the ring; slot s of ring position p is free again once
-    // every warp has released position p - STAGES on empty[s].
+    // Warp 0 forms the unit prefix over sequences and thread 0 starts the ring
+    // (slot s of ring position p is free again once every warp has released
+    // position p - STAGES on empty[s]); the other warps go straight to
+    // waiting for the first tile.
     RangeWalk<S> walk;  // used by thread 0 only
     int issued = 0;     // ring positions filled so far (thread 0)
-    if (tid == 0) {
-        walk.start(a, pre, pl, lo, hi, n_total, G);
-        for (; issued < S::kStages; ++issued) walk.fill(a, pre, pl, smem, meta, full, issued);
+    if (warp == 0) {
+        // ---- units per sequence-head, prefix-summed over sequences by a warp scan ----
+        int carry = 0;
+        if (lane == 0) pre[0] = 0;
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+            const int b = b0 + lane;
+            int units = 0;
+            if (b < a.B) {
+                const int P = __ldg(a.past_len + b);
+                const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
+                if (!ok && blockIdx.x == 0) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
+                units = ok ? (P + a.N + S::kTK - 1) / S::kTK + S::kPieceUnits : 0;
+                pl[b] = P;
+            }
+            int v = units;  // inclusive scan over the warp
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += n;
+            }
+            if (b < a.B) pre[b + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            const int HR = a.H_kv * a.n_rowblocks;
+            const long long n_total = (long long)pre[a.B] * HR;
+            const long long G = min((long long)gridDim.x, n_total);  // CTAs that get work
+            const long long lo = blockIdx.x < G ? n_total * blockIdx.x / G : 0;
+            const long long hi = blockIdx.x < G ? n_total * (blockIdx.x + 1) / G : 0;
+            walk.start(a, pre, pl, lo, hi, n_total, G);
+            for (; issued < S::kStages; ++issued) walk.fill(a, pre, pl, smem, meta, full, issued);
+        }
     }
-    __syncthreads();
 
     f32x2 qv[RB][S::kE / 2];
     f32x2 o[RB][S::kE / 2];
@@ -496,7 +488,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     bool timed_out = false;
     int first_unwaited = -1;  // first ring position this thread gave up waiting for
 
-    for (int pos = 0; lo < hi; ++pos) {
+    for (int pos = 0;; ++pos) {  // until the end marker
         const int s = pos % S::kStages;
         const uint32_t ph = (uint32_t)(pos / S::kStages) & 1u;
         if (tid == 0) {
