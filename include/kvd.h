@@ -113,7 +113,10 @@ size_t kvd_decode_workspace_bytes(int B, int H_q, int H_kv, int D, int N, int ma
  *   k_cache, v_cache  device, [B, H_kv, T_max, D], already appended
  *   scale             softmax scale; <= 0 selects 1/sqrt(D)
  *   workspace         device scratch of at least kvd_decode_workspace_bytes(...)
- *                     bytes, 256-byte aligned; no initial contents are needed.
+ *                     bytes, 256-byte aligned, zero-filled before its first use
+ *                     (kvd_workspace_init or any zero fill); every complete call
+ *                     leaves it zero-filled again, so it is reused as is.  Zero
+ *                     it again after a call that reported KVD_DEVERR_TIMEOUT.
  *                     Calls that run concurrently need distinct workspaces.
  * Supported: D in {64, 128}; dtype fp32 or bf16; H_q % H_kv == 0;
  * (H_q / H_kv) * N <= 128.
@@ -151,9 +154,10 @@ kvd_status kvd_decode_step(const void *q, void *k_cache, void *v_cache, const vo
  * current device, without launching anything: keys per tile, the most tiles
  * one sequence-head can have (from max_past_len + N), the persistent grid
  * (one CTA per resident slot; each CTA streams an equal share of all tiles)
- * and block, dynamic shared memory, kernels launched per call (2 when a
- * sequence-head can span CTAs and the merge pass runs, else 1) and the
- * workspace size.  Returns the same argument errors as kvd_decode_attention.
+ * and block, dynamic shared memory, kernels launched per call (2 when the
+ * ranges are long and a separate merge pass combines the heads split across
+ * CTAs, else 1: the kernel merges them itself) and the workspace size.
+ * Returns the same argument errors as kvd_decode_attention.
  */
 typedef struct kvd_plan_info {
     int tile_keys;
@@ -189,8 +193,8 @@ kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_
  *     before any stream capture on the device.
  *   - All calls on a device share the one scratch array: calls whose GPU work
  *     can overlap (unordered streams) race and give undefined results.
- *   - The scratch keeps the previous call's contents; no call needs it to
- *     start at zero.
+ *   - The scratch keeps the previous call's contents; each call clears the
+ *     part that must start at zero (its merge counters) before it launches.
  */
 kvd_status kvd_decode_attention_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                         void *out, const int32_t *past_len, int B, int H_q,
@@ -198,8 +202,8 @@ kvd_status kvd_decode_attention_noalloc(const void *q, const void *k_cache, cons
                                         float scale, kvd_dtype dtype, uint32_t *err_word,
                                         void *stream);
 
-/* kvd_workspace_init -- zero-fill a workspace on `stream` (asynchronous); optional,
- * kvd_decode_attention needs no particular initial contents. */
+/* kvd_workspace_init -- zero-fill a workspace on `stream` (asynchronous), as
+ * kvd_decode_attention and kvd_decode_step need before a workspace's first use. */
 kvd_status kvd_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /*

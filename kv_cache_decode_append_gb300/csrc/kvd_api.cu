@@ -69,6 +69,8 @@ OccEntry g_occ[256];
 int g_occ_n = 0;
 
 constexpr int kMaxSmemPerCta = 227 * 1024;
+// Ranges longer than this many tile units per CTA use the separate merge pass.
+constexpr int kLongRangeUnits = 32;
 
 kvd_status current_device(int *dev)
 {
@@ -126,7 +128,8 @@ struct Plan {
     AttnVariant v;
     int rows, rb, n_rowblocks;
     int grid, smem, launches, max_tiles;
-    size_t part_o_off, part_ml_off, seg_off, ws_bytes;
+    bool merge_pass;  // split heads merged by a second launch (else inside the kernel)
+    size_t part_o_off, part_ml_off, tickets_off, seg_off, ws_bytes;
 };
 
 kvd_status check_shapes(int B, int H_q, int H_kv, int D, int N, int max_past_len, kvd_dtype dtype)
@@ -147,9 +150,14 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     pl->rows = (H_q / H_kv) * N;
     pl->rb = pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : pl->rows <= 4 ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
-    const bool ok = dtype == KVD_F32 ? attn_variant_f32(D, pl->rb, &pl->v)
-                                     : attn_variant_bf16(D, pl->rb, &pl->v);
+    // The two builds of the kernels: with the separate merge pass, and
+    // merging split heads themselves (same shared memory layout and tiles).
+    AttnVariant vp, vt;
+    const bool ok = dtype == KVD_F32
+                        ? attn_variant_f32(D, pl->rb, &vp) && attn_variant_f32_tk(D, pl->rb, &vt)
+                        : attn_variant_bf16(D, pl->rb, &vp) && attn_variant_bf16_tk(D, pl->rb, &vt);
     if (!ok) return KVD_ERR_UNSUPPORTED;
+    pl->v = vp;
 
     // Shared memory holds the ring plus two per-sequence tables (B + 1 tile
     // prefix sums, B history lengths).
@@ -160,19 +168,30 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     int dev = 0, sms = 0, occ = 0;
     if ((st = current_device(&dev)) != KVD_OK) return st;
     if ((st = sm_count(dev, &sms)) != KVD_OK) return st;
-    // The attention and the fused-step kernels share the plan (and so the
-    // workspace layout): size the grid for the one with the lower occupancy.
-    int occ_fused = 0;
-    if ((st = occupancy(dev, pl->v.fn, pl->v.threads, pl->smem, &occ)) != KVD_OK) return st;
-    if ((st = occupancy(dev, pl->v.fused_fn, pl->v.threads, pl->smem, &occ_fused)) != KVD_OK) return st;
-    if (occ_fused < occ) occ = occ_fused;
+    // The attention and the fused-step kernels of both builds share the plan
+    // (and so the workspace layout): size the grid for the one with the
+    // lowest occupancy.
+    occ = 1 << 30;
+    for (const void *fn : {vp.fn, vp.fused_fn, vt.fn, vt.fused_fn}) {
+        int o = 0;
+        if ((st = occupancy(dev, fn, pl->v.threads, pl->smem, &o)) != KVD_OK) return st;
+        if (o < occ) occ = o;
+    }
 
-    // One CTA per resident slot; each takes an equal share of all tiles.  A
-    // sequence-head longer than one tile may span CTAs, so the merge runs.
+    // One CTA per resident slot; each takes an equal share of all tiles.
     pl->grid = sms * occ;
     const long long t_hint = (long long)max_past_len + N;
     pl->max_tiles = (int)((t_hint + pl->v.tile_keys - 1) / pl->v.tile_keys);
-    pl->launches = pl->max_tiles > 1 ? 2 : 1;
+    // Heads split across CTAs: merged inside the kernel by the CTA that
+    // finishes a head last, unless the ranges are long (at most
+    // kLongRangeUnits tile units per CTA, counted at max_past_len), where a
+    // second, early-launched merge pass measured faster than the merge at the
+    // tail of the last CTA.
+    const long long units_hint =
+        (long long)B * H_kv * pl->n_rowblocks * (pl->max_tiles + pl->v.piece_units);
+    pl->merge_pass = units_hint > (long long)kLongRangeUnits * pl->grid;
+    pl->launches = pl->merge_pass ? 2 : 1;
+    if (!pl->merge_pass) pl->v = vt;
 
     const size_t pieces = (size_t)pl->grid * 2 * pl->rb;
     size_t off = 0;
@@ -180,8 +199,10 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     off += round_up(pieces * D * sizeof(float), 256);
     pl->part_ml_off = off;
     off += round_up(pieces * 2 * sizeof(float), 256);
+    pl->tickets_off = off;
+    off += round_up((size_t)B * H_kv * pl->n_rowblocks * sizeof(int), 256);
     pl->seg_off = off;
-    off += round_up((size_t)B * H_kv * pl->n_rowblocks * 2 * sizeof(int), 256);
+    off += round_up((size_t)B * H_kv * pl->n_rowblocks * sizeof(int2), 256);
     pl->ws_bytes = off;
     return KVD_OK;
 }
@@ -297,6 +318,7 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     a.v_new = v_new;
     a.part_o = reinterpret_cast<float *>(ws + pl.part_o_off);
     a.part_ml = reinterpret_cast<float *>(ws + pl.part_ml_off);
+    a.tickets = reinterpret_cast<int *>(ws + pl.tickets_off);
     a.seg = reinterpret_cast<int2 *>(ws + pl.seg_off);
     a.err_word = err_word;
     a.B = B;
@@ -326,7 +348,7 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     cfg.dynamicSmemBytes = (size_t)pl.smem;
     if (cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.fused_fn : pl.v.fn, args) != cudaSuccess)
         return KVD_ERR_CUDA;
-    if (pl.launches == 2) {
+    if (pl.merge_pass) {  // one warp per query row of the split heads
         const long long warps = (long long)B * H_kv * pl.n_rowblocks * pl.rb;
         cfg.gridDim = dim3((unsigned)((warps * 32 + 127) / 128));
         cfg.blockDim = dim3(128);

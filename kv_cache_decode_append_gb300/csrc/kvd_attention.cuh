@@ -40,9 +40,20 @@
 //   * where the range leaves a sequence-head the warps merge their groups by
 //     log-sum-exp (shuffles) and then, between two CTA barriers, across warps
 //     (shared memory): the output is written directly when the sequence-head
-//     lies inside one CTA's range, else the piece goes to a partial slot
-//     (a CTA holds at most two: the head it continues and the head it
-//     starts) and attn_merge_kernel combines the pieces.
+//     lies inside one CTA's range, else the piece goes to a partial slot (a
+//     CTA holds at most two: the head it continues and the head it starts);
+//   * the pieces of split heads are merged by log-sum-exp in one of two ways,
+//     chosen per call by the host: (a) in the kernel: after its range, a CTA
+//     counts its pieces on their heads' tickets (one acquire-release atomic
+//     per piece, no waiting) and the CTA that completes a head's count merges
+//     its pieces and resets the ticket to zero; or (b) by attn_merge_kernel, a
+//     second launch that starts early (programmatic dependent launch) and
+//     merges once this grid has finished.  (a) saves the second launch and
+//     wins on short ranges; on long ranges (tens of tiles per CTA) the tail
+//     merge of the last CTA to finish costs more than (b), measured on GB300.
+//     Counting only once the range is done keeps memory fences out of the
+//     streaming phase, where a fence stalled for microseconds behind the
+//     CTA's in-flight bulk copies.
 //
 // Masked slots (past P+i for row i, or past the end of the sequence) never
 // feed the arithmetic: their scores are forced to -inf and value rows past
@@ -64,11 +75,15 @@ struct AttnArgs {
     float *part_o;           // [grid][2][RB][D]  piece partials (unnormalised)
     float *part_ml;          // [grid][2][RB][2]  (max in log2 units, sum)
     int2 *seg;               // [B*H_kv*n_rowblocks]: (first CTA, CTAs) of each sequence-head
+                             // (merge pass only)
+                             // (zero between calls: the merging CTA resets its ticket)
     uint32_t *err_word;
     int B, H_kv, T_max, N, max_past_len;
     int rows;         // query rows per (b, h): (H_q / H_kv) * N, contiguous in q and out
     int n_rowblocks;  // ceil(rows / RB)
     float qscale;     // softmax scale * log2(e)
+    int *tickets;     // [B*H_kv*n_rowblocks]: pieces of a split head counted so far (in-kernel
+                      // merge only; zero between calls: the merging CTA resets its ticket)
 };
 
 // Compile-time shape of one kernel variant.
@@ -104,12 +119,16 @@ template <typename T, int D, int RB> struct AttnShape {
     static constexpr int kEpiBytes = (kEpiFloats > kThreads ? kEpiFloats : kThreads) * 4;
     static constexpr int kMetaOff = kEpiOff + kEpiBytes;
     static constexpr int kBarOff = kMetaOff + kStages * 32;
-    static constexpr int kFixedBytes = kBarOff + 2 * kStages * 8;  // full and empty barriers
+    static constexpr int kJobOff = kBarOff + 2 * kStages * 8;     // after the full and empty barriers
+    static constexpr int kFixedBytes = kJobOff + 32;                // two pieces to count (4 ints each)
 
     static_assert(kRowBytes % 16 == 0, "rows must be whole 16-byte chunks");
     static_assert(kCpl >= 1 && kRowChunks % kL == 0, "lane mapping");
     static_assert(kNW >= 1 && kTK % kKpw == 0, "tile mapping");
     static_assert(kQOff % 128 == 0 && kEpiOff % 16 == 0 && kBarOff % 8 == 0, "alignment");
+    // the merge of a split head borrows the epilogue area (see merge_pieces)
+    static_assert((kThreads >= RB * D ? (kThreads / (RB * D) - 1) * (RB * D + 2 * RB) : 0) * 4 <= kEpiBytes,
+                  "merge scratch");
 };
 
 // Shared-memory bytes of a launch with B sequences: fixed part + tile prefix
@@ -122,7 +141,7 @@ template <typename S> constexpr size_t attn_smem_bytes(int B)
 // Per-stage description written by thread 0, read by every thread.
 struct TileMeta {
     int bh, rb, tile_k0, nk;      // pair, row block, global key index of tile row 0, rows loaded
-    int P, flags, n_chunks, slot; // history, kMeta*, CTAs sharing the head, partial slot
+    int P, flags, n_chunks, c_first; // history, kMeta*, CTAs sharing the head, the first of them
 };
 constexpr int kMetaFirst = 1;  // first tile of a piece: the stage also carries the q rows
 constexpr int kMetaLast = 2;   // last tile of a piece
@@ -297,14 +316,14 @@ __device__ __forceinline__ int owner_cta(long long t, long long n, long long G)
 // CTAs whose range crosses more head starts receive fewer tiles.  Per-head
 // values are computed once when the walk enters a head; a tile only costs a
 // few stores and the bulk copies.
-template <typename S> struct RangeWalk {
+template <typename S, bool kWriteSeg> struct RangeWalk {
     long long t, hi, n, G;  // unit of the next tile, end of range, units in total, working CTAs
     int b, hr, tin, tb;     // sequence, head x row block, tile within the head, its tiles
     int HR;                 // H_kv * n_rowblocks
     bool ended;
     bool piece_start;       // the next tile starts a piece (the head's first tile, or the range's)
     // per-head values
-    int bh, rb, P, T_b, n_chunks, slot, q_bytes;
+    int bh, rb, P, T_b, n_chunks, c_first, q_bytes;
     const unsigned char *kg, *vg, *qg;
     uint64_t policy;
 
@@ -316,15 +335,16 @@ template <typename S> struct RangeWalk {
         P = pl[b];
         T_b = P + a.N;
         const long long ts = t - tin;  // unit of the head's first tile
-        const int c_first = owner_cta(ts, n, G);
+        c_first = owner_cta(ts, n, G);
         n_chunks = owner_cta(ts + tb - 1, n, G) - c_first + 1;
-        slot = ((int)blockIdx.x == c_first) ? 1 : 0;
+        if constexpr (kWriteSeg) {  // the split's shape, for the merge pass
+            if (tin == 0) a.seg[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
+        }
         const size_t row = (size_t)bh * a.T_max;
         kg = static_cast<const unsigned char *>(a.k_cache) + row * S::kRowBytes;
         vg = static_cast<const unsigned char *>(a.v_cache) + row * S::kRowBytes;
         qg = static_cast<const unsigned char *>(a.q) + ((size_t)bh * a.rows + rb * S::kRB) * S::kRowBytes;
         q_bytes = min(S::kRB, a.rows - rb * S::kRB) * S::kRowBytes;
-        if (tin == 0) a.seg[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
     }
 
     // pre[b] = units of sequences 0..b-1 per head (a head of sequence b has
@@ -378,7 +398,7 @@ template <typename S> struct RangeWalk {
         mt.P = P;
         mt.flags = (piece_start ? kMetaFirst : 0) | ((tin == tb - 1 || t == hi - 1) ? kMetaLast : 0);
         mt.n_chunks = n_chunks;
-        mt.slot = slot;
+        mt.c_first = c_first;
         meta[s] = mt;
 
         const uint32_t bytes = (uint32_t)mt.nk * S::kRowBytes;
@@ -410,7 +430,90 @@ template <typename S> struct RangeWalk {
     }
 };
 
-template <typename T, int D, int RB, bool kFused>
+// A piece of a split head this CTA computed, or a head it merges.
+struct MergeJob {
+    int bh, rb, c_first, n_chunks;
+};
+
+// Merge the n_chunks pieces of a split head by log-sum-exp and write its
+// output rows, with every thread of the CTA.  Piece k is CTA c_first + k's
+// partial (slot 1 for k = 0, the head's first CTA, else slot 0).  The pieces
+// are split over kNG thread groups when the head has fewer output elements
+// than the CTA has threads; the groups then combine through scr (shared
+// memory, free on entry and again on return).
+template <typename T, int D, int RB, int kThreads>
+__device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &job, float *scr, int tid)
+{
+    using Ty = Elem<T>;
+    constexpr int kNE = RB * D;                                  // output elements of the head's rows
+    constexpr int kNG = kThreads >= kNE ? kThreads / kNE : 1;    // groups sharing out the pieces
+    constexpr int kPer = kThreads >= kNE ? 1 : kNE / kThreads;   // elements per thread
+    static_assert(kNG * kNE == kThreads || kPer * kThreads == kNE, "merge mapping");
+    const float kNegInf = __int_as_float(0xff800000);
+    const int g = kNG > 1 ? tid / kNE : 0;
+    const int e0 = kNG > 1 ? tid % kNE : tid;
+    float M[kPer], num[kPer], den[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        M[i] = kNegInf;
+        num[i] = 0.f;
+        den[i] = 0.f;
+    }
+    // The loads of a piece do not depend on the running values: each pass
+    // issues all of them before the updates.
+#pragma unroll 2
+    for (int k = g; k < job.n_chunks; k += kNG) {
+        const size_t pb = ((size_t)(job.c_first + k) * 2 + (k == 0)) * RB;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = e0 + i * kThreads, r = e / D, d = e % D;
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + pb + r);
+            const float o_k = __ldcg(a.part_o + (pb + r) * D + d);
+            const float Mn = fmaxf(M[i], ml.x);
+            const float wa = safe_weight(M[i], Mn), wb = safe_weight(ml.x, Mn);
+            num[i] = num[i] * wa + o_k * wb;
+            den[i] = den[i] * wa + ml.y * wb;
+            M[i] = Mn;
+        }
+    }
+    if constexpr (kNG > 1) {
+        // groups 1.. hand their running values to group 0
+        const int r = e0 / D, d = e0 % D;
+        float *s_num = scr, *s_ml = scr + (kNG - 1) * kNE;
+        if (g > 0) {
+            s_num[(g - 1) * kNE + e0] = num[0];
+            if (d == 0) {
+                s_ml[((g - 1) * RB + r) * 2 + 0] = M[0];
+                s_ml[((g - 1) * RB + r) * 2 + 1] = den[0];
+            }
+        }
+        __syncthreads();
+        if (g == 0) {
+#pragma unroll
+            for (int gg = 0; gg < kNG - 1; ++gg) {
+                const float m_g = s_ml[(gg * RB + r) * 2 + 0];
+                const float Mn = fmaxf(M[0], m_g);
+                const float wa = safe_weight(M[0], Mn), wb = safe_weight(m_g, Mn);
+                num[0] = num[0] * wa + s_num[gg * kNE + e0] * wb;
+                den[0] = den[0] * wa + s_ml[(gg * RB + r) * 2 + 1] * wb;
+                M[0] = Mn;
+            }
+        }
+        __syncthreads();
+    }
+    if (g == 0) {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = e0 + i * kThreads, r = e / D, d = e % D;
+            const int rg = job.rb * RB + r;
+            if (rg < a.rows) Ty::store(static_cast<T *>(a.out) + ((size_t)job.bh * a.rows + rg) * D + d, num[i] / den[i]);
+        }
+    }
+}
+
+// kFused: append inside (kvd_decode_step).  kTicketMerge: split heads are
+// merged at the end of this kernel (else by attn_merge_kernel).
+template <typename T, int D, int RB, bool kFused, bool kTicketMerge>
 __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     attn_balanced_kernel(const AttnArgs a)
 {
@@ -421,6 +524,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBarOff);
     uint64_t *empty = full + S::kStages;
     TileMeta *meta = reinterpret_cast<TileMeta *>(smem + S::kMetaOff);
+    MergeJob *jobs = reinterpret_cast<MergeJob *>(smem + S::kJobOff);  // this CTA's split pieces (two at most)
     int *pre = reinterpret_cast<int *>(smem + S::kFixedBytes);  // [B + 1] unit prefix per head
     int *pl = pre + a.B + 1;                                     // [B] history lengths
 
@@ -444,7 +548,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     // (slot s of ring position p is free again once every warp has released
     // position p - STAGES on empty[s]); the other warps go straight to
     // waiting for the first tile.
-    RangeWalk<S> walk;  // used by thread 0 only
+    RangeWalk<S, !kTicketMerge> walk;  // used by thread 0 only
     int issued = 0;     // ring positions filled so far (thread 0)
     if (warp == 0) {
         // ---- units per sequence-head, prefix-summed over sequences by a warp scan ----
@@ -487,6 +591,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     int lim[RB];
     bool timed_out = false;
     int first_unwaited = -1;  // first ring position this thread gave up waiting for
+    int n_pieces = 0;         // split pieces computed so far (two at most)
 
     for (int pos = 0;; ++pos) {  // until the end marker
         const int s = pos % S::kStages;
@@ -629,7 +734,9 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
         }
         __syncthreads();
         const bool single = (mt.n_chunks == 1);
-        const size_t pbase = ((size_t)blockIdx.x * 2 + mt.slot) * RB;
+        // A CTA holds at most two partial pieces: slot 1 for the head it starts
+        // (it is that head's first CTA), slot 0 for the head it continues.
+        const size_t pbase = ((size_t)blockIdx.x * 2 + ((int)blockIdx.x == mt.c_first ? 1 : 0)) * RB;
         for (int idx = tid; idx < RB * D; idx += S::kThreads) {
             const int r = idx / D, d = idx % D;
             const int rg = mt.rb * RB + r;
@@ -654,6 +761,40 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
                 }
             }
         }
+        if constexpr (kTicketMerge) {
+            if (!single) {  // (a range holds at most two split pieces: the head it continues, the head it starts)
+                if (tid == 0 && n_pieces < 2) jobs[n_pieces] = MergeJob{mt.bh, mt.rb, mt.c_first, mt.n_chunks};
+                ++n_pieces;
+            }
+        }
+    }
+
+    if constexpr (kTicketMerge) {
+        // ---- count this CTA's split pieces; merge the heads they complete ----
+        n_pieces = min(n_pieces, 2);
+        __syncthreads();  // every thread's share of the partials is written
+        if (tid == 0 && n_pieces > 0) {
+            // Each count releases this CTA's partials and, for the count that
+            // completes a head, acquires the other CTAs' (acquire-release atomics).
+            int seen[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                if (i < n_pieces) seen[i] = atomic_add_acq_rel_gpu(a.tickets + (size_t)jobs[i].bh * a.n_rowblocks + jobs[i].rb, 1);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                if (i < n_pieces && seen[i] == jobs[i].n_chunks - 1)
+                    a.tickets[(size_t)jobs[i].bh * a.n_rowblocks + jobs[i].rb] = 0;  // the next call starts from zero
+                else
+                    jobs[i].n_chunks = 0;  // another CTA completes this head (or no piece)
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const MergeJob job = jobs[i];
+            if (i < n_pieces && job.n_chunks)
+                merge_pieces<T, D, RB, S::kThreads>(a, job, reinterpret_cast<float *>(smem + S::kEpiOff), tid);
+        }
     }
 
     if (tid == 0 && timed_out && first_unwaited >= 0) {
@@ -666,8 +807,9 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
             }
         }
     }
-    // Let the dependent merge launch; its griddepcontrol.wait still waits for
-    // this whole grid to finish and flush.
+    // Let the next kernel on the stream (the merge pass, or the next call)
+    // launch; its griddepcontrol.wait still waits for this whole grid to
+    // finish and flush.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -734,49 +876,55 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
 struct AttnVariant {
     const void *fn;        // attention over an appended cache
     const void *fused_fn;  // append + attention (kvd_decode_step)
-    const void *merge_fn;
+    const void *merge_fn;  // the separate merge pass
     int threads;
     int fixed_smem_bytes;  // plus (2B + 1) ints, rounded to 16 bytes
     int tile_keys;
     int rows_per_block;
+    int piece_units;       // cost of a piece boundary in tile units
 };
 
-template <typename T, int D, int RB> AttnVariant make_variant()
+template <typename T, int D, int RB, bool kTicketMerge> AttnVariant make_variant()
 {
     using S = AttnShape<T, D, RB>;
     AttnVariant v;
-    v.fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false>);
-    v.fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true>);
-    v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, RB>);
+    v.fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false, kTicketMerge>);
+    v.fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, kTicketMerge>);
+    if constexpr (kTicketMerge) v.merge_fn = nullptr;
+    else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, RB>);
     v.threads = S::kThreads;
     v.fixed_smem_bytes = S::kFixedBytes;
     v.tile_keys = S::kTK;
     v.rows_per_block = RB;
+    v.piece_units = S::kPieceUnits;
     return v;
 }
 
-template <typename T, int D> bool pick_rb(int RB, AttnVariant *v)
+template <typename T, int D, bool kTicketMerge> bool pick_rb(int RB, AttnVariant *v)
 {
     switch (RB) {
-    case 1: *v = make_variant<T, D, 1>(); return true;
-    case 2: *v = make_variant<T, D, 2>(); return true;
-    case 4: *v = make_variant<T, D, 4>(); return true;
-    case 8: *v = make_variant<T, D, 8>(); return true;
+    case 1: *v = make_variant<T, D, 1, kTicketMerge>(); return true;
+    case 2: *v = make_variant<T, D, 2, kTicketMerge>(); return true;
+    case 4: *v = make_variant<T, D, 4, kTicketMerge>(); return true;
+    case 8: *v = make_variant<T, D, 8, kTicketMerge>(); return true;
     default: return false;
     }
 }
 
-template <typename T> bool pick_variant(int D, int RB, AttnVariant *v)
+template <typename T, bool kTicketMerge> bool pick_variant(int D, int RB, AttnVariant *v)
 {
     switch (D) {
-    case 64: return pick_rb<T, 64>(RB, v);
-    case 128: return pick_rb<T, 128>(RB, v);
+    case 64: return pick_rb<T, 64, kTicketMerge>(RB, v);
+    case 128: return pick_rb<T, 128, kTicketMerge>(RB, v);
     default: return false;
     }
 }
 
-// Defined in kvd_attn_f32.cu / kvd_attn_bf16.cu (one translation unit each).
+// One translation unit each: kvd_attn_{f32,bf16}.cu (merge pass) and
+// kvd_attn_{f32,bf16}_tk.cu (in-kernel merge).
 bool attn_variant_f32(int D, int RB, AttnVariant *v);
 bool attn_variant_bf16(int D, int RB, AttnVariant *v);
+bool attn_variant_f32_tk(int D, int RB, AttnVariant *v);
+bool attn_variant_bf16_tk(int D, int RB, AttnVariant *v);
 
 }  // namespace kvd

@@ -1,6 +1,7 @@
-// Instantiates the fp32 decode-attention kernels (D in {64, 128}, RB in {1, 2, 4, 8}).
+// Instantiates the fp32 decode-attention kernels with the separate merge pass
+// (D in {64, 128}, RB in {1, 2, 4, 8}).
 #include "kvd_attention.cuh"
 
 namespace kvd {
-bool attn_variant_f32(int D, int RB, AttnVariant *v) { return pick_variant<float>(D, RB, v); }
+bool attn_variant_f32(int D, int RB, AttnVariant *v) { return pick_variant<float, false>(D, RB, v); }
 }  // namespace kvd

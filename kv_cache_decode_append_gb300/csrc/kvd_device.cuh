@@ -227,6 +227,18 @@ template <> struct Elem<__nv_bfloat16> {
     }
 };
 
+// Atomic add at GPU scope with acquire-release semantics; returns the old
+// value.  Writes that precede it (this thread's, and those it has seen through
+// a CTA barrier) are visible to a thread whose own acquire-release atomic on
+// the same word reads this one's result, and so are that thread's later reads
+// (and, after a CTA barrier, its CTA's).
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void raise_error(uint32_t *err_word, uint32_t bit)
 {
     if (err_word != nullptr) atomicOr(err_word, bit);

@@ -13,9 +13,9 @@
 //     of device memory for it until the process exits;
 //   * all calls on a device share that one array: calls whose GPU work can
 //     overlap (different streams without ordering between them) race on it;
-//   * the array keeps whatever the previous call left in it; nothing in it
-//     has to start at zero, because each call writes every scratch word it
-//     later reads;
+//   * the array keeps whatever the previous call left in it; the part of it
+//     that must start at zero (the counters the kernel uses to merge heads
+//     split across CTAs) is cleared with cudaMemsetAsync before each launch;
 //   * shapes needing more than kNoAllocScratchBytes are rejected with
 //     KVD_ERR_WORKSPACE before anything is launched.
 #include <mutex>
@@ -72,6 +72,10 @@ extern "C" kvd_status kvd_decode_attention_noalloc(const void *q, const void *k_
     void *scratch = nullptr;
     const kvd_status st = noalloc_scratch(&scratch);
     if (st != KVD_OK) return st;
+    // Clear the used part (the kernel needs its merge counters at zero); a
+    // memset allocates nothing.
+    if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KVD_ERR_CUDA;
     return kvd_decode_attention(q, k_cache, v_cache, out, past_len, B, H_q, H_kv, T_max, D, N,
                                 max_past_len, scale, dtype, scratch, kNoAllocScratchBytes, err_word,
                                 stream);

@@ -183,11 +183,11 @@ def kvd_decode_plan(B: int, H_q: int, H_kv: int, D: int, N: int, max_past_len: i
 
 
 def alloc_workspace(B, H_q, H_kv, D, N, max_past_len, dtype, device=None) -> Optional[torch.Tensor]:
-    """A device workspace sized for these shapes (None when none is needed)."""
+    """A zero-filled device workspace sized for these shapes (None when none is needed)."""
     n = kvd_decode_workspace_bytes(B, H_q, H_kv, D, N, max_past_len, dtype)
     if n == 0:
         return None
-    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
 
 
 def kvd_workspace_init(workspace: Optional[torch.Tensor], stream=None) -> None:

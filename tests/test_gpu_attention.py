@@ -190,3 +190,23 @@ def test_repeated_calls_reuse_workspace(orc):
         torch.cuda.synchronize()
         ref = oracle_step(orc, t, past, "bf16")
         assert row_rel_err(out.double().cpu().numpy(), ref) <= TOL["bf16"]
+
+
+# Heads split across CTAs are merged inside the kernel on short ranges and by a
+# second launch on long ones: both ways, on ragged lengths.
+# (B, H_q, H_kv, D, T_max, max_past, launches)
+MERGE_MODES = [
+    (16, 32, 8, 128, 6200, 6100, 2),   # ~40 tile units per CTA: separate merge pass
+    (16, 32, 8, 128, 1100, 1000, 1),   # ~8 tile units per CTA: merged in the kernel
+]
+
+
+@pytest.mark.parametrize("case", MERGE_MODES, ids=["merge_pass", "in_kernel"])
+def test_merge_modes(orc, case):
+    B, H_q, H_kv, D, T_max, max_past, launches = case
+    assert kvd.kvd_decode_plan(B, H_q, H_kv, D, 1, max_past, "bf16")["launches"] == launches
+    gen = torch.Generator().manual_seed(9900 + launches)
+    past = torch.randint(0, max_past + 1, (B,), generator=gen, dtype=torch.int32)
+    past[3] = max_past
+    w = wl.Workload(0, "merge", L=1, B=B, H_q=H_q, H_kv=H_kv, D=D, N=1, dtype="bf16", T_max=T_max, P=0)
+    check(orc, w, past, seed_base=9910 + launches)

@@ -88,11 +88,11 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row(c_entry):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(c_entry):
-    # 4096 sequences x 128 KV heads need more than the built-in 4 MiB.
+    # 8192 sequences x 128 KV heads need more than the built-in 4 MiB.
     q = torch.zeros(64, dtype=torch.bfloat16, device=DEV)
-    past = torch.zeros(4096, dtype=torch.int32, device=DEV)
-    need = kvd.kvd_decode_workspace_bytes(4096, 128, 128, 128, 1, 10, "bf16")
+    past = torch.zeros(8192, dtype=torch.int32, device=DEV)
+    need = kvd.kvd_decode_workspace_bytes(8192, 128, 128, 128, 1, 10, "bf16")
     assert need > 4 << 20
     st = c_entry(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), past.data_ptr(),
-                 4096, 128, 128, 16, 128, 1, 10, 0.0, kvd.KVD_BF16, None, None)
+                 8192, 128, 128, 16, 128, 1, 10, 0.0, kvd.KVD_BF16, None, None)
     assert st == kvd.KVD_ERR_WORKSPACE
