@@ -62,6 +62,11 @@ class Oracle:
         lib.oracle_append.argtypes = [vp, vp, vp, vp, i32p, ci, ci, ci, ci, ci, ci]
         lib.oracle_decode_attention.restype = ci
         lib.oracle_decode_attention.argtypes = [vp, vp, vp, dp, i32p, ci, ci, ci, ci, ci, ci, cd, ci]
+        lib.oracle_paged_append.restype = ci
+        lib.oracle_paged_append.argtypes = [vp, vp, vp, vp, i32p, i32p, ci, ci, ci, ci, ci, ci, ci, ci]
+        lib.oracle_paged_decode_attention.restype = ci
+        lib.oracle_paged_decode_attention.argtypes = [vp, vp, vp, dp, i32p, i32p, ci, ci, ci, ci, ci, ci,
+                                                      ci, ci, cd, ci]
         lib.oracle_full_causal_attention.restype = ci
         lib.oracle_full_causal_attention.argtypes = [dp, dp, dp, dp, ci, ci, cd]
         self.lib = lib
@@ -115,6 +120,43 @@ class Oracle:
             out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
             past_len.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
             B, H_q, H_kv, T_max, D, N, float(scale), _DTYPES[dtype])
+        return out, int(st)
+
+    def paged_append(self, k_pages, v_pages, k_new, v_new, block_table, past_len, dtype: str) -> int:
+        """In place on ``k_pages``/``v_pages`` ([num_pages,H_kv,page_size,D]); returns the status."""
+        for a, n in ((k_pages, "k_pages"), (v_pages, "v_pages"), (k_new, "k_new"), (v_new, "v_new")):
+            self._check(a, dtype, n)
+        past_len = np.ascontiguousarray(past_len, dtype=np.int32)
+        block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+        num_pages, H_kv, page_size, D = k_pages.shape
+        B, max_pages = block_table.shape
+        N = k_new.shape[2]
+        if v_pages.shape != k_pages.shape or k_new.shape != (B, H_kv, N, D) or v_new.shape != k_new.shape:
+            raise ValueError("shape mismatch")
+        i32 = ctypes.POINTER(ctypes.c_int32)
+        return int(self.lib.oracle_paged_append(
+            k_pages.ctypes.data, v_pages.ctypes.data, k_new.ctypes.data, v_new.ctypes.data,
+            block_table.ctypes.data_as(i32), past_len.ctypes.data_as(i32),
+            B, H_kv, D, N, page_size, max_pages, num_pages, _DTYPES[dtype]))
+
+    def paged_decode_attention(self, q, k_pages, v_pages, block_table, past_len, dtype: str, scale=None):
+        """Returns ``(out float64 [B,H_q,N,D], status)`` for an already-appended paged cache."""
+        for a, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
+            self._check(a, dtype, n)
+        past_len = np.ascontiguousarray(past_len, dtype=np.int32)
+        block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+        B, H_q, N, D = q.shape
+        num_pages, H_kv, page_size, _ = k_pages.shape
+        max_pages = block_table.shape[1]
+        if scale is None:
+            scale = 1.0 / np.sqrt(D)
+        out = np.empty((B, H_q, N, D), dtype=np.float64)
+        i32 = ctypes.POINTER(ctypes.c_int32)
+        st = self.lib.oracle_paged_decode_attention(
+            q.ctypes.data, k_pages.ctypes.data, v_pages.ctypes.data,
+            out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+            block_table.ctypes.data_as(i32), past_len.ctypes.data_as(i32),
+            B, H_q, H_kv, D, N, page_size, max_pages, num_pages, float(scale), _DTYPES[dtype])
         return out, int(st)
 
     def full_causal_attention(self, qf, kf, vf, scale):

@@ -30,6 +30,19 @@
  *                             "Decode 单步到底在算什么";
  *                             openai-hub.com/news/2435, section
  *                             "一个很容易漏掉的错误", the offset-mask paragraph]
+ *   oracle_paged_append, oracle_paged_decode_attention
+ *                            the same two operations on a paged cache: the
+ *                            tokens of a sequence live in fixed-size pages
+ *                            found through a per-sequence block table, and
+ *                            new tokens are written into their page slots in
+ *                            place [jennyma11.github.io/infra/ch07-01, the note
+ *                            under code 1-2 (real engines write by slot, with
+ *                            PagedAttention); openai-hub.com/news/2435, section
+ *                            "显存测量最容易被分配器误导" (the allocator misleads
+ *                            memory measurements), which names PagedAttention as
+ *                            the remedy for reallocation]; defined here as the
+ *                            contiguous operations applied to the cache gathered
+ *                            through the block table
  *   oracle_full_causal_attention
  *                            the uncached route: ordinary causal attention of
  *                            T query rows over T keys (row t sees keys 0..t)
@@ -46,8 +59,15 @@
  *   - past_len[b] is the number of cached tokens BEFORE the append;
  *   - bf16 values are widened exactly (bf16 bits << 16 is the fp32 value).
  *
+ * Paged layout (a reading: the pages do not fix one): pages are
+ * [num_pages, H_kv, page_size, D] row-major; logical page j of sequence b is
+ * physical page block_table[b * max_pages + j]; token t of (b, h) is row
+ * t % page_size of head h in logical page t / page_size.
+ *
  * Status codes: 0 = ok, 1 = invalid argument, 2 = capacity (P + N > T_max or
- * P < 0 for some sequence; that sequence is left untouched).
+ * P < 0 for some sequence; that sequence is left untouched), 3 = a block-table
+ * entry that a sequence needs is outside [0, num_pages) (that sequence is left
+ * untouched / its output rows are NaN).
  */
 #include <math.h>
 #include <stdint.h>
@@ -235,4 +255,129 @@ int oracle_full_causal_attention(const double *qf, const double *kf, const doubl
     }
     free(scores);
     return 0;
+}
+
+/* Physical page of token t of sequence b, or -1 when the entry is out of range. */
+static long long paged_page(const int32_t *block_table, int b, long long t, int page_size,
+                            int max_pages, int num_pages)
+{
+    const long long j = t / page_size;
+    if (j < 0 || j >= max_pages) return -1;
+    const long long page = block_table[(size_t)b * (size_t)max_pages + (size_t)j];
+    if (page < 0 || page >= num_pages) return -1;
+    return page;
+}
+
+/* Whether every page holding tokens 0 .. n_tok-1 of sequence b is valid. */
+static int paged_pages_ok(const int32_t *block_table, int b, long long n_tok, int page_size,
+                          int max_pages, int num_pages)
+{
+    for (long long t = 0; t < n_tok; t += page_size)
+        if (paged_page(block_table, b, t, page_size, max_pages, num_pages) < 0) return 0;
+    return 1;
+}
+
+/*
+ * Paged append: for every sequence b, KV head h and new token i < N, with
+ * t = past_len[b] + i,
+ *   pages[page(b, t), h, t % page_size, :] = new[b, h, i, :]   (bit copy, K and V).
+ * A sequence whose tokens do not fit (t >= max_pages * page_size) or whose
+ * pages for tokens 0 .. past_len[b] + N - 1 are not all valid is left untouched.
+ */
+int oracle_paged_append(void *k_pages, void *v_pages, const void *k_new, const void *v_new,
+                        const int32_t *block_table, const int32_t *past_len, int B, int H_kv,
+                        int D, int N, int page_size, int max_pages, int num_pages, int dtype)
+{
+    const int s = elem_bytes(dtype);
+    if (!k_pages || !v_pages || !k_new || !v_new || !block_table || !past_len || s == 0 ||
+        B < 0 || H_kv <= 0 || D <= 0 || N <= 0 || page_size <= 0 || max_pages <= 0 || num_pages <= 0)
+        return 1;
+    int status = 0;
+    const size_t row = (size_t)D * (size_t)s;
+    const long long capacity = (long long)max_pages * page_size;
+    for (int b = 0; b < B; ++b) {
+        const long long P = past_len[b];
+        if (P < 0 || P + N > capacity) {
+            status = 2;
+            continue;
+        }
+        if (!paged_pages_ok(block_table, b, P + N, page_size, max_pages, num_pages)) {
+            if (status == 0) status = 3;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h) {
+            for (int i = 0; i < N; ++i) {
+                const long long t = P + i;
+                const long long page = paged_page(block_table, b, t, page_size, max_pages, num_pages);
+                const size_t dst = (((size_t)page * H_kv + h) * (size_t)page_size + (size_t)(t % page_size)) * row;
+                const size_t src = (((size_t)b * H_kv + h) * (size_t)N + (size_t)i) * row;
+                memcpy((char *)k_pages + dst, (const char *)k_new + src, row);
+                memcpy((char *)v_pages + dst, (const char *)v_new + src, row);
+            }
+        }
+    }
+    return status;
+}
+
+/*
+ * Paged decode attention: gather the keys and values of tokens
+ * 0 .. past_len[b] + N - 1 of every (b, h) from their pages into a contiguous
+ * [B, H_kv, max_pages * page_size, D] cache and apply oracle_decode_attention
+ * to it.  Rows of a sequence with an invalid past_len are NaN (status 2); rows
+ * of a sequence with an invalid page are NaN (status 3).
+ */
+int oracle_paged_decode_attention(const void *q, const void *k_pages, const void *v_pages,
+                                  double *out, const int32_t *block_table, const int32_t *past_len,
+                                  int B, int H_q, int H_kv, int D, int N, int page_size,
+                                  int max_pages, int num_pages, double scale, int dtype)
+{
+    const int s = elem_bytes(dtype);
+    if (!q || !k_pages || !v_pages || !out || !block_table || !past_len || s == 0 || B < 0 ||
+        H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || D <= 0 || N <= 0 || page_size <= 0 ||
+        max_pages <= 0 || num_pages <= 0)
+        return 1;
+    const long long T = (long long)max_pages * page_size;
+    const size_t row = (size_t)D * (size_t)s;
+    const size_t head_bytes = (size_t)T * row;
+    char *kc = (char *)calloc((size_t)B * H_kv, head_bytes);
+    char *vc = (char *)calloc((size_t)B * H_kv, head_bytes);
+    int32_t *pl = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+    if (!kc || !vc || !pl) {
+        free(kc);
+        free(vc);
+        free(pl);
+        return 1;
+    }
+    int bad_pages = 0;
+    pl[0] = 0;
+    for (int b = 0; b < B; ++b) {
+        const long long P = past_len[b];
+        pl[b] = past_len[b];
+        if (P < 0 || P + N > T) continue; /* reported as capacity below */
+        if (!paged_pages_ok(block_table, b, P + N, page_size, max_pages, num_pages)) {
+            pl[b] = -1; /* makes the contiguous oracle mark the rows NaN */
+            bad_pages = 1;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h) {
+            for (long long t = 0; t < P + N; ++t) {
+                const long long page = paged_page(block_table, b, t, page_size, max_pages, num_pages);
+                const size_t src = (((size_t)page * H_kv + h) * (size_t)page_size + (size_t)(t % page_size)) * row;
+                const size_t dst = (((size_t)b * H_kv + h) * (size_t)T + (size_t)t) * row;
+                memcpy(kc + dst, (const char *)k_pages + src, row);
+                memcpy(vc + dst, (const char *)v_pages + src, row);
+            }
+        }
+    }
+    int status = oracle_decode_attention(q, kc, vc, out, pl, B, H_q, H_kv, (int)T, D, N, scale, dtype);
+    if (status != 1) status = bad_pages ? 3 : 0;
+    /* a capacity violation of some sequence takes precedence, as in the contiguous oracle */
+    for (int b = 0; b < B && status != 1; ++b) {
+        const long long P = past_len[b];
+        if (P < 0 || P + N > T) status = 2;
+    }
+    free(kc);
+    free(vc);
+    free(pl);
+    return status;
 }

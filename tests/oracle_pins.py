@@ -12,7 +12,12 @@ oracle disagrees with something other than itself:
   row;
 * invariants       -- the pages' trap: with one new token a joint permutation
   of cached (K, V) pairs leaves the output unchanged, with several new tokens a
-  reversed old/new order changes it.
+  reversed old/new order changes it;
+* paged cache      -- with pages laid out from a contiguous cache and the
+  identity block table, paged append and paged attention give exactly the
+  contiguous results (pinned above); renumbering the physical pages (and
+  adding unused NaN pages) changes nothing; a needed page outside the pool is
+  reported and only its sequence is affected.
 
 ``test_oracle_pins.py`` runs them on the real oracle and on mutants of it with
 one planted mistake each, to show that every plausible mistake fails a pin.
@@ -273,6 +278,84 @@ def pin_reversed_order_trap(orc):
                 assert err < 1e-13, err
 
 
+# ---------------------------------------------------------------------------------
+# paged cache: pages [num_pages, H_kv, page_size, D]; logical page j of sequence b
+# is physical page block_table[b, j]
+def _to_pages(cache: torch.Tensor, page_size: int) -> torch.Tensor:
+    """Pages of a contiguous [B, H, T, D] cache, sequence b's page j at index b * (T / page_size) + j."""
+    B, H, T, D = cache.shape
+    assert T % page_size == 0
+    return cache.reshape(B, H, T // page_size, page_size, D).permute(0, 2, 1, 3, 4).reshape(
+        B * (T // page_size), H, page_size, D).contiguous()
+
+
+def _identity_table(B: int, max_pages: int) -> np.ndarray:
+    return np.arange(B * max_pages, dtype=np.int32).reshape(B, max_pages)
+
+
+def pin_paged_identity_layout(orc):
+    """Identity block table: paged append / attention = contiguous append / attention, bit for bit."""
+    for dtype, ps in (("f32", 4), ("bf16", 8)):
+        B, H_q, H_kv, D, N, T_max = 3, 4, 2, 16, 3, 32
+        past = [5, 0, T_max - N]
+        q, k_new, v_new, k_cache, v_cache, past_len = _problem(B, H_q, H_kv, D, N, T_max, past, dtype, 71)
+        k_cache = torch.where(torch.isnan(k_cache), torch.full_like(k_cache, 1.75), k_cache)
+        v_cache = torch.where(torch.isnan(v_cache), torch.full_like(v_cache, -0.5), v_cache)
+        table = _identity_table(B, T_max // ps)
+        kp, vp = to_np(_to_pages(k_cache, ps)), to_np(_to_pages(v_cache, ps))
+        st = orc.paged_append(kp, vp, to_np(k_new), to_np(v_new), table, past_len.numpy(), dtype)
+        assert st == 0
+        exp_k, exp_v = _appended(k_cache, v_cache, k_new, v_new, past_len)
+        assert np.array_equal(kp.view(np.uint8), to_np(_to_pages(exp_k, ps)).view(np.uint8))
+        assert np.array_equal(vp.view(np.uint8), to_np(_to_pages(exp_v, ps)).view(np.uint8))
+        paged, st = orc.paged_decode_attention(to_np(q), kp, vp, table, past_len.numpy(), dtype)
+        assert st == 0
+        flat = _oracle_decode(orc, q, exp_k, exp_v, past_len, dtype).numpy()
+        assert np.array_equal(paged, flat)
+
+
+def pin_paged_renumbered_pages(orc):
+    """Renumbering the physical pages and adding unused NaN pages changes nothing."""
+    for dtype, ps in (("f32", 8), ("bf16", 4)):
+        B, H_q, H_kv, D, N, T_max = 2, 6, 3, 8, 2, 24
+        q, k_new, v_new, k_cache, v_cache, past_len = _problem(B, H_q, H_kv, D, N, T_max, [9, 20], dtype, 81)
+        kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
+        kp, vp = _to_pages(kc, ps), _to_pages(vc, ps)
+        table = _identity_table(B, T_max // ps)
+        base, st = orc.paged_decode_attention(to_np(q), to_np(kp), to_np(vp), table, past_len.numpy(), dtype)
+        assert st == 0
+        n_used, n_pool = kp.shape[0], kp.shape[0] + 5
+        perm = torch.randperm(n_pool, generator=torch.Generator().manual_seed(5))[:n_used]
+        kp2 = torch.full((n_pool,) + tuple(kp.shape[1:]), float("nan"), dtype=kp.dtype)
+        vp2 = torch.full_like(kp2, float("nan"))
+        kp2[perm], vp2[perm] = kp, vp
+        table2 = perm.numpy().astype(np.int32)[table]
+        out, st = orc.paged_decode_attention(to_np(q), to_np(kp2), to_np(vp2), table2, past_len.numpy(), dtype)
+        assert st == 0
+        assert np.array_equal(out, base)
+
+
+def pin_paged_bad_page(orc):
+    """A needed block-table entry outside the pool is reported; other sequences are unaffected."""
+    dtype, ps = "f32", 4
+    B, H_q, H_kv, D, N, T_max = 2, 2, 2, 8, 1, 16
+    q, k_new, v_new, k_cache, v_cache, past_len = _problem(B, H_q, H_kv, D, N, T_max, [6, 6], dtype, 91)
+    kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
+    kp, vp = to_np(_to_pages(kc, ps)), to_np(_to_pages(vc, ps))
+    table = _identity_table(B, T_max // ps)
+    table[0, 3] = -1                       # not needed (tokens 0..6 use pages 0, 1): fine
+    good, st = orc.paged_decode_attention(to_np(q), kp, vp, table, past_len.numpy(), dtype)
+    assert st == 0 and np.isfinite(good).all()
+    table[1, 1] = kp.shape[0]              # needed by sequence 1: out of the pool
+    out, st = orc.paged_decode_attention(to_np(q), kp, vp, table, past_len.numpy(), dtype)
+    assert st == 3
+    assert np.array_equal(out[0], good[0]) and np.isnan(out[1]).all()
+    kp2 = kp.copy()
+    st = orc.paged_append(kp2, vp.copy(), to_np(k_new), to_np(v_new), table, past_len.numpy(), dtype)
+    assert st == 3
+    assert np.array_equal(kp2[4:].view(np.uint8), kp[4:].view(np.uint8))  # sequence 1 untouched
+
+
 ALL_PINS = [
     pin_cache_bytes,
     pin_append_is_concat,
@@ -283,4 +366,7 @@ ALL_PINS = [
     pin_full_causal_sdpa,
     pin_permutation_single_token,
     pin_reversed_order_trap,
+    pin_paged_identity_layout,
+    pin_paged_renumbered_pages,
+    pin_paged_bad_page,
 ]

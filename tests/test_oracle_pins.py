@@ -38,6 +38,16 @@ MUTANTS = [
      "[idx] << 16;", "[idx] << 15;"),
     ("size formula without the factor 2 for K and V",
      "(2LL * L * H_kv", "(1LL * L * H_kv"),
+    ("paged: page slot and page index swapped",
+     "const long long j = t / page_size;", "const long long j = t % page_size;"),
+    ("paged: block table read with the wrong row stride",
+     "block_table[(size_t)b * (size_t)max_pages + (size_t)j]", "block_table[(size_t)b + (size_t)j]"),
+    ("paged: pages gathered as token-major [page, slot, head]",
+     "const size_t src = (((size_t)page * H_kv + h) * (size_t)page_size + (size_t)(t % page_size)) * row;",
+     "const size_t src = (((size_t)page * page_size + (size_t)(t % page_size)) * H_kv + h) * row;"),
+    ("paged: append writes the token at the page start",
+     "(size_t)page_size + (size_t)(t % page_size)) * row;\n                const size_t src",
+     "(size_t)page_size + (size_t)(0)) * row;\n                const size_t src"),
 ]
 
 
