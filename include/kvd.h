@@ -68,6 +68,7 @@ typedef enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1 } kvd_dtype;
 /* Bits OR-ed into the device error word. */
 #define KVD_DEVERR_PAST_LEN 1u /* a sequence had an out-of-range past_len and was skipped */
 #define KVD_DEVERR_TIMEOUT 2u  /* a bounded shared-memory pipeline wait gave up */
+#define KVD_DEVERR_PAGE 4u     /* a paged call met a block-table entry outside [0, num_pages) */
 
 /*
  * kvd_append -- in-place cache update (step 1 of a decode step).
@@ -121,6 +122,8 @@ size_t kvd_decode_workspace_bytes(int B, int H_q, int H_kv, int D, int N, int ma
  * Supported: D in {64, 128}; dtype fp32 or bf16; H_q % H_kv == 0;
  * (H_q / H_kv) * N <= 128.
  * Returns KVD_OK or the first argument error found (see kvd_status).
+ * The workspace size does not depend on the cache layout: the paged calls
+ * below use the same kvd_decode_workspace_bytes.
  */
 kvd_status kvd_decode_attention(const void *q, const void *k_cache, const void *v_cache,
                                 void *out, const int32_t *past_len, int B, int H_q, int H_kv,
@@ -201,6 +204,54 @@ kvd_status kvd_decode_attention_noalloc(const void *q, const void *k_cache, cons
                                         int H_kv, int T_max, int D, int N, int max_past_len,
                                         float scale, kvd_dtype dtype, uint32_t *err_word,
                                         void *stream);
+
+/*
+ * Paged cache.  Real serving engines keep the cache in fixed-size pages and
+ * write new tokens into their page slots in place (PagedAttention:
+ * "7.1 自回归生成过程", section "Decode 阶段", note under code 1-2;
+ * "GPT-2缓存实测", section "显存测量最容易被分配器误导").  Here:
+ *
+ *   k_pages, v_pages  device, [num_pages, H_kv, page_size, D]: one page holds
+ *                     page_size consecutive tokens of one sequence for every KV
+ *                     head, each head's rows contiguous (a tile of keys is one
+ *                     contiguous run of a page)
+ *   block_table       device int32 [B, max_pages]: logical page j of sequence b
+ *                     is physical page block_table[b * max_pages + j]; token t
+ *                     of (b, h) is row t % page_size of head h in logical page
+ *                     t / page_size.  Only the entries of pages that hold tokens
+ *                     0 .. past_len[b] + N - 1 are read.
+ *   page_size         a power of two, >= 64 (a multiple of every tile size)
+ *   max_pages         entries per block-table row; the capacity of a sequence is
+ *                     max_pages * page_size tokens (the T_max of the contiguous
+ *                     calls: max_past_len + N must fit, else KVD_ERR_CAPACITY)
+ *   num_pages         pages in the pool
+ *
+ * Every other argument, the results and the workspace are those of the
+ * contiguous call of the same name.  A block-table entry outside
+ * [0, num_pages) that a sequence needs is found on the device: KVD_DEVERR_PAGE
+ * is OR-ed into *err_word, nothing is written to or read from outside the pool,
+ * and that sequence's cache writes for the bad page are skipped and its output
+ * rows are unspecified.
+ */
+kvd_status kvd_paged_append(void *k_pages, void *v_pages, const void *k_new, const void *v_new,
+                            const int32_t *block_table, const int32_t *past_len, int B, int H_kv,
+                            int D, int N, int page_size, int max_pages, int num_pages,
+                            int max_past_len, kvd_dtype dtype, uint32_t *err_word, void *stream);
+
+kvd_status kvd_paged_decode_attention(const void *q, const void *k_pages, const void *v_pages,
+                                      void *out, const int32_t *block_table,
+                                      const int32_t *past_len, int B, int H_q, int H_kv, int D,
+                                      int N, int page_size, int max_pages, int num_pages,
+                                      int max_past_len, float scale, kvd_dtype dtype,
+                                      void *workspace, size_t workspace_bytes, uint32_t *err_word,
+                                      void *stream);
+
+kvd_status kvd_paged_decode_step(const void *q, void *k_pages, void *v_pages, const void *k_new,
+                                 const void *v_new, void *out, const int32_t *block_table,
+                                 const int32_t *past_len, int B, int H_q, int H_kv, int D, int N,
+                                 int page_size, int max_pages, int num_pages, int max_past_len,
+                                 float scale, kvd_dtype dtype, void *workspace,
+                                 size_t workspace_bytes, uint32_t *err_word, void *stream);
 
 /* kvd_workspace_init -- zero-fill a workspace on `stream` (asynchronous), as
  * kvd_decode_attention and kvd_decode_step need before a workspace's first use. */

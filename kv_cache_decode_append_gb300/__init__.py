@@ -6,9 +6,10 @@ this package does not load the library; the first call does, and raises when
 it is missing.
 """
 from .kvd import (  # noqa: F401
-    KVD_BF16, KVD_DEVERR_PAST_LEN, KVD_DEVERR_TIMEOUT, KVD_ERR_CAPACITY, KVD_ERR_CUDA,
+    KVD_BF16, KVD_DEVERR_PAGE, KVD_DEVERR_PAST_LEN, KVD_DEVERR_TIMEOUT, KVD_ERR_CAPACITY, KVD_ERR_CUDA,
     KVD_ERR_INVALID_ARG, KVD_ERR_UNSUPPORTED, KVD_ERR_WORKSPACE, KVD_F32, KVD_OK, KvdError,
     alloc_workspace, kvd_append, kvd_cache_bytes, kvd_decode_attention, kvd_decode_attention_noalloc,
-    kvd_decode_plan, kvd_decode_step, kvd_decode_workspace_bytes,
+    kvd_decode_plan, kvd_decode_step, kvd_decode_workspace_bytes, kvd_paged_append,
+    kvd_paged_decode_attention, kvd_paged_decode_step,
     kvd_status_string, kvd_workspace_init, library_path, load, raw,
 )

@@ -50,6 +50,55 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a)
 }
 
 // ---------------------------------------------------------------------------
+// Paged kv_append: token t = P_b + i of (b, h) goes to row t % page_size of head
+// h in physical page block_table[b, t / page_size] of [num_pages, H_kv,
+// page_size, D] pages (PagedAttention slot writes: "7.1 自回归生成过程", note
+// under code 1-2).  Same thread mapping as append_kernel.
+struct PagedAppendArgs {
+    uint4 *k_pages;
+    uint4 *v_pages;
+    const uint4 *k_new;
+    const uint4 *v_new;
+    const int32_t *block_table;
+    const int32_t *past_len;
+    uint32_t *err_word;
+    int H_kv, N, max_past_len;
+    int page_shift, max_pages, num_pages;
+    int row_chunks;
+    long long total;
+};
+
+__global__ void __launch_bounds__(256) paged_append_kernel(const PagedAppendArgs a)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const int capacity = a.max_pages << a.page_shift;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < a.total;
+         idx += stride) {
+        const int c = (int)(idx % a.row_chunks);
+        const long long row = idx / a.row_chunks;  // (bh, i)
+        const int i = (int)(row % a.N);
+        const long long bh = row / a.N;
+        const int b = (int)(bh / a.H_kv);
+        const int h = (int)(bh % a.H_kv);
+        const int P = __ldg(a.past_len + b);
+        if (!past_len_ok(P, a.N, capacity, a.max_past_len)) {
+            if (c == 0 && i == 0 && h == 0) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
+            continue;
+        }
+        const int t = P + i;
+        const int page = __ldg(a.block_table + (size_t)b * a.max_pages + (t >> a.page_shift));
+        if (page < 0 || page >= a.num_pages) {
+            if (c == 0) raise_error(a.err_word, KVD_DEVERR_PAGE);
+            continue;
+        }
+        const long long slot = (((long long)page * a.H_kv + h) << a.page_shift) + (t & ((1 << a.page_shift) - 1));
+        const long long dst = slot * a.row_chunks + c;
+        stg128(a.k_pages + dst, ldg128_nc(a.k_new + idx));
+        stg128(a.v_pages + dst, ldg128_nc(a.v_new + idx));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Per-device facts, queried once.
 namespace {
 
@@ -129,7 +178,7 @@ struct Plan {
     int rows, rb, n_rowblocks;
     int grid, smem, launches, max_tiles;
     bool merge_pass;  // split heads merged by a second launch (else inside the kernel)
-    size_t part_o_off, part_ml_off, tickets_off, seg_off, ws_bytes;
+    size_t part_off, tickets_off, seg_off, ws_bytes;
 };
 
 kvd_status check_shapes(int B, int H_q, int H_kv, int D, int N, int max_past_len, kvd_dtype dtype)
@@ -142,21 +191,42 @@ kvd_status check_shapes(int B, int H_q, int H_kv, int D, int N, int max_past_len
     return KVD_OK;
 }
 
+// The two builds of the kernels for one cache layout: with the separate
+// merge pass (vp) and merging split heads themselves (vt); both have the same
+// shared memory layout and tiles.
+bool pick_builds(kvd_dtype dtype, int D, int rb, bool paged, AttnVariant *vp, AttnVariant *vt)
+{
+    if (paged)
+        return dtype == KVD_F32 ? attn_variant_f32_paged(D, rb, vp) && attn_variant_f32_tk_paged(D, rb, vt)
+                                : attn_variant_bf16_paged(D, rb, vp) && attn_variant_bf16_tk_paged(D, rb, vt);
+    return dtype == KVD_F32 ? attn_variant_f32(D, rb, vp) && attn_variant_f32_tk(D, rb, vt)
+                            : attn_variant_bf16(D, rb, vp) && attn_variant_bf16_tk(D, rb, vt);
+}
+
+// Lowest resident CTAs per SM over the attention and fused-step kernels of both builds.
+kvd_status min_occupancy(int dev, const AttnVariant &vp, const AttnVariant &vt, int smem, int *occ)
+{
+    *occ = 1 << 30;
+    for (const void *fn : {vp.fn, vp.fused_fn, vt.fn, vt.fused_fn}) {
+        int o = 0;
+        const kvd_status st = occupancy(dev, fn, vp.threads, smem, &o);
+        if (st != KVD_OK) return st;
+        if (o < *occ) *occ = o;
+    }
+    return KVD_OK;
+}
+
 kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, kvd_dtype dtype,
-                     Plan *pl)
+                     Plan *pl, bool paged = false)
 {
     kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
     if (st != KVD_OK) return st;
     pl->rows = (H_q / H_kv) * N;
     pl->rb = pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : pl->rows <= 4 ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
-    // The two builds of the kernels: with the separate merge pass, and
-    // merging split heads themselves (same shared memory layout and tiles).
-    AttnVariant vp, vt;
-    const bool ok = dtype == KVD_F32
-                        ? attn_variant_f32(D, pl->rb, &vp) && attn_variant_f32_tk(D, pl->rb, &vt)
-                        : attn_variant_bf16(D, pl->rb, &vp) && attn_variant_bf16_tk(D, pl->rb, &vt);
-    if (!ok) return KVD_ERR_UNSUPPORTED;
+    AttnVariant vp, vt, op, ot;  // this layout's builds, and the other layout's
+    if (!pick_builds(dtype, D, pl->rb, paged, &vp, &vt) || !pick_builds(dtype, D, pl->rb, !paged, &op, &ot))
+        return KVD_ERR_UNSUPPORTED;
     pl->v = vp;
 
     // Shared memory holds the ring plus two per-sequence tables (B + 1 tile
@@ -165,18 +235,15 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     if (smem > (size_t)kMaxSmemPerCta) return KVD_ERR_UNSUPPORTED;
     pl->smem = (int)smem;
 
-    int dev = 0, sms = 0, occ = 0;
+    int dev = 0, sms = 0, occ = 0, occ_other = 0;
     if ((st = current_device(&dev)) != KVD_OK) return st;
     if ((st = sm_count(dev, &sms)) != KVD_OK) return st;
-    // The attention and the fused-step kernels of both builds share the plan
-    // (and so the workspace layout): size the grid for the one with the
-    // lowest occupancy.
-    occ = 1 << 30;
-    for (const void *fn : {vp.fn, vp.fused_fn, vt.fn, vt.fused_fn}) {
-        int o = 0;
-        if ((st = occupancy(dev, fn, pl->v.threads, pl->smem, &o)) != KVD_OK) return st;
-        if (o < occ) occ = o;
-    }
+    // The attention and the fused-step kernels of both builds share the plan:
+    // size the grid for the one with the lowest occupancy.  The workspace is
+    // sized for the larger grid of the two cache layouts, so that one size
+    // (kvd_decode_workspace_bytes) serves contiguous and paged calls.
+    if ((st = min_occupancy(dev, vp, vt, pl->smem, &occ)) != KVD_OK) return st;
+    if ((st = min_occupancy(dev, op, ot, pl->smem, &occ_other)) != KVD_OK) return st;
 
     // One CTA per resident slot; each takes an equal share of all tiles.
     pl->grid = sms * occ;
@@ -193,12 +260,10 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     pl->launches = pl->merge_pass ? 2 : 1;
     if (!pl->merge_pass) pl->v = vt;
 
-    const size_t pieces = (size_t)pl->grid * 2 * pl->rb;
+    const size_t pieces = (size_t)sms * (occ > occ_other ? occ : occ_other) * 2 * pl->rb;
     size_t off = 0;
-    pl->part_o_off = off;
-    off += round_up(pieces * D * sizeof(float), 256);
-    pl->part_ml_off = off;
-    off += round_up(pieces * 2 * sizeof(float), 256);
+    pl->part_off = off;  // per piece row: o[D], m, l, 2 floats of padding (16-byte rows)
+    off += round_up(pieces * (D + 4) * sizeof(float), 256);
     pl->tickets_off = off;
     off += round_up((size_t)B * H_kv * pl->n_rowblocks * sizeof(int), 256);
     pl->seg_off = off;
@@ -287,14 +352,38 @@ kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_
 namespace {
 
 // Attention (k_new == v_new == null) or the fused step (append inside).
+// A paged cache: block table and pool geometry (null table = contiguous cache).
+struct PagedCache {
+    const int32_t *block_table;
+    int page_size, max_pages, num_pages;
+};
+
+// Checks of the paged geometry; on success *T_max = max_pages * page_size.
+kvd_status check_paged(const PagedCache &pc, int *T_max, int *page_shift)
+{
+    if (pc.block_table == nullptr || pc.max_pages < 1 || pc.num_pages < 1) return KVD_ERR_INVALID_ARG;
+    if (pc.page_size < 64 || (pc.page_size & (pc.page_size - 1)) != 0 || pc.page_size > (1 << 24))
+        return KVD_ERR_INVALID_ARG;
+    const long long cap = (long long)pc.max_pages * pc.page_size;
+    if (cap > 0x7fffffffLL) return KVD_ERR_INVALID_ARG;
+    *T_max = (int)cap;
+    int sh = 0;
+    while ((1 << sh) < pc.page_size) ++sh;
+    *page_shift = sh;
+    return KVD_OK;
+}
+
 kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache, const void *k_new,
                          const void *v_new, void *out, const int32_t *past_len, int B, int H_q, int H_kv,
                          int T_max, int D, int N, int max_past_len, float scale, kvd_dtype dtype,
-                         void *workspace, size_t workspace_bytes, uint32_t *err_word, void *stream)
+                         void *workspace, size_t workspace_bytes, uint32_t *err_word, void *stream,
+                         const PagedCache *paged = nullptr)
 {
     if (!q || !k_cache || !v_cache || !out || !past_len) return KVD_ERR_INVALID_ARG;
     kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
     if (st != KVD_OK) return st;
+    int page_shift = 0;
+    if (paged != nullptr && (st = check_paged(*paged, &T_max, &page_shift)) != KVD_OK) return st;
     if (T_max < 1) return KVD_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return KVD_ERR_INVALID_ARG;
@@ -302,7 +391,7 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     if (B == 0) return KVD_OK;
 
     Plan pl;
-    if ((st = make_plan(B, H_q, H_kv, D, N, max_past_len, dtype, &pl)) != KVD_OK) return st;
+    if ((st = make_plan(B, H_q, H_kv, D, N, max_past_len, dtype, &pl, paged != nullptr)) != KVD_OK) return st;
     if (workspace == nullptr || workspace_bytes < pl.ws_bytes ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return KVD_ERR_WORKSPACE;
@@ -316,10 +405,13 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     a.past_len = past_len;
     a.k_new = k_new;
     a.v_new = v_new;
-    a.part_o = reinterpret_cast<float *>(ws + pl.part_o_off);
-    a.part_ml = reinterpret_cast<float *>(ws + pl.part_ml_off);
-    a.tickets = reinterpret_cast<int *>(ws + pl.tickets_off);
-    a.seg = reinterpret_cast<int2 *>(ws + pl.seg_off);
+    a.part = reinterpret_cast<float *>(ws + pl.part_off);
+    // Separate regions: the tickets must stay zero while the same workspace
+    // serves calls in the other mode.
+    a.merge_state = ws + (pl.merge_pass ? pl.seg_off : pl.tickets_off);
+    a.block_table = paged != nullptr ? paged->block_table : nullptr;
+    a.num_pages = paged != nullptr ? paged->num_pages : 0;
+    a.page_shift = page_shift;
     a.err_word = err_word;
     a.B = B;
     a.H_kv = H_kv;
@@ -382,6 +474,81 @@ kvd_status kvd_decode_step(const void *q, void *k_cache, void *v_cache, const vo
     if (!aligned16(k_new) || !aligned16(v_new)) return KVD_ERR_INVALID_ARG;
     return decode_launch(q, k_cache, v_cache, k_new, v_new, out, past_len, B, H_q, H_kv, T_max, D, N,
                          max_past_len, scale, dtype, workspace, workspace_bytes, err_word, stream);
+}
+
+kvd_status kvd_paged_append(void *k_pages, void *v_pages, const void *k_new, const void *v_new,
+                            const int32_t *block_table, const int32_t *past_len, int B, int H_kv,
+                            int D, int N, int page_size, int max_pages, int num_pages,
+                            int max_past_len, kvd_dtype dtype, uint32_t *err_word, void *stream)
+{
+    const int s = elem_bytes(dtype);
+    if (s == 0) return KVD_ERR_UNSUPPORTED;
+    if (!k_pages || !v_pages || !k_new || !v_new || !past_len) return KVD_ERR_INVALID_ARG;
+    if (B < 0 || H_kv < 1 || D < 1 || N < 1 || max_past_len < 0) return KVD_ERR_INVALID_ARG;
+    int T_max = 0, page_shift = 0;
+    kvd_status st = check_paged(PagedCache{block_table, page_size, max_pages, num_pages}, &T_max, &page_shift);
+    if (st != KVD_OK) return st;
+    if (((long long)D * s) % 16 != 0) return KVD_ERR_UNSUPPORTED;
+    if (!aligned16(k_pages) || !aligned16(v_pages) || !aligned16(k_new) || !aligned16(v_new))
+        return KVD_ERR_INVALID_ARG;
+    if ((long long)max_past_len + N > T_max) return KVD_ERR_CAPACITY;
+    if (B == 0) return KVD_OK;
+
+    int dev = 0, sms = 0;
+    if ((st = current_device(&dev)) != KVD_OK) return st;
+    if ((st = sm_count(dev, &sms)) != KVD_OK) return st;
+
+    PagedAppendArgs a;
+    a.k_pages = static_cast<uint4 *>(k_pages);
+    a.v_pages = static_cast<uint4 *>(v_pages);
+    a.k_new = static_cast<const uint4 *>(k_new);
+    a.v_new = static_cast<const uint4 *>(v_new);
+    a.block_table = block_table;
+    a.past_len = past_len;
+    a.err_word = err_word;
+    a.H_kv = H_kv;
+    a.N = N;
+    a.max_past_len = max_past_len;
+    a.page_shift = page_shift;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.row_chunks = (int)(((long long)D * s) / 16);
+    a.total = (long long)B * H_kv * N * a.row_chunks;
+    const int threads = 256;
+    long long blocks = (a.total + threads - 1) / threads;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    void *args[] = {&a};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(&paged_append_kernel), dim3((unsigned)blocks),
+                            dim3(threads), args, 0, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_paged_decode_attention(const void *q, const void *k_pages, const void *v_pages,
+                                      void *out, const int32_t *block_table,
+                                      const int32_t *past_len, int B, int H_q, int H_kv, int D,
+                                      int N, int page_size, int max_pages, int num_pages,
+                                      int max_past_len, float scale, kvd_dtype dtype,
+                                      void *workspace, size_t workspace_bytes, uint32_t *err_word,
+                                      void *stream)
+{
+    const PagedCache pc{block_table, page_size, max_pages, num_pages};
+    return decode_launch(q, k_pages, v_pages, nullptr, nullptr, out, past_len, B, H_q, H_kv, 0, D, N,
+                         max_past_len, scale, dtype, workspace, workspace_bytes, err_word, stream, &pc);
+}
+
+kvd_status kvd_paged_decode_step(const void *q, void *k_pages, void *v_pages, const void *k_new,
+                                 const void *v_new, void *out, const int32_t *block_table,
+                                 const int32_t *past_len, int B, int H_q, int H_kv, int D, int N,
+                                 int page_size, int max_pages, int num_pages, int max_past_len,
+                                 float scale, kvd_dtype dtype, void *workspace,
+                                 size_t workspace_bytes, uint32_t *err_word, void *stream)
+{
+    if (!k_new || !v_new) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return KVD_ERR_INVALID_ARG;
+    const PagedCache pc{block_table, page_size, max_pages, num_pages};
+    return decode_launch(q, k_pages, v_pages, k_new, v_new, out, past_len, B, H_q, H_kv, 0, D, N,
+                         max_past_len, scale, dtype, workspace, workspace_bytes, err_word, stream, &pc);
 }
 
 kvd_status kvd_workspace_init(void *workspace, size_t workspace_bytes, void *stream)

@@ -64,27 +64,32 @@
 
 namespace kvd {
 
+// Kernel arguments, passed by value.  Kept at 128 bytes: on GB300 a larger
+// parameter block (even one more int) measured about 1 us slower per launch
+// of the long-context layer, so mode-specific fields share slots.
 struct AttnArgs {
     const void *q;           // [B, H_q, N, D]
-    const void *k_cache;     // [B, H_kv, T_max, D]
-    const void *v_cache;     // [B, H_kv, T_max, D]
+    const void *k_cache;     // contiguous [B, H_kv, T_max, D], or pages [num_pages, H_kv, page_size, D]
+    const void *v_cache;     // same layout as k_cache
     void *out;               // [B, H_q, N, D]
     const int32_t *past_len; // [B]
     const void *k_new;       // [B, H_kv, N, D]: fused step only (append inside)
     const void *v_new;       // [B, H_kv, N, D]: fused step only
-    float *part_o;           // [grid][2][RB][D]  piece partials (unnormalised)
-    float *part_ml;          // [grid][2][RB][2]  (max in log2 units, sum)
-    int2 *seg;               // [B*H_kv*n_rowblocks]: (first CTA, CTAs) of each sequence-head
-                             // (merge pass only)
-                             // (zero between calls: the merging CTA resets its ticket)
+    float *part;             // [grid][2][RB][D + 4]: piece partials o (unnormalised), m (log2 units), l
+    void *merge_state;       // merge pass: int2 [B*H_kv*n_rowblocks] (first CTA, CTAs) per
+                             // sequence-head; in-kernel merge: int tickets, the same count (pieces
+                             // counted so far; zero between calls: the merging CTA resets its ticket)
     uint32_t *err_word;
-    int B, H_kv, T_max, N, max_past_len;
+    const int32_t *block_table;  // paged only: [B, T_max >> page_shift] physical page of each logical page
+    int B, H_kv, T_max, N, max_past_len;  // paged: T_max = pages per sequence x page_size
     int rows;         // query rows per (b, h): (H_q / H_kv) * N, contiguous in q and out
     int n_rowblocks;  // ceil(rows / RB)
     float qscale;     // softmax scale * log2(e)
-    int *tickets;     // [B*H_kv*n_rowblocks]: pieces of a split head counted so far (in-kernel
-                      // merge only; zero between calls: the merging CTA resets its ticket)
+    int num_pages;    // paged only: pages in the pool
+    int page_shift;   // paged only: log2(page_size); page_size is a multiple of the tile keys
 };
+static_assert(sizeof(AttnArgs) == 128, "keep the kernel parameter block at 128 bytes");
+
 
 // Compile-time shape of one kernel variant.
 template <typename T, int D, int RB> struct AttnShape {
@@ -120,7 +125,8 @@ template <typename T, int D, int RB> struct AttnShape {
     static constexpr int kMetaOff = kEpiOff + kEpiBytes;
     static constexpr int kBarOff = kMetaOff + kStages * 32;
     static constexpr int kJobOff = kBarOff + 2 * kStages * 8;     // after the full and empty barriers
-    static constexpr int kFixedBytes = kJobOff + 32;                // two pieces to count (4 ints each)
+    static constexpr int kPageOff = kJobOff + 32;                   // two pieces to count (4 ints each)
+    static constexpr int kFixedBytes = kPageOff + 16;               // physical page of each stage (paged)
 
     static_assert(kRowBytes % 16 == 0, "rows must be whole 16-byte chunks");
     static_assert(kCpl >= 1 && kRowChunks % kL == 0, "lane mapping");
@@ -154,8 +160,10 @@ constexpr int kMetaEnd = 4;    // no more work
 // In a fused step (kFused) the new keys P..P+N-1 are not in the cache yet: in
 // the tiles that hold them (always on the masked path) their K/V rows are read
 // from k_new / v_new (kn, vn: the rows of this (b, h)) and, when kc / vc are
-// given, written to their cache slots by the lanes that read them.
-template <typename T, int D, int RB, bool kMasked, bool kFused>
+// given, written to their cache slots by the lanes that read them: kc + key
+// rows (contiguous cache: kc is the (b, h) row base), or kc + (key - tile_k0)
+// rows when kTileRel (paged cache: kc is the slot of the tile's first key).
+template <typename T, int D, int RB, bool kMasked, bool kFused, bool kTileRel = false>
 __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigned char *Vs,
                                           const f32x2 (&qv)[RB][AttnShape<T, D, RB>::kE / 2],
                                           f32x2 (&o)[RB][AttnShape<T, D, RB>::kE / 2], float (&m_run)[RB],
@@ -186,7 +194,7 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
                 if (kc != nullptr) {
 #pragma unroll
                     for (int c = 0; c < S::kCpl; ++c)
-                        stg128(kc + (size_t)key * S::kRowBytes + (c * S::kL + j) * 16, raw[u][c]);
+                        stg128(kc + (size_t)(kTileRel ? kk : key) * S::kRowBytes + (c * S::kL + j) * 16, raw[u][c]);
                 }
                 continue;
             }
@@ -263,7 +271,7 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
                 if (vc != nullptr) {
 #pragma unroll
                     for (int c = 0; c < S::kCpl; ++c)
-                        stg128(vc + (size_t)key * S::kRowBytes + (c * S::kL + j) * 16, raw[u][c]);
+                        stg128(vc + (size_t)(kTileRel ? kk : key) * S::kRowBytes + (c * S::kL + j) * 16, raw[u][c]);
                 }
                 continue;
             }
@@ -316,7 +324,7 @@ __device__ __forceinline__ int owner_cta(long long t, long long n, long long G)
 // CTAs whose range crosses more head starts receive fewer tiles.  Per-head
 // values are computed once when the walk enters a head; a tile only costs a
 // few stores and the bulk copies.
-template <typename S, bool kWriteSeg> struct RangeWalk {
+template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
     long long t, hi, n, G;  // unit of the next tile, end of range, units in total, working CTAs
     int b, hr, tin, tb;     // sequence, head x row block, tile within the head, its tiles
     int HR;                 // H_kv * n_rowblocks
@@ -326,6 +334,18 @@ template <typename S, bool kWriteSeg> struct RangeWalk {
     int bh, rb, P, T_b, n_chunks, c_first, q_bytes;
     const unsigned char *kg, *vg, *qg;
     uint64_t policy;
+    int page_next;          // paged: physical page of the next tile (loaded one tile ahead)
+    int head_rows;          // paged: row offset of head h inside a page, h * page_size
+
+    // Paged: start the load of the next tile's page-table entry; it is used
+    // one fill later, so its latency hides behind the current tile.
+    __device__ __forceinline__ void prefetch_page(const AttnArgs &a)
+    {
+        if constexpr (kPaged) {
+            if (t < hi)
+                page_next = __ldg(a.block_table + (size_t)b * (a.T_max >> a.page_shift) + ((tin * S::kTK) >> a.page_shift));
+        }
+    }
 
     __device__ __forceinline__ void enter_head(const AttnArgs &a, const int *pl)
     {
@@ -338,11 +358,17 @@ template <typename S, bool kWriteSeg> struct RangeWalk {
         c_first = owner_cta(ts, n, G);
         n_chunks = owner_cta(ts + tb - 1, n, G) - c_first + 1;
         if constexpr (kWriteSeg) {  // the split's shape, for the merge pass
-            if (tin == 0) a.seg[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
+            if (tin == 0) static_cast<int2 *>(a.merge_state)[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
         }
-        const size_t row = (size_t)bh * a.T_max;
-        kg = static_cast<const unsigned char *>(a.k_cache) + row * S::kRowBytes;
-        vg = static_cast<const unsigned char *>(a.v_cache) + row * S::kRowBytes;
+        if constexpr (kPaged) {
+            head_rows = h << a.page_shift;
+            kg = static_cast<const unsigned char *>(a.k_cache);
+            vg = static_cast<const unsigned char *>(a.v_cache);
+        } else {
+            const size_t row = (size_t)bh * a.T_max;
+            kg = static_cast<const unsigned char *>(a.k_cache) + row * S::kRowBytes;
+            vg = static_cast<const unsigned char *>(a.v_cache) + row * S::kRowBytes;
+        }
         qg = static_cast<const unsigned char *>(a.q) + ((size_t)bh * a.rows + rb * S::kRB) * S::kRowBytes;
         q_bytes = min(S::kRB, a.rows - rb * S::kRB) * S::kRowBytes;
     }
@@ -377,12 +403,15 @@ template <typename S, bool kWriteSeg> struct RangeWalk {
         tin = max(0, off - S::kPieceUnits);
         t = (long long)pre[b] * HR + (long long)hr * ub + S::kPieceUnits + tin;
         if (t < hi) enter_head(a, pl);
+        prefetch_page(a);
     }
 
     // Describe and load the next tile into slot s, or mark the end of work.
     __device__ __forceinline__ void fill(const AttnArgs &a, const int *pre, const int *pl,
                                          unsigned char *smem, TileMeta *meta, uint64_t *full, int s)
     {
+        // (paged) page of the tile: a tile never straddles a page
+        int page = 0;
         if (ended) return;
         if (t >= hi) {
             meta[s].flags = kMetaEnd;
@@ -403,7 +432,24 @@ template <typename S, bool kWriteSeg> struct RangeWalk {
 
         const uint32_t bytes = (uint32_t)mt.nk * S::kRowBytes;
         const uint32_t qbytes = piece_start ? (uint32_t)q_bytes : 0u;
-        const size_t off = (size_t)mt.tile_k0 * S::kRowBytes;
+        size_t off;
+        if constexpr (kPaged) {
+            page = page_next;
+            int *stage_page = reinterpret_cast<int *>(smem + S::kPageOff);
+            if (page < 0 || page >= a.num_pages) {
+                // Never read outside the pool: load page 0 instead, flag the
+                // error, and tell the fused step not to write this tile.
+                raise_error(a.err_word, KVD_DEVERR_PAGE);
+                stage_page[s] = -1;
+                page = 0;
+            } else {
+                stage_page[s] = page;
+            }
+            off = (((size_t)page * a.H_kv << a.page_shift) + head_rows +
+                   (mt.tile_k0 & ((1 << a.page_shift) - 1))) * S::kRowBytes;
+        } else {
+            off = (size_t)mt.tile_k0 * S::kRowBytes;
+        }
         unsigned char *dst = smem + S::kRingOff + s * 2 * S::kTileBytes;
         mbar_arrive_expect_tx(&full[s], 2u * bytes + qbytes);
         bulk_load_g2s(dst, kg + off, bytes, &full[s], policy);
@@ -427,6 +473,7 @@ template <typename S, bool kWriteSeg> struct RangeWalk {
             t += S::kPieceUnits;
             if (t < hi) enter_head(a, pl);
         }
+        prefetch_page(a);
     }
 };
 
@@ -467,8 +514,9 @@ __device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
             const int e = e0 + i * kThreads, r = e / D, d = e % D;
-            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + pb + r);
-            const float o_k = __ldcg(a.part_o + (pb + r) * D + d);
+            const float *pr = a.part + (pb + r) * (D + 4);
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(pr + D));
+            const float o_k = __ldcg(pr + d);
             const float Mn = fmaxf(M[i], ml.x);
             const float wa = safe_weight(M[i], Mn), wb = safe_weight(ml.x, Mn);
             num[i] = num[i] * wa + o_k * wb;
@@ -512,8 +560,9 @@ __device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &
 }
 
 // kFused: append inside (kvd_decode_step).  kTicketMerge: split heads are
-// merged at the end of this kernel (else by attn_merge_kernel).
-template <typename T, int D, int RB, bool kFused, bool kTicketMerge>
+// merged at the end of this kernel (else by attn_merge_kernel).  kPaged: the
+// cache is paged (block table), else contiguous [B, H_kv, T_max, D].
+template <typename T, int D, int RB, bool kFused, bool kTicketMerge, bool kPaged>
 __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     attn_balanced_kernel(const AttnArgs a)
 {
@@ -548,7 +597,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     // (slot s of ring position p is free again once every warp has released
     // position p - STAGES on empty[s]); the other warps go straight to
     // waiting for the first tile.
-    RangeWalk<S, !kTicketMerge> walk;  // used by thread 0 only
+    RangeWalk<S, !kTicketMerge, kPaged> walk;  // used by thread 0 only
     int issued = 0;     // ring positions filled so far (thread 0)
     if (warp == 0) {
         // ---- units per sequence-head, prefix-summed over sequences by a warp scan ----
@@ -661,14 +710,23 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
                 const size_t nrow = (size_t)mt.bh * a.N * S::kRowBytes;
                 kn = static_cast<const unsigned char *>(a.k_new) + nrow;
                 vn = static_cast<const unsigned char *>(a.v_new) + nrow;
-                if (mt.rb == 0) {  // one row block writes the new rows into the cache
+                if constexpr (kPaged) {
+                    // the slot of the tile's first key in its page (none if the page is invalid)
+                    const int page = reinterpret_cast<const int *>(smem + S::kPageOff)[s];
+                    if (mt.rb == 0 && page >= 0) {
+                        const size_t crow = (((size_t)page * a.H_kv + mt.bh % a.H_kv) << a.page_shift) +
+                                            (mt.tile_k0 & ((1 << a.page_shift) - 1));
+                        kc = static_cast<unsigned char *>(const_cast<void *>(a.k_cache)) + crow * S::kRowBytes;
+                        vc = static_cast<unsigned char *>(const_cast<void *>(a.v_cache)) + crow * S::kRowBytes;
+                    }
+                } else if (mt.rb == 0) {  // one row block writes the new rows into the cache
                     const size_t crow = (size_t)mt.bh * a.T_max * S::kRowBytes;
                     kc = static_cast<unsigned char *>(const_cast<void *>(a.k_cache)) + crow;
                     vc = static_cast<unsigned char *>(const_cast<void *>(a.v_cache)) + crow;
                 }
             }
-            attn_tile<T, D, RB, true, kFused>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim, k_end,
-                                              mt.P, kn, vn, kc, vc);
+            attn_tile<T, D, RB, true, kFused, kPaged>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim,
+                                                      k_end, mt.P, kn, vn, kc, vc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with slot s
@@ -754,10 +812,11 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
             if (single) {
                 Ty::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
             } else {
-                a.part_o[(pbase + r) * D + d] = num;
+                float *pr = a.part + (pbase + r) * (D + 4);
+                pr[d] = num;
                 if (d == 0) {
-                    a.part_ml[(pbase + r) * 2 + 0] = M;
-                    a.part_ml[(pbase + r) * 2 + 1] = den;
+                    pr[D] = M;
+                    pr[D + 1] = den;
                 }
             }
         }
@@ -774,16 +833,17 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
         n_pieces = min(n_pieces, 2);
         __syncthreads();  // every thread's share of the partials is written
         if (tid == 0 && n_pieces > 0) {
+            int *tickets = static_cast<int *>(a.merge_state);
             // Each count releases this CTA's partials and, for the count that
             // completes a head, acquires the other CTAs' (acquire-release atomics).
             int seen[2];
 #pragma unroll
             for (int i = 0; i < 2; ++i)
-                if (i < n_pieces) seen[i] = atomic_add_acq_rel_gpu(a.tickets + (size_t)jobs[i].bh * a.n_rowblocks + jobs[i].rb, 1);
+                if (i < n_pieces) seen[i] = atomic_add_acq_rel_gpu(tickets + (size_t)jobs[i].bh * a.n_rowblocks + jobs[i].rb, 1);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 if (i < n_pieces && seen[i] == jobs[i].n_chunks - 1)
-                    a.tickets[(size_t)jobs[i].bh * a.n_rowblocks + jobs[i].rb] = 0;  // the next call starts from zero
+                    tickets[(size_t)jobs[i].bh * a.n_rowblocks + jobs[i].rb] = 0;  // the next call starts from zero
                 else
                     jobs[i].n_chunks = 0;  // another CTA completes this head (or no piece)
             }
@@ -835,13 +895,13 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
     if (rg >= a.rows) return;
     const int P = __ldg(a.past_len + b);
     if (!past_len_ok(P, a.N, a.T_max, a.max_past_len)) return;  // reported by the split pass
-    const int2 seg = a.seg[u];
+    const int2 seg = static_cast<const int2 *>(a.merge_state)[u];
     if (seg.y <= 1) return;  // the split pass wrote this row directly
 
     float M = kNegInf;
     for (int k = lane; k < seg.y; k += 32) {
         const int c = seg.x + k;
-        M = fmaxf(M, a.part_ml[(((size_t)c * 2 + (k == 0)) * RB + r) * 2]);
+        M = fmaxf(M, a.part[(((size_t)c * 2 + (k == 0)) * RB + r) * (D + 4) + D]);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off /= 2) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -852,9 +912,10 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
     float den = 0.f;
     for (int k = 0; k < seg.y; ++k) {
         const size_t pidx = ((size_t)(seg.x + k) * 2 + (k == 0)) * RB + r;
-        const float w = safe_weight(a.part_ml[pidx * 2], M);
-        den = fmaf(w, a.part_ml[pidx * 2 + 1], den);
-        const float *po = a.part_o + pidx * D + lane * kDpl;
+        const float *pr = a.part + pidx * (D + 4);
+        const float w = safe_weight(pr[D], M);
+        den = fmaf(w, pr[D + 1], den);
+        const float *po = pr + lane * kDpl;
         if constexpr (kDpl == 4) {
             const float4 v = *reinterpret_cast<const float4 *>(po);
             acc[0] = fmaf(w, v.x, acc[0]);
@@ -884,12 +945,12 @@ struct AttnVariant {
     int piece_units;       // cost of a piece boundary in tile units
 };
 
-template <typename T, int D, int RB, bool kTicketMerge> AttnVariant make_variant()
+template <typename T, int D, int RB, bool kTicketMerge, bool kPaged> AttnVariant make_variant()
 {
     using S = AttnShape<T, D, RB>;
     AttnVariant v;
-    v.fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false, kTicketMerge>);
-    v.fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, kTicketMerge>);
+    v.fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false, kTicketMerge, kPaged>);
+    v.fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, kTicketMerge, kPaged>);
     if constexpr (kTicketMerge) v.merge_fn = nullptr;
     else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, RB>);
     v.threads = S::kThreads;
@@ -900,31 +961,35 @@ template <typename T, int D, int RB, bool kTicketMerge> AttnVariant make_variant
     return v;
 }
 
-template <typename T, int D, bool kTicketMerge> bool pick_rb(int RB, AttnVariant *v)
+template <typename T, int D, bool kTicketMerge, bool kPaged> bool pick_rb(int RB, AttnVariant *v)
 {
     switch (RB) {
-    case 1: *v = make_variant<T, D, 1, kTicketMerge>(); return true;
-    case 2: *v = make_variant<T, D, 2, kTicketMerge>(); return true;
-    case 4: *v = make_variant<T, D, 4, kTicketMerge>(); return true;
-    case 8: *v = make_variant<T, D, 8, kTicketMerge>(); return true;
+    case 1: *v = make_variant<T, D, 1, kTicketMerge, kPaged>(); return true;
+    case 2: *v = make_variant<T, D, 2, kTicketMerge, kPaged>(); return true;
+    case 4: *v = make_variant<T, D, 4, kTicketMerge, kPaged>(); return true;
+    case 8: *v = make_variant<T, D, 8, kTicketMerge, kPaged>(); return true;
     default: return false;
     }
 }
 
-template <typename T, bool kTicketMerge> bool pick_variant(int D, int RB, AttnVariant *v)
+template <typename T, bool kTicketMerge, bool kPaged> bool pick_variant(int D, int RB, AttnVariant *v)
 {
     switch (D) {
-    case 64: return pick_rb<T, 64, kTicketMerge>(RB, v);
-    case 128: return pick_rb<T, 128, kTicketMerge>(RB, v);
+    case 64: return pick_rb<T, 64, kTicketMerge, kPaged>(RB, v);
+    case 128: return pick_rb<T, 128, kTicketMerge, kPaged>(RB, v);
     default: return false;
     }
 }
 
-// One translation unit each: kvd_attn_{f32,bf16}.cu (merge pass) and
-// kvd_attn_{f32,bf16}_tk.cu (in-kernel merge).
+// One translation unit each: kvd_attn_{f32,bf16}[_tk][_paged].cu -- merge
+// pass or in-kernel merge (_tk), contiguous or paged cache (_paged).
 bool attn_variant_f32(int D, int RB, AttnVariant *v);
 bool attn_variant_bf16(int D, int RB, AttnVariant *v);
 bool attn_variant_f32_tk(int D, int RB, AttnVariant *v);
 bool attn_variant_bf16_tk(int D, int RB, AttnVariant *v);
+bool attn_variant_f32_paged(int D, int RB, AttnVariant *v);
+bool attn_variant_bf16_paged(int D, int RB, AttnVariant *v);
+bool attn_variant_f32_tk_paged(int D, int RB, AttnVariant *v);
+bool attn_variant_bf16_tk_paged(int D, int RB, AttnVariant *v);
 
 }  // namespace kvd

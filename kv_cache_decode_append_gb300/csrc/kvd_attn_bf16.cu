@@ -3,5 +3,5 @@
 #include "kvd_attention.cuh"
 
 namespace kvd {
-bool attn_variant_bf16(int D, int RB, AttnVariant *v) { return pick_variant<__nv_bfloat16, false>(D, RB, v); }
+bool attn_variant_bf16(int D, int RB, AttnVariant *v) { return pick_variant<__nv_bfloat16, false, false>(D, RB, v); }
 }  // namespace kvd

@@ -3,5 +3,5 @@
 #include "kvd_attention.cuh"
 
 namespace kvd {
-bool attn_variant_bf16_tk(int D, int RB, AttnVariant *v) { return pick_variant<__nv_bfloat16, true>(D, RB, v); }
+bool attn_variant_bf16_tk(int D, int RB, AttnVariant *v) { return pick_variant<__nv_bfloat16, true, false>(D, RB, v); }
 }  // namespace kvd

@@ -3,5 +3,5 @@
 #include "kvd_attention.cuh"
 
 namespace kvd {
-bool attn_variant_f32(int D, int RB, AttnVariant *v) { return pick_variant<float, false>(D, RB, v); }
+bool attn_variant_f32(int D, int RB, AttnVariant *v) { return pick_variant<float, false, false>(D, RB, v); }
 }  // namespace kvd

@@ -3,5 +3,5 @@
 #include "kvd_attention.cuh"
 
 namespace kvd {
-bool attn_variant_f32_tk(int D, int RB, AttnVariant *v) { return pick_variant<float, true>(D, RB, v); }
+bool attn_variant_f32_tk(int D, int RB, AttnVariant *v) { return pick_variant<float, true, false>(D, RB, v); }
 }  // namespace kvd

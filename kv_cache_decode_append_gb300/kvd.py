@@ -35,6 +35,7 @@ KVD_BF16 = 1
 
 KVD_DEVERR_PAST_LEN = 1
 KVD_DEVERR_TIMEOUT = 2
+KVD_DEVERR_PAGE = 4
 
 _TORCH_DTYPE = {torch.float32: KVD_F32, torch.bfloat16: KVD_BF16}
 _NAME_DTYPE = {"f32": KVD_F32, "bf16": KVD_BF16}
@@ -68,6 +69,14 @@ class _Lib:
         lib.kvd_decode_step.restype = ci
         lib.kvd_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
                                         vp, sz, u32p, vp]
+        lib.kvd_paged_append.restype = ci
+        lib.kvd_paged_append.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, u32p, vp]
+        lib.kvd_paged_decode_attention.restype = ci
+        lib.kvd_paged_decode_attention.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci,
+                                                   cf, ci, vp, sz, u32p, vp]
+        lib.kvd_paged_decode_step.restype = ci
+        lib.kvd_paged_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci,
+                                              ci, cf, ci, vp, sz, u32p, vp]
         lib.kvd_decode_attention_noalloc.restype = ci
         lib.kvd_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
                                                      ci, u32p, vp]
@@ -242,6 +251,87 @@ def kvd_decode_step(q, k_cache, v_cache, k_new, v_new, out, past_len, max_past_l
                              N, int(max_past_len), float(scale), _dtype_code(q), ws_ptr, ws_bytes,
                              _ptr(err_word), _stream_handle(stream))
     _check("kvd_decode_step", st)
+
+
+# ---------------------------------------------------------------------------------
+# paged cache: k_pages / v_pages [num_pages, H_kv, page_size, D], block_table int32 [B, max_pages]
+def _paged_geometry(k_pages, v_pages, block_table, B: int):
+    _need_cuda("block_table", block_table, torch.int32)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_pages]")
+    if v_pages.shape != k_pages.shape or k_pages.dim() != 4:
+        raise ValueError("k_pages and v_pages must be the same [num_pages, H_kv, page_size, D]")
+    num_pages, H_kv, page_size, D = k_pages.shape
+    return num_pages, H_kv, page_size, D, block_table.shape[1]
+
+
+def kvd_paged_append(k_pages, v_pages, k_new, v_new, block_table, past_len, max_past_len: int,
+                     err_word=None, stream=None) -> None:
+    """Write ``k_new``/``v_new`` [B,H_kv,N,D] into the page slots of tokens ``past_len[b] + i``."""
+    for n, t in (("k_pages", k_pages), ("v_pages", v_pages), ("k_new", k_new), ("v_new", v_new)):
+        _need_cuda(n, t, k_pages.dtype)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, _, N, _ = k_new.shape
+    num_pages, H_kv, page_size, D, max_pages = _paged_geometry(k_pages, v_pages, block_table, B)
+    if tuple(k_new.shape) != (B, H_kv, N, D) or v_new.shape != k_new.shape:
+        raise ValueError("shape mismatch between the pages and the new K/V")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    st = raw.kvd_paged_append(k_pages.data_ptr(), v_pages.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                              block_table.data_ptr(), past_len.data_ptr(), B, H_kv, D, N, page_size,
+                              max_pages, num_pages, int(max_past_len), _dtype_code(k_pages), _ptr(err_word),
+                              _stream_handle(stream))
+    _check("kvd_paged_append", st)
+
+
+def kvd_paged_decode_attention(q, k_pages, v_pages, out, block_table, past_len, max_past_len: int,
+                               scale: float = 0.0, workspace: Optional[torch.Tensor] = None,
+                               err_word=None, stream=None) -> None:
+    """kvd_decode_attention over a paged cache (workspace from alloc_workspace, same shapes)."""
+    for n, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages), ("out", out)):
+        _need_cuda(n, t, q.dtype)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_q, N, D = q.shape
+    num_pages, H_kv, page_size, Dp, max_pages = _paged_geometry(k_pages, v_pages, block_table, B)
+    if out.shape != q.shape or Dp != D:
+        raise ValueError("shape mismatch between q, out and the pages")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = raw.kvd_paged_decode_attention(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), out.data_ptr(),
+                                        block_table.data_ptr(), past_len.data_ptr(), B, H_q, H_kv, D, N,
+                                        page_size, max_pages, num_pages, int(max_past_len), float(scale),
+                                        _dtype_code(q), ws_ptr, ws_bytes, _ptr(err_word), _stream_handle(stream))
+    _check("kvd_paged_decode_attention", st)
+
+
+def kvd_paged_decode_step(q, k_pages, v_pages, k_new, v_new, out, block_table, past_len, max_past_len: int,
+                          scale: float = 0.0, workspace: Optional[torch.Tensor] = None, err_word=None,
+                          stream=None) -> None:
+    """kvd_decode_step over a paged cache: append into the page slots and attend, one launch."""
+    for n, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages), ("k_new", k_new),
+                 ("v_new", v_new), ("out", out)):
+        _need_cuda(n, t, q.dtype)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_q, N, D = q.shape
+    num_pages, H_kv, page_size, Dp, max_pages = _paged_geometry(k_pages, v_pages, block_table, B)
+    if out.shape != q.shape or Dp != D or tuple(k_new.shape) != (B, H_kv, N, D) or v_new.shape != k_new.shape:
+        raise ValueError("shape mismatch between q, out, the pages and the new K/V")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = raw.kvd_paged_decode_step(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), k_new.data_ptr(),
+                                   v_new.data_ptr(), out.data_ptr(), block_table.data_ptr(), past_len.data_ptr(),
+                                   B, H_q, H_kv, D, N, page_size, max_pages, num_pages, int(max_past_len),
+                                   float(scale), _dtype_code(q), ws_ptr, ws_bytes, _ptr(err_word),
+                                   _stream_handle(stream))
+    _check("kvd_paged_decode_step", st)
 
 
 def kvd_decode_attention_noalloc(q, k_cache, v_cache, out, past_len, max_past_len: int,

@@ -122,3 +122,36 @@ def layer_inputs(w: Workload, layer: int, past_len: torch.Tensor, device="cpu",
     k_cache.masked_fill_(tail, fill)
     v_cache.masked_fill_(tail, fill)
     return {"q": q, "k_new": k_new, "v_new": v_new, "k_cache": k_cache, "v_cache": v_cache}
+
+
+def to_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, page_size: int, extra_pages: int = 0,
+             seed: int = 0, fill: float = float("nan")):
+    """Lay contiguous [B,H_kv,T_max,D] caches out as a shuffled page pool.
+
+    Returns ``(k_pages, v_pages, block_table)``: pages [num_pages, H_kv, page_size, D]
+    with ``num_pages = B * max_pages + extra_pages`` (``max_pages = ceil(T_max /
+    page_size)``), logical page j of sequence b stored at the seeded random physical
+    page ``block_table[b, j]``; unused pages and the padding past T_max hold ``fill``.
+    """
+    B, H, T, D = k_cache.shape
+    max_pages = -(-T // page_size)
+    pad = max_pages * page_size - T
+    dev = k_cache.device
+
+    def logical(c):
+        if pad:
+            c = torch.cat([c, torch.full((B, H, pad, D), fill, dtype=c.dtype, device=dev)], dim=2)
+        return c.reshape(B, H, max_pages, page_size, D).permute(0, 2, 1, 3, 4).reshape(
+            B * max_pages, H, page_size, D)
+
+    n_used = B * max_pages
+    num_pages = n_used + extra_pages
+    g = torch.Generator("cpu").manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)[:n_used]
+    out = []
+    for c in (k_cache, v_cache):
+        pages = torch.full((num_pages, H, page_size, D), fill, dtype=c.dtype, device=dev)
+        pages[perm.to(dev)] = logical(c)
+        out.append(pages)
+    table = perm.to(torch.int32).view(B, max_pages).to(dev)
+    return out[0], out[1], table

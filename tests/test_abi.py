@@ -110,3 +110,31 @@ def test_workspace_query_rejects_bad_shapes(lib):
     assert lib.kvd_decode_workspace_bytes(1, 3, 2, 64, 1, 10, 1) == 0
     assert lib.kvd_decode_workspace_bytes(1, 4, 2, 80, 1, 10, 1) == 0
     assert lib.kvd_decode_workspace_bytes(1, 4, 2, 64, 0, 10, 1) == 0
+
+
+def _paged_attn(lib, q=A, k=A, v=A, out=A, table=A, past=A, B=1, H_q=4, H_kv=2, D=64, N=1,
+                page_size=64, max_pages=4, num_pages=8, max_past=10, dtype=1):
+    return lib.kvd_paged_decode_attention(q, k, v, out, table, past, B, H_q, H_kv, D, N, page_size,
+                                          max_pages, num_pages, max_past, 0.0, dtype, None, 0, None, None)
+
+
+def _paged_append(lib, k=A, v=A, kn=A, vn=A, table=A, past=A, B=1, H_kv=2, D=64, N=1, page_size=64,
+                  max_pages=4, num_pages=8, max_past=10, dtype=1):
+    return lib.kvd_paged_append(k, v, kn, vn, table, past, B, H_kv, D, N, page_size, max_pages, num_pages,
+                                max_past, dtype, None, None)
+
+
+def test_paged_argument_errors(lib):
+    for call in (_paged_attn, _paged_append):
+        assert call(lib, table=0) == 1                    # no block table
+        assert call(lib, page_size=48) == 1               # not a power of two
+        assert call(lib, page_size=32) == 1               # smaller than a tile
+        assert call(lib, max_pages=0) == 1
+        assert call(lib, num_pages=0) == 1
+        assert call(lib, max_past=256, N=1) == 2          # 4 pages x 64 tokens hold 256
+        assert call(lib, k=A + 8) == 1                    # misaligned pages
+        assert call(lib, B=0) == 0
+    assert _paged_attn(lib, D=96) == 3
+    assert _paged_attn(lib, H_q=3) == 1
+    assert lib.kvd_paged_decode_step(A, A, A, 0, A, A, A, A, 1, 4, 2, 64, 1, 64, 4, 8, 10, 0.0, 1,
+                                     None, 0, None, None) == 1   # k_new missing
