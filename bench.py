@@ -211,8 +211,14 @@ def whole_job_gbs(bytes_per_step_per_rank: int, steps: int, elapsed_max_s: float
 
 
 def oracle_layer_step(orc, host, past_np, dtype):
-    st = orc.append(host["k_cache"], host["v_cache"], host["k_new"], host["v_new"], past_np, dtype)
-    out, st2 = orc.decode_attention(host["q"], host["k_cache"], host["v_cache"], past_np, dtype)
+    if "k_pages" in host:  # paged layout
+        st = orc.paged_append(host["k_pages"], host["v_pages"], host["k_new"], host["v_new"], host["table"],
+                              past_np, dtype)
+        out, st2 = orc.paged_decode_attention(host["q"], host["k_pages"], host["v_pages"], host["table"],
+                                              past_np, dtype)
+    else:
+        st = orc.append(host["k_cache"], host["v_cache"], host["k_new"], host["v_new"], past_np, dtype)
+        out, st2 = orc.decode_attention(host["q"], host["k_cache"], host["v_cache"], past_np, dtype)
     if st != 0 or st2 != 0:
         raise RuntimeError("oracle rejected the workload")
     return out
@@ -221,6 +227,8 @@ def oracle_layer_step(orc, host, past_np, dtype):
 def to_host_np(t: torch.Tensor):
     import numpy as np
     t = t.detach().contiguous().cpu()
+    if t.dtype == torch.int32:
+        return t.numpy().copy()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16).copy()
     return t.numpy().copy()
@@ -284,7 +292,15 @@ def run_gpu(args, w, rank, world, local):
     past = wl.past_lens(w)
     max_past = int(past.max())
     past_d = past.to(dev)
-    layers = [wl.layer_inputs(w, l, past, device=dev, tail_fill="zero") for l in range(w.L)]
+    paged = args.layout == "paged"
+    layers = []
+    for l in range(w.L):
+        x = wl.layer_inputs(w, l, past, device=dev, tail_fill="zero")
+        if paged:  # the same data as a shuffled page pool with a block table
+            x["k_pages"], x["v_pages"], x["table"] = wl.to_paged(
+                x.pop("k_cache"), x.pop("v_cache"), args.page_size, seed=l, fill=0.0,
+                shuffle=args.page_order == "shuffled")
+        layers.append(x)
     outs = [torch.empty_like(x["q"]) for x in layers]
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, w.torch_dtype, dev)
@@ -297,7 +313,15 @@ def run_gpu(args, w, rank, world, local):
     def layer_step(l):
         x = layers[l]
         # the current stream: the capture stream inside torch.cuda.graph
-        if fused:
+        if paged and fused:
+            kvd.kvd_paged_decode_step(x["q"], x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], outs[l],
+                                      x["table"], past_d, max_past, 0.0, ws, err)
+        elif paged:
+            kvd.kvd_paged_append(x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], x["table"], past_d,
+                                 max_past, err)
+            kvd.kvd_paged_decode_attention(x["q"], x["k_pages"], x["v_pages"], outs[l], x["table"], past_d,
+                                           max_past, 0.0, ws, err)
+        elif fused:
             kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l], past_d,
                                 max_past, 0.0, ws, err)
         else:
@@ -331,7 +355,13 @@ def run_gpu(args, w, rank, world, local):
     with torch.cuda.graph(attn_graph):
         for l in range(w.L):
             x = layers[l]
-            if fused:  # the dominant kernel is the fused step itself
+            if paged and fused:
+                kvd.kvd_paged_decode_step(x["q"], x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], outs[l],
+                                          x["table"], past_d, max_past, 0.0, ws, err)
+            elif paged:
+                kvd.kvd_paged_decode_attention(x["q"], x["k_pages"], x["v_pages"], outs[l], x["table"], past_d,
+                                               max_past, 0.0, ws, err)
+            elif fused:  # the dominant kernel is the fused step itself
                 kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l],
                                     past_d, max_past, 0.0, ws, err)
             else:
@@ -435,6 +465,8 @@ def run_gpu(args, w, rank, world, local):
             "l2": f"no flush: inputs larger than L2 ({bytes_step / 1e9:.1f} GB per step)"
             if bytes_step > 2 * 126e6 else "warm L2 (inputs smaller than L2)",
             "parallelism": f"replicas x{world}",
+            "cache_layout": (f"paged: {args.page_size}-token pages, {args.page_order} pool, block table"
+                             if paged else "contiguous [B, H_kv, T_max, D]"),
         },
         "us_per_layer_step": round(ms_step * 1e3 / w.L, 3),
         "frac_of_peak": round(gbs / world / peak, 4),
@@ -452,7 +484,7 @@ def run_gpu(args, w, rank, world, local):
             "frac": round(achieved / peak, 4),
             "algorithmic_bytes_per_launch": a_bytes,
             "plan": plan,
-            "traffic": profiled_traffic(),
+            "traffic": None if paged else profiled_traffic(),
         },
         "cpu_baseline": {
             "value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
@@ -481,6 +513,11 @@ def main():
     ap.add_argument("--path", default="fused", choices=["fused", "separate"],
                     help="fused: kvd_decode_step per layer; separate: kvd_append + kvd_decode_attention")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"],
+                    help="KV cache layout (paged: kvd_paged_* on a shuffled page pool)")
+    ap.add_argument("--page-size", type=int, default=64, help="tokens per page for --layout paged")
+    ap.add_argument("--page-order", default="shuffled", choices=["shuffled", "sequential"],
+                    help="physical page order of the pool for --layout paged")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -335,7 +335,7 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
     const unsigned char *kg, *vg, *qg;
     uint64_t policy;
     int page_next;          // paged: physical page of the next tile (loaded one tile ahead)
-    int head_rows;          // paged: row offset of head h inside a page, h * page_size
+    const int32_t *bt_row;  // paged: block-table row of the current sequence
 
     // Paged: start the load of the next tile's page-table entry; it is used
     // one fill later, so its latency hides behind the current tile.
@@ -343,7 +343,7 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
     {
         if constexpr (kPaged) {
             if (t < hi)
-                page_next = __ldg(a.block_table + (size_t)b * (a.T_max >> a.page_shift) + ((tin * S::kTK) >> a.page_shift));
+                page_next = __ldg(bt_row + ((tin * S::kTK) >> a.page_shift));
         }
     }
 
@@ -361,9 +361,10 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
             if (tin == 0) static_cast<int2 *>(a.merge_state)[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
         }
         if constexpr (kPaged) {
-            head_rows = h << a.page_shift;
-            kg = static_cast<const unsigned char *>(a.k_cache);
-            vg = static_cast<const unsigned char *>(a.v_cache);
+            const size_t hoff = ((size_t)h << a.page_shift) * S::kRowBytes;
+            kg = static_cast<const unsigned char *>(a.k_cache) + hoff;
+            vg = static_cast<const unsigned char *>(a.v_cache) + hoff;
+            bt_row = a.block_table + (size_t)b * (a.T_max >> a.page_shift);
         } else {
             const size_t row = (size_t)bh * a.T_max;
             kg = static_cast<const unsigned char *>(a.k_cache) + row * S::kRowBytes;
@@ -436,7 +437,7 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
         if constexpr (kPaged) {
             page = page_next;
             int *stage_page = reinterpret_cast<int *>(smem + S::kPageOff);
-            if (page < 0 || page >= a.num_pages) {
+            if ((unsigned)page >= (unsigned)a.num_pages) {
                 // Never read outside the pool: load page 0 instead, flag the
                 // error, and tell the fused step not to write this tile.
                 raise_error(a.err_word, KVD_DEVERR_PAGE);
@@ -445,8 +446,10 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
             } else {
                 stage_page[s] = page;
             }
-            off = (((size_t)page * a.H_kv << a.page_shift) + head_rows +
-                   (mt.tile_k0 & ((1 << a.page_shift) - 1))) * S::kRowBytes;
+            // (kg already points at head h's rows of page 0; few operations
+            // here, as this runs on the producer's critical path every tile)
+            off = (size_t)page * (((size_t)a.H_kv * S::kRowBytes) << a.page_shift) +
+                  (size_t)(mt.tile_k0 & ((1 << a.page_shift) - 1)) * S::kRowBytes;
         } else {
             off = (size_t)mt.tile_k0 * S::kRowBytes;
         }

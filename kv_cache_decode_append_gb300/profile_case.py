@@ -3,7 +3,8 @@
     python -m kv_cache_decode_append_gb300.profile_case --workload gqa_longctx_b32_bf16 --launches 3
 
 Each launch is one kvd_append + kvd_decode_attention (or, with --fused, one
-kvd_decode_step) on the same layer, so a
+kvd_decode_step; with --layout paged, their paged forms on a shuffled page
+pool) on the same layer, so a
 profiler filtered on a kernel name sees ``--launches`` identical launches with
 the full-size per-layer working set (for the default workload 2 x 545 MB of
 cache, larger than L2) and nothing else on the device.
@@ -24,6 +25,8 @@ def main():
     ap.add_argument("--n-new", type=int, default=None)
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--fused", action="store_true", help="kvd_decode_step instead of append + attention")
+    ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"])
+    ap.add_argument("--page-size", type=int, default=64)
     args = ap.parse_args()
     w = wl.WORKLOADS[args.workload]
     if args.n_new is not None:
@@ -36,8 +39,16 @@ def main():
     past_d = past.to(dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, w.torch_dtype, dev)
+    if args.layout == "paged":
+        kp, vp, table = wl.to_paged(x.pop("k_cache"), x.pop("v_cache"), args.page_size, fill=0.0)
     for _ in range(args.launches):
-        if args.fused:
+        if args.layout == "paged" and args.fused:
+            kvd.kvd_paged_decode_step(x["q"], kp, vp, x["k_new"], x["v_new"], out, table, past_d, max_past, 0.0,
+                                      ws, err)
+        elif args.layout == "paged":
+            kvd.kvd_paged_append(kp, vp, x["k_new"], x["v_new"], table, past_d, max_past, err)
+            kvd.kvd_paged_decode_attention(x["q"], kp, vp, out, table, past_d, max_past, 0.0, ws, err)
+        elif args.fused:
             kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], out, past_d,
                                 max_past, 0.0, ws, err)
         else:

@@ -125,13 +125,14 @@ def layer_inputs(w: Workload, layer: int, past_len: torch.Tensor, device="cpu",
 
 
 def to_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, page_size: int, extra_pages: int = 0,
-             seed: int = 0, fill: float = float("nan")):
+             seed: int = 0, fill: float = float("nan"), shuffle: bool = True):
     """Lay contiguous [B,H_kv,T_max,D] caches out as a shuffled page pool.
 
     Returns ``(k_pages, v_pages, block_table)``: pages [num_pages, H_kv, page_size, D]
     with ``num_pages = B * max_pages + extra_pages`` (``max_pages = ceil(T_max /
     page_size)``), logical page j of sequence b stored at the seeded random physical
-    page ``block_table[b, j]``; unused pages and the padding past T_max hold ``fill``.
+    page ``block_table[b, j]`` (or, without ``shuffle``, at page ``b * max_pages + j``);
+    unused pages and the padding past T_max hold ``fill``.
     """
     B, H, T, D = k_cache.shape
     max_pages = -(-T // page_size)
@@ -147,7 +148,7 @@ def to_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, page_size: int, extra
     n_used = B * max_pages
     num_pages = n_used + extra_pages
     g = torch.Generator("cpu").manual_seed(seed)
-    perm = torch.randperm(num_pages, generator=g)[:n_used]
+    perm = torch.randperm(num_pages, generator=g)[:n_used] if shuffle else torch.arange(n_used)
     out = []
     for c in (k_cache, v_cache):
         pages = torch.full((num_pages, H, page_size, D), fill, dtype=c.dtype, device=dev)
