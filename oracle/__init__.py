@@ -4,8 +4,8 @@ TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product package
 (``kv_cache_decode_append_gb300``) never imports it and shares no code with it.
 
-Arrays are numpy: fp32 data as ``float32``, bf16 data as ``uint16`` holding the
-raw bf16 bits.  Outputs of the attention routines are ``float64``.
+Arrays are numpy: fp32 data as ``float32``, bf16 and fp16 data as ``uint16``
+holding the raw bits.  Outputs of the attention routines are ``float64``.
 """
 from __future__ import annotations
 
@@ -21,8 +21,8 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
-F32, BF16 = 0, 1
-_DTYPES = {"f32": F32, "bf16": BF16}
+F32, BF16, F16 = 0, 1, 2
+_DTYPES = {"f32": F32, "bf16": BF16, "f16": F16}
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +67,8 @@ class Oracle:
         lib.oracle_paged_decode_attention.restype = ci
         lib.oracle_paged_decode_attention.argtypes = [vp, vp, vp, dp, i32p, i32p, ci, ci, ci, ci, ci, ci,
                                                       ci, ci, cd, ci]
+        lib.oracle_widen.restype = ci
+        lib.oracle_widen.argtypes = [vp, dp, cll, ci]
         lib.oracle_full_causal_attention.restype = ci
         lib.oracle_full_causal_attention.argtypes = [dp, dp, dp, dp, ci, ci, cd]
         self.lib = lib
@@ -82,6 +84,15 @@ class Oracle:
             raise ValueError(f"{name} must be C-contiguous")
 
     # -- entry points --------------------------------------------------------------
+    def widen(self, arr: np.ndarray, dtype: str) -> np.ndarray:
+        """The stored values of ``arr`` (oracle representation) as float64."""
+        self._check(arr, dtype, "arr")
+        out = np.empty(arr.shape, dtype=np.float64)
+        if self.lib.oracle_widen(arr.ctypes.data, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                 arr.size, _DTYPES[dtype]) != 0:
+            raise ValueError("oracle_widen rejected its arguments")
+        return out
+
     def cache_bytes(self, L, B, H_kv, D, T, bytes_per_elem) -> int:
         return int(self.lib.oracle_cache_bytes(L, B, H_kv, D, T, bytes_per_elem))
 

@@ -57,7 +57,8 @@
  *   - GQA: query head hq uses KV head hq / (H_q / H_kv) (consecutive query
  *     heads share one KV head);
  *   - past_len[b] is the number of cached tokens BEFORE the append;
- *   - bf16 values are widened exactly (bf16 bits << 16 is the fp32 value).
+ *   - bf16 values are widened exactly (bf16 bits << 16 is the fp32 value);
+ *     fp16 values exactly from the IEEE binary16 encoding.
  *
  * Paged layout (a reading: the pages do not fix one): pages are
  * [num_pages, H_kv, page_size, D] row-major; logical page j of sequence b is
@@ -77,11 +78,27 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
 
 static int elem_bytes(int dtype)
 {
-    return dtype == ORACLE_F32 ? 4 : (dtype == ORACLE_BF16 ? 2 : 0);
+    return dtype == ORACLE_F32 ? 4 : ((dtype == ORACLE_BF16 || dtype == ORACLE_F16) ? 2 : 0);
+}
+
+/* An IEEE 754 binary16 value (1 sign, 5 exponent, 10 fraction bits, bias 15)
+ * as a double, exactly: normal numbers are (1024 + fraction) * 2^(exponent - 25),
+ * subnormals fraction * 2^-24, exponent 31 is infinity (fraction 0) or NaN. */
+static double half_bits_to_double(uint16_t h)
+{
+    const int sign = h >> 15, expo = (h >> 10) & 0x1f, frac = h & 0x3ff;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -24);
+    else if (expo == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), expo - 25);
+    return sign ? -v : v;
 }
 
 /* One stored element widened to double.  A bf16 value is the upper half of
@@ -90,6 +107,9 @@ static double load_elem(const void *base, size_t idx, int dtype)
 {
     if (dtype == ORACLE_F32) {
         return (double)((const float *)base)[idx];
+    }
+    if (dtype == ORACLE_F16) {
+        return half_bits_to_double(((const uint16_t *)base)[idx]);
     }
     uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
     float f;
@@ -380,4 +400,12 @@ int oracle_paged_decode_attention(const void *q, const void *k_pages, const void
     free(vc);
     free(pl);
     return status;
+}
+
+/* The dtype's stored values widened to double (test hook for the widening pins). */
+int oracle_widen(const void *src, double *dst, long long n, int dtype)
+{
+    if (!src || !dst || n < 0 || elem_bytes(dtype) == 0) return 1;
+    for (long long i = 0; i < n; ++i) dst[i] = load_elem(src, (size_t)i, dtype);
+    return 0;
 }

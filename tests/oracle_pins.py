@@ -36,16 +36,19 @@ _UNITS = {"B": 1, "KiB": 1024, "MiB": 1024 ** 2}
 
 # ---------------------------------------------------------------------------------
 # helpers (no attention arithmetic here: inputs and conversions only)
+_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
 def _rand(shape, seed, dtype):
     g = torch.Generator("cpu").manual_seed(seed)
     t = torch.randn(shape, generator=g, dtype=torch.float32)
-    return t.to(torch.bfloat16) if dtype == "bf16" else t
+    return t.to(_TORCH[dtype])
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
     """Oracle representation: float32, or uint16 raw bits for bf16."""
     t = t.contiguous()
-    if t.dtype == torch.bfloat16:
+    if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).numpy().view(np.uint16).copy()
     return t.numpy().copy()
 
@@ -151,7 +154,7 @@ def pin_single_visible_key(orc):
     assert torch.equal(torch.isnan(out), torch.isnan(want))
     fin = ~torch.isnan(want)
     assert torch.equal(out[fin], want[fin])
-    for dtype in ("f32", "bf16"):
+    for dtype in ("f32", "bf16", "f16"):
         q, k_new, v_new, k_cache, v_cache, past_len = _problem(2, 4, 2, 16, 1, 5, [0, 0], dtype, 11)
         kc, vc = _appended(k_cache, v_cache, k_new, v_new, past_len)
         out = _oracle_decode(orc, q, kc, vc, past_len, dtype)
@@ -159,9 +162,21 @@ def pin_single_visible_key(orc):
         assert torch.equal(out, want)
 
 
+def pin_widening_all_patterns(orc):
+    """Every bf16 and fp16 bit pattern widens to the value torch's own conversion gives."""
+    bits = torch.arange(1 << 16, dtype=torch.int32).to(torch.int16)
+    for dtype, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        vals = bits.view(tdt)
+        got = orc.widen(to_np(vals), dtype)
+        want = vals.to(torch.float64).numpy()
+        assert np.array_equal(np.isnan(got), np.isnan(want))
+        fin = ~np.isnan(want)
+        assert np.array_equal(got[fin], want[fin])
+
+
 def pin_identical_keys_mean(orc):
     """All keys equal: equal weights, so row i is the mean of the P+i+1 visible value rows."""
-    for dtype in ("f32", "bf16"):
+    for dtype in ("f32", "bf16", "f16"):
         B, H_q, H_kv, D, N, T_max = 2, 4, 2, 8, 4, 16
         past = [5, 9]
         q, k_new, v_new, k_cache, v_cache, past_len = _problem(B, H_q, H_kv, D, N, T_max, past, dtype, 21)
@@ -181,7 +196,7 @@ def pin_identical_keys_mean(orc):
 def pin_dominant_key(orc):
     """One key aligned with q far above the rest: softmax puts all weight on it."""
     D, T_max = 16, 12
-    for dtype in ("f32", "bf16"):
+    for dtype in ("f32", "bf16", "f16"):
         q, k_new, v_new, k_cache, v_cache, past_len = _problem(1, 2, 1, D, 2, T_max, [7], dtype, 31)
         q[:] = _rand((D,), 5, dtype)
         for j in (0, 3, 6):  # history positions, visible to both new rows
@@ -221,6 +236,7 @@ _ROUTE_CASES = [
     (2, 8, 2, 128, 3, 33, [30, 7], "bf16", None),
     (3, 8, 1, 64, 16, 48, [32, 0, 5], "bf16", 0.3),
     (1, 6, 3, 128, 5, 21, [16], "f32", 1.7),
+    (2, 8, 4, 64, 2, 24, [9, 21], "f16", None),
 ]
 
 
@@ -360,6 +376,7 @@ ALL_PINS = [
     pin_cache_bytes,
     pin_append_is_concat,
     pin_single_visible_key,
+    pin_widening_all_patterns,
     pin_identical_keys_mean,
     pin_dominant_key,
     pin_route_b_sdpa,

@@ -36,6 +36,10 @@ MUTANTS = [
      "(size_t)(P + i)) * row;", "(size_t)(i)) * row;"),
     ("bf16 widened with the wrong shift",
      "[idx] << 16;", "[idx] << 15;"),
+    ("fp16 exponent bias off by one",
+     "ldexp((double)(1024 + frac), expo - 25)", "ldexp((double)(1024 + frac), expo - 24)"),
+    ("fp16 subnormals scaled as normals",
+     "v = ldexp((double)frac, -24);", "v = ldexp((double)(1024 + frac), -25);"),
     ("size formula without the factor 2 for K and V",
      "(2LL * L * H_kv", "(1LL * L * H_kv"),
     ("paged: page slot and page index swapped",
