@@ -229,7 +229,7 @@ def to_host_np(t: torch.Tensor):
     t = t.detach().contiguous().cpu()
     if t.dtype == torch.int32:
         return t.numpy().copy()
-    if t.dtype == torch.bfloat16:
+    if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).numpy().view(np.uint16).copy()
     return t.numpy().copy()
 

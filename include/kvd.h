@@ -26,8 +26,8 @@
  *
  * Conventions for every entry point
  *   - Layouts are dense row-major: caches [B, H_kv, T_max, D]; q and out
- *     [B, H_q, N, D]; k_new and v_new [B, H_kv, N, D].  One dtype (fp32 or
- *     bf16) covers q, caches, new K/V and out; arithmetic accumulates in fp32.
+ *     [B, H_q, N, D]; k_new and v_new [B, H_kv, N, D].  One dtype (fp32, bf16
+ *     or fp16) covers q, caches, new K/V and out; arithmetic accumulates in fp32.
  *   - Pointers named as device pointers must be CUDA device memory of the
  *     current device and 16-byte aligned.  Every buffer is owned by the caller;
  *     the library allocates nothing, keeps no pointer after the call returns,
@@ -63,7 +63,7 @@ typedef enum kvd_status {
     KVD_ERR_CUDA = 5         /* a CUDA call or launch failed */
 } kvd_status;
 
-typedef enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1 } kvd_dtype;
+typedef enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1, KVD_F16 = 2 } kvd_dtype;
 
 /* Bits OR-ed into the device error word. */
 #define KVD_DEVERR_PAST_LEN 1u /* a sequence had an out-of-range past_len and was skipped */
@@ -84,7 +84,7 @@ typedef enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1 } kvd_dtype;
  *   max_past_len      host bound on every past_len[b] (checked on the device)
  *   err_word          device uint32 or NULL (see conventions)
  * Returns KVD_OK, KVD_ERR_INVALID_ARG, KVD_ERR_CAPACITY, KVD_ERR_UNSUPPORTED or
- * KVD_ERR_CUDA.  D may be any positive multiple of 8 (bf16) or 4 (fp32).
+ * KVD_ERR_CUDA.  D may be any positive multiple of 8 (bf16, fp16) or 4 (fp32).
  */
 kvd_status kvd_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
                       const int32_t *past_len, int B, int H_kv, int T_max, int D, int N,
@@ -110,7 +110,7 @@ size_t kvd_decode_workspace_bytes(int B, int H_q, int H_kv, int D, int N, int ma
  * Slots j > P+i (including any stale or NaN slot past P+N-1) are never read.
  *
  *   q, out            device, [B, H_q, N, D]; out gets the input dtype
- *                     (bf16 rounded to nearest even from the fp32 result)
+ *                     (bf16 / fp16 rounded to nearest even from the fp32 result)
  *   k_cache, v_cache  device, [B, H_kv, T_max, D], already appended
  *   scale             softmax scale; <= 0 selects 1/sqrt(D)
  *   workspace         device scratch of at least kvd_decode_workspace_bytes(...)
@@ -119,7 +119,7 @@ size_t kvd_decode_workspace_bytes(int B, int H_q, int H_kv, int D, int N, int ma
  *                     leaves it zero-filled again, so it is reused as is.  Zero
  *                     it again after a call that reported KVD_DEVERR_TIMEOUT.
  *                     Calls that run concurrently need distinct workspaces.
- * Supported: D in {64, 128}; dtype fp32 or bf16; H_q % H_kv == 0;
+ * Supported: D in {64, 128}; dtype fp32, bf16 or fp16; H_q % H_kv == 0;
  * (H_q / H_kv) * N <= 128.
  * Returns KVD_OK or the first argument error found (see kvd_status).
  * The workspace size does not depend on the cache layout: the paged calls
@@ -259,7 +259,7 @@ kvd_status kvd_workspace_init(void *workspace, size_t workspace_bytes, void *str
 
 /*
  * kvd_cache_bytes -- bytes of K and V caches for L layers:
- *   2 * L * H_kv * D * T * B * (4 for fp32, 2 for bf16); 0 on invalid input.
+ *   2 * L * H_kv * D * T * B * (4 for fp32, 2 for bf16 and fp16); 0 on invalid input.
  */
 size_t kvd_cache_bytes(int L, int B, int H_kv, int D, int T, kvd_dtype dtype);
 

@@ -168,7 +168,7 @@ kvd_status occupancy(int dev, const void *fn, int threads, int smem, int *ctas_p
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int elem_bytes(kvd_dtype dt) { return dt == KVD_F32 ? 4 : (dt == KVD_BF16 ? 2 : 0); }
+int elem_bytes(kvd_dtype dt) { return dt == KVD_F32 ? 4 : ((dt == KVD_BF16 || dt == KVD_F16) ? 2 : 0); }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -196,11 +196,19 @@ kvd_status check_shapes(int B, int H_q, int H_kv, int D, int N, int max_past_len
 // shared memory layout and tiles.
 bool pick_builds(kvd_dtype dtype, int D, int rb, bool paged, AttnVariant *vp, AttnVariant *vt)
 {
-    if (paged)
-        return dtype == KVD_F32 ? attn_variant_f32_paged(D, rb, vp) && attn_variant_f32_tk_paged(D, rb, vt)
-                                : attn_variant_bf16_paged(D, rb, vp) && attn_variant_bf16_tk_paged(D, rb, vt);
-    return dtype == KVD_F32 ? attn_variant_f32(D, rb, vp) && attn_variant_f32_tk(D, rb, vt)
-                            : attn_variant_bf16(D, rb, vp) && attn_variant_bf16_tk(D, rb, vt);
+    switch (dtype) {
+    case KVD_F32:
+        return paged ? attn_variant_f32_paged(D, rb, vp) && attn_variant_f32_tk_paged(D, rb, vt)
+                     : attn_variant_f32(D, rb, vp) && attn_variant_f32_tk(D, rb, vt);
+    case KVD_BF16:
+        return paged ? attn_variant_bf16_paged(D, rb, vp) && attn_variant_bf16_tk_paged(D, rb, vt)
+                     : attn_variant_bf16(D, rb, vp) && attn_variant_bf16_tk(D, rb, vt);
+    case KVD_F16:
+        return paged ? attn_variant_f16_paged(D, rb, vp) && attn_variant_f16_tk_paged(D, rb, vt)
+                     : attn_variant_f16(D, rb, vp) && attn_variant_f16_tk(D, rb, vt);
+    default:
+        return false;
+    }
 }
 
 // Lowest resident CTAs per SM over the attention and fused-step kernels of both builds.

@@ -984,7 +984,7 @@ template <typename T, bool kTicketMerge, bool kPaged> bool pick_variant(int D, i
     }
 }
 
-// One translation unit each: kvd_attn_{f32,bf16}[_tk][_paged].cu -- merge
+// One translation unit each: kvd_attn_{f32,bf16,f16}[_tk][_paged].cu -- merge
 // pass or in-kernel merge (_tk), contiguous or paged cache (_paged).
 bool attn_variant_f32(int D, int RB, AttnVariant *v);
 bool attn_variant_bf16(int D, int RB, AttnVariant *v);
@@ -994,5 +994,9 @@ bool attn_variant_f32_paged(int D, int RB, AttnVariant *v);
 bool attn_variant_bf16_paged(int D, int RB, AttnVariant *v);
 bool attn_variant_f32_tk_paged(int D, int RB, AttnVariant *v);
 bool attn_variant_bf16_tk_paged(int D, int RB, AttnVariant *v);
+bool attn_variant_f16(int D, int RB, AttnVariant *v);
+bool attn_variant_f16_tk(int D, int RB, AttnVariant *v);
+bool attn_variant_f16_paged(int D, int RB, AttnVariant *v);
+bool attn_variant_f16_tk_paged(int D, int RB, AttnVariant *v);
 
 }  // namespace kvd

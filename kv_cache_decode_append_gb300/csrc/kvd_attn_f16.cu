@@ -1,0 +1,7 @@
+// Instantiates the fp16 decode-attention kernels with the separate merge pass
+// (D in {64, 128}, RB in {1, 2, 4, 8}).
+#include "kvd_attention.cuh"
+
+namespace kvd {
+bool attn_variant_f16(int D, int RB, AttnVariant *v) { return pick_variant<__half, false, false>(D, RB, v); }
+}  // namespace kvd

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -225,6 +226,38 @@ template <> struct Elem<__nv_bfloat16> {
     {
         *dst = __float2bfloat16_rn(v);
     }
+};
+
+template <> struct Elem<__half> {
+    static constexpr int kBytes = 2;
+    static constexpr int kPerChunk = 8;
+    // element 2k in the low half of word k, element 2k+1 in the high half
+    __device__ __forceinline__ static float2 pair(uint32_t w)
+    {
+        __half2 h;
+        memcpy(&h, &w, sizeof h);
+        return __half22float2(h);
+    }
+    __device__ __forceinline__ static void widen(const uint4 &c, float *f)
+    {
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 p = pair(w[k]);
+            f[2 * k] = p.x;
+            f[2 * k + 1] = p.y;
+        }
+    }
+    __device__ __forceinline__ static void widen2(const uint4 &c, f32x2 *f)
+    {
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 p = pair(w[k]);
+            f[k] = pack2(p.x, p.y);
+        }
+    }
+    __device__ __forceinline__ static void store(__half *dst, float v) { *dst = __float2half_rn(v); }
 };
 
 // Atomic add at GPU scope with acquire-release semantics; returns the old

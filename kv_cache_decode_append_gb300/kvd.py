@@ -32,13 +32,14 @@ KVD_ERR_CUDA = 5
 
 KVD_F32 = 0
 KVD_BF16 = 1
+KVD_F16 = 2
 
 KVD_DEVERR_PAST_LEN = 1
 KVD_DEVERR_TIMEOUT = 2
 KVD_DEVERR_PAGE = 4
 
-_TORCH_DTYPE = {torch.float32: KVD_F32, torch.bfloat16: KVD_BF16}
-_NAME_DTYPE = {"f32": KVD_F32, "bf16": KVD_BF16}
+_TORCH_DTYPE = {torch.float32: KVD_F32, torch.bfloat16: KVD_BF16, torch.float16: KVD_F16}
+_NAME_DTYPE = {"f32": KVD_F32, "bf16": KVD_BF16, "f16": KVD_F16}
 
 
 class KvdError(RuntimeError):

@@ -26,7 +26,7 @@ from typing import Optional, Tuple
 
 import torch
 
-DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 @dataclass(frozen=True)
@@ -39,7 +39,7 @@ class Workload:
     H_kv: int                # KV heads
     D: int                   # head dim
     N: int                   # new tokens per sequence
-    dtype: str               # "f32" | "bf16" (cache, q, new K/V and output)
+    dtype: str               # "f32" | "bf16" | "f16" (cache, q, new K/V and output)
     T_max: int               # preallocated slots per cache row
     P: Optional[int] = None                  # history length (same for every sequence)
     P_range: Optional[Tuple[int, int]] = None  # inclusive range, drawn per sequence
