@@ -21,8 +21,8 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
-F32, BF16, F16 = 0, 1, 2
-_DTYPES = {"f32": F32, "bf16": BF16, "f16": F16}
+F32, BF16, F16, E4M3 = 0, 1, 2, 3
+_DTYPES = {"f32": F32, "bf16": BF16, "f16": F16, "e4m3": E4M3}
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +67,15 @@ class Oracle:
         lib.oracle_paged_decode_attention.restype = ci
         lib.oracle_paged_decode_attention.argtypes = [vp, vp, vp, dp, i32p, i32p, ci, ci, ci, ci, ci, ci,
                                                       ci, ci, cd, ci]
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_append_e4m3.restype = ci
+        lib.oracle_append_e4m3.argtypes = [u8p, u8p, vp, vp, i32p, ci, ci, ci, ci, ci, ci, ctypes.c_float,
+                                           ctypes.c_float]
+        lib.oracle_decode_attention_e4m3.restype = ci
+        lib.oracle_decode_attention_e4m3.argtypes = [vp, u8p, u8p, dp, i32p, ci, ci, ci, ci, ci, ci, cd, ci,
+                                                     cd, cd]
+        lib.oracle_quantize_e4m3.restype = ci
+        lib.oracle_quantize_e4m3.argtypes = [ctypes.POINTER(ctypes.c_float), u8p, cll]
         lib.oracle_widen.restype = ci
         lib.oracle_widen.argtypes = [vp, dp, cll, ci]
         lib.oracle_full_causal_attention.restype = ci
@@ -77,7 +86,7 @@ class Oracle:
     # -- helpers ---------------------------------------------------------------
     @staticmethod
     def _check(arr: np.ndarray, dtype: str, name: str) -> None:
-        want = np.float32 if dtype == "f32" else np.uint16
+        want = {"f32": np.float32, "e4m3": np.uint8}.get(dtype, np.uint16)
         if arr.dtype != want:
             raise TypeError(f"{name}: expected {np.dtype(want)} for {dtype}, got {arr.dtype}")
         if not arr.flags.c_contiguous:
@@ -92,6 +101,54 @@ class Oracle:
                                  arr.size, _DTYPES[dtype]) != 0:
             raise ValueError("oracle_widen rejected its arguments")
         return out
+
+    def quantize_e4m3(self, x: np.ndarray) -> np.ndarray:
+        """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating at 448."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty(x.shape, dtype=np.uint8)
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        if self.lib.oracle_quantize_e4m3(x.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                         out.ctypes.data_as(u8p), x.size) != 0:
+            raise ValueError("oracle_quantize_e4m3 rejected its arguments")
+        return out
+
+    def append_e4m3(self, k_cache, v_cache, k_new, v_new, past_len, new_dtype: str, k_scale: float,
+                    v_scale: float) -> int:
+        """In place on the uint8 E4M3 caches [B,H_kv,T_max,D]; returns the status."""
+        self._check(k_cache, "e4m3", "k_cache")
+        self._check(v_cache, "e4m3", "v_cache")
+        self._check(k_new, new_dtype, "k_new")
+        self._check(v_new, new_dtype, "v_new")
+        past_len = np.ascontiguousarray(past_len, dtype=np.int32)
+        B, H_kv, T_max, D = k_cache.shape
+        N = k_new.shape[2]
+        if v_cache.shape != k_cache.shape or k_new.shape != (B, H_kv, N, D) or v_new.shape != k_new.shape:
+            raise ValueError("shape mismatch")
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        return int(self.lib.oracle_append_e4m3(
+            k_cache.ctypes.data_as(u8p), v_cache.ctypes.data_as(u8p), k_new.ctypes.data, v_new.ctypes.data,
+            past_len.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), B, H_kv, T_max, D, N,
+            _DTYPES[new_dtype], float(k_scale), float(v_scale)))
+
+    def decode_attention_e4m3(self, q, k_cache, v_cache, past_len, q_dtype: str, k_scale: float,
+                              v_scale: float, scale=None):
+        """Returns ``(out float64 [B,H_q,N,D], status)`` over appended E4M3 caches."""
+        self._check(q, q_dtype, "q")
+        self._check(k_cache, "e4m3", "k_cache")
+        self._check(v_cache, "e4m3", "v_cache")
+        past_len = np.ascontiguousarray(past_len, dtype=np.int32)
+        B, H_q, N, D = q.shape
+        _, H_kv, T_max, _ = k_cache.shape
+        if scale is None:
+            scale = 1.0 / np.sqrt(D)
+        out = np.empty((B, H_q, N, D), dtype=np.float64)
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        st = self.lib.oracle_decode_attention_e4m3(
+            q.ctypes.data, k_cache.ctypes.data_as(u8p), v_cache.ctypes.data_as(u8p),
+            out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+            past_len.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            B, H_q, H_kv, T_max, D, N, float(scale), _DTYPES[q_dtype], float(k_scale), float(v_scale))
+        return out, int(st)
 
     def cache_bytes(self, L, B, H_kv, D, T, bytes_per_elem) -> int:
         return int(self.lib.oracle_cache_bytes(L, B, H_kv, D, T, bytes_per_elem))

@@ -43,6 +43,17 @@
  *                            the remedy for reallocation]; defined here as the
  *                            contiguous operations applied to the cache gathered
  *                            through the block table
+ *   oracle_append_e4m3, oracle_decode_attention_e4m3
+ *                            the same two operations with an 8-bit floating-point
+ *                            (E4M3) cache and per-tensor K and V scales: the pages
+ *                            name FP8 among the cache precisions used in serving
+ *                            and say quantization pays most at decode
+ *                            [openai-hub.com/news/2435, section "实验到底测了什么"
+ *                             (what the experiment measured), the paragraph after the
+ *                             configuration table; jennyma11.github.io/infra/ch07-01,
+ *                             section "Decode 阶段"];
+ *                            they give no format, so the format and the scaling
+ *                            are a reading (see the design notes)
  *   oracle_full_causal_attention
  *                            the uncached route: ordinary causal attention of
  *                            T query rows over T keys (row t sees keys 0..t)
@@ -58,7 +69,8 @@
  *     heads share one KV head);
  *   - past_len[b] is the number of cached tokens BEFORE the append;
  *   - bf16 values are widened exactly (bf16 bits << 16 is the fp32 value);
- *     fp16 values exactly from the IEEE binary16 encoding.
+ *     fp16 values exactly from the IEEE binary16 encoding; E4M3 codes (an
+ *     8-bit cache format) exactly from their encoding, times a per-tensor scale.
  *
  * Paged layout (a reading: the pages do not fix one): pages are
  * [num_pages, H_kv, page_size, D] row-major; logical page j of sequence b is
@@ -78,11 +90,30 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2, ORACLE_E4M3 = 3 };
 
 static int elem_bytes(int dtype)
 {
-    return dtype == ORACLE_F32 ? 4 : ((dtype == ORACLE_BF16 || dtype == ORACLE_F16) ? 2 : 0);
+    if (dtype == ORACLE_F32) return 4;
+    if (dtype == ORACLE_BF16 || dtype == ORACLE_F16) return 2;
+    return dtype == ORACLE_E4M3 ? 1 : 0;
+}
+
+/* An 8-bit E4M3 value (1 sign, 4 exponent, 3 fraction bits, bias 7; no
+ * infinities, exponent 15 with fraction 7 is NaN, the largest finite value is
+ * 448) as a double: normal numbers (8 + fraction) * 2^(exponent - 10),
+ * subnormals fraction * 2^-9. */
+static double e4m3_bits_to_double(uint8_t c)
+{
+    const int sign = c >> 7, expo = (c >> 3) & 0xf, frac = c & 0x7;
+    double v;
+    if (expo == 15 && frac == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)frac, -9);
+    else
+        v = ldexp((double)(8 + frac), expo - 10);
+    return sign ? -v : v;
 }
 
 /* An IEEE 754 binary16 value (1 sign, 5 exponent, 10 fraction bits, bias 15)
@@ -110,6 +141,9 @@ static double load_elem(const void *base, size_t idx, int dtype)
     }
     if (dtype == ORACLE_F16) {
         return half_bits_to_double(((const uint16_t *)base)[idx]);
+    }
+    if (dtype == ORACLE_E4M3) {
+        return e4m3_bits_to_double(((const uint8_t *)base)[idx]);
     }
     uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
     float f;
@@ -188,11 +222,13 @@ int oracle_append(void *k_cache, void *v_cache, const void *k_new, const void *v
  * out is double [B, H_q, N, D].  Rows of a sequence with an invalid
  * past_len (P < 0 or P + N > T_max) are set to NaN and status 2 is returned.
  */
-int oracle_decode_attention(const void *q, const void *k_cache, const void *v_cache,
-                            double *out, const int32_t *past_len, int B, int H_q,
-                            int H_kv, int T_max, int D, int N, double scale, int dtype)
+static int decode_attention_impl(const void *q, const void *k_cache, const void *v_cache,
+                                 double *out, const int32_t *past_len, int B, int H_q,
+                                 int H_kv, int T_max, int D, int N, double scale, int dtype,
+                                 int kv_dtype, double k_scale, double v_scale)
 {
     if (!q || !k_cache || !v_cache || !out || !past_len || elem_bytes(dtype) == 0 ||
+        elem_bytes(kv_dtype) == 0 ||
         B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || T_max <= 0 || D <= 0 || N <= 0)
         return 1;
     const int g = H_q / H_kv;
@@ -223,7 +259,7 @@ int oracle_decode_attention(const void *q, const void *k_cache, const void *v_ca
                     const size_t k_row = (kv_head + (size_t)j) * (size_t)D;
                     double dot = 0.0;
                     for (int d = 0; d < D; ++d)
-                        dot += load_elem(q, q_row + d, dtype) * load_elem(k_cache, k_row + d, dtype);
+                        dot += load_elem(q, q_row + d, dtype) * (k_scale * load_elem(k_cache, k_row + d, kv_dtype));
                     scores[j] = scale * dot;
                     if (scores[j] > m) m = scores[j];
                 }
@@ -234,7 +270,7 @@ int oracle_decode_attention(const void *q, const void *k_cache, const void *v_ca
                     const double w = exp(scores[j] - m);
                     const size_t v_row = (kv_head + (size_t)j) * (size_t)D;
                     wsum += w;
-                    for (int d = 0; d < D; ++d) o[d] += w * load_elem(v_cache, v_row + d, dtype);
+                    for (int d = 0; d < D; ++d) o[d] += w * (v_scale * load_elem(v_cache, v_row + d, kv_dtype));
                 }
                 for (int d = 0; d < D; ++d) o[d] /= wsum;
             }
@@ -242,6 +278,14 @@ int oracle_decode_attention(const void *q, const void *k_cache, const void *v_ca
         }
     }
     return status;
+}
+
+int oracle_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                            double *out, const int32_t *past_len, int B, int H_q,
+                            int H_kv, int T_max, int D, int N, double scale, int dtype)
+{
+    return decode_attention_impl(q, k_cache, v_cache, out, past_len, B, H_q, H_kv, T_max, D, N,
+                                 scale, dtype, dtype, 1.0, 1.0);
 }
 
 /*
@@ -407,5 +451,88 @@ int oracle_widen(const void *src, double *dst, long long n, int dtype)
 {
     if (!src || !dst || n < 0 || elem_bytes(dtype) == 0) return 1;
     for (long long i = 0; i < n; ++i) dst[i] = load_elem(src, (size_t)i, dtype);
+    return 0;
+}
+
+/*
+ * E4M3 quantization of one fp32 value: the nearest finite E4M3 value, ties to
+ * the even code (the one whose fraction ends in 0), magnitudes beyond 448
+ * saturated to 448 (the conversion saturates instead of overflowing), NaN
+ * kept NaN.  Written as a search over the 127 non-negative finite codes, in
+ * increasing order of value.
+ */
+static uint8_t e4m3_from_float(float x)
+{
+    if (isnan(x)) return 0x7f;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    int best = 0;
+    double best_err = a;  /* code 0 is +0 */
+    for (int c = 1; c < 0x7f; ++c) {
+        const double err = fabs(e4m3_bits_to_double((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/*
+ * Append with an E4M3 cache: as oracle_append, with the stored code of each
+ * new element x (new_dtype: fp32, bf16 or fp16) being the quantization of the
+ * fp32 quotient x / scale (k_scale for K, v_scale for V), divided in fp32.
+ */
+int oracle_append_e4m3(uint8_t *k_cache, uint8_t *v_cache, const void *k_new, const void *v_new,
+                       const int32_t *past_len, int B, int H_kv, int T_max, int D, int N,
+                       int new_dtype, float k_scale, float v_scale)
+{
+    if (!k_cache || !v_cache || !k_new || !v_new || !past_len || elem_bytes(new_dtype) == 0 ||
+        new_dtype == ORACLE_E4M3 || B < 0 || H_kv <= 0 || T_max <= 0 || D <= 0 || N <= 0 ||
+        !(k_scale > 0.0f) || !(v_scale > 0.0f))
+        return 1;
+    int status = 0;
+    for (int b = 0; b < B; ++b) {
+        const long long P = past_len[b];
+        if (P < 0 || P + N > T_max) {
+            status = 2;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h) {
+            for (int i = 0; i < N; ++i) {
+                const size_t dst = (((size_t)b * H_kv + h) * (size_t)T_max + (size_t)(P + i)) * (size_t)D;
+                const size_t src = (((size_t)b * H_kv + h) * (size_t)N + (size_t)i) * (size_t)D;
+                for (int d = 0; d < D; ++d) {
+                    const float kx = (float)load_elem(k_new, src + d, new_dtype);
+                    const float vx = (float)load_elem(v_new, src + d, new_dtype);
+                    k_cache[dst + d] = e4m3_from_float(kx / k_scale);
+                    v_cache[dst + d] = e4m3_from_float(vx / v_scale);
+                }
+            }
+        }
+    }
+    return status;
+}
+
+/*
+ * Decode attention over an E4M3 cache: as oracle_decode_attention with key j
+ * = k_scale * K[b,h,j,:] and value j = v_scale * V[b,h,j,:] (the stored codes
+ * decoded exactly); q in q_dtype (fp32, bf16 or fp16).
+ */
+int oracle_decode_attention_e4m3(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                 double *out, const int32_t *past_len, int B, int H_q, int H_kv,
+                                 int T_max, int D, int N, double scale, int q_dtype, double k_scale,
+                                 double v_scale)
+{
+    if (q_dtype == ORACLE_E4M3) return 1;
+    return decode_attention_impl(q, k_cache, v_cache, out, past_len, B, H_q, H_kv, T_max, D, N, scale,
+                                 q_dtype, ORACLE_E4M3, k_scale, v_scale);
+}
+
+/* E4M3 codes of n fp32 values (test hook for the quantization pins). */
+int oracle_quantize_e4m3(const float *src, uint8_t *dst, long long n)
+{
+    if (!src || !dst || n < 0) return 1;
+    for (long long i = 0; i < n; ++i) dst[i] = e4m3_from_float(src[i]);
     return 0;
 }

@@ -372,6 +372,97 @@ def pin_paged_bad_page(orc):
     assert np.array_equal(kp2[4:].view(np.uint8), kp[4:].view(np.uint8))  # sequence 1 untouched
 
 
+# ---------------------------------------------------------------------------------
+# E4M3 cache
+def _e4m3_values() -> torch.Tensor:
+    """All 256 E4M3 codes as torch float8_e4m3fn values."""
+    return torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+
+
+def pin_e4m3_decode_all_codes(orc):
+    """Every E4M3 code decodes to the value torch's float8_e4m3fn conversion gives."""
+    vals = _e4m3_values()
+    got = orc.widen(vals.view(torch.uint8).numpy().copy(), "e4m3")
+    want = vals.to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    fin = ~np.isnan(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert np.nanmax(np.abs(got)) == 448.0
+
+
+def pin_e4m3_quantize(orc):
+    """Quantization = torch's round-to-nearest-even float8_e4m3fn cast inside +-448
+    (random values, every exact midpoint between neighbouring codes and its two
+    float32 neighbours, subnormals, signed zeros); saturation to +-448 beyond."""
+    vals = _e4m3_values().to(torch.float64)
+    fin = vals[~torch.isnan(vals)]
+    pos = torch.sort(torch.unique(fin[fin >= 0])).values
+    mids = ((pos[1:] + pos[:-1]) / 2).to(torch.float32)
+    up = torch.nextafter(mids, torch.full_like(mids, float("inf")))
+    dn = torch.nextafter(mids, torch.full_like(mids, -float("inf")))
+    g = torch.Generator().manual_seed(17)
+    rnd = torch.cat([torch.randn(20000, generator=g) * 50, torch.rand(5000, generator=g) * 0.03])
+    x = torch.cat([mids, up, dn, -mids, -up, -dn, rnd.clamp(-448, 448), torch.tensor([0.0, -0.0, 448.0, -448.0])])
+    got = orc.quantize_e4m3(x.numpy())
+    want = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want)
+    big = np.array([448.5, 464.0, 1e6, np.inf, -500.0, -np.inf], dtype=np.float32)
+    assert np.array_equal(orc.quantize_e4m3(big), np.array([126, 126, 126, 126, 254, 254], dtype=np.uint8))
+    assert orc.quantize_e4m3(np.array([np.nan], dtype=np.float32))[0] & 0x7f == 0x7f
+
+
+def pin_e4m3_append(orc):
+    """The E4M3 append stores the quantized fp32 quotient new / scale in the new slots only."""
+    for new_dtype in ("bf16", "f32"):
+        B, H, T_max, D, N = 2, 3, 9, 16, 2
+        past = torch.tensor([3, 7], dtype=torch.int32)
+        k_new = _rand((B, H, N, D), 61, new_dtype) * 7
+        v_new = _rand((B, H, N, D), 62, new_dtype) * 0.02
+        k_scale, v_scale = 0.75, 3.0e-4
+        kc = np.full((B, H, T_max, D), 0xA5, dtype=np.uint8)
+        vc = kc.copy()
+        st = orc.append_e4m3(kc, vc, to_np(k_new), to_np(v_new), past.numpy(), new_dtype, k_scale, v_scale)
+        assert st == 0
+        kq = (k_new.float() / torch.tensor(k_scale, dtype=torch.float32)).to(torch.float8_e4m3fn)
+        vq = (v_new.float() / torch.tensor(v_scale, dtype=torch.float32)).to(torch.float8_e4m3fn)
+        exp_k = np.full_like(kc, 0xA5)
+        exp_v = exp_k.copy()
+        for b, P in enumerate(past.tolist()):
+            exp_k[b, :, P:P + N] = kq[b].view(torch.uint8).numpy()
+            exp_v[b, :, P:P + N] = vq[b].view(torch.uint8).numpy()
+        assert np.array_equal(kc, exp_k) and np.array_equal(vc, exp_v)
+
+
+def pin_e4m3_attention(orc):
+    """E4M3 attention = attention over the exactly dequantized cache: bit for bit the
+    fp32 oracle when the scales are powers of two (the products are exact), and
+    library SDPA in float64 for general scales."""
+    B, H_q, H_kv, D, N, T_max = 2, 8, 2, 32, 3, 20
+    past = torch.tensor([6, 17], dtype=torch.int32)
+    g = torch.Generator().manual_seed(23)
+    k8 = torch.randint(0, 256, (B, H_kv, T_max, D), generator=g, dtype=torch.int32).to(torch.uint8)
+    v8 = torch.randint(0, 256, (B, H_kv, T_max, D), generator=g, dtype=torch.int32).to(torch.uint8)
+    for c in (k8, v8):  # no NaN codes in the visible slots
+        c[(c & 0x7f) == 0x7f] = 0x3c
+    q = _rand((B, H_q, N, D), 24, "bf16")
+    for k_scale, v_scale in ((0.25, 8.0), (0.0173, 3.7)):
+        out, st = orc.decode_attention_e4m3(to_np(q), k8.numpy(), v8.numpy(), past.numpy(), "bf16", k_scale, v_scale)
+        assert st == 0
+        kd = k8.view(torch.float8_e4m3fn).to(torch.float64) * k_scale
+        vd = v8.view(torch.float8_e4m3fn).to(torch.float64) * v_scale
+        if k_scale == 0.25:
+            flat, st = orc.decode_attention(to_np(q.float()), kd.float().numpy(), vd.float().numpy(),
+                                            past.numpy(), "f32")
+            assert st == 0 and np.array_equal(out, flat)
+        want = torch.stack([
+            F.scaled_dot_product_attention(
+                to_f64(q[b])[None], kd[b, :, : int(P) + N][None], vd[b, :, : int(P) + N][None],
+                attn_mask=(torch.arange(int(P) + N)[None, :] <= (int(P) + torch.arange(N))[:, None]),
+                scale=1.0 / D ** 0.5, enable_gqa=True)[0]
+            for b, P in enumerate(past)])
+        assert _max_rel(torch.from_numpy(out), want) < 1e-12
+
+
 ALL_PINS = [
     pin_cache_bytes,
     pin_append_is_concat,
@@ -386,4 +477,8 @@ ALL_PINS = [
     pin_paged_identity_layout,
     pin_paged_renumbered_pages,
     pin_paged_bad_page,
+    pin_e4m3_decode_all_codes,
+    pin_e4m3_quantize,
+    pin_e4m3_append,
+    pin_e4m3_attention,
 ]

@@ -28,7 +28,8 @@ MUTANTS = [
     ("softmax weights not normalised",
      "for (int d = 0; d < D; ++d) o[d] /= wsum;", "for (int d = 0; d < D; ++d) o[d] /= 1.0;"),
     ("value rows read from the K cache",
-     "o[d] += w * load_elem(v_cache, v_row + d, dtype);", "o[d] += w * load_elem(k_cache, v_row + d, dtype);"),
+     "o[d] += w * (v_scale * load_elem(v_cache, v_row + d, kv_dtype));",
+     "o[d] += w * (v_scale * load_elem(k_cache, v_row + d, kv_dtype));"),
     ("every new row uses the first query row",
      "* (size_t)N + (size_t)i) * (size_t)D;\n                const size_t kv_head",
      "* (size_t)N + (size_t)0) * (size_t)D;\n                const size_t kv_head"),
@@ -38,6 +39,15 @@ MUTANTS = [
      "[idx] << 16;", "[idx] << 15;"),
     ("fp16 exponent bias off by one",
      "ldexp((double)(1024 + frac), expo - 25)", "ldexp((double)(1024 + frac), expo - 24)"),
+    ("e4m3 exponent bias off by one",
+     "v = ldexp((double)(8 + frac), expo - 10);", "v = ldexp((double)(8 + frac), expo - 9);"),
+    ("e4m3 ties rounded away from even",
+     "(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    ("e4m3 append without the scale",
+     "e4m3_from_float(kx / k_scale)", "e4m3_from_float(kx)"),
+    ("e4m3 attention ignores the V scale",
+     "o[d] += w * (v_scale * load_elem(v_cache, v_row + d, kv_dtype));",
+     "o[d] += w * (load_elem(v_cache, v_row + d, kv_dtype));"),
     ("fp16 subnormals scaled as normals",
      "v = ldexp((double)frac, -24);", "v = ldexp((double)(1024 + frac), -25);"),
     ("size formula without the factor 2 for K and V",
