@@ -63,7 +63,8 @@ typedef enum kvd_status {
     KVD_ERR_CUDA = 5         /* a CUDA call or launch failed */
 } kvd_status;
 
-typedef enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1, KVD_F16 = 2 } kvd_dtype;
+/* Element types.  KVD_E4M3 is a cache format only (see the _e4m3 calls). */
+typedef enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1, KVD_F16 = 2, KVD_E4M3 = 3 } kvd_dtype;
 
 /* Bits OR-ed into the device error word. */
 #define KVD_DEVERR_PAST_LEN 1u /* a sequence had an out-of-range past_len and was skipped */
@@ -252,6 +253,48 @@ kvd_status kvd_paged_decode_step(const void *q, void *k_pages, void *v_pages, co
                                  int page_size, int max_pages, int num_pages, int max_past_len,
                                  float scale, kvd_dtype dtype, void *workspace,
                                  size_t workspace_bytes, uint32_t *err_word, void *stream);
+
+/*
+ * 8-bit cache (E4M3).  Serving stacks also keep the cache in FP8, and decode is
+ * where quantization pays most ("GPT-2缓存实测", section "实验到底测了什么", the
+ * paragraph after the configuration table; "7.1 自回归生成过程", section "Decode
+ * 阶段").  Here the K and V caches hold E4M3 codes (1 sign, 4 exponent, 3
+ * fraction bits, bias 7, no infinities, largest finite value 448) with one
+ * scale per cache: a stored code c stands for k_scale * value(c) (K) or
+ * v_scale * value(c) (V).  q, new K/V and out are bf16 (the append also takes
+ * fp32 or fp16 new rows), arithmetic is fp32.
+ *
+ *   k_cache, v_cache  device, [B, H_kv, T_max, D] bytes (E4M3 codes), D a
+ *                     multiple of 16; contiguous layout only
+ *   k_scale, v_scale  positive, finite
+ *
+ * kvd_append_e4m3 stores, for each new element x, the code of the fp32
+ * quotient x / scale rounded to the nearest E4M3 value (ties to the even code,
+ * magnitudes beyond 448 saturate to 448).  kvd_decode_attention_e4m3 and
+ * kvd_decode_step_e4m3 are kvd_decode_attention / kvd_decode_step over such a
+ * cache (the fused step quantizes the new rows exactly as kvd_append_e4m3
+ * does).  Workspace: kvd_decode_workspace_bytes(..., KVD_E4M3).  Query rows
+ * per KV head are processed in blocks of at most 4.  Other arguments, errors
+ * and device-side checks as for the bf16 calls; any other entry point given
+ * KVD_E4M3 returns KVD_ERR_UNSUPPORTED, except kvd_append / kvd_paged_append,
+ * which copy already-quantized rows bit for bit.
+ */
+kvd_status kvd_append_e4m3(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                           const int32_t *past_len, int B, int H_kv, int T_max, int D, int N,
+                           int max_past_len, kvd_dtype new_dtype, float k_scale, float v_scale,
+                           uint32_t *err_word, void *stream);
+
+kvd_status kvd_decode_attention_e4m3(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                     const int32_t *past_len, int B, int H_q, int H_kv, int T_max, int D,
+                                     int N, int max_past_len, float scale, float k_scale, float v_scale,
+                                     void *workspace, size_t workspace_bytes, uint32_t *err_word,
+                                     void *stream);
+
+kvd_status kvd_decode_step_e4m3(const void *q, void *k_cache, void *v_cache, const void *k_new,
+                                const void *v_new, void *out, const int32_t *past_len, int B, int H_q,
+                                int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                                float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                                uint32_t *err_word, void *stream);
 
 /* kvd_workspace_init -- zero-fill a workspace on `stream` (asynchronous), as
  * kvd_decode_attention and kvd_decode_step need before a workspace's first use. */

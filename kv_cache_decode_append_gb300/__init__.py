@@ -10,6 +10,7 @@ from .kvd import (  # noqa: F401
     KVD_ERR_INVALID_ARG, KVD_ERR_UNSUPPORTED, KVD_ERR_WORKSPACE, KVD_F16, KVD_F32, KVD_OK, KvdError,
     alloc_workspace, kvd_append, kvd_cache_bytes, kvd_decode_attention, kvd_decode_attention_noalloc,
     kvd_decode_plan, kvd_decode_step, kvd_decode_workspace_bytes, kvd_paged_append,
-    kvd_paged_decode_attention, kvd_paged_decode_step,
+    kvd_paged_decode_attention, kvd_paged_decode_step, KVD_E4M3, kvd_append_e4m3,
+    kvd_decode_attention_e4m3, kvd_decode_step_e4m3,
     kvd_status_string, kvd_workspace_init, library_path, load, raw,
 )

@@ -99,6 +99,46 @@ __global__ void __launch_bounds__(256) paged_append_kernel(const PagedAppendArgs
 }
 
 // ---------------------------------------------------------------------------
+// E4M3 kv_append: as append_kernel, with each new element x (type T) stored as
+// the E4M3 code of x / scale (k_scale for K, v_scale for V).  One thread
+// writes one 16-code chunk of K and of V (reading 16 elements of each).
+struct AppendE4m3Args {
+    uint4 *k_cache;
+    uint4 *v_cache;
+    const unsigned char *k_new;
+    const unsigned char *v_new;
+    const int32_t *past_len;
+    uint32_t *err_word;
+    int H_kv, T_max, N, max_past_len;
+    int row_chunks;   // 16-code chunks per cache row (D / 16)
+    float k_scale, v_scale;
+    long long total;  // B * H_kv * N * row_chunks
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) append_e4m3_kernel(const AppendE4m3Args a)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < a.total;
+         idx += stride) {
+        const int c = (int)(idx % a.row_chunks);
+        const long long row = idx / a.row_chunks;  // (bh, i)
+        const int i = (int)(row % a.N);
+        const long long bh = row / a.N;
+        const int b = (int)(bh / a.H_kv);
+        const int P = __ldg(a.past_len + b);
+        if (!past_len_ok(P, a.N, a.T_max, a.max_past_len)) {
+            if (c == 0 && i == 0 && bh % a.H_kv == 0) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
+            continue;
+        }
+        const long long dst = (bh * a.T_max + P + i) * a.row_chunks + c;
+        const size_t src = (size_t)idx * 16 * sizeof(T);  // 16 elements of T per chunk
+        stg128(a.k_cache + dst, e4m3_chunk_from<T>(a.k_new + src, a.k_scale));
+        stg128(a.v_cache + dst, e4m3_chunk_from<T>(a.v_new + src, a.v_scale));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Per-device facts, queried once.
 namespace {
 
@@ -168,7 +208,16 @@ kvd_status occupancy(int dev, const void *fn, int threads, int smem, int *ctas_p
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int elem_bytes(kvd_dtype dt) { return dt == KVD_F32 ? 4 : ((dt == KVD_BF16 || dt == KVD_F16) ? 2 : 0); }
+int elem_bytes(kvd_dtype dt)
+{
+    switch (dt) {
+    case KVD_F32: return 4;
+    case KVD_BF16:
+    case KVD_F16: return 2;
+    case KVD_E4M3: return 1;
+    default: return 0;
+    }
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -206,6 +255,8 @@ bool pick_builds(kvd_dtype dtype, int D, int rb, bool paged, AttnVariant *vp, At
     case KVD_F16:
         return paged ? attn_variant_f16_paged(D, rb, vp) && attn_variant_f16_tk_paged(D, rb, vt)
                      : attn_variant_f16(D, rb, vp) && attn_variant_f16_tk(D, rb, vt);
+    case KVD_E4M3:  // bf16 q / out over an E4M3 cache, contiguous only
+        return !paged && attn_variant_e4m3(D, rb, vp) && attn_variant_e4m3_tk(D, rb, vt);
     default:
         return false;
     }
@@ -230,11 +281,14 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
     if (st != KVD_OK) return st;
     pl->rows = (H_q / H_kv) * N;
-    pl->rb = pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : pl->rows <= 4 ? 4 : 8;
+    pl->rb = pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : (pl->rows <= 4 || dtype == KVD_E4M3) ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
     AttnVariant vp, vt, op, ot;  // this layout's builds, and the other layout's
-    if (!pick_builds(dtype, D, pl->rb, paged, &vp, &vt) || !pick_builds(dtype, D, pl->rb, !paged, &op, &ot))
-        return KVD_ERR_UNSUPPORTED;
+    if (!pick_builds(dtype, D, pl->rb, paged, &vp, &vt)) return KVD_ERR_UNSUPPORTED;
+    if (!pick_builds(dtype, D, pl->rb, !paged, &op, &ot)) {  // (no other layout: E4M3)
+        op = vp;
+        ot = vt;
+    }
     pl->v = vp;
 
     // Shared memory holds the ring plus two per-sequence tables (B + 1 tile
@@ -385,11 +439,16 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
                          const void *v_new, void *out, const int32_t *past_len, int B, int H_q, int H_kv,
                          int T_max, int D, int N, int max_past_len, float scale, kvd_dtype dtype,
                          void *workspace, size_t workspace_bytes, uint32_t *err_word, void *stream,
-                         const PagedCache *paged = nullptr)
+                         const PagedCache *paged = nullptr, const float *e4m3_scales = nullptr)
 {
     if (!q || !k_cache || !v_cache || !out || !past_len) return KVD_ERR_INVALID_ARG;
     kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
     if (st != KVD_OK) return st;
+    // An E4M3 cache only through the _e4m3 entry points (which pass its scales).
+    if ((dtype == KVD_E4M3) != (e4m3_scales != nullptr)) return KVD_ERR_UNSUPPORTED;
+    if (e4m3_scales != nullptr &&
+        !(e4m3_scales[0] > 0.f && e4m3_scales[0] < INFINITY && e4m3_scales[1] > 0.f && e4m3_scales[1] < INFINITY))
+        return KVD_ERR_INVALID_ARG;
     int page_shift = 0;
     if (paged != nullptr && (st = check_paged(*paged, &T_max, &page_shift)) != KVD_OK) return st;
     if (T_max < 1) return KVD_ERR_INVALID_ARG;
@@ -417,7 +476,10 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     // Separate regions: the tickets must stay zero while the same workspace
     // serves calls in the other mode.
     a.merge_state = ws + (pl.merge_pass ? pl.seg_off : pl.tickets_off);
-    a.block_table = paged != nullptr ? paged->block_table : nullptr;
+    if (e4m3_scales != nullptr)
+        a.kv_scale = make_float2(e4m3_scales[0], e4m3_scales[1]);
+    else
+        a.block_table = paged != nullptr ? paged->block_table : nullptr;
     a.num_pages = paged != nullptr ? paged->num_pages : 0;
     a.page_shift = page_shift;
     a.err_word = err_word;
@@ -429,7 +491,8 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     a.rows = pl.rows;
     a.n_rowblocks = pl.n_rowblocks;
     const float sc = (scale > 0.f) ? scale : 1.0f / sqrtf((float)D);
-    a.qscale = sc * kLog2e;
+    // (E4M3: key = k_scale x stored code, folded into the q pre-scale)
+    a.qscale = sc * kLog2e * (e4m3_scales != nullptr ? e4m3_scales[0] : 1.0f);
 
     // Both kernels are programmatic dependents of whatever precedes them on
     // the stream: they start early and wait (griddepcontrol.wait) before
@@ -557,6 +620,80 @@ kvd_status kvd_paged_decode_step(const void *q, void *k_pages, void *v_pages, co
     const PagedCache pc{block_table, page_size, max_pages, num_pages};
     return decode_launch(q, k_pages, v_pages, k_new, v_new, out, past_len, B, H_q, H_kv, 0, D, N,
                          max_past_len, scale, dtype, workspace, workspace_bytes, err_word, stream, &pc);
+}
+
+kvd_status kvd_append_e4m3(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                           const int32_t *past_len, int B, int H_kv, int T_max, int D, int N,
+                           int max_past_len, kvd_dtype new_dtype, float k_scale, float v_scale,
+                           uint32_t *err_word, void *stream)
+{
+    if (new_dtype != KVD_F32 && new_dtype != KVD_BF16 && new_dtype != KVD_F16) return KVD_ERR_UNSUPPORTED;
+    if (!k_cache || !v_cache || !k_new || !v_new || !past_len) return KVD_ERR_INVALID_ARG;
+    if (B < 0 || H_kv < 1 || T_max < 1 || D < 1 || N < 1 || max_past_len < 0) return KVD_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f && k_scale < INFINITY && v_scale > 0.f && v_scale < INFINITY)) return KVD_ERR_INVALID_ARG;
+    if (D % 16 != 0) return KVD_ERR_UNSUPPORTED;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+        return KVD_ERR_INVALID_ARG;
+    if ((long long)max_past_len + N > T_max) return KVD_ERR_CAPACITY;
+    if (B == 0) return KVD_OK;
+
+    int dev = 0, sms = 0;
+    kvd_status st;
+    if ((st = current_device(&dev)) != KVD_OK) return st;
+    if ((st = sm_count(dev, &sms)) != KVD_OK) return st;
+
+    AppendE4m3Args a;
+    a.k_cache = static_cast<uint4 *>(k_cache);
+    a.v_cache = static_cast<uint4 *>(v_cache);
+    a.k_new = static_cast<const unsigned char *>(k_new);
+    a.v_new = static_cast<const unsigned char *>(v_new);
+    a.past_len = past_len;
+    a.err_word = err_word;
+    a.H_kv = H_kv;
+    a.T_max = T_max;
+    a.N = N;
+    a.max_past_len = max_past_len;
+    a.row_chunks = D / 16;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.total = (long long)B * H_kv * N * a.row_chunks;
+    const int threads = 256;
+    long long blocks = (a.total + threads - 1) / threads;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    const void *fn = new_dtype == KVD_F32    ? reinterpret_cast<const void *>(&append_e4m3_kernel<float>)
+                     : new_dtype == KVD_BF16 ? reinterpret_cast<const void *>(&append_e4m3_kernel<__nv_bfloat16>)
+                                             : reinterpret_cast<const void *>(&append_e4m3_kernel<__half>);
+    void *args[] = {&a};
+    return cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(threads), args, 0, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_decode_attention_e4m3(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                     const int32_t *past_len, int B, int H_q, int H_kv, int T_max, int D,
+                                     int N, int max_past_len, float scale, float k_scale, float v_scale,
+                                     void *workspace, size_t workspace_bytes, uint32_t *err_word,
+                                     void *stream)
+{
+    const float scales[2] = {k_scale, v_scale};
+    return decode_launch(q, k_cache, v_cache, nullptr, nullptr, out, past_len, B, H_q, H_kv, T_max, D, N,
+                         max_past_len, scale, KVD_E4M3, workspace, workspace_bytes, err_word, stream, nullptr,
+                         scales);
+}
+
+kvd_status kvd_decode_step_e4m3(const void *q, void *k_cache, void *v_cache, const void *k_new,
+                                const void *v_new, void *out, const int32_t *past_len, int B, int H_q,
+                                int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                                float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                                uint32_t *err_word, void *stream)
+{
+    if (!k_new || !v_new) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return KVD_ERR_INVALID_ARG;
+    const float scales[2] = {k_scale, v_scale};
+    return decode_launch(q, k_cache, v_cache, k_new, v_new, out, past_len, B, H_q, H_kv, T_max, D, N,
+                         max_past_len, scale, KVD_E4M3, workspace, workspace_bytes, err_word, stream, nullptr,
+                         scales);
 }
 
 kvd_status kvd_workspace_init(void *workspace, size_t workspace_bytes, void *stream)

@@ -60,6 +60,8 @@
 // the end of the sequence are replaced by zeros before the weighted sum.
 #pragma once
 
+#include <type_traits>
+
 #include "kvd_device.cuh"
 
 namespace kvd {
@@ -80,7 +82,10 @@ struct AttnArgs {
                              // sequence-head; in-kernel merge: int tickets, the same count (pieces
                              // counted so far; zero between calls: the merging CTA resets its ticket)
     uint32_t *err_word;
-    const int32_t *block_table;  // paged only: [B, T_max >> page_shift] physical page of each logical page
+    union {
+        const int32_t *block_table;  // paged: [B, T_max >> page_shift] physical page of each logical page
+        float2 kv_scale;             // E4M3 cache: (k_scale, v_scale), stored code = value / scale
+    };
     int B, H_kv, T_max, N, max_past_len;  // paged: T_max = pages per sequence x page_size
     int rows;         // query rows per (b, h): (H_q / H_kv) * N, contiguous in q and out
     int n_rowblocks;  // ceil(rows / RB)
@@ -91,15 +96,21 @@ struct AttnArgs {
 static_assert(sizeof(AttnArgs) == 128, "keep the kernel parameter block at 128 bytes");
 
 
-// Compile-time shape of one kernel variant.
-template <typename T, int D, int RB> struct AttnShape {
-    using Ty = Elem<T>;
+// Compile-time shape of one kernel variant: q / out elements T, cache
+// elements C (T, or E4M3 codes with bf16 q).
+template <typename T, int D, int RB, typename C = T> struct AttnShape {
+    using Ty = Elem<C>;   // cache rows (the K/V tiles)
+    using Tq = Elem<T>;   // q, new K/V and out rows
     static constexpr int kRB = RB;
-    static constexpr int kRowBytes = D * Ty::kBytes;
+    static constexpr int kRowBytes = D * Ty::kBytes;   // one cache row
+    static constexpr int kQRowBytes = D * Tq::kBytes;  // one q / new K/V / out row
+    static constexpr int kQChunks = Ty::kPerChunk * Tq::kBytes / 16;  // q chunks per cache chunk
     static constexpr int kRowChunks = kRowBytes / 16;
     // Lanes per key: 8 keeps each 8-lane shared-memory phase on one 128-byte
-    // run of a row (no bank conflicts); 16 when 8 would need > 64 q registers.
-    static constexpr int kL = ((kRowChunks / 8) * Ty::kPerChunk * RB <= 64) ? 8 : 16;
+    // run of a row (no bank conflicts); 16 when 8 would need > 64 q registers;
+    // never more than a row's chunks (64-byte E4M3 rows: 4).
+    static constexpr int kLw = ((kRowChunks / 8) * Ty::kPerChunk * RB <= 64) ? 8 : 16;
+    static constexpr int kL = kLw < kRowChunks ? kLw : kRowChunks;
     static constexpr int kCpl = kRowChunks / kL;       // 16-byte chunks per lane per row
     static constexpr int kE = kCpl * Ty::kPerChunk;    // head-dim elements per lane
     static constexpr int kGpw = 32 / kL;               // key groups per warp
@@ -110,7 +121,7 @@ template <typename T, int D, int RB> struct AttnShape {
     static constexpr int kKpw = kGpw * kKpg;           // keys per warp per tile
     static constexpr int kTileBytes = kTK * kRowBytes; // one of K or V
     static constexpr int kStages = (2 * kTileBytes <= 16384) ? 4 : 3;
-    static constexpr int kQSlotBytes = RB * kRowBytes;
+    static constexpr int kQSlotBytes = RB * kQRowBytes;
     // Cost of a piece boundary in tile units for the static split (a sweep
     // over 0..8 on GB300 put the best at 2 for both the 32 KB tiles of D=128
     // bf16 and the 16 KB tiles of D=64 bf16).
@@ -129,6 +140,7 @@ template <typename T, int D, int RB> struct AttnShape {
     static constexpr int kFixedBytes = kPageOff + 16;               // physical page of each stage (paged)
 
     static_assert(kRowBytes % 16 == 0, "rows must be whole 16-byte chunks");
+    static_assert(kQChunks >= 1, "q chunks per cache chunk");
     static_assert(kCpl >= 1 && kRowChunks % kL == 0, "lane mapping");
     static_assert(kNW >= 1 && kTK % kKpw == 0, "tile mapping");
     static_assert(kQOff % 128 == 0 && kEpiOff % 16 == 0 && kBarOff % 8 == 0, "alignment");
@@ -163,17 +175,20 @@ constexpr int kMetaEnd = 4;    // no more work
 // given, written to their cache slots by the lanes that read them: kc + key
 // rows (contiguous cache: kc is the (b, h) row base), or kc + (key - tile_k0)
 // rows when kTileRel (paged cache: kc is the slot of the tile's first key).
-template <typename T, int D, int RB, bool kMasked, bool kFused, bool kTileRel = false>
+// With an E4M3 cache (C != T) the new rows are quantized on the way in
+// (kv_scale: the K and V scales), exactly as the E4M3 append stores them.
+template <typename T, int D, int RB, bool kMasked, bool kFused, bool kTileRel = false, typename C = T>
 __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigned char *Vs,
-                                          const f32x2 (&qv)[RB][AttnShape<T, D, RB>::kE / 2],
-                                          f32x2 (&o)[RB][AttnShape<T, D, RB>::kE / 2], float (&m_run)[RB],
+                                          const f32x2 (&qv)[RB][AttnShape<T, D, RB, C>::kE / 2],
+                                          f32x2 (&o)[RB][AttnShape<T, D, RB, C>::kE / 2], float (&m_run)[RB],
                                           float (&l_run)[RB], int warp, int grp, int j,
                                           int tile_k0, const int (&lim)[RB], int k_end, int P,
                                           const unsigned char *kn, const unsigned char *vn,
-                                          unsigned char *kc, unsigned char *vc)
+                                          unsigned char *kc, unsigned char *vc, float2 kv_scale = float2{})
 {
-    using S = AttnShape<T, D, RB>;
-    using Ty = Elem<T>;
+    using S = AttnShape<T, D, RB, C>;
+    using Ty = Elem<C>;
+    constexpr bool kQuant = !std::is_same<T, C>::value;
     constexpr int E2 = S::kE / 2;
     constexpr int P2 = Ty::kPerChunk / 2;  // pairs per 16-byte chunk
     const float kNegInf = __int_as_float(0xff800000);
@@ -188,9 +203,14 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
         if constexpr (kMasked && kFused) {
             const int key = tile_k0 + kk;
             if (key >= P && key < k_end) {
-                const unsigned char *src = kn + (size_t)(key - P) * S::kRowBytes;
+                const unsigned char *src = kn + (size_t)(key - P) * S::kQRowBytes;
 #pragma unroll
-                for (int c = 0; c < S::kCpl; ++c) raw[u][c] = ldg128_nc(src + (c * S::kL + j) * 16);
+                for (int c = 0; c < S::kCpl; ++c) {
+                    if constexpr (kQuant)
+                        raw[u][c] = e4m3_chunk_from<T>(src + (c * S::kL + j) * S::kQChunks * 16, kv_scale.x);
+                    else
+                        raw[u][c] = ldg128_nc(src + (c * S::kL + j) * 16);
+                }
                 if (kc != nullptr) {
 #pragma unroll
                     for (int c = 0; c < S::kCpl; ++c)
@@ -265,9 +285,14 @@ __device__ __forceinline__ void attn_tile(const unsigned char *Ks, const unsigne
         if constexpr (kMasked && kFused) {
             const int key = tile_k0 + kk;
             if (key >= P && key < k_end) {
-                const unsigned char *src = vn + (size_t)(key - P) * S::kRowBytes;
+                const unsigned char *src = vn + (size_t)(key - P) * S::kQRowBytes;
 #pragma unroll
-                for (int c = 0; c < S::kCpl; ++c) raw[u][c] = ldg128_nc(src + (c * S::kL + j) * 16);
+                for (int c = 0; c < S::kCpl; ++c) {
+                    if constexpr (kQuant)
+                        raw[u][c] = e4m3_chunk_from<T>(src + (c * S::kL + j) * S::kQChunks * 16, kv_scale.y);
+                    else
+                        raw[u][c] = ldg128_nc(src + (c * S::kL + j) * 16);
+                }
                 if (vc != nullptr) {
 #pragma unroll
                     for (int c = 0; c < S::kCpl; ++c)
@@ -370,8 +395,8 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
             kg = static_cast<const unsigned char *>(a.k_cache) + row * S::kRowBytes;
             vg = static_cast<const unsigned char *>(a.v_cache) + row * S::kRowBytes;
         }
-        qg = static_cast<const unsigned char *>(a.q) + ((size_t)bh * a.rows + rb * S::kRB) * S::kRowBytes;
-        q_bytes = min(S::kRB, a.rows - rb * S::kRB) * S::kRowBytes;
+        qg = static_cast<const unsigned char *>(a.q) + ((size_t)bh * a.rows + rb * S::kRB) * S::kQRowBytes;
+        q_bytes = min(S::kRB, a.rows - rb * S::kRB) * S::kQRowBytes;
     }
 
     // pre[b] = units of sequences 0..b-1 per head (a head of sequence b has
@@ -491,7 +516,7 @@ struct MergeJob {
 // are split over kNG thread groups when the head has fewer output elements
 // than the CTA has threads; the groups then combine through scr (shared
 // memory, free on entry and again on return).
-template <typename T, int D, int RB, int kThreads>
+template <typename T, int D, int RB, int kThreads, bool kScaleV = false>
 __device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &job, float *scr, int tid)
 {
     using Ty = Elem<T>;
@@ -557,7 +582,13 @@ __device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &
         for (int i = 0; i < kPer; ++i) {
             const int e = e0 + i * kThreads, r = e / D, d = e % D;
             const int rg = job.rb * RB + r;
-            if (rg < a.rows) Ty::store(static_cast<T *>(a.out) + ((size_t)job.bh * a.rows + rg) * D + d, num[i] / den[i]);
+            if (rg < a.rows) {
+                if constexpr (kScaleV)  // E4M3 cache: values are stored / v_scale
+                    Ty::store(static_cast<T *>(a.out) + ((size_t)job.bh * a.rows + rg) * D + d,
+                              num[i] / den[i] * a.kv_scale.y);
+                else
+                    Ty::store(static_cast<T *>(a.out) + ((size_t)job.bh * a.rows + rg) * D + d, num[i] / den[i]);
+            }
         }
     }
 }
@@ -565,12 +596,15 @@ __device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &
 // kFused: append inside (kvd_decode_step).  kTicketMerge: split heads are
 // merged at the end of this kernel (else by attn_merge_kernel).  kPaged: the
 // cache is paged (block table), else contiguous [B, H_kv, T_max, D].
-template <typename T, int D, int RB, bool kFused, bool kTicketMerge, bool kPaged>
+template <typename T, int D, int RB, bool kFused, bool kTicketMerge, bool kPaged, typename C = T>
 __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
     attn_balanced_kernel(const AttnArgs a)
 {
-    using S = AttnShape<T, D, RB>;
-    using Ty = Elem<T>;
+    using S = AttnShape<T, D, RB, C>;
+    using Ty = Elem<C>;                                // cache rows
+    using Tq = Elem<T>;                                // q / out rows
+    constexpr bool kQuant = !std::is_same<T, C>::value;  // E4M3 cache: scales apply
+    static_assert(!(kQuant && kPaged), "the E4M3 cache is contiguous only");
     const float kNegInf = __int_as_float(0xff800000);
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBarOff);
@@ -689,8 +723,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
                     const f32x2 qs2 = pack2(a.qscale, a.qscale);
 #pragma unroll
                     for (int c = 0; c < S::kCpl; ++c)
-                        Ty::widen2(lds128(qs + r * S::kRowBytes + (c * S::kL + j) * 16),
-                                   &qv[r][c * (Ty::kPerChunk / 2)]);
+#pragma unroll
+                        for (int qc = 0; qc < S::kQChunks; ++qc)  // the q elements of cache chunk c*L + j
+                            Tq::widen2(lds128(qs + r * S::kQRowBytes + ((c * S::kL + j) * S::kQChunks + qc) * 16),
+                                       &qv[r][c * (Ty::kPerChunk / 2) + qc * (Tq::kPerChunk / 2)]);
 #pragma unroll
                     for (int e = 0; e < S::kE / 2; ++e) qv[r][e] = mul2(qv[r][e], qs2);
                 } else {
@@ -704,13 +740,13 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
         // Tiles below every row's limit (and, in a fused step, below the new
         // keys) take the unmasked path; the rest the masked one.
         if (mt.tile_k0 + S::kTK <= mt.P + (kFused ? 0 : 1)) {
-            attn_tile<T, D, RB, false, kFused>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim, k_end,
-                                               mt.P, nullptr, nullptr, nullptr, nullptr);
+            attn_tile<T, D, RB, false, kFused, false, C>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0,
+                                                         lim, k_end, mt.P, nullptr, nullptr, nullptr, nullptr);
         } else {
             const unsigned char *kn = nullptr, *vn = nullptr;
             unsigned char *kc = nullptr, *vc = nullptr;
             if constexpr (kFused) {
-                const size_t nrow = (size_t)mt.bh * a.N * S::kRowBytes;
+                const size_t nrow = (size_t)mt.bh * a.N * S::kQRowBytes;
                 kn = static_cast<const unsigned char *>(a.k_new) + nrow;
                 vn = static_cast<const unsigned char *>(a.v_new) + nrow;
                 if constexpr (kPaged) {
@@ -728,8 +764,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
                     vc = static_cast<unsigned char *>(const_cast<void *>(a.v_cache)) + crow;
                 }
             }
-            attn_tile<T, D, RB, true, kFused, kPaged>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0, lim,
-                                                      k_end, mt.P, kn, vn, kc, vc);
+            float2 kvs = float2{};
+            if constexpr (kQuant) kvs = a.kv_scale;
+            attn_tile<T, D, RB, true, kFused, kPaged, C>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0,
+                                                         lim, k_end, mt.P, kn, vn, kc, vc, kvs);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with slot s
@@ -813,7 +851,11 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
                 den = fmaf(wt, ep_l[w * RB + r], den);
             }
             if (single) {
-                Ty::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
+                if constexpr (kQuant)  // values are stored / v_scale
+                    Tq::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d,
+                              num / den * a.kv_scale.y);
+                else
+                    Tq::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
             } else {
                 float *pr = a.part + (pbase + r) * (D + 4);
                 pr[d] = num;
@@ -856,7 +898,8 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
         for (int i = 0; i < 2; ++i) {
             const MergeJob job = jobs[i];
             if (i < n_pieces && job.n_chunks)
-                merge_pieces<T, D, RB, S::kThreads>(a, job, reinterpret_cast<float *>(smem + S::kEpiOff), tid);
+                merge_pieces<T, D, RB, S::kThreads, kQuant>(a, job, reinterpret_cast<float *>(smem + S::kEpiOff),
+                                                            tid);
         }
     }
 
@@ -878,7 +921,8 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
 
 // Second pass: log-sum-exp merge of the pieces of one query row per warp.
 //   M = max_c m_c;  w_c = 2^(m_c - M);  out = sum_c w_c o_c / sum_c w_c l_c
-template <typename T, int D, int RB>
+// (times v_scale with an E4M3 cache: kScaleV).
+template <typename T, int D, int RB, bool kScaleV = false>
 __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
 {
     using Ty = Elem<T>;
@@ -933,7 +977,12 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
     const int bh = b * a.H_kv + h;
     T *out = static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + lane * kDpl;
 #pragma unroll
-    for (int k = 0; k < kDpl; ++k) Ty::store(out + k, acc[k] / den);
+    for (int k = 0; k < kDpl; ++k) {
+        if constexpr (kScaleV)
+            Ty::store(out + k, acc[k] / den * a.kv_scale.y);
+        else
+            Ty::store(out + k, acc[k] / den);
+    }
 }
 
 // Launch facts of one compiled variant, for the host planner.
@@ -948,14 +997,15 @@ struct AttnVariant {
     int piece_units;       // cost of a piece boundary in tile units
 };
 
-template <typename T, int D, int RB, bool kTicketMerge, bool kPaged> AttnVariant make_variant()
+template <typename T, int D, int RB, bool kTicketMerge, bool kPaged, typename C = T> AttnVariant make_variant()
 {
-    using S = AttnShape<T, D, RB>;
+    using S = AttnShape<T, D, RB, C>;
+    constexpr bool kQuant = !std::is_same<T, C>::value;
     AttnVariant v;
-    v.fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false, kTicketMerge, kPaged>);
-    v.fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, kTicketMerge, kPaged>);
+    v.fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false, kTicketMerge, kPaged, C>);
+    v.fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, kTicketMerge, kPaged, C>);
     if constexpr (kTicketMerge) v.merge_fn = nullptr;
-    else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, RB>);
+    else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, RB, kQuant>);
     v.threads = S::kThreads;
     v.fixed_smem_bytes = S::kFixedBytes;
     v.tile_keys = S::kTK;
@@ -964,22 +1014,28 @@ template <typename T, int D, int RB, bool kTicketMerge, bool kPaged> AttnVariant
     return v;
 }
 
-template <typename T, int D, bool kTicketMerge, bool kPaged> bool pick_rb(int RB, AttnVariant *v)
+template <typename T, int D, bool kTicketMerge, bool kPaged, typename C = T> bool pick_rb(int RB, AttnVariant *v)
 {
     switch (RB) {
-    case 1: *v = make_variant<T, D, 1, kTicketMerge, kPaged>(); return true;
-    case 2: *v = make_variant<T, D, 2, kTicketMerge, kPaged>(); return true;
-    case 4: *v = make_variant<T, D, 4, kTicketMerge, kPaged>(); return true;
-    case 8: *v = make_variant<T, D, 8, kTicketMerge, kPaged>(); return true;
+    case 1: *v = make_variant<T, D, 1, kTicketMerge, kPaged, C>(); return true;
+    case 2: *v = make_variant<T, D, 2, kTicketMerge, kPaged, C>(); return true;
+    case 4: *v = make_variant<T, D, 4, kTicketMerge, kPaged, C>(); return true;
+    case 8:  // (an E4M3 cache keeps row blocks of at most 4: 8 would need twice the q registers)
+        if constexpr (std::is_same<T, C>::value) {
+            *v = make_variant<T, D, 8, kTicketMerge, kPaged>();
+            return true;
+        } else {
+            return false;
+        }
     default: return false;
     }
 }
 
-template <typename T, bool kTicketMerge, bool kPaged> bool pick_variant(int D, int RB, AttnVariant *v)
+template <typename T, bool kTicketMerge, bool kPaged, typename C = T> bool pick_variant(int D, int RB, AttnVariant *v)
 {
     switch (D) {
-    case 64: return pick_rb<T, 64, kTicketMerge, kPaged>(RB, v);
-    case 128: return pick_rb<T, 128, kTicketMerge, kPaged>(RB, v);
+    case 64: return pick_rb<T, 64, kTicketMerge, kPaged, C>(RB, v);
+    case 128: return pick_rb<T, 128, kTicketMerge, kPaged, C>(RB, v);
     default: return false;
     }
 }
@@ -998,5 +1054,7 @@ bool attn_variant_f16(int D, int RB, AttnVariant *v);
 bool attn_variant_f16_tk(int D, int RB, AttnVariant *v);
 bool attn_variant_f16_paged(int D, int RB, AttnVariant *v);
 bool attn_variant_f16_tk_paged(int D, int RB, AttnVariant *v);
+bool attn_variant_e4m3(int D, int RB, AttnVariant *v);      // bf16 q / out, E4M3 cache
+bool attn_variant_e4m3_tk(int D, int RB, AttnVariant *v);
 
 }  // namespace kvd

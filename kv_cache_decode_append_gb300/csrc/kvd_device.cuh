@@ -6,6 +6,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -259,6 +260,63 @@ template <> struct Elem<__half> {
     }
     __device__ __forceinline__ static void store(__half *dst, float v) { *dst = __float2half_rn(v); }
 };
+
+// E4M3 codes (8-bit floating point: 1 sign, 4 exponent, 3 fraction bits, no
+// infinities, largest finite 448), 16 to a 16-byte chunk, widened exactly
+// with the hardware conversion (two codes to an f16 pair, then to fp32).
+template <> struct Elem<__nv_fp8_e4m3> {
+    static constexpr int kBytes = 1;
+    static constexpr int kPerChunk = 16;
+    __device__ __forceinline__ static float2 pair(uint32_t two_codes)
+    {
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
+        __half2 h;
+        memcpy(&h, &h2, sizeof h);
+        return __half22float2(h);
+    }
+    // the chunk as eight fp32 pairs (codes 2k, 2k+1)
+    __device__ __forceinline__ static void widen2(const uint4 &c, f32x2 *f)
+    {
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 lo = pair(w[k] & 0xffffu), hi = pair(w[k] >> 16);
+            f[2 * k] = pack2(lo.x, lo.y);
+            f[2 * k + 1] = pack2(hi.x, hi.y);
+        }
+    }
+};
+
+// Two fp32 values as two E4M3 codes, lo in the low byte: round to nearest
+// even, magnitudes beyond 448 saturate to 448.
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi)
+{
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// One 16-code E4M3 chunk from the 16 elements of type T at src (16-byte
+// aligned): each element x is stored as the code of the fp32 quotient
+// x / scale (IEEE division).  Used by the E4M3 append and by the fused step,
+// so both store the same bits.
+template <typename T>
+__device__ __forceinline__ uint4 e4m3_chunk_from(const unsigned char *src, float scale)
+{
+    constexpr int kIn = 16 / Elem<T>::kPerChunk;  // input chunks of T
+    float x[16];
+#pragma unroll
+    for (int c = 0; c < kIn; ++c) Elem<T>::widen(ldg128_nc(src + c * 16), x + c * Elem<T>::kPerChunk);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t lo = e4m3x2_from_f32(__fdiv_rn(x[4 * k], scale), __fdiv_rn(x[4 * k + 1], scale));
+        const uint32_t hi = e4m3x2_from_f32(__fdiv_rn(x[4 * k + 2], scale), __fdiv_rn(x[4 * k + 3], scale));
+        w[k] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // Atomic add at GPU scope with acquire-release semantics; returns the old
 // value.  Writes that precede it (this thread's, and those it has seen through

@@ -33,13 +33,14 @@ KVD_ERR_CUDA = 5
 KVD_F32 = 0
 KVD_BF16 = 1
 KVD_F16 = 2
+KVD_E4M3 = 3
 
 KVD_DEVERR_PAST_LEN = 1
 KVD_DEVERR_TIMEOUT = 2
 KVD_DEVERR_PAGE = 4
 
 _TORCH_DTYPE = {torch.float32: KVD_F32, torch.bfloat16: KVD_BF16, torch.float16: KVD_F16}
-_NAME_DTYPE = {"f32": KVD_F32, "bf16": KVD_BF16, "f16": KVD_F16}
+_NAME_DTYPE = {"f32": KVD_F32, "bf16": KVD_BF16, "f16": KVD_F16, "e4m3": KVD_E4M3}
 
 
 class KvdError(RuntimeError):
@@ -78,6 +79,14 @@ class _Lib:
         lib.kvd_paged_decode_step.restype = ci
         lib.kvd_paged_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci,
                                               ci, cf, ci, vp, sz, u32p, vp]
+        lib.kvd_append_e4m3.restype = ci
+        lib.kvd_append_e4m3.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, cf, u32p, vp]
+        lib.kvd_decode_attention_e4m3.restype = ci
+        lib.kvd_decode_attention_e4m3.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, cf, cf,
+                                                  vp, sz, u32p, vp]
+        lib.kvd_decode_step_e4m3.restype = ci
+        lib.kvd_decode_step_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, cf, cf,
+                                             vp, sz, u32p, vp]
         lib.kvd_decode_attention_noalloc.restype = ci
         lib.kvd_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
                                                      ci, u32p, vp]
@@ -333,6 +342,88 @@ def kvd_paged_decode_step(q, k_pages, v_pages, k_new, v_new, out, block_table, p
                                    float(scale), _dtype_code(q), ws_ptr, ws_bytes, _ptr(err_word),
                                    _stream_handle(stream))
     _check("kvd_paged_decode_step", st)
+
+
+# ---------------------------------------------------------------------------------
+# E4M3 cache: k_cache / v_cache uint8 [B,H_kv,T_max,D] codes; q, new K/V, out bf16
+def _need_e4m3_cache(name: str, t: torch.Tensor) -> None:
+    """An E4M3 cache: uint8 codes or torch.float8_e4m3fn (the same bytes)."""
+    _need_cuda(name, t)
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise ValueError(f"{name} must be uint8 E4M3 codes or float8_e4m3fn, got {t.dtype}")
+
+
+def kvd_append_e4m3(k_cache, v_cache, k_new, v_new, past_len, max_past_len: int, k_scale: float,
+                    v_scale: float, err_word=None, stream=None) -> None:
+    """Quantize ``k_new``/``v_new`` [B,H_kv,N,D] (fp32, bf16 or fp16) into E4M3 slots ``past_len[b] + i``."""
+    _need_e4m3_cache("k_cache", k_cache)
+    _need_e4m3_cache("v_cache", v_cache)
+    for n, t in (("k_new", k_new), ("v_new", v_new)):
+        _need_cuda(n, t, k_new.dtype)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_kv, T_max, D = k_cache.shape
+    N = k_new.shape[2]
+    if v_cache.shape != k_cache.shape or tuple(k_new.shape) != (B, H_kv, N, D) or v_new.shape != k_new.shape:
+        raise ValueError("shape mismatch between caches and new K/V")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    st = raw.kvd_append_e4m3(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                             past_len.data_ptr(), B, H_kv, T_max, D, N, int(max_past_len), _dtype_code(k_new),
+                             float(k_scale), float(v_scale), _ptr(err_word), _stream_handle(stream))
+    _check("kvd_append_e4m3", st)
+
+
+def kvd_decode_attention_e4m3(q, k_cache, v_cache, out, past_len, max_past_len: int, k_scale: float,
+                              v_scale: float, scale: float = 0.0, workspace: Optional[torch.Tensor] = None,
+                              err_word=None, stream=None) -> None:
+    """Attention of the bf16 rows of ``q`` over E4M3 caches (workspace: alloc_workspace(..., "e4m3"))."""
+    for n, t in (("q", q), ("out", out)):
+        _need_cuda(n, t, torch.bfloat16)
+    _need_e4m3_cache("k_cache", k_cache)
+    _need_e4m3_cache("v_cache", v_cache)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_q, N, D = q.shape
+    _, H_kv, T_max, _ = k_cache.shape
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError("shape mismatch between q, out and the caches")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = raw.kvd_decode_attention_e4m3(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                       past_len.data_ptr(), B, H_q, H_kv, T_max, D, N, int(max_past_len),
+                                       float(scale), float(k_scale), float(v_scale), ws_ptr, ws_bytes,
+                                       _ptr(err_word), _stream_handle(stream))
+    _check("kvd_decode_attention_e4m3", st)
+
+
+def kvd_decode_step_e4m3(q, k_cache, v_cache, k_new, v_new, out, past_len, max_past_len: int, k_scale: float,
+                         v_scale: float, scale: float = 0.0, workspace: Optional[torch.Tensor] = None,
+                         err_word=None, stream=None) -> None:
+    """kvd_decode_step over E4M3 caches: quantize the bf16 new rows into their slots and attend, one launch."""
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("out", out)):
+        _need_cuda(n, t, torch.bfloat16)
+    _need_e4m3_cache("k_cache", k_cache)
+    _need_e4m3_cache("v_cache", v_cache)
+    _need_cuda("past_len", past_len, torch.int32)
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_q, N, D = q.shape
+    _, H_kv, T_max, _ = k_cache.shape
+    if (out.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B
+            or k_cache.shape[3] != D or tuple(k_new.shape) != (B, H_kv, N, D) or v_new.shape != k_new.shape):
+        raise ValueError("shape mismatch between q, out, the caches and the new K/V")
+    if past_len.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = raw.kvd_decode_step_e4m3(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
+                                  v_new.data_ptr(), out.data_ptr(), past_len.data_ptr(), B, H_q, H_kv, T_max, D,
+                                  N, int(max_past_len), float(scale), float(k_scale), float(v_scale), ws_ptr,
+                                  ws_bytes, _ptr(err_word), _stream_handle(stream))
+    _check("kvd_decode_step_e4m3", st)
 
 
 def kvd_decode_attention_noalloc(q, k_cache, v_cache, out, past_len, max_past_len: int,

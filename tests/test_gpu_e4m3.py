@@ -1,0 +1,148 @@
+"""E4M3 (8-bit) caches on the GPU: kvd_append_e4m3, kvd_decode_attention_e4m3 and
+kvd_decode_step_e4m3 against the oracle (append bit for bit, attention within the
+bf16 tolerance), the fused step bit-identical to append + attention."""
+import numpy as np
+import pytest
+import torch
+
+import kv_cache_decode_append_gb300 as kvd
+from kv_cache_decode_append_gb300 import workloads as wl
+from helpers import TOL, row_rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+K_SCALE, V_SCALE = 0.05, 0.02
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    return oracle.load()
+
+
+def _inputs(w, past, seed, device="cpu", new_dtype=torch.bfloat16):
+    """bf16 q and new rows; E4M3 history codes (torch's float8 cast of N(0,1)/scale),
+    NaN codes (0x7f) from slot P on."""
+    past = torch.as_tensor(past, dtype=torch.int32)
+    t = wl.layer_inputs(w, 0, past, device=device, seed_base=seed)
+    codes = {}
+    for key, sc in (("k_cache", K_SCALE), ("v_cache", V_SCALE)):
+        c = (torch.nan_to_num(t.pop(key).float()) / sc).to(torch.float8_e4m3fn).view(torch.uint8)
+        tail = torch.arange(w.T_max, device=device).view(1, 1, -1, 1) >= past.to(device).view(-1, 1, 1, 1)
+        codes[key] = c.masked_fill(tail, 0x7F).contiguous()
+    t.update(codes)
+    for key in ("k_new", "v_new"):
+        t[key] = t[key].to(new_dtype)
+    return past, t
+
+
+def _gpu(w, past, t, fused=False):
+    max_past = int(past.max())
+    g = {k: v.to(DEV).clone() for k, v in t.items()}
+    past_d = past.to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, "e4m3", DEV)
+    out = torch.full_like(g["q"], float("nan"))
+    if fused:
+        kvd.kvd_decode_step_e4m3(g["q"], g["k_cache"], g["v_cache"], g["k_new"], g["v_new"], out, past_d, max_past,
+                                 K_SCALE, V_SCALE, 0.0, ws, err)
+    else:
+        kvd.kvd_append_e4m3(g["k_cache"], g["v_cache"], g["k_new"], g["v_new"], past_d, max_past, K_SCALE, V_SCALE,
+                            err)
+        kvd.kvd_decode_attention_e4m3(g["q"], g["k_cache"], g["v_cache"], out, past_d, max_past, K_SCALE, V_SCALE,
+                                      0.0, ws, err)
+    torch.cuda.synchronize()
+    return out, g, int(err.item())
+
+
+def _same_bits(a, b):
+    return np.array_equal(to_np(a).view(np.uint8), to_np(b).view(np.uint8))
+
+
+def _oracle(orc, w, past, t):
+    h = {k: (v.cpu().numpy().copy() if v.dtype == torch.uint8 else to_np(v)) for k, v in t.items()}
+    nd = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[t["k_new"].dtype]
+    assert orc.append_e4m3(h["k_cache"], h["v_cache"], h["k_new"], h["v_new"], past.numpy(), nd, K_SCALE,
+                           V_SCALE) == 0
+    ref, st = orc.decode_attention_e4m3(h["q"], h["k_cache"], h["v_cache"], past.numpy(), "bf16", K_SCALE, V_SCALE)
+    assert st == 0
+    return ref, h
+
+
+def _check(orc, w, past, seed, device="cpu", fused_too=True):
+    past, t = _inputs(w, past, seed, device)
+    out, g, err = _gpu(w, past, t)
+    assert err == 0
+    ref, h = _oracle(orc, w, past, t)
+    assert np.array_equal(g["k_cache"].cpu().numpy(), h["k_cache"])
+    assert np.array_equal(g["v_cache"].cpu().numpy(), h["v_cache"])
+    assert row_rel_err(out.double().cpu().numpy(), ref) <= TOL["bf16"]
+    if fused_too:
+        out2, g2, err2 = _gpu(w, past, t, fused=True)
+        assert err2 == 0
+        assert _same_bits(g2["k_cache"], g["k_cache"]) and _same_bits(g2["v_cache"], g["v_cache"])
+        assert _same_bits(out2, out)
+
+
+# (B, H_q, H_kv, D, N, T_max, past)
+E4M3_CASES = [
+    (8, 12, 12, 64, 1, 1024, [1023, 0, 512, 1, 64, 900, 333, 1000]),  # GPT-2 shapes, batch 8
+    (4, 32, 8, 128, 1, 3000, [2999, 17, 1500, 2048]),                 # GQA 4 rows, ragged
+    (3, 16, 2, 128, 1, 900, [899, 450, 0]),                           # 8 rows: two row blocks of 4
+    (2, 8, 2, 64, 5, 700, [63, 600]),                                 # chunk of 5 across a tile
+    (1, 4, 4, 128, 3, 3, [0]),                                        # empty history, P + N = T_max
+]
+
+
+@pytest.mark.parametrize("case", E4M3_CASES, ids=[f"e4m3_{i}" for i in range(len(E4M3_CASES))])
+def test_e4m3_parity(orc, case):
+    B, H_q, H_kv, D, N, T_max, past = case
+    w = wl.Workload(0, "e4m3", L=1, B=B, H_q=H_q, H_kv=H_kv, D=D, N=N, dtype="bf16", T_max=T_max, P=0)
+    _check(orc, w, past, seed=9600 + D + N)
+
+
+@pytest.mark.parametrize("new_dtype", [torch.float32, torch.float16], ids=["f32", "f16"])
+def test_e4m3_append_other_input_types(orc, new_dtype):
+    w = wl.Workload(0, "e4m3a", L=1, B=2, H_q=4, H_kv=2, D=128, N=3, dtype="bf16", T_max=300, P=0)
+    past, t = _inputs(w, [17, 290], 9700, new_dtype=new_dtype)
+    t["k_new"] = t["k_new"] * 40  # some quotients beyond 448: saturation
+    _, g, err = _gpu(w, past, t)
+    assert err == 0
+    _, h = _oracle(orc, w, past, t)
+    assert np.array_equal(g["k_cache"].cpu().numpy(), h["k_cache"])
+    assert np.array_equal(g["v_cache"].cpu().numpy(), h["v_cache"])
+    assert (h["k_cache"][:, :, 17:20] & 0x7F == 0x7E).any()  # saturated codes were exercised
+
+
+@pytest.mark.parametrize("case", [(16, 32, 8, 128, 6200, 6100, 2), (16, 32, 8, 128, 1100, 1000, 1)],
+                         ids=["merge_pass", "in_kernel"])
+def test_e4m3_merge_modes(orc, case):
+    B, H_q, H_kv, D, T_max, max_past, launches = case
+    assert kvd.kvd_decode_plan(B, H_q, H_kv, D, 1, max_past, "e4m3")["launches"] == launches
+    gen = torch.Generator().manual_seed(9800 + launches)
+    past = torch.randint(0, max_past + 1, (B,), generator=gen, dtype=torch.int32)
+    past[2] = max_past
+    w = wl.Workload(0, "e4m3m", L=1, B=B, H_q=H_q, H_kv=H_kv, D=D, N=1, dtype="bf16", T_max=T_max, P=0)
+    _check(orc, w, past, seed=9810 + launches)
+
+
+def test_e4m3_gqa_longctx_full_size(orc):
+    """The long-context workload's shapes and lengths at full size with an E4M3 cache."""
+    w = wl.WORKLOADS["gqa_longctx_b32_bf16"]
+    _check(orc, w, wl.past_lens(w), seed=9900, device=DEV)
+
+
+def test_e4m3_rejects_misuse():
+    q = torch.zeros((1, 4, 1, 64), dtype=torch.bfloat16, device=DEV)
+    kc = torch.zeros((1, 2, 16, 64), dtype=torch.uint8, device=DEV)
+    past = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = kvd.alloc_workspace(1, 4, 2, 64, 1, 8, "e4m3", DEV)
+    with pytest.raises(kvd.KvdError) as e:  # a scale must be positive
+        kvd.kvd_decode_attention_e4m3(q, kc, kc, torch.empty_like(q), past, 8, 0.0, 1.0, 0.0, ws)
+    assert e.value.status == kvd.KVD_ERR_INVALID_ARG
+    assert kvd.raw.kvd_decode_attention(q.data_ptr(), kc.data_ptr(), kc.data_ptr(), q.data_ptr(), past.data_ptr(),
+                                        1, 4, 2, 16, 64, 1, 8, 0.0, kvd.KVD_E4M3, ws.data_ptr(), ws.numel(), None,
+                                        None) == kvd.KVD_ERR_UNSUPPORTED
