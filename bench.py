@@ -46,20 +46,22 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_step_gqa_longctx_b32.md
 
 # ---------------------------------------------------------------------------------
 # algorithmic bytes (the roofline's per-unit figures)
-def attn_bytes(w: wl.Workload, past) -> int:
-    """K/V read over P_b + N keys of every (b, h_kv), plus Q read and O written."""
+def attn_bytes(w: wl.Workload, past, cache_elem: int = 0) -> int:
+    """K/V read over P_b + N keys of every (b, h_kv), plus Q read and O written
+    (cache_elem: bytes per cache element when the cache type differs, E4M3: 1)."""
     s = w.elem_bytes
+    c = cache_elem or s
     keys = sum(int(p) + w.N for p in past)
-    return 2 * w.H_kv * w.D * s * keys + 2 * w.B * w.H_q * w.N * w.D * s
+    return 2 * w.H_kv * w.D * c * keys + 2 * w.B * w.H_q * w.N * w.D * s
 
 
-def append_bytes(w: wl.Workload) -> int:
-    """New K and V read, and the same bytes written into the cache."""
-    return 4 * w.B * w.H_kv * w.N * w.D * w.elem_bytes
+def append_bytes(w: wl.Workload, cache_elem: int = 0) -> int:
+    """New K and V read, and written into the cache (in the cache's element size)."""
+    return 2 * w.B * w.H_kv * w.N * w.D * (w.elem_bytes + (cache_elem or w.elem_bytes))
 
 
-def layer_bytes(w, past) -> int:
-    return attn_bytes(w, past) + append_bytes(w)
+def layer_bytes(w, past, cache_elem: int = 0) -> int:
+    return attn_bytes(w, past, cache_elem) + append_bytes(w, cache_elem)
 
 
 # ---------------------------------------------------------------------------------
@@ -210,8 +212,16 @@ def whole_job_gbs(bytes_per_step_per_rank: int, steps: int, elapsed_max_s: float
     return world * bytes_per_step_per_rank * steps / elapsed_max_s / 1e9
 
 
+E4M3_SCALES = (0.05, 0.02)  # k_scale, v_scale of the E4M3 cache runs (N(0,1) data)
+
+
 def oracle_layer_step(orc, host, past_np, dtype):
-    if "k_pages" in host:  # paged layout
+    if host["k_cache" if "k_cache" in host else "k_pages"].dtype == "uint8":  # E4M3 cache
+        st = orc.append_e4m3(host["k_cache"], host["v_cache"], host["k_new"], host["v_new"], past_np, dtype,
+                             *E4M3_SCALES)
+        out, st2 = orc.decode_attention_e4m3(host["q"], host["k_cache"], host["v_cache"], past_np, dtype,
+                                             *E4M3_SCALES)
+    elif "k_pages" in host:  # paged layout
         st = orc.paged_append(host["k_pages"], host["v_pages"], host["k_new"], host["v_new"], host["table"],
                               past_np, dtype)
         out, st2 = orc.paged_decode_attention(host["q"], host["k_pages"], host["v_pages"], host["table"],
@@ -227,7 +237,7 @@ def oracle_layer_step(orc, host, past_np, dtype):
 def to_host_np(t: torch.Tensor):
     import numpy as np
     t = t.detach().contiguous().cpu()
-    if t.dtype == torch.int32:
+    if t.dtype in (torch.int32, torch.uint8):
         return t.numpy().copy()
     if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).numpy().view(np.uint16).copy()
@@ -293,9 +303,16 @@ def run_gpu(args, w, rank, world, local):
     max_past = int(past.max())
     past_d = past.to(dev)
     paged = args.layout == "paged"
+    e4m3 = args.cache == "e4m3"
+    if e4m3 and (paged or w.dtype != "bf16"):
+        raise SystemExit("--cache e4m3 needs a bf16 workload and the contiguous layout")
+    cache_elem = 1 if e4m3 else 0
     layers = []
     for l in range(w.L):
         x = wl.layer_inputs(w, l, past, device=dev, tail_fill="zero")
+        if e4m3:  # the same data as E4M3 codes (torch's float8 cast of value / scale)
+            for key, sc in zip(("k_cache", "v_cache"), E4M3_SCALES):
+                x[key] = (x[key].float() / sc).to(torch.float8_e4m3fn).view(torch.uint8)
         if paged:  # the same data as a shuffled page pool with a block table
             x["k_pages"], x["v_pages"], x["table"] = wl.to_paged(
                 x.pop("k_cache"), x.pop("v_cache"), args.page_size, seed=l, fill=0.0,
@@ -303,8 +320,9 @@ def run_gpu(args, w, rank, world, local):
         layers.append(x)
     outs = [torch.empty_like(x["q"]) for x in layers]
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, w.torch_dtype, dev)
-    plan = kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, w.torch_dtype)
+    plan_dtype = "e4m3" if e4m3 else w.torch_dtype
+    ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, plan_dtype, dev)
+    plan = kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, plan_dtype)
     merge = plan["launches"] == 2
     launches_per_layer = plan["launches"] + (0 if args.path == "fused" else 1)
 
@@ -313,7 +331,15 @@ def run_gpu(args, w, rank, world, local):
     def layer_step(l):
         x = layers[l]
         # the current stream: the capture stream inside torch.cuda.graph
-        if paged and fused:
+        if e4m3 and fused:
+            kvd.kvd_decode_step_e4m3(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l], past_d,
+                                     max_past, *E4M3_SCALES, 0.0, ws, err)
+        elif e4m3:
+            kvd.kvd_append_e4m3(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past,
+                                *E4M3_SCALES, err)
+            kvd.kvd_decode_attention_e4m3(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past,
+                                          *E4M3_SCALES, 0.0, ws, err)
+        elif paged and fused:
             kvd.kvd_paged_decode_step(x["q"], x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], outs[l],
                                       x["table"], past_d, max_past, 0.0, ws, err)
         elif paged:
@@ -355,7 +381,13 @@ def run_gpu(args, w, rank, world, local):
     with torch.cuda.graph(attn_graph):
         for l in range(w.L):
             x = layers[l]
-            if paged and fused:
+            if e4m3 and fused:
+                kvd.kvd_decode_step_e4m3(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l],
+                                         past_d, max_past, *E4M3_SCALES, 0.0, ws, err)
+            elif e4m3:
+                kvd.kvd_decode_attention_e4m3(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past,
+                                              *E4M3_SCALES, 0.0, ws, err)
+            elif paged and fused:
                 kvd.kvd_paged_decode_step(x["q"], x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], outs[l],
                                           x["table"], past_d, max_past, 0.0, ws, err)
             elif paged:
@@ -431,17 +463,17 @@ def run_gpu(args, w, rank, world, local):
 
     if rank != 0:
         return
-    bytes_step = w.L * layer_bytes(w, past.tolist())
+    bytes_step = w.L * layer_bytes(w, past.tolist(), cache_elem)
     gbs = whole_job_gbs(bytes_step, args.steps, elapsed_max, world)
     ms_step = elapsed_max / args.steps * 1e3
     peak, peak_kind = measured_peak()
-    a_bytes = layer_bytes(w, past.tolist()) if fused else attn_bytes(w, past.tolist())
+    a_bytes = layer_bytes(w, past.tolist(), cache_elem) if fused else attn_bytes(w, past.tolist(), cache_elem)
     achieved = a_bytes / attn_per_launch / 1e9
 
     # CPU baseline: the oracle on layer 0's data, all host cores, ~10 s
     host = {k: to_host_np(v) for k, v in layers[0].items()}
     reps, cpu_el, cores = time_oracle(w, host, past, budget_s=args.cpu_seconds)
-    cpu_gbs = reps * layer_bytes(w, past.tolist()) / cpu_el / 1e9
+    cpu_gbs = reps * layer_bytes(w, past.tolist(), cache_elem) / cpu_el / 1e9
 
     line = {
         "metric": METRIC,
@@ -467,6 +499,8 @@ def run_gpu(args, w, rank, world, local):
             "parallelism": f"replicas x{world}",
             "cache_layout": (f"paged: {args.page_size}-token pages, {args.page_order} pool, block table"
                              if paged else "contiguous [B, H_kv, T_max, D]"),
+            "cache_dtype": (f"e4m3 (k_scale {E4M3_SCALES[0]}, v_scale {E4M3_SCALES[1]}; q, new K/V, out bf16)"
+                            if e4m3 else w.dtype),
         },
         "us_per_layer_step": round(ms_step * 1e3 / w.L, 3),
         "frac_of_peak": round(gbs / world / peak, 4),
@@ -484,7 +518,7 @@ def run_gpu(args, w, rank, world, local):
             "frac": round(achieved / peak, 4),
             "algorithmic_bytes_per_launch": a_bytes,
             "plan": plan,
-            "traffic": None if paged else profiled_traffic(),
+            "traffic": None if (paged or e4m3) else profiled_traffic(),
         },
         "cpu_baseline": {
             "value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
@@ -516,6 +550,8 @@ def main():
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"],
                     help="KV cache layout (paged: kvd_paged_* on a shuffled page pool)")
     ap.add_argument("--page-size", type=int, default=64, help="tokens per page for --layout paged")
+    ap.add_argument("--cache", default="same", choices=["same", "e4m3"],
+                    help="cache element type: the workload's, or E4M3 codes (bf16 workloads)")
     ap.add_argument("--page-order", default="shuffled", choices=["shuffled", "sequential"],
                     help="physical page order of the pool for --layout paged")
     args = ap.parse_args()

@@ -70,6 +70,7 @@ typedef enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1, KVD_F16 = 2, KVD_E4M3 = 3 } 
 #define KVD_DEVERR_PAST_LEN 1u /* a sequence had an out-of-range past_len and was skipped */
 #define KVD_DEVERR_TIMEOUT 2u  /* a bounded shared-memory pipeline wait gave up */
 #define KVD_DEVERR_PAGE 4u     /* a paged call met a block-table entry outside [0, num_pages) */
+#define KVD_DEVERR_INTERNAL 8u /* a launch found an internal invariant broken and did nothing */
 
 /*
  * kvd_append -- in-place cache update (step 1 of a decode step).
@@ -160,8 +161,9 @@ kvd_status kvd_decode_step(const void *q, void *k_cache, void *v_cache, const vo
  * (one CTA per resident slot; each CTA streams an equal share of all tiles)
  * and block, dynamic shared memory, kernels launched per call (2 when the
  * ranges are long and a separate merge pass combines the heads split across
- * CTAs, else 1: the kernel merges them itself) and the workspace size.
- * Returns the same argument errors as kvd_decode_attention.
+ * CTAs, else 1: the kernel merges them itself), the workspace size, the query
+ * rows per block and whether the tensor-core kernel runs.  Returns the same
+ * argument errors as kvd_decode_attention.
  */
 typedef struct kvd_plan_info {
     int tile_keys;
@@ -171,6 +173,9 @@ typedef struct kvd_plan_info {
     int smem_bytes;
     int launches;
     size_t workspace_bytes;
+    int rows_per_block;  /* query rows of a (b, h) handled together */
+    int tensor_cores;    /* 1: the tensor-core kernel (bf16 / fp16 contiguous caches with
+                            (H_q / H_kv) * N >= 16 query rows per KV head), 0: CUDA cores */
 } kvd_plan_info;
 
 kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len,

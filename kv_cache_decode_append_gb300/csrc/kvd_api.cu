@@ -160,6 +160,50 @@ int g_occ_n = 0;
 constexpr int kMaxSmemPerCta = 227 * 1024;
 // Ranges longer than this many tile units per CTA use the separate merge pass.
 constexpr int kLongRangeUnits = 32;
+// Query rows per KV head from which the tensor-core kernel (16-row blocks) is used.
+constexpr int kMmaMinRows = 16;
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to the
+// driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_looked_up = false;
+
+kvd_status encode_fn(EncodeTiledFn *fn)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode_looked_up) {
+        g_encode_looked_up = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    *fn = g_encode;
+    return g_encode != nullptr ? KVD_OK : KVD_ERR_CUDA;
+}
+
+// A 2-D tensor map over a contiguous cache viewed as [rows, D] 16-bit
+// elements, in boxes of 64 rows x 64 elements (128 bytes), 128-byte swizzle.
+kvd_status encode_cache_map(CUtensorMap *map, const void *cache, long long rows, int D, kvd_dtype dtype)
+{
+    EncodeTiledFn fn;
+    kvd_status st = encode_fn(&fn);
+    if (st != KVD_OK) return st;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, dtype == KVD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                          const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_CUDA;
+}
 
 kvd_status current_device(int *dev)
 {
@@ -227,6 +271,7 @@ struct Plan {
     int rows, rb, n_rowblocks;
     int grid, smem, launches, max_tiles;
     bool merge_pass;  // split heads merged by a second launch (else inside the kernel)
+    bool mma;         // tensor-core kernel (16-row blocks, tiles by tensor map)
     size_t part_off, tickets_off, seg_off, ws_bytes;
 };
 
@@ -281,13 +326,24 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
     if (st != KVD_OK) return st;
     pl->rows = (H_q / H_kv) * N;
-    pl->rb = pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : (pl->rows <= 4 || dtype == KVD_E4M3) ? 4 : 8;
+    // Many query rows per KV head (chunked decode with GQA): the tensor-core
+    // kernel in blocks of 16 rows, for 16-bit contiguous caches.
+    pl->mma = pl->rows >= kMmaMinRows && !paged && (dtype == KVD_BF16 || dtype == KVD_F16);
+    pl->rb = pl->mma ? 16 : pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : (pl->rows <= 4 || dtype == KVD_E4M3) ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
     AttnVariant vp, vt, op, ot;  // this layout's builds, and the other layout's
-    if (!pick_builds(dtype, D, pl->rb, paged, &vp, &vt)) return KVD_ERR_UNSUPPORTED;
-    if (!pick_builds(dtype, D, pl->rb, !paged, &op, &ot)) {  // (no other layout: E4M3)
+    if (pl->mma) {
+        const bool ok = dtype == KVD_BF16 ? attn_variant_mma_bf16(D, &vp) && attn_variant_mma_bf16_tk(D, &vt)
+                                          : attn_variant_mma_f16(D, &vp) && attn_variant_mma_f16_tk(D, &vt);
+        if (!ok) return KVD_ERR_UNSUPPORTED;
         op = vp;
         ot = vt;
+    } else {
+        if (!pick_builds(dtype, D, pl->rb, paged, &vp, &vt)) return KVD_ERR_UNSUPPORTED;
+        if (!pick_builds(dtype, D, pl->rb, !paged, &op, &ot)) {  // (no other layout: E4M3)
+            op = vp;
+            ot = vt;
+        }
     }
     pl->v = vp;
 
@@ -406,6 +462,8 @@ kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_
     info->smem_bytes = pl.smem;
     info->launches = pl.launches;
     info->workspace_bytes = pl.ws_bytes;
+    info->rows_per_block = pl.rb;
+    info->tensor_cores = pl.mma ? 1 : 0;
     return KVD_OK;
 }
 
@@ -509,8 +567,19 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     cfg.gridDim = dim3((unsigned)pl.grid);
     cfg.blockDim = dim3(pl.v.threads);
     cfg.dynamicSmemBytes = (size_t)pl.smem;
-    if (cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.fused_fn : pl.v.fn, args) != cudaSuccess)
+    if (pl.v.tma) {
+        // the K and V tensor maps, passed by value after the arguments
+        const long long rows_total = (long long)B * H_kv * T_max;
+        if (rows_total + 64 > 0x7fffffffLL) return KVD_ERR_UNSUPPORTED;  // 32-bit box coordinates
+        alignas(64) CUtensorMap tmk, tmv;
+        if ((st = encode_cache_map(&tmk, k_cache, rows_total, D, dtype)) != KVD_OK) return st;
+        if ((st = encode_cache_map(&tmv, v_cache, rows_total, D, dtype)) != KVD_OK) return st;
+        void *targs[] = {&a, &tmk, &tmv};
+        if (cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.fused_fn : pl.v.fn, targs) != cudaSuccess)
+            return KVD_ERR_CUDA;
+    } else if (cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.fused_fn : pl.v.fn, args) != cudaSuccess) {
         return KVD_ERR_CUDA;
+    }
     if (pl.merge_pass) {  // one warp per query row of the split heads
         const long long warps = (long long)B * H_kv * pl.n_rowblocks * pl.rb;
         cfg.gridDim = dim3((unsigned)((warps * 32 + 127) / 128));

@@ -101,6 +101,7 @@ static_assert(sizeof(AttnArgs) == 128, "keep the kernel parameter block at 128 b
 template <typename T, int D, int RB, typename C = T> struct AttnShape {
     using Ty = Elem<C>;   // cache rows (the K/V tiles)
     using Tq = Elem<T>;   // q, new K/V and out rows
+    static constexpr bool kTma = false;  // tiles arrive by 1-D bulk copies
     static constexpr int kRB = RB;
     static constexpr int kRowBytes = D * Ty::kBytes;   // one cache row
     static constexpr int kQRowBytes = D * Tq::kBytes;  // one q / new K/V / out row
@@ -361,6 +362,7 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
     uint64_t policy;
     int page_next;          // paged: physical page of the next tile (loaded one tile ahead)
     const int32_t *bt_row;  // paged: block-table row of the current sequence
+    const void *tm_k, *tm_v;  // tensor-map tiles (S::kTma): the K and V tensor maps
 
     // Paged: start the load of the next tile's page-table entry; it is used
     // one fill later, so its latency hides behind the current tile.
@@ -479,9 +481,22 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
             off = (size_t)mt.tile_k0 * S::kRowBytes;
         }
         unsigned char *dst = smem + S::kRingOff + s * 2 * S::kTileBytes;
-        mbar_arrive_expect_tx(&full[s], 2u * bytes + qbytes);
-        bulk_load_g2s(dst, kg + off, bytes, &full[s], policy);
-        bulk_load_g2s(dst + S::kTileBytes, vg + off, bytes, &full[s], policy);
+        if constexpr (S::kTma) {
+            // whole boxes of kTK rows (rows past the head are masked, or zero
+            // past the tensor), 128-byte swizzled, kBoxes per K or V tile
+            (void)off;
+            mbar_arrive_expect_tx(&full[s], 2u * S::kTileBytes + qbytes);
+            const int y = bh * a.T_max + mt.tile_k0;
+#pragma unroll
+            for (int bx = 0; bx < S::kBoxes; ++bx) {
+                tma_load_2d(dst + bx * S::kBoxBytes, tm_k, bx * S::kBoxCols, y, &full[s], policy);
+                tma_load_2d(dst + S::kTileBytes + bx * S::kBoxBytes, tm_v, bx * S::kBoxCols, y, &full[s], policy);
+            }
+        } else {
+            mbar_arrive_expect_tx(&full[s], 2u * bytes + qbytes);
+            bulk_load_g2s(dst, kg + off, bytes, &full[s], policy);
+            bulk_load_g2s(dst + S::kTileBytes, vg + off, bytes, &full[s], policy);
+        }
         if (qbytes) bulk_load_g2s(smem + S::kQOff + s * S::kQSlotBytes, qg, qbytes, &full[s], policy);
 
         // advance to the next tile of the flattened list (skipping the next
@@ -597,7 +612,7 @@ __device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &
 // merged at the end of this kernel (else by attn_merge_kernel).  kPaged: the
 // cache is paged (block table), else contiguous [B, H_kv, T_max, D].
 template <typename T, int D, int RB, bool kFused, bool kTicketMerge, bool kPaged, typename C = T>
-__global__ void __launch_bounds__(AttnShape<T, D, RB>::kThreads)
+__global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     attn_balanced_kernel(const AttnArgs a)
 {
     using S = AttnShape<T, D, RB, C>;
@@ -995,6 +1010,7 @@ struct AttnVariant {
     int tile_keys;
     int rows_per_block;
     int piece_units;       // cost of a piece boundary in tile units
+    bool tma = false;      // tensor-core kernel: takes the K and V tensor maps
 };
 
 template <typename T, int D, int RB, bool kTicketMerge, bool kPaged, typename C = T> AttnVariant make_variant()
@@ -1056,5 +1072,10 @@ bool attn_variant_f16_paged(int D, int RB, AttnVariant *v);
 bool attn_variant_f16_tk_paged(int D, int RB, AttnVariant *v);
 bool attn_variant_e4m3(int D, int RB, AttnVariant *v);      // bf16 q / out, E4M3 cache
 bool attn_variant_e4m3_tk(int D, int RB, AttnVariant *v);
+// tensor-core kernels (kvd_attention_mma.cuh): 16-row blocks, contiguous caches
+bool attn_variant_mma_bf16(int D, AttnVariant *v);
+bool attn_variant_mma_bf16_tk(int D, AttnVariant *v);
+bool attn_variant_mma_f16(int D, AttnVariant *v);
+bool attn_variant_mma_f16_tk(int D, AttnVariant *v);
 
 }  // namespace kvd

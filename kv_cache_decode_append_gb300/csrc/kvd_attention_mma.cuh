@@ -1,0 +1,513 @@
+// kvd_attention_mma.cuh -- split-T decode attention on the tensor cores.
+//
+// The same computation as attn_balanced_kernel (offset-causal GQA decode
+// attention with a statically balanced split over T and a log-sum-exp merge;
+// "7.1 自回归生成过程", code 1-2; "GPT-2缓存实测：千倍计算只快6倍", section
+// "一个很容易漏掉的错误"), for blocks of 16 query rows: S = Q.K^T and O += P.V
+// are dense contractions per tile, run as mma.sync m16n8k16 (bf16 or fp16
+// operands, fp32 accumulators) instead of packed FMAs.  This serves chunked
+// decode with many rows per KV head (g * N >= 16, where the CUDA-core kernel
+// would need several row blocks and re-read K/V for each), and moves the
+// per-element work of every decode off the CUDA cores.
+//
+// Differences from attn_balanced_kernel:
+//   * tiles arrive by 2-D TMA through tensor maps over the cache viewed as
+//     [B*H_kv*T_max, D], in boxes of 64 keys x 128 bytes with the 128-byte
+//     swizzle, so that ldmatrix reads 8 keys at one column chunk without bank
+//     conflicts (a plain row-major tile would serialize those reads 8 ways);
+//   * a warp owns 16 keys of each 64-key tile and all 16 rows; its Q
+//     fragments stay in registers for the piece, S lives in the MMA
+//     accumulators, and the softmax weights P are repacked from the S
+//     accumulators straight into the A fragments of the P.V MMA;
+//   * scores are scaled after the MMA (Q stays exact in its 16-bit type); P
+//     enters the MMA rounded to the operand type while the normaliser l sums
+//     the fp32 weights;
+//   * value rows past the end of a sequence are zeroed in shared memory
+//     before they reach the MMA (a zero weight times a stale NaN would still
+//     be NaN); in a fused step the new rows are written into the tile (and
+//     the cache) before the tile is read.
+#pragma once
+
+#include "kvd_attention.cuh"
+
+namespace kvd {
+
+// Compile-time shape of a tensor-core variant: 16 query rows, 64-key tiles,
+// 4 warps of 16 keys.  Member names match AttnShape where RangeWalk and the
+// epilogue use them.
+template <typename T, int D> struct MmaShape {
+    using Tq = Elem<T>;
+    static constexpr bool kTma = true;
+    static constexpr int kRB = 16;
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kQRowBytes = D * 2;
+    static constexpr int kTK = 64;
+    static constexpr int kNW = 4;
+    static constexpr int kThreads = kNW * 32;
+    static constexpr int kKpw = kTK / kNW;             // keys per warp per tile (16)
+    static constexpr int kBoxCols = 64;                // 16-bit elements per 128-byte box row
+    static constexpr int kBoxes = D / kBoxCols;
+    static constexpr int kBoxBytes = kTK * 128;        // one box: 64 rows x 128 bytes
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;
+    static constexpr int kStages = (D == 128) ? 2 : 4;
+    static constexpr int kQSlotBytes = kRB * kQRowBytes;
+    static constexpr int kPieceUnits = 2;
+    static constexpr int kKSteps = D / 16;             // k-steps of S = Q.K^T
+    static constexpr int kNTiles = D / 8;              // 8-wide output column tiles of O
+
+    static constexpr int kRingOff = 0;                 // 1024-aligned boxes (swizzle pattern)
+    static constexpr int kQOff = kRingOff + kStages * 2 * kTileBytes;
+    static constexpr int kEpiOff = kQOff + kStages * kQSlotBytes;
+    static constexpr int kEpiFloats = ((kNW * kRB * (D + 2) + 3) / 4) * 4;
+    static constexpr int kEpiBytes = kEpiFloats * 4;
+    static constexpr int kMetaOff = kEpiOff + kEpiBytes;
+    static constexpr int kBarOff = kMetaOff + kStages * 32;
+    static constexpr int kJobOff = kBarOff + 2 * kStages * 8;
+    static constexpr int kPageOff = kJobOff + 32;
+    static constexpr int kFixedBytes = kPageOff + 16;
+
+    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(kBoxBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+};
+
+// Shared-memory address of the 16-byte chunk c (0 .. D/8-1) of tile row r in
+// a K or V tile of 128-byte-swizzled boxes starting at shared address tile.
+// The 128-byte swizzle moves the 16-byte chunk of address bits [6:4] by
+// bits [9:7] (XOR); applied to the actual address it holds for any
+// 128-byte-aligned box.
+template <typename S> __device__ __forceinline__ uint32_t mma_chunk_addr(uint32_t tile, int r, int c)
+{
+    const uint32_t lin = tile + (c >> 3) * S::kBoxBytes + r * 128 + ((c & 7) << 4);
+    return lin ^ ((lin >> 3) & 0x70u);
+}
+
+// One tile for one warp: its 16 keys kb .. kb+15 of the tile, 16 rows.
+//   qa     Q A-fragments per k-step (rows g, g+8; columns 16s + 2t, +8)
+//   oacc   O accumulators per 8-column tile (C layout: rows g, g+8)
+//   m, l   running max (log2 units) and this lane's share of the weight sum,
+//          for rows g and g+8
+// kMasked: per-key limits apply (lim: first key each row may not see), and
+// value rows at or past k_end are zeroed first.
+template <typename T, int D, bool kMasked>
+__device__ __forceinline__ void mma_tile(unsigned char *Ks, unsigned char *Vs,
+                                         const uint32_t (&qa)[MmaShape<T, D>::kKSteps][4],
+                                         float (&oacc)[MmaShape<T, D>::kNTiles][4], float (&m)[2],
+                                         float (&l)[2], int warp, int lane, int tile_k0,
+                                         const int (&lim)[2], int k_end, float qscale)
+{
+    using S = MmaShape<T, D>;
+    const float kNegInf = __int_as_float(0xff800000);
+    constexpr float kRescaleThreshold = 8.0f;
+    const int t = lane & 3;
+    const int kb = warp * S::kKpw;
+    const uint32_t k_base = smem_addr(Ks), v_base = smem_addr(Vs);
+
+    // ---- S = Q . K^T for the warp's 16 keys (two 8-key column tiles) ----
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+    {
+        // ldmatrix.x4: matrices (keys kb.., chunk 2s), (kb.., 2s+1), (kb+8.., 2s), (kb+8.., 2s+1)
+        const int key = kb + ((lane >> 4) << 3) + (lane & 7);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < S::kKSteps; ++ks) {
+            uint32_t b[4];
+            ldmatrix_x4_addr(b, mma_chunk_addr<S>(k_base, key, 2 * ks + csel));
+            mma_16816<T>(sacc[0], qa[ks], b[0], b[1]);
+            mma_16816<T>(sacc[1], qa[ks], b[2], b[3]);
+        }
+    }
+
+    // ---- scale, mask, online softmax (rows g: e = 0,1; g+8: e = 2,3) ----
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            sacc[nt][e] *= qscale;
+            if constexpr (kMasked) {
+                const int key = tile_k0 + kb + nt * 8 + 2 * t + (e & 1);
+                if (key >= lim[e >> 1]) sacc[nt][e] = kNegInf;
+            }
+        }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        float mt = fmaxf(fmaxf(sacc[0][2 * r], sacc[0][2 * r + 1]), fmaxf(sacc[1][2 * r], sacc[1][2 * r + 1]));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        if (mt > m[r] + kRescaleThreshold) {
+            const float alpha = fast_exp2(m[r] - mt);
+            l[r] *= alpha;
+#pragma unroll
+            for (int nt = 0; nt < S::kNTiles; ++nt) {
+                oacc[nt][2 * r] *= alpha;
+                oacc[nt][2 * r + 1] *= alpha;
+            }
+            m[r] = mt;
+        }
+        const float mu = (m[r] == kNegInf) ? 0.f : m[r];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 2 * r; e < 2 * r + 2; ++e) {
+                const float p = fast_exp2(sacc[nt][e] - mu);
+                l[r] += p;
+                sacc[nt][e] = p;
+            }
+    }
+    // P as the A fragments of P . V (the S accumulator layout is the A layout)
+    const uint32_t pa[4] = {pack_pair<T>(sacc[0][0], sacc[0][1]), pack_pair<T>(sacc[0][2], sacc[0][3]),
+                            pack_pair<T>(sacc[1][0], sacc[1][1]), pack_pair<T>(sacc[1][2], sacc[1][3])};
+
+    // ---- value rows past the end of the sequence: zero (a NaN times 0 is NaN) ----
+    if constexpr (kMasked) {
+        if (tile_k0 + kb + S::kKpw > k_end) {
+            for (int idx = lane; idx < S::kKpw * (D / 8); idx += 32) {
+                const int r = kb + idx / (D / 8), c = idx % (D / 8);
+                if (tile_k0 + r >= k_end) sts128(mma_chunk_addr<S>(v_base, r, c), make_uint4(0u, 0u, 0u, 0u));
+            }
+            fence_proxy_async_shared();  // before the slot is refilled by a bulk copy
+            __syncwarp();
+        }
+    }
+
+    // ---- O += P . V: ldmatrix.trans matrices (keys kb.., chunk c), (kb+8.., c), (kb.., c+1), (kb+8.., c+1) ----
+    {
+        const int key = kb + (((lane >> 3) & 1) << 3) + (lane & 7);
+        const int csel = lane >> 4;
+#pragma unroll
+        for (int c = 0; c < S::kNTiles; c += 2) {
+            uint32_t b[4];
+            ldmatrix_x4_trans_addr(b, mma_chunk_addr<S>(v_base, key, c + csel));
+            mma_16816<T>(oacc[c], pa, b[0], b[1]);
+            mma_16816<T>(oacc[c + 1], pa, b[2], b[3]);
+        }
+    }
+}
+
+// In a fused step the tile holding new keys P .. P+N-1 has stale cache rows:
+// the warp copies its new rows from k_new / v_new into the tile (and, when
+// kc / vc are given, into the cache) before the tile is read.
+template <typename T, int D>
+__device__ __forceinline__ void mma_insert_new_rows(unsigned char *Ks, unsigned char *Vs, int warp, int lane,
+                                                    int tile_k0, int P, int k_end, const unsigned char *kn,
+                                                    const unsigned char *vn, unsigned char *kc, unsigned char *vc)
+{
+    using S = MmaShape<T, D>;
+    const int kb = warp * S::kKpw;
+    const int lo = max(kb, P - tile_k0), hi = min(kb + S::kKpw, k_end - tile_k0);
+    if (lo >= hi) return;
+    for (int idx = lane; idx < (hi - lo) * (D / 8); idx += 32) {
+        const int r = lo + idx / (D / 8), c = idx % (D / 8);
+        const int key = tile_k0 + r;
+        const size_t nrow = (size_t)(key - P) * S::kRowBytes + c * 16;
+        const uint4 kv = ldg128_nc(kn + nrow), vv = ldg128_nc(vn + nrow);
+        sts128(mma_chunk_addr<S>(smem_addr(Ks), r, c), kv);
+        sts128(mma_chunk_addr<S>(smem_addr(Vs), r, c), vv);
+        if (kc != nullptr) {
+            stg128(kc + (size_t)key * S::kRowBytes + c * 16, kv);
+            stg128(vc + (size_t)key * S::kRowBytes + c * 16, vv);
+        }
+    }
+    fence_proxy_async_shared();  // before the slot is refilled by a bulk copy
+    __syncwarp();
+}
+
+// The tensor-core kernel.  Same split, ring, epilogue and merges as
+// attn_balanced_kernel; tiles by TMA through the K and V tensor maps.
+template <typename T, int D, bool kFused, bool kTicketMerge>
+__global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
+    attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v)
+{
+    using S = MmaShape<T, D>;
+    using Tq = Elem<T>;
+    constexpr int RB = S::kRB;
+    const float kNegInf = __int_as_float(0xff800000);
+    extern __shared__ __align__(1024) unsigned char smem_mma[];
+    unsigned char *smem = smem_mma;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBarOff);
+    uint64_t *empty = full + S::kStages;
+    TileMeta *meta = reinterpret_cast<TileMeta *>(smem + S::kMetaOff);
+    MergeJob *jobs = reinterpret_cast<MergeJob *>(smem + S::kJobOff);
+    int *pre = reinterpret_cast<int *>(smem + S::kFixedBytes);
+    int *pl = pre + a.B + 1;
+
+    const int tid = threadIdx.x;
+    const int warp = tid / 32, lane = tid % 32;
+    const int g = lane >> 2, t = lane & 3;
+
+    // The swizzled boxes need 1024-byte-aligned shared memory; the dynamic
+    // shared memory of a CTA starts so aligned, which is checked rather than
+    // assumed (every thread takes the same branch).
+    if ((smem_addr(smem) & 1023u) != 0) {
+        if (tid == 0) raise_error(a.err_word, KVD_DEVERR_INTERNAL);
+        return;
+    }
+
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < S::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], S::kNW);
+        }
+        fence_mbar_init();
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncthreads();
+
+    RangeWalk<S, !kTicketMerge, false> walk;
+    int issued = 0;
+    if (warp == 0) {
+        int carry = 0;
+        if (lane == 0) pre[0] = 0;
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+            const int b = b0 + lane;
+            int units = 0;
+            if (b < a.B) {
+                const int P = __ldg(a.past_len + b);
+                const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
+                if (!ok && blockIdx.x == 0) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
+                units = ok ? (P + a.N + S::kTK - 1) / S::kTK + S::kPieceUnits : 0;
+                pl[b] = P;
+            }
+            int v = units;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += n;
+            }
+            if (b < a.B) pre[b + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            const int HR = a.H_kv * a.n_rowblocks;
+            const long long n_total = (long long)pre[a.B] * HR;
+            const long long G = min((long long)gridDim.x, n_total);
+            const long long lo = blockIdx.x < G ? n_total * blockIdx.x / G : 0;
+            const long long hi = blockIdx.x < G ? n_total * (blockIdx.x + 1) / G : 0;
+            walk.tm_k = &tm_k;
+            walk.tm_v = &tm_v;
+            walk.start(a, pre, pl, lo, hi, n_total, G);
+            for (; issued < S::kStages; ++issued) walk.fill(a, pre, pl, smem, meta, full, issued);
+        }
+    }
+
+    uint32_t qa[S::kKSteps][4];
+    float oacc[S::kNTiles][4];
+    float m_run[2], l_run[2];
+    int lim[2];
+    bool timed_out = false;
+    int first_unwaited = -1;
+    int n_pieces = 0;
+
+    for (int pos = 0;; ++pos) {
+        const int s = pos % S::kStages;
+        const uint32_t ph = (uint32_t)(pos / S::kStages) & 1u;
+        if (tid == 0) {
+            while (issued <= pos && !walk.ended) {
+                const int fs = issued % S::kStages;
+                const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
+                if (!timed_out && !mbar_wait_bounded(&empty[fs], fph)) {
+                    timed_out = true;
+                    raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+                }
+                walk.fill(a, pre, pl, smem, meta, full, fs);
+                ++issued;
+            }
+        }
+        if (!timed_out && !mbar_wait_bounded(&full[s], ph)) {
+            timed_out = true;
+            first_unwaited = pos;
+            raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+        }
+        const TileMeta mt = meta[s];
+        if (mt.flags & kMetaEnd) break;
+        unsigned char *Ks = smem + S::kRingOff + s * 2 * S::kTileBytes;
+        unsigned char *Vs = Ks + S::kTileBytes;
+
+        if (mt.flags & kMetaFirst) {
+            // Q fragments of the 16 rows (rows past the block's rows are zero)
+            const unsigned char *qs = smem + S::kQOff + s * S::kQSlotBytes;
+            const int q_rows = min(RB, a.rows - mt.rb * RB);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int rg = mt.rb * RB + g + 8 * r;
+                lim[r] = mt.P + 1 + (rg % a.N);
+                m_run[r] = kNegInf;
+                l_run[r] = 0.f;
+            }
+#pragma unroll
+            for (int nt = 0; nt < S::kNTiles; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < S::kKSteps; ++ks)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = g + ((e & 1) << 3);
+                    const int col = 16 * ks + 2 * t + ((e >> 1) << 3);
+                    qa[ks][e] = row < q_rows ? *reinterpret_cast<const uint32_t *>(qs + row * S::kQRowBytes + col * 2)
+                                             : 0u;
+                }
+        }
+
+        const int k_end = mt.tile_k0 + mt.nk;
+        if (mt.tile_k0 + S::kTK <= mt.P + (kFused ? 0 : 1)) {
+            mma_tile<T, D, false>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
+        } else {
+            if constexpr (kFused) {
+                const size_t nrow = (size_t)mt.bh * a.N * S::kRowBytes;
+                unsigned char *kc = nullptr, *vc = nullptr;
+                if (mt.rb == 0) {  // one row block writes the new rows into the cache
+                    const size_t crow = (size_t)mt.bh * a.T_max * S::kRowBytes;
+                    kc = static_cast<unsigned char *>(const_cast<void *>(a.k_cache)) + crow;
+                    vc = static_cast<unsigned char *>(const_cast<void *>(a.v_cache)) + crow;
+                }
+                mma_insert_new_rows<T, D>(Ks, Vs, warp, lane, mt.tile_k0, mt.P, k_end,
+                                          static_cast<const unsigned char *>(a.k_new) + nrow,
+                                          static_cast<const unsigned char *>(a.v_new) + nrow, kc, vc);
+            }
+            mma_tile<T, D, true>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+
+        if (tid == 0 && !walk.ended && issued < pos + 1 + S::kStages) {
+            const int fs = issued % S::kStages;
+            const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
+            if (mbar_test_wait(&empty[fs], fph)) {
+                walk.fill(a, pre, pl, smem, meta, full, fs);
+                ++issued;
+            }
+        }
+
+        if (!(mt.flags & kMetaLast)) continue;
+
+        // ---- end of a piece: each warp's (o, m, l) to shared memory, then
+        //      the warps merged by log-sum-exp ----
+        float *ep_o = reinterpret_cast<float *>(smem + S::kEpiOff);
+        float *ep_m = ep_o + S::kNW * RB * D;
+        float *ep_l = ep_m + S::kNW * RB;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+        }
+        __syncthreads();  // the previous piece's readers are done with the shared area
+#pragma unroll
+        for (int nt = 0; nt < S::kNTiles; ++nt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                *reinterpret_cast<float2 *>(ep_o + (warp * RB + g + 8 * r) * D + nt * 8 + 2 * t) =
+                    make_float2(oacc[nt][2 * r], oacc[nt][2 * r + 1]);
+        if (t == 0) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                ep_m[warp * RB + g + 8 * r] = m_run[r];
+                ep_l[warp * RB + g + 8 * r] = l_run[r];
+            }
+        }
+        __syncthreads();
+        const bool single = (mt.n_chunks == 1);
+        const size_t pbase = ((size_t)blockIdx.x * 2 + ((int)blockIdx.x == mt.c_first ? 1 : 0)) * RB;
+        for (int idx = tid; idx < RB * D; idx += S::kThreads) {
+            const int r = idx / D, d = idx % D;
+            const int rg = mt.rb * RB + r;
+            if (rg >= a.rows) continue;
+            float M = kNegInf;
+#pragma unroll
+            for (int w = 0; w < S::kNW; ++w) M = fmaxf(M, ep_m[w * RB + r]);
+            float num = 0.f, den = 0.f;
+#pragma unroll
+            for (int w = 0; w < S::kNW; ++w) {
+                const float wt = safe_weight(ep_m[w * RB + r], M);
+                num = fmaf(wt, ep_o[(w * RB + r) * D + d], num);
+                den = fmaf(wt, ep_l[w * RB + r], den);
+            }
+            if (single) {
+                Tq::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
+            } else {
+                float *pr = a.part + (pbase + r) * (D + 4);
+                pr[d] = num;
+                if (d == 0) {
+                    pr[D] = M;
+                    pr[D + 1] = den;
+                }
+            }
+        }
+        if constexpr (kTicketMerge) {
+            if (!single) {
+                if (tid == 0 && n_pieces < 2) jobs[n_pieces] = MergeJob{mt.bh, mt.rb, mt.c_first, mt.n_chunks};
+                ++n_pieces;
+            }
+        }
+    }
+
+    if constexpr (kTicketMerge) {
+        n_pieces = min(n_pieces, 2);
+        __syncthreads();
+        if (tid == 0 && n_pieces > 0) {
+            int *tickets = static_cast<int *>(a.merge_state);
+            int seen[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                if (i < n_pieces) seen[i] = atomic_add_acq_rel_gpu(tickets + (size_t)jobs[i].bh * a.n_rowblocks + jobs[i].rb, 1);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                if (i < n_pieces && seen[i] == jobs[i].n_chunks - 1)
+                    tickets[(size_t)jobs[i].bh * a.n_rowblocks + jobs[i].rb] = 0;
+                else
+                    jobs[i].n_chunks = 0;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const MergeJob job = jobs[i];
+            if (i < n_pieces && job.n_chunks)
+                merge_pieces<T, D, RB, S::kThreads>(a, job, reinterpret_cast<float *>(smem + S::kEpiOff), tid);
+        }
+    }
+
+    if (tid == 0 && timed_out && first_unwaited >= 0) {
+        const uint64_t t0 = global_timer_ns();
+        for (int p = first_unwaited; p < issued; ++p) {
+            const uint32_t ph2 = (uint32_t)(p / S::kStages) & 1u;
+            while (!mbar_try_wait(&full[p % S::kStages], ph2) && global_timer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename T, int D, bool kTicketMerge> AttnVariant make_mma_variant()
+{
+    using S = MmaShape<T, D>;
+    AttnVariant v;
+    v.fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, false, kTicketMerge>);
+    v.fused_fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, true, kTicketMerge>);
+    if constexpr (kTicketMerge) v.merge_fn = nullptr;
+    else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, S::kRB>);
+    v.threads = S::kThreads;
+    v.fixed_smem_bytes = S::kFixedBytes;
+    v.tile_keys = S::kTK;
+    v.rows_per_block = S::kRB;
+    v.piece_units = S::kPieceUnits;
+    v.tma = true;
+    return v;
+}
+
+template <typename T, bool kTicketMerge> bool pick_mma_variant(int D, AttnVariant *v)
+{
+    switch (D) {
+    case 64: *v = make_mma_variant<T, 64, kTicketMerge>(); return true;
+    case 128: *v = make_mma_variant<T, 128, kTicketMerge>(); return true;
+    default: return false;
+    }
+}
+
+}  // namespace kvd

@@ -38,6 +38,7 @@ KVD_E4M3 = 3
 KVD_DEVERR_PAST_LEN = 1
 KVD_DEVERR_TIMEOUT = 2
 KVD_DEVERR_PAGE = 4
+KVD_DEVERR_INTERNAL = 8
 
 _TORCH_DTYPE = {torch.float32: KVD_F32, torch.bfloat16: KVD_BF16, torch.float16: KVD_F16}
 _NAME_DTYPE = {"f32": KVD_F32, "bf16": KVD_BF16, "f16": KVD_F16, "e4m3": KVD_E4M3}
@@ -52,7 +53,8 @@ class KvdError(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("tile_keys", ctypes.c_int), ("max_tiles", ctypes.c_int), ("grid", ctypes.c_int),
                 ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("launches", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("rows_per_block", ctypes.c_int),
+                ("tensor_cores", ctypes.c_int)]
 
 
 class _Lib:

@@ -3,9 +3,11 @@ kvd_paged_decode_step against the paged oracle, and against the contiguous path.
 
 Pages come from the contiguous inputs laid out as a shuffled pool with unused
 NaN pages (workloads.to_paged).  Over the same logical data the paged kernels
-run the same tiles in the same order as the contiguous ones, so their outputs
-must match the contiguous outputs bit for bit; the paged append must write
-exactly the page slots the oracle writes and nothing else.
+run the same tiles in the same order as the contiguous CUDA-core kernels, so
+their outputs must match those bit for bit (the contiguous path runs the
+tensor-core kernel instead from 16 query rows per KV head: then both are only
+compared with the oracle); the paged append must write exactly the page slots
+the oracle writes and nothing else.
 """
 import numpy as np
 import pytest
@@ -83,7 +85,10 @@ def _check(orc, w, past, page_size, seed):
     ref, st = orc.paged_decode_attention(h["q"], kpo, vpo, to_np(table), past.numpy(), w.dtype)
     assert st == 0
     assert row_rel_err(out.double().cpu().numpy(), ref) <= TOL[w.dtype]
-    assert _same_bits(out, _contiguous(w, past, t))
+    # (bit-identical to the contiguous path when that also runs the CUDA-core
+    # kernel; with 16+ query rows per KV head it runs the tensor-core kernel)
+    if kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, int(past.max()), w.dtype)["tensor_cores"] == 0:
+        assert _same_bits(out, _contiguous(w, past, t))
     # fused step: same pages and same output bits as append + attention
     out2, kpd2, vpd2, err2 = _run(w, past, t, kp, vp, table, fused=True)
     assert err2 == 0
