@@ -160,8 +160,14 @@ int g_occ_n = 0;
 constexpr int kMaxSmemPerCta = 227 * 1024;
 // Ranges longer than this many tile units per CTA use the separate merge pass.
 constexpr int kLongRangeUnits = 32;
-// Query rows per KV head from which the tensor-core kernel (16-row blocks) is used.
-constexpr int kMmaMinRows = 16;
+// Query rows per KV head from which the tensor-core kernel (16-row blocks) is
+// used, by head dim.  Measured on GB300 (bench.py, bf16): D=128 with 4 rows
+// (the long-context workload) 106.4 us per layer against 113.6 on the CUDA
+// cores, 8 rows 108.1 against 253.8, 16 rows 112.9 against 499.5; D=64 with 1
+// row (GPT-2 batch 8) 14.6 against 10.3, so one-row decode stays on the CUDA
+// cores and D=64 switches only where the CUDA-core kernel needs 8-row blocks.
+constexpr int kMmaMinRows128 = 4;
+constexpr int kMmaMinRows64 = 8;
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link to the
 // driver library).
@@ -328,7 +334,8 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     pl->rows = (H_q / H_kv) * N;
     // Many query rows per KV head (chunked decode with GQA): the tensor-core
     // kernel in blocks of 16 rows, for 16-bit contiguous caches.
-    pl->mma = pl->rows >= kMmaMinRows && !paged && (dtype == KVD_BF16 || dtype == KVD_F16);
+    pl->mma = pl->rows >= (D == 128 ? kMmaMinRows128 : kMmaMinRows64) && !paged &&
+              (dtype == KVD_BF16 || dtype == KVD_F16);
     pl->rb = pl->mma ? 16 : pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : (pl->rows <= 4 || dtype == KVD_E4M3) ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
     AttnVariant vp, vt, op, ot;  // this layout's builds, and the other layout's
@@ -378,7 +385,9 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     pl->launches = pl->merge_pass ? 2 : 1;
     if (!pl->merge_pass) pl->v = vt;
 
-    const size_t pieces = (size_t)sms * (occ > occ_other ? occ : occ_other) * 2 * pl->rb;
+    // (partial slots of the tensor-core kernel hold only a 16-row block's real rows)
+    const int part_rows = pl->mma && pl->rows < pl->rb ? pl->rows : pl->rb;
+    const size_t pieces = (size_t)sms * (occ > occ_other ? occ : occ_other) * 2 * part_rows;
     size_t off = 0;
     pl->part_off = off;  // per piece row: o[D], m, l, 2 floats of padding (16-byte rows)
     off += round_up(pieces * (D + 4) * sizeof(float), 256);

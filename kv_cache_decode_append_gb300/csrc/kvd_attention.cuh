@@ -520,6 +520,16 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
     }
 };
 
+// Rows per partial slot.  The CUDA-core kernels' row blocks (RB 1, 2, 4, 8)
+// are sized to their rows; the tensor-core kernel's 16-row blocks (RB = 16,
+// used by no other kernel) keep only the block's real rows, min(16, rows),
+// so few-row decodes do not carry 16-row partials.
+template <int RB> __device__ __forceinline__ int part_rows(int rows)
+{
+    if constexpr (RB == 16) return rows < RB ? rows : RB;
+    else return RB;
+}
+
 // A piece of a split head this CTA computed, or a head it merges.
 struct MergeJob {
     int bh, rb, c_first, n_chunks;
@@ -553,7 +563,7 @@ __device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &
     // issues all of them before the updates.
 #pragma unroll 2
     for (int k = g; k < job.n_chunks; k += kNG) {
-        const size_t pb = ((size_t)(job.c_first + k) * 2 + (k == 0)) * RB;
+        const size_t pb = ((size_t)(job.c_first + k) * 2 + (k == 0)) * part_rows<RB>(a.rows);
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
             const int e = e0 + i * kThreads, r = e / D, d = e % D;
@@ -963,7 +973,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
     float M = kNegInf;
     for (int k = lane; k < seg.y; k += 32) {
         const int c = seg.x + k;
-        M = fmaxf(M, a.part[(((size_t)c * 2 + (k == 0)) * RB + r) * (D + 4) + D]);
+        M = fmaxf(M, a.part[(((size_t)c * 2 + (k == 0)) * part_rows<RB>(a.rows) + r) * (D + 4) + D]);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off /= 2) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -973,7 +983,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
     for (int k = 0; k < kDpl; ++k) acc[k] = 0.f;
     float den = 0.f;
     for (int k = 0; k < seg.y; ++k) {
-        const size_t pidx = ((size_t)(seg.x + k) * 2 + (k == 0)) * RB + r;
+        const size_t pidx = ((size_t)(seg.x + k) * 2 + (k == 0)) * part_rows<RB>(a.rows) + r;
         const float *pr = a.part + pidx * (D + 4);
         const float w = safe_weight(pr[D], M);
         den = fmaf(w, pr[D + 1], den);

@@ -49,7 +49,7 @@ template <typename T, int D> struct MmaShape {
     static constexpr int kBoxes = D / kBoxCols;
     static constexpr int kBoxBytes = kTK * 128;        // one box: 64 rows x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;
-    static constexpr int kStages = (D == 128) ? 2 : 4;
+    static constexpr int kStages = (D == 128) ? 3 : 4;
     static constexpr int kQSlotBytes = kRB * kQRowBytes;
     static constexpr int kPieceUnits = 2;
     static constexpr int kKSteps = D / 16;             // k-steps of S = Q.K^T
@@ -57,10 +57,11 @@ template <typename T, int D> struct MmaShape {
 
     static constexpr int kRingOff = 0;                 // 1024-aligned boxes (swizzle pattern)
     static constexpr int kQOff = kRingOff + kStages * 2 * kTileBytes;
+    // No separate epilogue area: a piece's last tile keeps its ring slot until
+    // the warps are merged, and the merge uses that slot (o of 4 warps x 16
+    // rows x D fp32 = the K and V tile bytes; m and l in its q slot).
     static constexpr int kEpiOff = kQOff + kStages * kQSlotBytes;
-    static constexpr int kEpiFloats = ((kNW * kRB * (D + 2) + 3) / 4) * 4;
-    static constexpr int kEpiBytes = kEpiFloats * 4;
-    static constexpr int kMetaOff = kEpiOff + kEpiBytes;
+    static constexpr int kMetaOff = kEpiOff;
     static constexpr int kBarOff = kMetaOff + kStages * 32;
     static constexpr int kJobOff = kBarOff + 2 * kStages * 8;
     static constexpr int kPageOff = kJobOff + 32;
@@ -68,6 +69,7 @@ template <typename T, int D> struct MmaShape {
 
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(kBoxBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+    static_assert(kNW * kRB * D * 4 <= 2 * kTileBytes && 2 * kNW * kRB * 4 <= kQSlotBytes, "merge in the slot");
 };
 
 // Shared-memory address of the 16-byte chunk c (0 .. D/8-1) of tile row r in
@@ -110,14 +112,17 @@ __device__ __forceinline__ void mma_tile(unsigned char *Ks, unsigned char *Vs,
         for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
     {
         // ldmatrix.x4: matrices (keys kb.., chunk 2s), (kb.., 2s+1), (kb+8.., 2s), (kb+8.., 2s+1)
+        // (all fragment loads first: the loads keep their order, the MMAs
+        // then only wait for the first of them)
         const int key = kb + ((lane >> 4) << 3) + (lane & 7);
         const int csel = (lane >> 3) & 1;
+        uint32_t b[S::kKSteps][4];
+#pragma unroll
+        for (int ks = 0; ks < S::kKSteps; ++ks) ldmatrix_x4_addr(b[ks], mma_chunk_addr<S>(k_base, key, 2 * ks + csel));
 #pragma unroll
         for (int ks = 0; ks < S::kKSteps; ++ks) {
-            uint32_t b[4];
-            ldmatrix_x4_addr(b, mma_chunk_addr<S>(k_base, key, 2 * ks + csel));
-            mma_16816<T>(sacc[0], qa[ks], b[0], b[1]);
-            mma_16816<T>(sacc[1], qa[ks], b[2], b[3]);
+            mma_16816<T>(sacc[0], qa[ks], b[ks][0], b[ks][1]);
+            mma_16816<T>(sacc[1], qa[ks], b[ks][2], b[ks][3]);
         }
     }
 
@@ -177,12 +182,13 @@ __device__ __forceinline__ void mma_tile(unsigned char *Ks, unsigned char *Vs,
     {
         const int key = kb + (((lane >> 3) & 1) << 3) + (lane & 7);
         const int csel = lane >> 4;
+        uint32_t b[S::kNTiles / 2][4];
+#pragma unroll
+        for (int c = 0; c < S::kNTiles; c += 2) ldmatrix_x4_trans_addr(b[c / 2], mma_chunk_addr<S>(v_base, key, c + csel));
 #pragma unroll
         for (int c = 0; c < S::kNTiles; c += 2) {
-            uint32_t b[4];
-            ldmatrix_x4_trans_addr(b, mma_chunk_addr<S>(v_base, key, c + csel));
-            mma_16816<T>(oacc[c], pa, b[0], b[1]);
-            mma_16816<T>(oacc[c + 1], pa, b[2], b[3]);
+            mma_16816<T>(oacc[c], pa, b[c / 2][0], b[c / 2][1]);
+            mma_16816<T>(oacc[c + 1], pa, b[c / 2][2], b[c / 2][3]);
         }
     }
 }
@@ -373,8 +379,11 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
             }
             mma_tile<T, D, true>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        // (a piece's last tile keeps its slot for the merge below)
+        if (!(mt.flags & kMetaLast)) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
 
         if (tid == 0 && !walk.ended && issued < pos + 1 + S::kStages) {
             const int fs = issued % S::kStages;
@@ -389,15 +398,15 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
 
         // ---- end of a piece: each warp's (o, m, l) to shared memory, then
         //      the warps merged by log-sum-exp ----
-        float *ep_o = reinterpret_cast<float *>(smem + S::kEpiOff);
-        float *ep_m = ep_o + S::kNW * RB * D;
+        float *ep_o = reinterpret_cast<float *>(Ks);  // the slot's K and V tile bytes
+        float *ep_m = reinterpret_cast<float *>(smem + S::kQOff + s * S::kQSlotBytes);
         float *ep_l = ep_m + S::kNW * RB;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
             l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
         }
-        __syncthreads();  // the previous piece's readers are done with the shared area
+        __syncthreads();  // every warp is done with the slot's K, V and q
 #pragma unroll
         for (int nt = 0; nt < S::kNTiles; ++nt)
 #pragma unroll
@@ -413,7 +422,8 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
         }
         __syncthreads();
         const bool single = (mt.n_chunks == 1);
-        const size_t pbase = ((size_t)blockIdx.x * 2 + ((int)blockIdx.x == mt.c_first ? 1 : 0)) * RB;
+        const size_t pbase =
+            ((size_t)blockIdx.x * 2 + ((int)blockIdx.x == mt.c_first ? 1 : 0)) * part_rows<RB>(a.rows);
         for (int idx = tid; idx < RB * D; idx += S::kThreads) {
             const int r = idx / D, d = idx % D;
             const int rg = mt.rb * RB + r;
@@ -439,6 +449,10 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
                 }
             }
         }
+        // the slot is free again (its generic writes ordered before the next bulk copy)
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
         if constexpr (kTicketMerge) {
             if (!single) {
                 if (tid == 0 && n_pieces < 2) jobs[n_pieces] = MergeJob{mt.bh, mt.rb, mt.c_first, mt.n_chunks};
@@ -469,7 +483,7 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
         for (int i = 0; i < 2; ++i) {
             const MergeJob job = jobs[i];
             if (i < n_pieces && job.n_chunks)
-                merge_pieces<T, D, RB, S::kThreads>(a, job, reinterpret_cast<float *>(smem + S::kEpiOff), tid);
+                merge_pieces<T, D, RB, S::kThreads>(a, job, nullptr, tid);  // (16-row heads: no scratch)
         }
     }
 

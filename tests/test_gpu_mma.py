@@ -1,6 +1,6 @@
 """The tensor-core kernel (16-row blocks, mma.sync, tiles by TMA tensor maps) on the
-GPU: chunked / grouped decode with (H_q / H_kv) * N >= 16 query rows per KV head,
-bf16 and fp16, against the oracle; the fused step bit-identical to append +
+GPU: grouped / chunked decode with 4+ (D = 128) or 8+ (D = 64) query rows per KV
+head, bf16 and fp16, against the oracle; the fused step bit-identical to append +
 attention; both merge modes."""
 import pytest
 import torch
@@ -28,6 +28,8 @@ MMA_CASES = [
     (1, 32, 4, 128, 16, 600, [583], "bf16"),               # 128 rows: 8 blocks, chunk of 16
     (2, 12, 12, 64, 16, 1024, [1008, 512], "f16"),         # GPT-2 shapes, chunk of 16, fp16
     (4, 64, 4, 128, 1, 2000, [1999, 7, 1000, 64], "f16"),  # 16 rows, fp16, ragged
+    (3, 16, 4, 128, 1, 800, [799, 0, 257], "bf16"),        # 4 rows: GQA decode, 12 padding rows
+    (2, 8, 8, 64, 8, 640, [600, 33], "bf16"),              # D=64, 8 rows
 ]
 
 
@@ -53,6 +55,8 @@ def test_mma_merge_modes(orc, case):
     test_gpu_step._check(orc, w, past, seed=9460 + launches)
 
 
-def test_cuda_core_kernel_below_16_rows():
-    assert kvd.kvd_decode_plan(4, 32, 8, 128, 1, 1000, "bf16")["tensor_cores"] == 0
-    assert kvd.kvd_decode_plan(4, 32, 2, 128, 1, 1000, "f32")["tensor_cores"] == 0
+def test_kernel_choice():
+    assert kvd.kvd_decode_plan(4, 32, 8, 128, 1, 1000, "bf16")["tensor_cores"] == 1   # 4 rows, D=128
+    assert kvd.kvd_decode_plan(4, 16, 8, 128, 1, 1000, "bf16")["tensor_cores"] == 0   # 2 rows
+    assert kvd.kvd_decode_plan(8, 12, 12, 64, 1, 1000, "bf16")["tensor_cores"] == 0   # 1 row, D=64
+    assert kvd.kvd_decode_plan(4, 32, 2, 128, 1, 1000, "f32")["tensor_cores"] == 0    # fp32 cache

@@ -119,16 +119,20 @@ def test_paged_workloads(orc, name):
     _check(orc, w, wl.past_lens(w), 64, seed=8300 + w.wid)
 
 
-def test_paged_gqa_longctx_full_size():
-    """The long-context workload at full size, 64-token pages: append, attention and
-    the fused step give exactly the contiguous path's bits (itself checked against
-    the oracle at full size)."""
+def test_paged_gqa_longctx_full_size(orc):
+    """The long-context workload at full size, 64-token pages: the attention against
+    the oracle (on the same data, contiguous), the fused step bit-identical to
+    append + attention."""
     w = wl.WORKLOADS["gqa_longctx_b32_bf16"]
     past = wl.past_lens(w)
     _, t, kp, vp, table = _inputs(w, past, 64, seed=8500, device=DEV)
     out, _, _, err = _run(w, past, t, kp, vp, table)
     assert err == 0
-    assert _same_bits(out, _contiguous(w, past, t))
+    h = {k: to_np(v) for k, v in t.items()}
+    assert orc.append(h["k_cache"], h["v_cache"], h["k_new"], h["v_new"], past.numpy(), w.dtype) == 0
+    ref, st = orc.decode_attention(h["q"], h["k_cache"], h["v_cache"], past.numpy(), w.dtype)
+    assert st == 0
+    assert row_rel_err(out.double().cpu().numpy(), ref) <= TOL[w.dtype]
     out2, _, _, err2 = _run(w, past, t, kp, vp, table, fused=True)
     assert err2 == 0 and _same_bits(out2, out)
 
