@@ -334,17 +334,16 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     pl->rows = (H_q / H_kv) * N;
     // Many query rows per KV head (chunked decode with GQA): the tensor-core
     // kernel in blocks of 16 rows, for 16-bit contiguous caches.
-    pl->mma = pl->rows >= (D == 128 ? kMmaMinRows128 : kMmaMinRows64) && !paged &&
-              (dtype == KVD_BF16 || dtype == KVD_F16);
+    pl->mma = pl->rows >= (D == 128 ? kMmaMinRows128 : kMmaMinRows64) && (dtype == KVD_BF16 || dtype == KVD_F16);
     pl->rb = pl->mma ? 16 : pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : (pl->rows <= 4 || dtype == KVD_E4M3) ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
     AttnVariant vp, vt, op, ot;  // this layout's builds, and the other layout's
     if (pl->mma) {
-        const bool ok = dtype == KVD_BF16 ? attn_variant_mma_bf16(D, &vp) && attn_variant_mma_bf16_tk(D, &vt)
-                                          : attn_variant_mma_f16(D, &vp) && attn_variant_mma_f16_tk(D, &vt);
-        if (!ok) return KVD_ERR_UNSUPPORTED;
-        op = vp;
-        ot = vt;
+        const auto builds = [&](bool pg, AttnVariant *p, AttnVariant *t) {
+            return dtype == KVD_BF16 ? attn_variant_mma_bf16(D, pg, p) && attn_variant_mma_bf16_tk(D, pg, t)
+                                     : attn_variant_mma_f16(D, pg, p) && attn_variant_mma_f16_tk(D, pg, t);
+        };
+        if (!builds(paged, &vp, &vt) || !builds(!paged, &op, &ot)) return KVD_ERR_UNSUPPORTED;
     } else {
         if (!pick_builds(dtype, D, pl->rb, paged, &vp, &vt)) return KVD_ERR_UNSUPPORTED;
         if (!pick_builds(dtype, D, pl->rb, !paged, &op, &ot)) {  // (no other layout: E4M3)
@@ -577,8 +576,10 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     cfg.blockDim = dim3(pl.v.threads);
     cfg.dynamicSmemBytes = (size_t)pl.smem;
     if (pl.v.tma) {
-        // the K and V tensor maps, passed by value after the arguments
-        const long long rows_total = (long long)B * H_kv * T_max;
+        // the K and V tensor maps, passed by value after the arguments (rows:
+        // the contiguous cache's B*H_kv*T_max, or the pool's pages x heads x slots)
+        const long long rows_total = paged != nullptr ? (long long)paged->num_pages * H_kv * paged->page_size
+                                                      : (long long)B * H_kv * T_max;
         if (rows_total + 64 > 0x7fffffffLL) return KVD_ERR_UNSUPPORTED;  // 32-bit box coordinates
         alignas(64) CUtensorMap tmk, tmv;
         if ((st = encode_cache_map(&tmk, k_cache, rows_total, D, dtype)) != KVD_OK) return st;

@@ -486,7 +486,11 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
             // past the tensor), 128-byte swizzled, kBoxes per K or V tile
             (void)off;
             mbar_arrive_expect_tx(&full[s], 2u * S::kTileBytes + qbytes);
-            const int y = bh * a.T_max + mt.tile_k0;
+            int y;  // first row of the tile in the tensor map's [rows, D] view
+            if constexpr (kPaged)
+                y = ((page * a.H_kv + (bh - b * a.H_kv)) << a.page_shift) + (mt.tile_k0 & ((1 << a.page_shift) - 1));
+            else
+                y = bh * a.T_max + mt.tile_k0;
 #pragma unroll
             for (int bx = 0; bx < S::kBoxes; ++bx) {
                 tma_load_2d(dst + bx * S::kBoxBytes, tm_k, bx * S::kBoxCols, y, &full[s], policy);
@@ -1082,10 +1086,10 @@ bool attn_variant_f16_paged(int D, int RB, AttnVariant *v);
 bool attn_variant_f16_tk_paged(int D, int RB, AttnVariant *v);
 bool attn_variant_e4m3(int D, int RB, AttnVariant *v);      // bf16 q / out, E4M3 cache
 bool attn_variant_e4m3_tk(int D, int RB, AttnVariant *v);
-// tensor-core kernels (kvd_attention_mma.cuh): 16-row blocks, contiguous caches
-bool attn_variant_mma_bf16(int D, AttnVariant *v);
-bool attn_variant_mma_bf16_tk(int D, AttnVariant *v);
-bool attn_variant_mma_f16(int D, AttnVariant *v);
-bool attn_variant_mma_f16_tk(int D, AttnVariant *v);
+// tensor-core kernels (kvd_attention_mma.cuh): 16-row blocks, contiguous or paged caches
+bool attn_variant_mma_bf16(int D, bool paged, AttnVariant *v);
+bool attn_variant_mma_bf16_tk(int D, bool paged, AttnVariant *v);
+bool attn_variant_mma_f16(int D, bool paged, AttnVariant *v);
+bool attn_variant_mma_f16_tk(int D, bool paged, AttnVariant *v);
 
 }  // namespace kvd

@@ -12,7 +12,8 @@
 //
 // Differences from attn_balanced_kernel:
 //   * tiles arrive by 2-D TMA through tensor maps over the cache viewed as
-//     [B*H_kv*T_max, D], in boxes of 64 keys x 128 bytes with the 128-byte
+//     [B*H_kv*T_max, D] (or a page pool as [num_pages*H_kv*page_size, D]),
+//     in boxes of 64 keys x 128 bytes with the 128-byte
 //     swizzle, so that ldmatrix reads 8 keys at one column chunk without bank
 //     conflicts (a plain row-major tile would serialize those reads 8 ways);
 //   * a warp owns 16 keys of each 64-key tile and all 16 rows; its Q
@@ -195,7 +196,8 @@ __device__ __forceinline__ void mma_tile(unsigned char *Ks, unsigned char *Vs,
 
 // In a fused step the tile holding new keys P .. P+N-1 has stale cache rows:
 // the warp copies its new rows from k_new / v_new into the tile (and, when
-// kc / vc are given, into the cache) before the tile is read.
+// kc / vc are given, into the cache: kc, vc address the cache row of the
+// tile's first key) before the tile is read.
 template <typename T, int D>
 __device__ __forceinline__ void mma_insert_new_rows(unsigned char *Ks, unsigned char *Vs, int warp, int lane,
                                                     int tile_k0, int P, int k_end, const unsigned char *kn,
@@ -213,8 +215,8 @@ __device__ __forceinline__ void mma_insert_new_rows(unsigned char *Ks, unsigned 
         sts128(mma_chunk_addr<S>(smem_addr(Ks), r, c), kv);
         sts128(mma_chunk_addr<S>(smem_addr(Vs), r, c), vv);
         if (kc != nullptr) {
-            stg128(kc + (size_t)key * S::kRowBytes + c * 16, kv);
-            stg128(vc + (size_t)key * S::kRowBytes + c * 16, vv);
+            stg128(kc + (size_t)r * S::kRowBytes + c * 16, kv);
+            stg128(vc + (size_t)r * S::kRowBytes + c * 16, vv);
         }
     }
     fence_proxy_async_shared();  // before the slot is refilled by a bulk copy
@@ -222,8 +224,10 @@ __device__ __forceinline__ void mma_insert_new_rows(unsigned char *Ks, unsigned 
 }
 
 // The tensor-core kernel.  Same split, ring, epilogue and merges as
-// attn_balanced_kernel; tiles by TMA through the K and V tensor maps.
-template <typename T, int D, bool kFused, bool kTicketMerge>
+// attn_balanced_kernel; tiles by TMA through the K and V tensor maps (over
+// the contiguous cache viewed as [B*H_kv*T_max, D], or over the page pool
+// viewed as [num_pages*H_kv*page_size, D] when kPaged).
+template <typename T, int D, bool kFused, bool kTicketMerge, bool kPaged>
 __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
     attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v)
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
 
-    RangeWalk<S, !kTicketMerge, false> walk;
+    RangeWalk<S, !kTicketMerge, kPaged> walk;
     int issued = 0;
     if (warp == 0) {
         int carry = 0;
@@ -368,10 +372,19 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
             if constexpr (kFused) {
                 const size_t nrow = (size_t)mt.bh * a.N * S::kRowBytes;
                 unsigned char *kc = nullptr, *vc = nullptr;
-                if (mt.rb == 0) {  // one row block writes the new rows into the cache
-                    const size_t crow = (size_t)mt.bh * a.T_max * S::kRowBytes;
-                    kc = static_cast<unsigned char *>(const_cast<void *>(a.k_cache)) + crow;
-                    vc = static_cast<unsigned char *>(const_cast<void *>(a.v_cache)) + crow;
+                size_t crow = 0;  // cache row of the tile's first key
+                bool write = mt.rb == 0;  // one row block writes the new rows into the cache
+                if constexpr (kPaged) {
+                    const int page = reinterpret_cast<const int *>(smem + S::kPageOff)[s];
+                    write = write && page >= 0;  // (none into an invalid page)
+                    crow = (((size_t)page * a.H_kv + mt.bh % a.H_kv) << a.page_shift) +
+                           (mt.tile_k0 & ((1 << a.page_shift) - 1));
+                } else {
+                    crow = (size_t)mt.bh * a.T_max + mt.tile_k0;
+                }
+                if (write) {
+                    kc = static_cast<unsigned char *>(const_cast<void *>(a.k_cache)) + crow * S::kRowBytes;
+                    vc = static_cast<unsigned char *>(const_cast<void *>(a.v_cache)) + crow * S::kRowBytes;
                 }
                 mma_insert_new_rows<T, D>(Ks, Vs, warp, lane, mt.tile_k0, mt.P, k_end,
                                           static_cast<const unsigned char *>(a.k_new) + nrow,
@@ -498,12 +511,12 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <typename T, int D, bool kTicketMerge> AttnVariant make_mma_variant()
+template <typename T, int D, bool kTicketMerge, bool kPaged> AttnVariant make_mma_variant()
 {
     using S = MmaShape<T, D>;
     AttnVariant v;
-    v.fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, false, kTicketMerge>);
-    v.fused_fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, true, kTicketMerge>);
+    v.fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, false, kTicketMerge, kPaged>);
+    v.fused_fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, true, kTicketMerge, kPaged>);
     if constexpr (kTicketMerge) v.merge_fn = nullptr;
     else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, S::kRB>);
     v.threads = S::kThreads;
@@ -515,11 +528,14 @@ template <typename T, int D, bool kTicketMerge> AttnVariant make_mma_variant()
     return v;
 }
 
-template <typename T, bool kTicketMerge> bool pick_mma_variant(int D, AttnVariant *v)
+template <typename T, bool kTicketMerge> bool pick_mma_variant(int D, bool paged, AttnVariant *v)
 {
     switch (D) {
-    case 64: *v = make_mma_variant<T, 64, kTicketMerge>(); return true;
-    case 128: *v = make_mma_variant<T, 128, kTicketMerge>(); return true;
+    case 64: *v = paged ? make_mma_variant<T, 64, kTicketMerge, true>() : make_mma_variant<T, 64, kTicketMerge, false>();
+        return true;
+    case 128:
+        *v = paged ? make_mma_variant<T, 128, kTicketMerge, true>() : make_mma_variant<T, 128, kTicketMerge, false>();
+        return true;
     default: return false;
     }
 }

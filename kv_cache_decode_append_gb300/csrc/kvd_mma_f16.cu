@@ -1,7 +1,7 @@
 // Instantiates the f16 tensor-core decode-attention kernels with the separate merge pass
-// (D in {64, 128}, 16-row blocks).
+// (D in {64, 128}, 16-row blocks, contiguous and paged caches).
 #include "kvd_attention_mma.cuh"
 
 namespace kvd {
-bool attn_variant_mma_f16(int D, AttnVariant *v) { return pick_mma_variant<__half, false>(D, v); }
+bool attn_variant_mma_f16(int D, bool paged, AttnVariant *v) { return pick_mma_variant<__half, false>(D, paged, v); }
 }  // namespace kvd

@@ -3,11 +3,11 @@ kvd_paged_decode_step against the paged oracle, and against the contiguous path.
 
 Pages come from the contiguous inputs laid out as a shuffled pool with unused
 NaN pages (workloads.to_paged).  Over the same logical data the paged kernels
-run the same tiles in the same order as the contiguous CUDA-core kernels, so
-their outputs must match those bit for bit (the contiguous path runs the
-tensor-core kernel instead from 16 query rows per KV head: then both are only
-compared with the oracle); the paged append must write exactly the page slots
-the oracle writes and nothing else.
+run the same tiles in the same order as the contiguous ones (the planner picks
+the CUDA-core or the tensor-core kernel from the shapes alone, whatever the
+layout), so their outputs must match the contiguous outputs bit for bit; the
+paged append must write exactly the page slots the oracle writes and nothing
+else.
 """
 import numpy as np
 import pytest
@@ -85,10 +85,7 @@ def _check(orc, w, past, page_size, seed):
     ref, st = orc.paged_decode_attention(h["q"], kpo, vpo, to_np(table), past.numpy(), w.dtype)
     assert st == 0
     assert row_rel_err(out.double().cpu().numpy(), ref) <= TOL[w.dtype]
-    # (bit-identical to the contiguous path when that also runs the CUDA-core
-    # kernel; with 16+ query rows per KV head it runs the tensor-core kernel)
-    if kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, int(past.max()), w.dtype)["tensor_cores"] == 0:
-        assert _same_bits(out, _contiguous(w, past, t))
+    assert _same_bits(out, _contiguous(w, past, t))
     # fused step: same pages and same output bits as append + attention
     out2, kpd2, vpd2, err2 = _run(w, past, t, kp, vp, table, fused=True)
     assert err2 == 0
@@ -121,8 +118,8 @@ def test_paged_workloads(orc, name):
 
 def test_paged_gqa_longctx_full_size(orc):
     """The long-context workload at full size, 64-token pages: the attention against
-    the oracle (on the same data, contiguous), the fused step bit-identical to
-    append + attention."""
+    the oracle (on the same data, contiguous) and bit for bit against the contiguous
+    path, the fused step bit-identical to append + attention."""
     w = wl.WORKLOADS["gqa_longctx_b32_bf16"]
     past = wl.past_lens(w)
     _, t, kp, vp, table = _inputs(w, past, 64, seed=8500, device=DEV)
@@ -133,6 +130,7 @@ def test_paged_gqa_longctx_full_size(orc):
     ref, st = orc.decode_attention(h["q"], h["k_cache"], h["v_cache"], past.numpy(), w.dtype)
     assert st == 0
     assert row_rel_err(out.double().cpu().numpy(), ref) <= TOL[w.dtype]
+    assert _same_bits(out, _contiguous(w, past, t))
     out2, _, _, err2 = _run(w, past, t, kp, vp, table, fused=True)
     assert err2 == 0 and _same_bits(out2, out)
 
@@ -170,3 +168,26 @@ def test_paged_bad_page_is_flagged_and_contained():
         keep[page3] = False
         assert _same_bits(kpd[keep.to(DEV)], kpd_good[keep.to(DEV)])
         assert _same_bits(kpd[page3], kp[page3])
+
+
+@pytest.mark.parametrize("ps", [64, 256])
+def test_paged_tensor_core_bad_page(ps):
+    """A bad block-table entry on the tensor-core kernel (4 rows per KV head): flagged,
+    contained to its sequence, no write into the pool for it."""
+    w = wl.Workload(0, "badm", L=1, B=3, H_q=16, H_kv=4, D=128, N=1, dtype="bf16", T_max=1024, P=0)
+    assert kvd.kvd_decode_plan(3, 16, 4, 128, 1, 700, "bf16")["tensor_cores"] == 1
+    past = torch.tensor([700, 300, 64], dtype=torch.int32)
+    _, t, kp, vp, table = _inputs(w, past, ps, seed=8900 + ps)
+    good, kpd_good, _, err = _run(w, past, t, kp, vp, table, fused=True)
+    assert err == 0
+    bad_table = table.clone()
+    last = 300 // ps                      # sequence 1's page holding its new token
+    bad_table[1, last] = kp.shape[0] + 3
+    out, kpd, _, err = _run(w, past, t, kp, vp, bad_table, fused=True)
+    assert err & kvd.KVD_DEVERR_PAGE
+    assert _same_bits(out[0], good[0]) and _same_bits(out[2], good[2])
+    page = int(table[1, last])
+    keep = torch.ones(kp.shape[0], dtype=torch.bool)
+    keep[page] = False
+    assert _same_bits(kpd[keep.to(DEV)], kpd_good[keep.to(DEV)])
+    assert _same_bits(kpd[page], kp[page])
