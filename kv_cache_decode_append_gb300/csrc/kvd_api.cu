@@ -168,6 +168,9 @@ constexpr int kLongRangeUnits = 32;
 // cores and D=64 switches only where the CUDA-core kernel needs 8-row blocks.
 constexpr int kMmaMinRows128 = 4;
 constexpr int kMmaMinRows64 = 8;
+// E4M3 caches (D = 128 only): widening the codes on the CUDA cores costs more
+// than the saved bytes, so every row count goes to the tensor cores.
+constexpr int kMmaMinRowsE4m3 = 1;
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link to the
 // driver library).
@@ -193,18 +196,22 @@ kvd_status encode_fn(EncodeTiledFn *fn)
     return g_encode != nullptr ? KVD_OK : KVD_ERR_CUDA;
 }
 
-// A 2-D tensor map over a contiguous cache viewed as [rows, D] 16-bit
-// elements, in boxes of 64 rows x 64 elements (128 bytes), 128-byte swizzle.
+// A 2-D tensor map over a cache viewed as [rows, D] elements (16-bit, or
+// 8-bit E4M3 codes), in boxes of 64 rows x 128 bytes, 128-byte swizzle.
 kvd_status encode_cache_map(CUtensorMap *map, const void *cache, long long rows, int D, kvd_dtype dtype)
 {
     EncodeTiledFn fn;
     kvd_status st = encode_fn(&fn);
     if (st != KVD_OK) return st;
+    const int es = dtype == KVD_E4M3 ? 1 : 2;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {64, 64};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * es};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), 64};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(map, dtype == KVD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    const CUtensorMapDataType ty = dtype == KVD_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : dtype == KVD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = fn(map, ty, 2,
                           const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -334,11 +341,16 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     pl->rows = (H_q / H_kv) * N;
     // Many query rows per KV head (chunked decode with GQA): the tensor-core
     // kernel in blocks of 16 rows, for 16-bit contiguous caches.
-    pl->mma = pl->rows >= (D == 128 ? kMmaMinRows128 : kMmaMinRows64) && (dtype == KVD_BF16 || dtype == KVD_F16);
+    pl->mma = (pl->rows >= (D == 128 ? kMmaMinRows128 : kMmaMinRows64) && (dtype == KVD_BF16 || dtype == KVD_F16)) ||
+              (dtype == KVD_E4M3 && D == 128 && pl->rows >= kMmaMinRowsE4m3);
     pl->rb = pl->mma ? 16 : pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : (pl->rows <= 4 || dtype == KVD_E4M3) ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
     AttnVariant vp, vt, op, ot;  // this layout's builds, and the other layout's
-    if (pl->mma) {
+    if (pl->mma && dtype == KVD_E4M3) {
+        if (!attn_variant_mma_e4m3(D, &vp) || !attn_variant_mma_e4m3_tk(D, &vt)) return KVD_ERR_UNSUPPORTED;
+        op = vp;
+        ot = vt;
+    } else if (pl->mma) {
         const auto builds = [&](bool pg, AttnVariant *p, AttnVariant *t) {
             return dtype == KVD_BF16 ? attn_variant_mma_bf16(D, pg, p) && attn_variant_mma_bf16_tk(D, pg, t)
                                      : attn_variant_mma_f16(D, pg, p) && attn_variant_mma_f16_tk(D, pg, t);

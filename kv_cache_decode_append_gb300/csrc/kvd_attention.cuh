@@ -1091,5 +1091,7 @@ bool attn_variant_mma_bf16(int D, bool paged, AttnVariant *v);
 bool attn_variant_mma_bf16_tk(int D, bool paged, AttnVariant *v);
 bool attn_variant_mma_f16(int D, bool paged, AttnVariant *v);
 bool attn_variant_mma_f16_tk(int D, bool paged, AttnVariant *v);
+bool attn_variant_mma_e4m3(int D, AttnVariant *v);  // bf16 q / out, E4M3 cache, D = 128
+bool attn_variant_mma_e4m3_tk(int D, AttnVariant *v);
 
 }  // namespace kvd

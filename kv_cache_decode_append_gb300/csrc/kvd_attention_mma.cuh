@@ -36,21 +36,22 @@ namespace kvd {
 // Compile-time shape of a tensor-core variant: 16 query rows, 64-key tiles,
 // 4 warps of 16 keys.  Member names match AttnShape where RangeWalk and the
 // epilogue use them.
-template <typename T, int D> struct MmaShape {
+template <typename T, int D, typename C = T> struct MmaShape {
     using Tq = Elem<T>;
+    static constexpr bool k8 = sizeof(C) == 1;         // E4M3 cache (8-bit codes)
     static constexpr bool kTma = true;
     static constexpr int kRB = 16;
-    static constexpr int kRowBytes = D * 2;
+    static constexpr int kRowBytes = D * (int)sizeof(C);
     static constexpr int kQRowBytes = D * 2;
     static constexpr int kTK = 64;
     static constexpr int kNW = 4;
     static constexpr int kThreads = kNW * 32;
     static constexpr int kKpw = kTK / kNW;             // keys per warp per tile (16)
-    static constexpr int kBoxCols = 64;                // 16-bit elements per 128-byte box row
+    static constexpr int kBoxCols = 128 / (int)sizeof(C);  // elements per 128-byte box row
     static constexpr int kBoxes = D / kBoxCols;
     static constexpr int kBoxBytes = kTK * 128;        // one box: 64 rows x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;
-    static constexpr int kStages = (D == 128) ? 3 : 4;
+    static constexpr int kStages = (D == 128 && !k8) ? 3 : 4;
     static constexpr int kQSlotBytes = kRB * kQRowBytes;
     static constexpr int kPieceUnits = 2;
     static constexpr int kKSteps = D / 16;             // k-steps of S = Q.K^T
@@ -58,11 +59,14 @@ template <typename T, int D> struct MmaShape {
 
     static constexpr int kRingOff = 0;                 // 1024-aligned boxes (swizzle pattern)
     static constexpr int kQOff = kRingOff + kStages * 2 * kTileBytes;
-    // No separate epilogue area: a piece's last tile keeps its ring slot until
-    // the warps are merged, and the merge uses that slot (o of 4 warps x 16
-    // rows x D fp32 = the K and V tile bytes; m and l in its q slot).
+    // With 16-bit caches there is no separate epilogue area: a piece's last
+    // tile keeps its ring slot until the warps are merged, and the merge uses
+    // that slot (o of 4 warps x 16 rows x D fp32 = the K and V tile bytes; m
+    // and l in its q slot).  8-bit tiles are too small for that: an area.
+    static constexpr bool kMergeInSlot = kNW * kRB * D * 4 <= 2 * kTileBytes;
     static constexpr int kEpiOff = kQOff + kStages * kQSlotBytes;
-    static constexpr int kMetaOff = kEpiOff;
+    static constexpr int kEpiBytes = kMergeInSlot ? 0 : ((kNW * kRB * (D + 2) * 4 + 15) / 16) * 16;
+    static constexpr int kMetaOff = kEpiOff + kEpiBytes;
     static constexpr int kBarOff = kMetaOff + kStages * 32;
     static constexpr int kJobOff = kBarOff + 2 * kStages * 8;
     static constexpr int kPageOff = kJobOff + 32;
@@ -70,7 +74,8 @@ template <typename T, int D> struct MmaShape {
 
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(kBoxBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
-    static_assert(kNW * kRB * D * 4 <= 2 * kTileBytes && 2 * kNW * kRB * 4 <= kQSlotBytes, "merge in the slot");
+    static_assert(2 * kNW * kRB * 4 <= kQSlotBytes, "m and l in the q slot");
+    static_assert(!k8 || D == 128, "E4M3 tiles: one 128-byte box per row");
 };
 
 // Shared-memory address of the 16-byte chunk c (0 .. D/8-1) of tile row r in
@@ -194,24 +199,156 @@ __device__ __forceinline__ void mma_tile(unsigned char *Ks, unsigned char *Vs,
     }
 }
 
+// One tile for one warp over an E4M3 cache (D = 128, one 128-byte box per
+// row).  The codes are widened to fp16 on the way into the fragments:
+//   * K: ldmatrix.x4 of the 16-bit view gives lane (g, t) key g's codes
+//     16c + 4t .. 4t+3 of chunk c; one cvt per code pair makes the two B
+//     registers of k-step c.  That is a fixed permutation of the contraction
+//     index within each 16-column step, applied to Q as well (qa holds, in
+//     the slots of columns 2t, 2t+1, 2t+8, 2t+9, the q values of columns 4t,
+//     4t+1, 4t+2, 4t+3), so S is unchanged.
+//   * V: ldmatrix.x4.trans of the 16-bit view gives lane (g, t) the codes of
+//     keys 2t, 2t+1 at columns 2g, 2g+1 of chunk c; byte permutes split them
+//     into an even-column and an odd-column 8-wide tile (oacc[2c], oacc[2c+1])
+//     whose column g is 16c + 2g and 16c + 2g + 1.
+//   * sfac: per row, the score factor (scale * log2 e * k_scale, times the
+//     power of two by which the row's q was brought into fp16 range).
+// Value rows at or past k_end are zeroed first when kMasked.
+template <int D, bool kMasked>
+__device__ __forceinline__ void mma_tile_e4m3(unsigned char *Ks, unsigned char *Vs, const uint32_t (&qa)[D / 16][4],
+                                              float (&oacc)[D / 8][4], float (&m)[2], float (&l)[2], int warp,
+                                              int lane, int tile_k0, const int (&lim)[2], int k_end,
+                                              const float (&sfac)[2])
+{
+    using S = MmaShape<__nv_bfloat16, D, __nv_fp8_e4m3>;
+    const float kNegInf = __int_as_float(0xff800000);
+    constexpr float kRescaleThreshold = 8.0f;
+    const int t = lane & 3;
+    const int kb = warp * S::kKpw;
+    const uint32_t k_base = smem_addr(Ks), v_base = smem_addr(Vs);
+
+    // ---- S = Q . K^T: matrices (keys kb.., chunk c), (kb+8.., c), (kb.., c+1), (kb+8.., c+1) ----
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+    {
+        const int key = kb + (((lane >> 3) & 1) << 3) + (lane & 7);
+        const int csel = lane >> 4;
+        uint32_t r[D / 32][4];
+#pragma unroll
+        for (int c = 0; c < D / 16; c += 2) ldmatrix_x4_addr(r[c / 2], mma_chunk_addr<S>(k_base, key, c + csel));
+#pragma unroll
+        for (int c = 0; c < D / 16; c += 2)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // chunk c + h: registers 2h (keys kb..) and 2h+1 (kb+8..)
+                const uint32_t k0 = r[c / 2][2 * h], k1 = r[c / 2][2 * h + 1];
+                mma_16816<__half>(sacc[0], qa[c + h], e4m3x2_to_f16x2(k0 & 0xffffu), e4m3x2_to_f16x2(k0 >> 16));
+                mma_16816<__half>(sacc[1], qa[c + h], e4m3x2_to_f16x2(k1 & 0xffffu), e4m3x2_to_f16x2(k1 >> 16));
+            }
+    }
+
+    // ---- scale, mask, online softmax (as mma_tile) ----
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            sacc[nt][e] *= sfac[e >> 1];
+            if constexpr (kMasked) {
+                const int key = tile_k0 + kb + nt * 8 + 2 * t + (e & 1);
+                if (key >= lim[e >> 1]) sacc[nt][e] = kNegInf;
+            }
+        }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        float mt = fmaxf(fmaxf(sacc[0][2 * rr], sacc[0][2 * rr + 1]), fmaxf(sacc[1][2 * rr], sacc[1][2 * rr + 1]));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        if (mt > m[rr] + kRescaleThreshold) {
+            const float alpha = fast_exp2(m[rr] - mt);
+            l[rr] *= alpha;
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                oacc[nt][2 * rr] *= alpha;
+                oacc[nt][2 * rr + 1] *= alpha;
+            }
+            m[rr] = mt;
+        }
+        const float mu = (m[rr] == kNegInf) ? 0.f : m[rr];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 2 * rr; e < 2 * rr + 2; ++e) {
+                const float p = fast_exp2(sacc[nt][e] - mu);
+                l[rr] += p;
+                sacc[nt][e] = p;
+            }
+    }
+    const uint32_t pa[4] = {pack_pair<__half>(sacc[0][0], sacc[0][1]), pack_pair<__half>(sacc[0][2], sacc[0][3]),
+                            pack_pair<__half>(sacc[1][0], sacc[1][1]), pack_pair<__half>(sacc[1][2], sacc[1][3])};
+
+    if constexpr (kMasked) {
+        if (tile_k0 + kb + S::kKpw > k_end) {
+            for (int idx = lane; idx < S::kKpw * (D / 16); idx += 32) {
+                const int rr = kb + idx / (D / 16), c = idx % (D / 16);
+                if (tile_k0 + rr >= k_end) sts128(mma_chunk_addr<S>(v_base, rr, c), make_uint4(0u, 0u, 0u, 0u));
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+        }
+    }
+
+    // ---- O += P . V ----
+    {
+        const int key = kb + (((lane >> 3) & 1) << 3) + (lane & 7);
+        const int csel = lane >> 4;
+        uint32_t r[D / 32][4];
+#pragma unroll
+        for (int c = 0; c < D / 16; c += 2) ldmatrix_x4_trans_addr(r[c / 2], mma_chunk_addr<S>(v_base, key, c + csel));
+#pragma unroll
+        for (int c = 0; c < D / 16; c += 2)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // chunk c + h
+                const uint32_t v0 = r[c / 2][2 * h], v1 = r[c / 2][2 * h + 1];  // keys kb+2t.., kb+8+2t..
+                mma_16816<__half>(oacc[2 * (c + h)], pa, e4m3x2_to_f16x2(__byte_perm(v0, 0, 0x0020)),
+                                  e4m3x2_to_f16x2(__byte_perm(v1, 0, 0x0020)));
+                mma_16816<__half>(oacc[2 * (c + h) + 1], pa, e4m3x2_to_f16x2(__byte_perm(v0, 0, 0x0031)),
+                                  e4m3x2_to_f16x2(__byte_perm(v1, 0, 0x0031)));
+            }
+    }
+}
+
 // In a fused step the tile holding new keys P .. P+N-1 has stale cache rows:
 // the warp copies its new rows from k_new / v_new into the tile (and, when
 // kc / vc are given, into the cache: kc, vc address the cache row of the
 // tile's first key) before the tile is read.
-template <typename T, int D>
+// With an E4M3 cache (C != T) the new rows are quantized as kvd_append_e4m3
+// stores them (kv_scale: K and V scales).
+template <typename T, int D, typename C = T>
 __device__ __forceinline__ void mma_insert_new_rows(unsigned char *Ks, unsigned char *Vs, int warp, int lane,
                                                     int tile_k0, int P, int k_end, const unsigned char *kn,
-                                                    const unsigned char *vn, unsigned char *kc, unsigned char *vc)
+                                                    const unsigned char *vn, unsigned char *kc, unsigned char *vc,
+                                                    float2 kv_scale = float2{})
 {
-    using S = MmaShape<T, D>;
+    using S = MmaShape<T, D, C>;
     const int kb = warp * S::kKpw;
     const int lo = max(kb, P - tile_k0), hi = min(kb + S::kKpw, k_end - tile_k0);
     if (lo >= hi) return;
-    for (int idx = lane; idx < (hi - lo) * (D / 8); idx += 32) {
-        const int r = lo + idx / (D / 8), c = idx % (D / 8);
+    constexpr int kChunks = S::kRowBytes / 16;  // 16-byte chunks per cache row
+    for (int idx = lane; idx < (hi - lo) * kChunks; idx += 32) {
+        const int r = lo + idx / kChunks, c = idx % kChunks;
         const int key = tile_k0 + r;
-        const size_t nrow = (size_t)(key - P) * S::kRowBytes + c * 16;
-        const uint4 kv = ldg128_nc(kn + nrow), vv = ldg128_nc(vn + nrow);
+        uint4 kv, vv;
+        if constexpr (S::k8) {  // 16 new elements per chunk of codes
+            const size_t nrow = (size_t)(key - P) * S::kQRowBytes + c * 32;
+            kv = e4m3_chunk_from<T>(kn + nrow, kv_scale.x);
+            vv = e4m3_chunk_from<T>(vn + nrow, kv_scale.y);
+        } else {
+            const size_t nrow = (size_t)(key - P) * S::kRowBytes + c * 16;
+            kv = ldg128_nc(kn + nrow);
+            vv = ldg128_nc(vn + nrow);
+        }
         sts128(mma_chunk_addr<S>(smem_addr(Ks), r, c), kv);
         sts128(mma_chunk_addr<S>(smem_addr(Vs), r, c), vv);
         if (kc != nullptr) {
@@ -227,13 +364,16 @@ __device__ __forceinline__ void mma_insert_new_rows(unsigned char *Ks, unsigned 
 // attn_balanced_kernel; tiles by TMA through the K and V tensor maps (over
 // the contiguous cache viewed as [B*H_kv*T_max, D], or over the page pool
 // viewed as [num_pages*H_kv*page_size, D] when kPaged).
-template <typename T, int D, bool kFused, bool kTicketMerge, bool kPaged>
-__global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
+// C: the cache element type (T, or E4M3 codes with bf16 T: contiguous only).
+template <typename T, int D, bool kFused, bool kTicketMerge, bool kPaged, typename C = T>
+__global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads)
     attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v)
 {
-    using S = MmaShape<T, D>;
+    using S = MmaShape<T, D, C>;
     using Tq = Elem<T>;
+    constexpr bool k8 = S::k8;
+    static_assert(!(k8 && kPaged), "the E4M3 cache is contiguous only");
     constexpr int RB = S::kRB;
     const float kNegInf = __int_as_float(0xff800000);
     extern __shared__ __align__(1024) unsigned char smem_mma[];
@@ -309,6 +449,7 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
     uint32_t qa[S::kKSteps][4];
     float oacc[S::kNTiles][4];
     float m_run[2], l_run[2];
+    float sfac[2];  // E4M3: per-row score factor (see mma_tile_e4m3)
     int lim[2];
     bool timed_out = false;
     int first_unwaited = -1;
@@ -354,23 +495,68 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
             for (int nt = 0; nt < S::kNTiles; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.f;
+            if constexpr (k8) {
+                // fp16 fragments with the permuted column order of mma_tile_e4m3
+                // (slots 2t, 2t+1 | 2t+8, 2t+9 hold columns 4t, 4t+1 | 4t+2, 4t+3);
+                // a row whose largest |q| reaches 2^15 is scaled by an exact power
+                // of two into fp16 range, and the factor goes into its scores.
+                float qf[2][S::kKSteps][4];
+                float amax[2] = {0.f, 0.f};
 #pragma unroll
-            for (int ks = 0; ks < S::kKSteps; ++ks)
+                for (int r = 0; r < 2; ++r) {
+                    const int row = g + 8 * r;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int row = g + ((e & 1) << 3);
-                    const int col = 16 * ks + 2 * t + ((e >> 1) << 3);
-                    qa[ks][e] = row < q_rows ? *reinterpret_cast<const uint32_t *>(qs + row * S::kQRowBytes + col * 2)
-                                             : 0u;
+                    for (int ks = 0; ks < S::kKSteps; ++ks) {
+                        uint2 raw = make_uint2(0u, 0u);
+                        if (row < q_rows) raw = *reinterpret_cast<const uint2 *>(qs + row * S::kQRowBytes + (16 * ks + 4 * t) * 2);
+                        qf[r][ks][0] = __uint_as_float(raw.x << 16);
+                        qf[r][ks][1] = __uint_as_float(raw.x & 0xffff0000u);
+                        qf[r][ks][2] = __uint_as_float(raw.y << 16);
+                        qf[r][ks][3] = __uint_as_float(raw.y & 0xffff0000u);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) amax[r] = fmaxf(amax[r], fabsf(qf[r][ks][e]));
+                    }
+                    amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 1));
+                    amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 2));
+                    // exponent of amax minus 14, at least 0: amax / 2^shift < 2^15
+                    const int ex = (int)((__float_as_uint(amax[r]) >> 23) & 0xffu) - 127;
+                    const int shift = ex >= 15 ? ex - 14 : 0;
+                    const float down = __uint_as_float((uint32_t)(127 - shift) << 23);  // 2^-shift
+                    sfac[r] = a.qscale * __uint_as_float((uint32_t)(127 + shift) << 23);
+#pragma unroll
+                    for (int ks = 0; ks < S::kKSteps; ++ks)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) qf[r][ks][e] *= down;
                 }
+#pragma unroll
+                for (int ks = 0; ks < S::kKSteps; ++ks) {
+                    qa[ks][0] = pack_pair<__half>(qf[0][ks][0], qf[0][ks][1]);
+                    qa[ks][1] = pack_pair<__half>(qf[1][ks][0], qf[1][ks][1]);
+                    qa[ks][2] = pack_pair<__half>(qf[0][ks][2], qf[0][ks][3]);
+                    qa[ks][3] = pack_pair<__half>(qf[1][ks][2], qf[1][ks][3]);
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < S::kKSteps; ++ks)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int row = g + ((e & 1) << 3);
+                        const int col = 16 * ks + 2 * t + ((e >> 1) << 3);
+                        qa[ks][e] = row < q_rows ? *reinterpret_cast<const uint32_t *>(qs + row * S::kQRowBytes + col * 2)
+                                                 : 0u;
+                    }
+            }
         }
 
         const int k_end = mt.tile_k0 + mt.nk;
         if (mt.tile_k0 + S::kTK <= mt.P + (kFused ? 0 : 1)) {
-            mma_tile<T, D, false>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
+            if constexpr (k8)
+                mma_tile_e4m3<D, false>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, sfac);
+            else
+                mma_tile<T, D, false>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
         } else {
             if constexpr (kFused) {
-                const size_t nrow = (size_t)mt.bh * a.N * S::kRowBytes;
+                const size_t nrow = (size_t)mt.bh * a.N * S::kQRowBytes;
                 unsigned char *kc = nullptr, *vc = nullptr;
                 size_t crow = 0;  // cache row of the tile's first key
                 bool write = mt.rb == 0;  // one row block writes the new rows into the cache
@@ -386,14 +572,20 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
                     kc = static_cast<unsigned char *>(const_cast<void *>(a.k_cache)) + crow * S::kRowBytes;
                     vc = static_cast<unsigned char *>(const_cast<void *>(a.v_cache)) + crow * S::kRowBytes;
                 }
-                mma_insert_new_rows<T, D>(Ks, Vs, warp, lane, mt.tile_k0, mt.P, k_end,
-                                          static_cast<const unsigned char *>(a.k_new) + nrow,
-                                          static_cast<const unsigned char *>(a.v_new) + nrow, kc, vc);
+                float2 kvs = float2{};
+                if constexpr (k8) kvs = a.kv_scale;
+                mma_insert_new_rows<T, D, C>(Ks, Vs, warp, lane, mt.tile_k0, mt.P, k_end,
+                                             static_cast<const unsigned char *>(a.k_new) + nrow,
+                                             static_cast<const unsigned char *>(a.v_new) + nrow, kc, vc, kvs);
             }
-            mma_tile<T, D, true>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
+            if constexpr (k8)
+                mma_tile_e4m3<D, true>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, sfac);
+            else
+                mma_tile<T, D, true>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
         }
-        // (a piece's last tile keeps its slot for the merge below)
-        if (!(mt.flags & kMetaLast)) {
+        // (a piece's last tile keeps its slot for the merge below, when the
+        // merge fits in it)
+        if (!S::kMergeInSlot || !(mt.flags & kMetaLast)) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
@@ -411,21 +603,34 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
 
         // ---- end of a piece: each warp's (o, m, l) to shared memory, then
         //      the warps merged by log-sum-exp ----
-        float *ep_o = reinterpret_cast<float *>(Ks);  // the slot's K and V tile bytes
-        float *ep_m = reinterpret_cast<float *>(smem + S::kQOff + s * S::kQSlotBytes);
+        float *ep_o = S::kMergeInSlot ? reinterpret_cast<float *>(Ks)  // the slot's K and V tile bytes
+                                      : reinterpret_cast<float *>(smem + S::kEpiOff);
+        float *ep_m = S::kMergeInSlot ? reinterpret_cast<float *>(smem + S::kQOff + s * S::kQSlotBytes)
+                                      : ep_o + S::kNW * RB * D;
         float *ep_l = ep_m + S::kNW * RB;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
             l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
         }
-        __syncthreads();  // every warp is done with the slot's K, V and q
+        __syncthreads();  // every warp is done with the slot's K, V and q (or the previous merge)
+        if constexpr (k8) {
+            // even / odd column tiles of chunk c: lane (g, t) holds columns 16c + 4t .. 4t+3
 #pragma unroll
-        for (int nt = 0; nt < S::kNTiles; ++nt)
+            for (int c = 0; c < D / 16; ++c)
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
-                *reinterpret_cast<float2 *>(ep_o + (warp * RB + g + 8 * r) * D + nt * 8 + 2 * t) =
-                    make_float2(oacc[nt][2 * r], oacc[nt][2 * r + 1]);
+                for (int r = 0; r < 2; ++r)
+                    *reinterpret_cast<float4 *>(ep_o + (warp * RB + g + 8 * r) * D + 16 * c + 4 * t) =
+                        make_float4(oacc[2 * c][2 * r], oacc[2 * c + 1][2 * r], oacc[2 * c][2 * r + 1],
+                                    oacc[2 * c + 1][2 * r + 1]);
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < S::kNTiles; ++nt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    *reinterpret_cast<float2 *>(ep_o + (warp * RB + g + 8 * r) * D + nt * 8 + 2 * t) =
+                        make_float2(oacc[nt][2 * r], oacc[nt][2 * r + 1]);
+        }
         if (t == 0) {
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
@@ -452,7 +657,10 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
                 den = fmaf(wt, ep_l[w * RB + r], den);
             }
             if (single) {
-                Tq::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
+                if constexpr (k8)  // values are stored / v_scale
+                    Tq::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den * a.kv_scale.y);
+                else
+                    Tq::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
             } else {
                 float *pr = a.part + (pbase + r) * (D + 4);
                 pr[d] = num;
@@ -462,10 +670,12 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
                 }
             }
         }
-        // the slot is free again (its generic writes ordered before the next bulk copy)
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if constexpr (S::kMergeInSlot) {
+            // the slot is free again (its generic writes ordered before the next bulk copy)
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
         if constexpr (kTicketMerge) {
             if (!single) {
                 if (tid == 0 && n_pieces < 2) jobs[n_pieces] = MergeJob{mt.bh, mt.rb, mt.c_first, mt.n_chunks};
@@ -496,7 +706,7 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
         for (int i = 0; i < 2; ++i) {
             const MergeJob job = jobs[i];
             if (i < n_pieces && job.n_chunks)
-                merge_pieces<T, D, RB, S::kThreads>(a, job, nullptr, tid);  // (16-row heads: no scratch)
+                merge_pieces<T, D, RB, S::kThreads, k8>(a, job, nullptr, tid);  // (16-row heads: no scratch)
         }
     }
 
@@ -511,14 +721,14 @@ __global__ void __launch_bounds__(MmaShape<T, D>::kThreads)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <typename T, int D, bool kTicketMerge, bool kPaged> AttnVariant make_mma_variant()
+template <typename T, int D, bool kTicketMerge, bool kPaged, typename C = T> AttnVariant make_mma_variant()
 {
-    using S = MmaShape<T, D>;
+    using S = MmaShape<T, D, C>;
     AttnVariant v;
-    v.fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, false, kTicketMerge, kPaged>);
-    v.fused_fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, true, kTicketMerge, kPaged>);
+    v.fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, false, kTicketMerge, kPaged, C>);
+    v.fused_fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, true, kTicketMerge, kPaged, C>);
     if constexpr (kTicketMerge) v.merge_fn = nullptr;
-    else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, S::kRB>);
+    else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, S::kRB, S::k8>);
     v.threads = S::kThreads;
     v.fixed_smem_bytes = S::kFixedBytes;
     v.tile_keys = S::kTK;
@@ -526,6 +736,14 @@ template <typename T, int D, bool kTicketMerge, bool kPaged> AttnVariant make_mm
     v.piece_units = S::kPieceUnits;
     v.tma = true;
     return v;
+}
+
+// bf16 q / out over an E4M3 cache: D = 128, contiguous.
+template <bool kTicketMerge> bool pick_mma_e4m3_variant(int D, AttnVariant *v)
+{
+    if (D != 128) return false;
+    *v = make_mma_variant<__nv_bfloat16, 128, kTicketMerge, false, __nv_fp8_e4m3>();
+    return true;
 }
 
 template <typename T, bool kTicketMerge> bool pick_mma_variant(int D, bool paged, AttnVariant *v)

@@ -379,6 +379,15 @@ template <> struct Elem<__nv_fp8_e4m3> {
     }
 };
 
+// Two E4M3 codes (the low 16 bits) as an fp16 pair, exactly (every E4M3
+// value is an fp16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
+    return h2;
+}
+
 // Two fp32 values as two E4M3 codes, lo in the low byte: round to nearest
 // even, magnitudes beyond 448 saturate to 448.
 __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi)
