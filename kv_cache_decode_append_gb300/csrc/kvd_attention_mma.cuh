@@ -125,11 +125,24 @@ __device__ __forceinline__ void mma_tile(unsigned char *Ks, unsigned char *Vs,
         uint32_t b[S::kKSteps][4];
 #pragma unroll
         for (int ks = 0; ks < S::kKSteps; ++ks) ldmatrix_x4_addr(b[ks], mma_chunk_addr<S>(k_base, key, 2 * ks + csel));
+        // odd k-steps into a second set of accumulators: two dependency chains
+        // of kKSteps / 2 MMAs instead of one of kKSteps
+        float sodd[2][4];
 #pragma unroll
-        for (int ks = 0; ks < S::kKSteps; ++ks) {
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sodd[nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < S::kKSteps; ks += 2) {
             mma_16816<T>(sacc[0], qa[ks], b[ks][0], b[ks][1]);
             mma_16816<T>(sacc[1], qa[ks], b[ks][2], b[ks][3]);
+            mma_16816<T>(sodd[0], qa[ks + 1], b[ks + 1][0], b[ks + 1][1]);
+            mma_16816<T>(sodd[1], qa[ks + 1], b[ks + 1][2], b[ks + 1][3]);
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
     }
 
     // ---- scale, mask, online softmax (rows g: e = 0,1; g+8: e = 2,3) ----
@@ -239,14 +252,24 @@ __device__ __forceinline__ void mma_tile_e4m3(unsigned char *Ks, unsigned char *
         uint32_t r[D / 32][4];
 #pragma unroll
         for (int c = 0; c < D / 16; c += 2) ldmatrix_x4_addr(r[c / 2], mma_chunk_addr<S>(k_base, key, c + csel));
+        float sodd[2][4];  // odd chunks: a second dependency chain (as in mma_tile)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sodd[nt][e] = 0.f;
 #pragma unroll
         for (int c = 0; c < D / 16; c += 2)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // chunk c + h: registers 2h (keys kb..) and 2h+1 (kb+8..)
                 const uint32_t k0 = r[c / 2][2 * h], k1 = r[c / 2][2 * h + 1];
-                mma_16816<__half>(sacc[0], qa[c + h], e4m3x2_to_f16x2(k0 & 0xffffu), e4m3x2_to_f16x2(k0 >> 16));
-                mma_16816<__half>(sacc[1], qa[c + h], e4m3x2_to_f16x2(k1 & 0xffffu), e4m3x2_to_f16x2(k1 >> 16));
+                float (&acc)[2][4] = h ? sodd : sacc;
+                mma_16816<__half>(acc[0], qa[c + h], e4m3x2_to_f16x2(k0 & 0xffffu), e4m3x2_to_f16x2(k0 >> 16));
+                mma_16816<__half>(acc[1], qa[c + h], e4m3x2_to_f16x2(k1 & 0xffffu), e4m3x2_to_f16x2(k1 >> 16));
             }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
     }
 
     // ---- scale, mask, online softmax (as mma_tile) ----

@@ -26,6 +26,8 @@ def main():
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--fused", action="store_true", help="kvd_decode_step instead of append + attention")
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"])
+    ap.add_argument("--cache", default="same", choices=["same", "e4m3"],
+                    help="E4M3 cache codes (k_scale 0.05, v_scale 0.02) for a bf16 workload")
     ap.add_argument("--page-size", type=int, default=64)
     args = ap.parse_args()
     w = wl.WORKLOADS[args.workload]
@@ -41,8 +43,20 @@ def main():
     ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, w.torch_dtype, dev)
     if args.layout == "paged":
         kp, vp, table = wl.to_paged(x.pop("k_cache"), x.pop("v_cache"), args.page_size, fill=0.0)
+    e4m3 = args.cache == "e4m3"
+    if e4m3:
+        for key, sc in (("k_cache", 0.05), ("v_cache", 0.02)):
+            x[key] = (x[key].float() / sc).to(torch.float8_e4m3fn).view(torch.uint8)
+        ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, "e4m3", dev)
     for _ in range(args.launches):
-        if args.layout == "paged" and args.fused:
+        if e4m3 and args.fused:
+            kvd.kvd_decode_step_e4m3(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], out, past_d,
+                                     max_past, 0.05, 0.02, 0.0, ws, err)
+        elif e4m3:
+            kvd.kvd_append_e4m3(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past, 0.05, 0.02, err)
+            kvd.kvd_decode_attention_e4m3(x["q"], x["k_cache"], x["v_cache"], out, past_d, max_past, 0.05, 0.02, 0.0,
+                                          ws, err)
+        elif args.layout == "paged" and args.fused:
             kvd.kvd_paged_decode_step(x["q"], kp, vp, x["k_new"], x["v_new"], out, table, past_d, max_past, 0.0,
                                       ws, err)
         elif args.layout == "paged":
