@@ -51,7 +51,10 @@ template <typename T, int D, typename C = T> struct MmaShape {
     static constexpr int kBoxes = D / kBoxCols;
     static constexpr int kBoxBytes = kTK * 128;        // one box: 64 rows x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;
-    static constexpr int kStages = (D == 128 && !k8) ? 3 : 4;
+    // E4M3: 3 stages, so that three CTAs (12 warps) share an SM; the
+    // widening makes its tiles latency-bound with fewer warps
+    static constexpr int kStages = (D == 128) ? 3 : 4;
+    static constexpr int kMinBlocks = k8 ? 3 : 1;     // CTAs per SM the registers must allow
     static constexpr int kQSlotBytes = kRB * kQRowBytes;
     static constexpr int kPieceUnits = 2;
     static constexpr int kKSteps = D / 16;             // k-steps of S = Q.K^T
@@ -59,14 +62,14 @@ template <typename T, int D, typename C = T> struct MmaShape {
 
     static constexpr int kRingOff = 0;                 // 1024-aligned boxes (swizzle pattern)
     static constexpr int kQOff = kRingOff + kStages * 2 * kTileBytes;
-    // With 16-bit caches there is no separate epilogue area: a piece's last
-    // tile keeps its ring slot until the warps are merged, and the merge uses
-    // that slot (o of 4 warps x 16 rows x D fp32 = the K and V tile bytes; m
-    // and l in its q slot).  8-bit tiles are too small for that: an area.
-    static constexpr bool kMergeInSlot = kNW * kRB * D * 4 <= 2 * kTileBytes;
-    static constexpr int kEpiOff = kQOff + kStages * kQSlotBytes;
-    static constexpr int kEpiBytes = kMergeInSlot ? 0 : ((kNW * kRB * (D + 2) * 4 + 15) / 16) * 16;
-    static constexpr int kMetaOff = kEpiOff + kEpiBytes;
+    // No separate epilogue area: a piece's last tile keeps its ring slot
+    // until the warps are merged, and the merge uses that slot (o of 4 warps
+    // x 16 rows x D fp32 = the K and V tile bytes of a 16-bit cache; m and l
+    // in its q slot).  8-bit tiles hold half of that: the warps are merged in
+    // two phases (warps 2, 3 folded into warps 0, 1 first).
+    static constexpr int kMergePhases = (kNW * kRB * D * 4 <= 2 * kTileBytes) ? 1 : 2;
+    static constexpr int kMergeWarps = kNW / kMergePhases;  // warps whose o is in the slot at once
+    static constexpr int kMetaOff = kQOff + kStages * kQSlotBytes;
     static constexpr int kBarOff = kMetaOff + kStages * 32;
     static constexpr int kJobOff = kBarOff + 2 * kStages * 8;
     static constexpr int kPageOff = kJobOff + 32;
@@ -75,6 +78,7 @@ template <typename T, int D, typename C = T> struct MmaShape {
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(kBoxBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
     static_assert(2 * kNW * kRB * 4 <= kQSlotBytes, "m and l in the q slot");
+    static_assert(kMergeWarps * kRB * D * 4 <= 2 * kTileBytes, "merge in the slot");
     static_assert(!k8 || D == 128, "E4M3 tiles: one 128-byte box per row");
 };
 
@@ -389,7 +393,7 @@ __device__ __forceinline__ void mma_insert_new_rows(unsigned char *Ks, unsigned 
 // viewed as [num_pages*H_kv*page_size, D] when kPaged).
 // C: the cache element type (T, or E4M3 codes with bf16 T: contiguous only).
 template <typename T, int D, bool kFused, bool kTicketMerge, bool kPaged, typename C = T>
-__global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads)
+__global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>::kMinBlocks)
     attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v)
 {
@@ -606,9 +610,8 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads)
             else
                 mma_tile<T, D, true>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
         }
-        // (a piece's last tile keeps its slot for the merge below, when the
-        // merge fits in it)
-        if (!S::kMergeInSlot || !(mt.flags & kMetaLast)) {
+        // (a piece's last tile keeps its slot for the merge below)
+        if (!(mt.flags & kMetaLast)) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
@@ -625,42 +628,80 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads)
         if (!(mt.flags & kMetaLast)) continue;
 
         // ---- end of a piece: each warp's (o, m, l) to shared memory, then
-        //      the warps merged by log-sum-exp ----
-        float *ep_o = S::kMergeInSlot ? reinterpret_cast<float *>(Ks)  // the slot's K and V tile bytes
-                                      : reinterpret_cast<float *>(smem + S::kEpiOff);
-        float *ep_m = S::kMergeInSlot ? reinterpret_cast<float *>(smem + S::kQOff + s * S::kQSlotBytes)
-                                      : ep_o + S::kNW * RB * D;
+        //      the warps merged by log-sum-exp (in the slot's K and V tile
+        //      bytes; m and l in its q slot) ----
+        float *ep_o = reinterpret_cast<float *>(Ks);
+        float *ep_m = reinterpret_cast<float *>(smem + S::kQOff + s * S::kQSlotBytes);
         float *ep_l = ep_m + S::kNW * RB;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
             l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
         }
-        __syncthreads();  // every warp is done with the slot's K, V and q (or the previous merge)
-        if constexpr (k8) {
-            // even / odd column tiles of chunk c: lane (g, t) holds columns 16c + 4t .. 4t+3
+        // this warp's (o, m, l) as merge entry w; with fold, entry w is
+        // instead read back and merged into the registers
+        auto exchange = [&](int w, bool fold) {
+            float wa[2], wb[2];
+            if (fold) {
 #pragma unroll
-            for (int c = 0; c < D / 16; ++c)
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-                    *reinterpret_cast<float4 *>(ep_o + (warp * RB + g + 8 * r) * D + 16 * c + 4 * t) =
-                        make_float4(oacc[2 * c][2 * r], oacc[2 * c + 1][2 * r], oacc[2 * c][2 * r + 1],
-                                    oacc[2 * c + 1][2 * r + 1]);
-        } else {
-#pragma unroll
-            for (int nt = 0; nt < S::kNTiles; ++nt)
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-                    *reinterpret_cast<float2 *>(ep_o + (warp * RB + g + 8 * r) * D + nt * 8 + 2 * t) =
-                        make_float2(oacc[nt][2 * r], oacc[nt][2 * r + 1]);
-        }
-        if (t == 0) {
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                ep_m[warp * RB + g + 8 * r] = m_run[r];
-                ep_l[warp * RB + g + 8 * r] = l_run[r];
+                for (int r = 0; r < 2; ++r) {
+                    const float mo = ep_m[w * RB + g + 8 * r];
+                    const float M = fmaxf(m_run[r], mo);
+                    wa[r] = safe_weight(m_run[r], M);
+                    wb[r] = safe_weight(mo, M);
+                    l_run[r] = l_run[r] * wa[r] + ep_l[w * RB + g + 8 * r] * wb[r];
+                    m_run[r] = M;
+                }
             }
+            if constexpr (k8) {
+                // even / odd column tiles of chunk c: lane (g, t) holds columns 16c + 4t .. 4t+3
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        float4 *p = reinterpret_cast<float4 *>(ep_o + (w * RB + g + 8 * r) * D + 16 * c + 4 * t);
+                        if (fold) {
+                            const float4 o = *p;
+                            oacc[2 * c][2 * r] = oacc[2 * c][2 * r] * wa[r] + o.x * wb[r];
+                            oacc[2 * c + 1][2 * r] = oacc[2 * c + 1][2 * r] * wa[r] + o.y * wb[r];
+                            oacc[2 * c][2 * r + 1] = oacc[2 * c][2 * r + 1] * wa[r] + o.z * wb[r];
+                            oacc[2 * c + 1][2 * r + 1] = oacc[2 * c + 1][2 * r + 1] * wa[r] + o.w * wb[r];
+                        } else {
+                            *p = make_float4(oacc[2 * c][2 * r], oacc[2 * c + 1][2 * r], oacc[2 * c][2 * r + 1],
+                                             oacc[2 * c + 1][2 * r + 1]);
+                        }
+                    }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < S::kNTiles; ++nt)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        float2 *p = reinterpret_cast<float2 *>(ep_o + (w * RB + g + 8 * r) * D + nt * 8 + 2 * t);
+                        if (fold) {
+                            const float2 o = *p;
+                            oacc[nt][2 * r] = oacc[nt][2 * r] * wa[r] + o.x * wb[r];
+                            oacc[nt][2 * r + 1] = oacc[nt][2 * r + 1] * wa[r] + o.y * wb[r];
+                        } else {
+                            *p = make_float2(oacc[nt][2 * r], oacc[nt][2 * r + 1]);
+                        }
+                    }
+            }
+            if (!fold && t == 0) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    ep_m[w * RB + g + 8 * r] = m_run[r];
+                    ep_l[w * RB + g + 8 * r] = l_run[r];
+                }
+            }
+        };
+        __syncthreads();  // every warp is done with the slot's K, V and q (or the previous merge)
+        if constexpr (S::kMergePhases == 2) {
+            if (warp >= S::kMergeWarps) exchange(warp - S::kMergeWarps, false);
+            __syncthreads();
+            if (warp < S::kMergeWarps) exchange(warp, true);
+            __syncthreads();  // the folded entries are read before they are overwritten
         }
+        if (warp < S::kMergeWarps) exchange(warp, false);
         __syncthreads();
         const bool single = (mt.n_chunks == 1);
         const size_t pbase =
@@ -671,10 +712,10 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads)
             if (rg >= a.rows) continue;
             float M = kNegInf;
 #pragma unroll
-            for (int w = 0; w < S::kNW; ++w) M = fmaxf(M, ep_m[w * RB + r]);
+            for (int w = 0; w < S::kMergeWarps; ++w) M = fmaxf(M, ep_m[w * RB + r]);
             float num = 0.f, den = 0.f;
 #pragma unroll
-            for (int w = 0; w < S::kNW; ++w) {
+            for (int w = 0; w < S::kMergeWarps; ++w) {
                 const float wt = safe_weight(ep_m[w * RB + r], M);
                 num = fmaf(wt, ep_o[(w * RB + r) * D + d], num);
                 den = fmaf(wt, ep_l[w * RB + r], den);
@@ -693,12 +734,10 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads)
                 }
             }
         }
-        if constexpr (S::kMergeInSlot) {
-            // the slot is free again (its generic writes ordered before the next bulk copy)
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-        }
+        // the slot is free again (its generic writes ordered before the next bulk copy)
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
         if constexpr (kTicketMerge) {
             if (!single) {
                 if (tid == 0 && n_pieces < 2) jobs[n_pieces] = MergeJob{mt.bh, mt.rb, mt.c_first, mt.n_chunks};

@@ -117,7 +117,7 @@ def test_e4m3_append_other_input_types(orc, new_dtype):
     assert (h["k_cache"][:, :, 17:20] & 0x7F == 0x7E).any()  # saturated codes were exercised
 
 
-@pytest.mark.parametrize("case", [(16, 32, 8, 128, 6200, 6100, 2), (16, 32, 8, 128, 1100, 1000, 1)],
+@pytest.mark.parametrize("case", [(16, 32, 8, 128, 9300, 9200, 2), (16, 32, 8, 128, 1100, 1000, 1)],
                          ids=["merge_pass", "in_kernel"])
 def test_e4m3_merge_modes(orc, case):
     B, H_q, H_kv, D, T_max, max_past, launches = case
