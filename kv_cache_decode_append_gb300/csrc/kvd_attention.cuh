@@ -657,6 +657,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     }
     // Every input may come from the previous kernel on the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The next kernel on the stream may launch now: its CTAs take the SM
+    // slots this grid frees and run up to their own griddepcontrol.wait,
+    // which still waits for this whole grid to finish and flush.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();  // barrier initialisation visible to every thread
 
     // Warp 0 forms the unit prefix over sequences and thread 0 starts the ring
@@ -942,10 +946,6 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
             }
         }
     }
-    // Let the next kernel on the stream (the merge pass, or the next call)
-    // launch; its griddepcontrol.wait still waits for this whole grid to
-    // finish and flush.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Second pass: log-sum-exp merge of the pieces of one query row per warp.

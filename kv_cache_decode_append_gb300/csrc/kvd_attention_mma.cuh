@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         fence_mbar_init();
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // (as attn_balanced_kernel)
     __syncthreads();
 
     RangeWalk<S, !kTicketMerge, kPaged> walk;
@@ -780,7 +781,6 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
             }
         }
     }
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <typename T, int D, bool kTicketMerge, bool kPaged, typename C = T> AttnVariant make_mma_variant()
