@@ -174,9 +174,12 @@ typedef struct kvd_plan_info {
     int launches;
     size_t workspace_bytes;
     int rows_per_block;  /* query rows of a (b, h) handled together */
-    int tensor_cores;    /* 1: the tensor-core kernel (bf16 / fp16 caches, contiguous or
-                            paged, with (H_q / H_kv) * N >= 4 query rows per KV head for
-                            D = 128, >= 8 for D = 64), 0: the CUDA-core kernel */
+    int tensor_cores;    /* 2: the tcgen05 kernel (bf16 / fp16 caches, contiguous or paged,
+                            with (H_q / H_kv) * N >= 17 query rows per KV head: blocks of
+                            128 rows, each K/V tile read once per block);
+                            1: the mma.sync tensor-core kernel (bf16 / fp16 caches with
+                            4 .. 16 rows for D = 128, 8 .. 16 for D = 64; E4M3 caches
+                            with D = 128); 0: the CUDA-core kernel */
 } kvd_plan_info;
 
 kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len,

@@ -171,6 +171,10 @@ constexpr int kMmaMinRows64 = 8;
 // E4M3 caches (D = 128 only): widening the codes on the CUDA cores costs more
 // than the saved bytes, so every row count goes to the tensor cores.
 constexpr int kMmaMinRowsE4m3 = 1;
+// Query rows per KV head from which bf16 / fp16 caches go to the tcgen05
+// kernel (128-row blocks: every K/V tile read once for all rows), where the
+// 16-row mma.sync blocks would read each tile once per block.
+constexpr int kTc5MinRows = 17;
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link to the
 // driver library).
@@ -196,9 +200,10 @@ kvd_status encode_fn(EncodeTiledFn *fn)
     return g_encode != nullptr ? KVD_OK : KVD_ERR_CUDA;
 }
 
-// A 2-D tensor map over a cache viewed as [rows, D] elements (16-bit, or
-// 8-bit E4M3 codes), in boxes of 64 rows x 128 bytes, 128-byte swizzle.
-kvd_status encode_cache_map(CUtensorMap *map, const void *cache, long long rows, int D, kvd_dtype dtype)
+// A 2-D tensor map over a cache (or q) viewed as [rows, D] elements (16-bit,
+// or 8-bit E4M3 codes), in boxes of box_rows rows x 128 bytes, 128-byte swizzle.
+kvd_status encode_cache_map(CUtensorMap *map, const void *cache, long long rows, int D, kvd_dtype dtype,
+                            int box_rows = 64)
 {
     EncodeTiledFn fn;
     kvd_status st = encode_fn(&fn);
@@ -206,7 +211,7 @@ kvd_status encode_cache_map(CUtensorMap *map, const void *cache, long long rows,
     const int es = dtype == KVD_E4M3 ? 1 : 2;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)D * es};
-    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), 64};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType ty = dtype == KVD_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : dtype == KVD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -285,6 +290,7 @@ struct Plan {
     int grid, smem, launches, max_tiles;
     bool merge_pass;  // split heads merged by a second launch (else inside the kernel)
     bool mma;         // tensor-core kernel (16-row blocks, tiles by tensor map)
+    bool tc5;         // tcgen05 kernel (128-row blocks, tiles and q by tensor map)
     size_t part_off, tickets_off, seg_off, ws_bytes;
 };
 
@@ -339,14 +345,24 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
     if (st != KVD_OK) return st;
     pl->rows = (H_q / H_kv) * N;
-    // Many query rows per KV head (chunked decode with GQA): the tensor-core
-    // kernel in blocks of 16 rows, for 16-bit contiguous caches.
-    pl->mma = (pl->rows >= (D == 128 ? kMmaMinRows128 : kMmaMinRows64) && (dtype == KVD_BF16 || dtype == KVD_F16)) ||
-              (dtype == KVD_E4M3 && D == 128 && pl->rows >= kMmaMinRowsE4m3);
-    pl->rb = pl->mma ? 16 : pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : (pl->rows <= 4 || dtype == KVD_E4M3) ? 4 : 8;
+    // Many query rows per KV head (chunked decode with GQA): the tensor cores,
+    // in blocks of 16 rows (mma.sync) or, for 16-bit caches from kTc5MinRows
+    // rows, of 128 rows (tcgen05).  The choice does not depend on the cache
+    // layout, so paged and contiguous calls give the same bits.
+    const bool f16_family = dtype == KVD_BF16 || dtype == KVD_F16;
+    pl->tc5 = f16_family && pl->rows >= kTc5MinRows;
+    pl->mma = !pl->tc5 && ((pl->rows >= (D == 128 ? kMmaMinRows128 : kMmaMinRows64) && f16_family) ||
+                           (dtype == KVD_E4M3 && D == 128 && pl->rows >= kMmaMinRowsE4m3));
+    pl->rb = pl->tc5 ? 128 : pl->mma ? 16 : pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : (pl->rows <= 4 || dtype == KVD_E4M3) ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
     AttnVariant vp, vt, op, ot;  // this layout's builds, and the other layout's
-    if (pl->mma && dtype == KVD_E4M3) {
+    if (pl->tc5) {
+        const auto builds = [&](bool pg, AttnVariant *p, AttnVariant *t) {
+            return dtype == KVD_BF16 ? attn_variant_tc5_bf16(D, pg, p) && attn_variant_tc5_bf16_tk(D, pg, t)
+                                     : attn_variant_tc5_f16(D, pg, p) && attn_variant_tc5_f16_tk(D, pg, t);
+        };
+        if (!builds(paged, &vp, &vt) || !builds(!paged, &op, &ot)) return KVD_ERR_UNSUPPORTED;
+    } else if (pl->mma && dtype == KVD_E4M3) {
         if (!attn_variant_mma_e4m3(D, &vp) || !attn_variant_mma_e4m3_tk(D, &vt)) return KVD_ERR_UNSUPPORTED;
         op = vp;
         ot = vt;
@@ -396,8 +412,8 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     pl->launches = pl->merge_pass ? 2 : 1;
     if (!pl->merge_pass) pl->v = vt;
 
-    // (partial slots of the tensor-core kernel hold only a 16-row block's real rows)
-    const int part_rows = pl->mma && pl->rows < pl->rb ? pl->rows : pl->rb;
+    // (partial slots of the tensor-core kernels hold only a block's real rows)
+    const int part_rows = (pl->mma || pl->tc5) && pl->rows < pl->rb ? pl->rows : pl->rb;
     const size_t pieces = (size_t)sms * (occ > occ_other ? occ : occ_other) * 2 * part_rows;
     size_t off = 0;
     pl->part_off = off;  // per piece row: o[D], m, l, 2 floats of padding (16-byte rows)
@@ -483,7 +499,7 @@ kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_
     info->launches = pl.launches;
     info->workspace_bytes = pl.ws_bytes;
     info->rows_per_block = pl.rb;
-    info->tensor_cores = pl.mma ? 1 : 0;
+    info->tensor_cores = pl.tc5 ? 2 : pl.mma ? 1 : 0;
     return KVD_OK;
 }
 
@@ -596,7 +612,13 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
         alignas(64) CUtensorMap tmk, tmv;
         if ((st = encode_cache_map(&tmk, k_cache, rows_total, D, dtype)) != KVD_OK) return st;
         if ((st = encode_cache_map(&tmv, v_cache, rows_total, D, dtype)) != KVD_OK) return st;
-        void *targs[] = {&a, &tmk, &tmv};
+        alignas(64) CUtensorMap tmq;
+        void *targs[] = {&a, &tmk, &tmv, &tmq};
+        if (pl.v.q_map) {  // q viewed as [B * H_q * N, D], 128-row boxes (one row block)
+            const long long q_rows = (long long)B * H_kv * pl.rows;
+            if (q_rows + pl.rb > 0x7fffffffLL) return KVD_ERR_UNSUPPORTED;
+            if ((st = encode_cache_map(&tmq, q, q_rows, D, dtype, pl.rb)) != KVD_OK) return st;
+        }
         if (cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.fused_fn : pl.v.fn, targs) != cudaSuccess)
             return KVD_ERR_CUDA;
     } else if (cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.fused_fn : pl.v.fn, args) != cudaSuccess) {

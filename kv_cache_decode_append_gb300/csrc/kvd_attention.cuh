@@ -102,6 +102,7 @@ template <typename T, int D, int RB, typename C = T> struct AttnShape {
     using Ty = Elem<C>;   // cache rows (the K/V tiles)
     using Tq = Elem<T>;   // q, new K/V and out rows
     static constexpr bool kTma = false;  // tiles arrive by 1-D bulk copies
+    static constexpr bool kQInRing = true;  // a piece's q rows ride with its first tile
     static constexpr int kRB = RB;
     static constexpr int kRowBytes = D * Ty::kBytes;   // one cache row
     static constexpr int kQRowBytes = D * Tq::kBytes;  // one q / new K/V / out row
@@ -459,7 +460,7 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
         meta[s] = mt;
 
         const uint32_t bytes = (uint32_t)mt.nk * S::kRowBytes;
-        const uint32_t qbytes = piece_start ? (uint32_t)q_bytes : 0u;
+        const uint32_t qbytes = (S::kQInRing && piece_start) ? (uint32_t)q_bytes : 0u;
         size_t off;
         if constexpr (kPaged) {
             page = page_next;
@@ -525,12 +526,12 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
 };
 
 // Rows per partial slot.  The CUDA-core kernels' row blocks (RB 1, 2, 4, 8)
-// are sized to their rows; the tensor-core kernel's 16-row blocks (RB = 16,
-// used by no other kernel) keep only the block's real rows, min(16, rows),
-// so few-row decodes do not carry 16-row partials.
+// are sized to their rows; the tensor-core kernels' 16- and 128-row blocks
+// (used by no other kernel) keep only the block's real rows, min(RB, rows),
+// so few-row decodes do not carry padded partials.
 template <int RB> __device__ __forceinline__ int part_rows(int rows)
 {
-    if constexpr (RB == 16) return rows < RB ? rows : RB;
+    if constexpr (RB >= 16) return rows < RB ? rows : RB;
     else return RB;
 }
 
@@ -1025,6 +1026,7 @@ struct AttnVariant {
     int rows_per_block;
     int piece_units;       // cost of a piece boundary in tile units
     bool tma = false;      // tensor-core kernel: takes the K and V tensor maps
+    bool q_map = false;    // tcgen05 kernel: also a Q tensor map (128-row boxes)
 };
 
 template <typename T, int D, int RB, bool kTicketMerge, bool kPaged, typename C = T> AttnVariant make_variant()
@@ -1093,5 +1095,10 @@ bool attn_variant_mma_f16(int D, bool paged, AttnVariant *v);
 bool attn_variant_mma_f16_tk(int D, bool paged, AttnVariant *v);
 bool attn_variant_mma_e4m3(int D, AttnVariant *v);  // bf16 q / out, E4M3 cache, D = 128
 bool attn_variant_mma_e4m3_tk(int D, AttnVariant *v);
+// tcgen05 kernels (kvd_attention_tc5.cuh): 128-row blocks, contiguous or paged caches
+bool attn_variant_tc5_bf16(int D, bool paged, AttnVariant *v);
+bool attn_variant_tc5_bf16_tk(int D, bool paged, AttnVariant *v);
+bool attn_variant_tc5_f16(int D, bool paged, AttnVariant *v);
+bool attn_variant_tc5_f16_tk(int D, bool paged, AttnVariant *v);
 
 }  // namespace kvd

@@ -40,6 +40,7 @@ template <typename T, int D, typename C = T> struct MmaShape {
     using Tq = Elem<T>;
     static constexpr bool k8 = sizeof(C) == 1;         // E4M3 cache (8-bit codes)
     static constexpr bool kTma = true;
+    static constexpr bool kQInRing = true;
     static constexpr int kRB = 16;
     static constexpr int kRowBytes = D * (int)sizeof(C);
     static constexpr int kQRowBytes = D * 2;

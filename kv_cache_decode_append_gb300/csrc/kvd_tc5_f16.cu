@@ -1,0 +1,7 @@
+// Instantiates the f16 tcgen05 decode-attention kernels whose split heads go to the separate merge pass
+// (D in {64, 128}, 128-row blocks, contiguous and paged caches).
+#include "kvd_attention_tc5.cuh"
+
+namespace kvd {
+bool attn_variant_tc5_f16(int D, bool paged, AttnVariant *v) { return pick_tc5_variant<__half, false>(D, paged, v); }
+}  // namespace kvd

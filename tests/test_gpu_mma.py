@@ -20,12 +20,13 @@ def orc():
     return oracle.load()
 
 
-# (B, H_q, H_kv, D, N, T_max, past, dtype)
+# (B, H_q, H_kv, D, N, T_max, past, dtype) -- 4 .. 16 rows per KV head (more go to
+# the tcgen05 kernel: test_gpu_tc5.py)
 MMA_CASES = [
     (2, 32, 2, 128, 1, 900, [899, 130], "bf16"),           # 16 rows: one full block
-    (3, 8, 1, 128, 4, 700, [512, 0, 695], "bf16"),         # 32 rows: two blocks, empty history
-    (2, 16, 2, 64, 3, 1100, [1000, 61], "bf16"),           # 24 rows: a full and a partial block
-    (1, 32, 4, 128, 16, 600, [583], "bf16"),               # 128 rows: 8 blocks, chunk of 16
+    (3, 8, 1, 128, 2, 700, [512, 0, 695], "bf16"),         # 16 rows, chunk of 2, empty history
+    (2, 16, 2, 64, 2, 1100, [1000, 61], "bf16"),           # D=64, 16 rows
+    (1, 32, 8, 128, 3, 600, [583], "bf16"),                # 12 rows: chunk of 3, 4 padding rows
     (2, 12, 12, 64, 16, 1024, [1008, 512], "f16"),         # GPT-2 shapes, chunk of 16, fp16
     (4, 64, 4, 128, 1, 2000, [1999, 7, 1000, 64], "f16"),  # 16 rows, fp16, ragged
     (3, 16, 4, 128, 1, 800, [799, 0, 257], "bf16"),        # 4 rows: GQA decode, 12 padding rows
@@ -60,3 +61,6 @@ def test_kernel_choice():
     assert kvd.kvd_decode_plan(4, 16, 8, 128, 1, 1000, "bf16")["tensor_cores"] == 0   # 2 rows
     assert kvd.kvd_decode_plan(8, 12, 12, 64, 1, 1000, "bf16")["tensor_cores"] == 0   # 1 row, D=64
     assert kvd.kvd_decode_plan(4, 32, 2, 128, 1, 1000, "f32")["tensor_cores"] == 0    # fp32 cache
+    assert kvd.kvd_decode_plan(4, 32, 2, 128, 1, 1000, "bf16")["tensor_cores"] == 1   # 16 rows
+    assert kvd.kvd_decode_plan(4, 17, 1, 128, 1, 1000, "bf16")["tensor_cores"] == 2   # 17 rows: tcgen05
+    assert kvd.kvd_decode_plan(4, 8, 8, 64, 3, 1000, "f16")["tensor_cores"] == 0      # 3 rows, D=64
