@@ -22,13 +22,14 @@
 //   * warps 0-3, the softmax warps: thread r owns query row r (tensor-memory
 //     lane r).  It loads the row's 64 scores, masks them, keeps the running
 //     max and sum in registers (a row is one thread: no shuffles), writes the
-//     weights P (bf16 / fp16) to shared memory as the A operand of the next
-//     P . V, rescales its O row in tensor memory when the max grows by more
-//     than 2^8, and at the end of a piece reads O back and writes the output
-//     row or the piece's partial (o, m, l).
-// Operands are 128-byte swizzled in shared memory: Q, K and P K-major (the
-// contraction index contiguous), V MN-major (D contiguous), each described to
-// the tensor core by a shared-memory matrix descriptor.
+//     weights P (bf16 / fp16) into its tensor-memory lane as the A operand of
+//     the next P . V (no shared-memory round trip), rescales its O row in
+//     tensor memory when the max grows by more than 2^8, and at the end of a
+//     piece reads O back and writes the output row or the piece's partial
+//     (o, m, l).
+// Shared-memory operands are 128-byte swizzled: Q and K K-major (the head
+// dimension contiguous), V MN-major (D contiguous), each described to the
+// tensor core by a shared-memory matrix descriptor.
 //
 // Every mbarrier is waited for phase by phase in order, so a parity never
 // stands for two phases; every wait is bounded and also ends when another
@@ -95,6 +96,21 @@ __device__ __forceinline__ void tc5_mma_f16(uint32_t d_tmem, uint64_t a_desc, ui
         "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
         "}\n" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same with A (M rows x K) in tensor memory at a_tmem: row i in lane i,
+// two 16-bit elements per 32-bit column, K / 2 consecutive columns.
+__device__ __forceinline__ void tc5_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        "  .reg .pred p;\n"
+        "  setp.ne.b32 p, %4, 0;\n"
+        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -175,33 +191,34 @@ template <typename T, int D> struct Tc5Shape {
     static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = kTK * 128;    // K / V box: 64 keys x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;
-    static constexpr int kStages = D == 128 ? 4 : 8;
+    // (a ring slot is released by its tile's P . V: the stages beyond the
+    // two being computed are the copies in flight)
+    static constexpr int kStages = D == 128 ? 5 : 8;
     static constexpr int kPieceUnits = 2;
     static constexpr int kQBoxBytes = kRB * 128;   // Q box: 128 rows x 128 bytes
     static constexpr int kQBytes = kBoxes * kQBoxBytes;
-    static constexpr int kPBytes = kRB * kTK * 2;  // P: 128 rows x 64 keys, one box
-    static constexpr int kThreads = 192;
-    static constexpr int kTmemCols = 256;
+    static constexpr int kThreads = 224;
+    static constexpr int kTmemCols = 512;
     static constexpr int kTmemS = 0;               // two score buffers of 64 columns
     static constexpr int kTmemO = 128;             // O: D columns
+    static constexpr int kTmemP = 256;             // two P buffers of 32 columns (64 keys, 16-bit pairs)
 
     static constexpr int kRingOff = 0;
     static constexpr int kQOff = kRingOff + kStages * 2 * kTileBytes;  // the Q buffer
     static constexpr int kQSlotBytes = 0;          // (no q in the ring stages)
-    static constexpr int kPOff = kQOff + kQBytes;  // two P buffers
-    static constexpr int kMetaOff = kPOff + 2 * kPBytes;
+    static constexpr int kMetaOff = kQOff + kQBytes;
     static constexpr int kBarOff = kMetaOff + kStages * (int)sizeof(TileMeta);
     // full[kStages], empty[kStages], q_full, q_empty, s_full[2], s_free[2],
-    // p_full[2], p_empty[2], mma_done
-    static constexpr int kNumBars = 2 * kStages + 11;
+    // p_full[2], p_empty[2], mma_done[2] (the S and the P . V issuer)
+    static constexpr int kNumBars = 2 * kStages + 12;
     static constexpr int kJobOff = kBarOff + kNumBars * 8;
     static constexpr int kPageOff = kJobOff + 2 * (int)sizeof(MergeJob);
     static constexpr int kMiscOff = kPageOff + 4 * kStages;  // tensor-memory base, abort flag
     static constexpr int kFixedBytes = kMiscOff + 16;
 
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(kQOff % 1024 == 0 && kPOff % 1024 == 0 && kTileBytes % 1024 == 0, "swizzle atoms");
-    static_assert(kTmemO + D <= kTmemCols, "tensor memory columns");
+    static_assert(kQOff % 1024 == 0 && kTileBytes % 1024 == 0, "swizzle atoms");
+    static_assert(kTmemO + D <= kTmemP && kTmemP + 2 * (kTK / 2) <= kTmemCols, "tensor memory columns");
     static_assert(kFixedBytes + 4096 <= 227 * 1024, "shared memory");
 };
 
@@ -305,7 +322,7 @@ __device__ __forceinline__ void tc5_merge_rows(const AttnArgs &a, const MergeJob
 // split heads merged at the end of the kernel by the CTA that completes them,
 // else by the separate merge pass; kPaged: tiles from a page pool.
 template <typename T, int D, bool kFused, bool kTicketMerge, bool kPaged>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     attn_tc5_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q)
 {
@@ -351,7 +368,8 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&p_full[i], 128);
             mbar_init(&p_empty[i], 1);
         }
-        mbar_init(mma_done, 1);
+        mbar_init(&mma_done[0], 1);
+        mbar_init(&mma_done[1], 1);
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -367,7 +385,6 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = misc[0];
     const uint32_t ring = smem_addr(smem + S::kRingOff);
     const uint32_t qbuf = smem_addr(smem + S::kQOff);
-    const uint32_t pbuf = smem_addr(smem + S::kPOff);
 
     if (warp == 4) {
         // ---- producer: unit prefix over sequences (warp scan), then the walk ----
@@ -446,30 +463,11 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
     } else if (warp == 5) {
-        // ---- MMA warp ----
+        // ---- S warp: repairs the tiles, one thread issues S_j = Q . K_j^T ----
         constexpr uint32_t kIdescS = tc5_idesc<kBf16>(128, S::kTK, false, false);
-        constexpr uint32_t kIdescO = tc5_idesc<kBf16>(128, D, false, true);
         bool dead = false;
-        int pos = 0, n_pieces = 0;
-        int prev_st = 0;
-        bool prev_first = false;
-        // O += P_j . V_j of the tile at ring stage st_j (accumulating unless
-        // it is its piece's first tile); then P buffer and ring slot are free
-        auto issue_pv = [&](int j, int st_j, bool first_j) -> bool {
-            if (!tc5_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u, abort)) return false;
-            tc5_fence_after();
-            const uint32_t vt = ring + st_j * 2 * S::kTileBytes + S::kTileBytes;
-            const uint32_t pt = pbuf + (j & 1) * S::kPBytes;
-#pragma unroll
-            for (int ks = 0; ks < S::kTK / 16; ++ks)
-                tc5_mma_f16(tmem + S::kTmemO, tc5_desc(pt + ks * 32, 0u, 1024u),
-                            tc5_desc(vt + ks * 16 * 128, (uint32_t)S::kBoxBytes, 1024u), kIdescO,
-                            (ks > 0 || !first_j) ? 1u : 0u);
-            tc5_commit(&p_empty[j & 1]);
-            tc5_commit(&empty[st_j]);
-            return true;
-        };
-        for (;; ++pos) {
+        int n_pieces = 0;
+        for (int pos = 0;; ++pos) {
             const int st = pos % S::kStages;
             int ok = 1;
             if (lane == 0) ok = tc5_wait(&full[st], (uint32_t)(pos / S::kStages) & 1u, abort) ? 1 : 0;
@@ -506,11 +504,10 @@ __global__ void __launch_bounds__(192, 1)
                 __syncwarp();
             }
             if (lane == 0) {
-                if (first && !tc5_wait(q_full, (uint32_t)(n_pieces - 1) & 1u, abort)) dead = true;
+                if (first && !tc5_wait(q_full, (uint32_t)(n_pieces - 1) & 1u, abort)) ok = 0;
                 // the score buffer was last read by the softmax of tile pos - 2
-                if (!dead && pos >= 2 && !tc5_wait(&s_free[pos & 1], (uint32_t)((pos >> 1) - 1) & 1u, abort))
-                    dead = true;
-                if (!dead) {
+                if (ok && pos >= 2 && !tc5_wait(&s_free[pos & 1], (uint32_t)((pos >> 1) - 1) & 1u, abort)) ok = 0;
+                if (ok) {
                     tc5_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
@@ -520,28 +517,63 @@ __global__ void __launch_bounds__(192, 1)
                                     ks > 0 ? 1u : 0u);
                     tc5_commit(&s_full[pos & 1]);
                     if (mt.flags & kMetaLast) tc5_commit(q_empty);
-                    if (pos >= 1 && !issue_pv(pos - 1, prev_st, prev_first)) dead = true;
                 }
             }
-            dead = __shfl_sync(0xffffffffu, dead ? 1 : 0, 0) != 0;
-            if (dead) break;
-            prev_st = st;
-            prev_first = first;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                dead = true;
+                break;
+            }
         }
         if (lane == 0) {
-            if (!dead && pos >= 1 && !issue_pv(pos - 1, prev_st, prev_first)) dead = true;
             if (dead) {
                 *abort = 1u;
                 raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
             }
-            // every MMA is complete before the tensor memory is read for the
-            // last time or freed
-            tc5_commit(mma_done);
-            mbar_wait_bounded(mma_done, 0u);
+            tc5_commit(&mma_done[0]);  // this thread's MMAs complete before the tensor memory is freed
+            mbar_wait_bounded(&mma_done[0], 0u);
+        }
+        __syncwarp();
+    } else if (warp == 6) {
+        // ---- P . V warp: one thread issues O += P_j . V_j once P_j is written ----
+        if (lane == 0) {
+            constexpr uint32_t kIdescO = tc5_idesc<kBf16>(128, D, false, true);
+            bool dead = false;
+            for (int j = 0;; ++j) {
+                const int st = j % S::kStages;
+                // the tile's meta (the slot is released by this thread, so its
+                // phase cannot run ahead)
+                if (!tc5_wait(&full[st], (uint32_t)(j / S::kStages) & 1u, abort)) {
+                    dead = true;
+                    break;
+                }
+                const TileMeta mt = meta[st];
+                if (mt.flags & kMetaEnd) break;
+                if (!tc5_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u, abort)) {
+                    dead = true;
+                    break;
+                }
+                tc5_fence_after();
+                const uint32_t vt = ring + st * 2 * S::kTileBytes + S::kTileBytes;
+                const uint32_t pt = tmem + S::kTmemP + (j & 1) * (S::kTK / 2);  // P_j in tensor memory
+                const bool first = (mt.flags & kMetaFirst) != 0;
+#pragma unroll
+                for (int ks = 0; ks < S::kTK / 16; ++ks)
+                    tc5_mma_f16_ts(tmem + S::kTmemO, pt + ks * 8,
+                                   tc5_desc(vt + ks * 16 * 128, (uint32_t)S::kBoxBytes, 1024u), kIdescO,
+                                   (ks > 0 || !first) ? 1u : 0u);
+                tc5_commit(&p_empty[j & 1]);  // P buffer j & 1 and O are free / final
+                tc5_commit(&empty[st]);       // the ring slot is free
+            }
+            if (dead) {
+                *abort = 1u;
+                raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+            }
+            tc5_commit(&mma_done[1]);
+            mbar_wait_bounded(&mma_done[1], 0u);
         }
         __syncwarp();
     } else {
-        // ---- softmax warps: thread tid owns row tid of the block ----
+        // ---- softmax warps 0-3: thread tid owns row tid of the block ----
         const int r = tid;
         const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
         float m_run = kNegInf, l_run = 0.f;
@@ -650,12 +682,8 @@ __global__ void __launch_bounds__(192, 1)
                     tc5_st32(lane_addr + S::kTmemO + c0, o);
                 }
             }
-            // row r of P: 8 chunks of 16 bytes, 128-byte swizzle
-            const uint32_t prow = pbuf + pb * S::kPBytes + r * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                sts128(prow + ((c ^ (r & 7)) << 4), make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-            fence_proxy_async_shared();  // generic writes before the tensor core reads P
+            // row r of P into its tensor-memory lane (P buffer pb)
+            tc5_st32(lane_addr + S::kTmemP + pb * (S::kTK / 2), pk);
             tc5_fence_before();
             mbar_arrive(&p_full[pb]);
 
