@@ -194,7 +194,10 @@ template <typename T, int D> struct Tc5Shape {
     // (a ring slot is released by its tile's P . V: the stages beyond the
     // two being computed are the copies in flight)
     static constexpr int kStages = D == 128 ? 5 : 8;
-    static constexpr int kPieceUnits = 2;
+    // Cost of a piece boundary in tile units for the static split: a piece
+    // ends with its 128-row epilogue and starts with a Q load (measured on
+    // GB300 at 128 rows per KV head: 2 units 191.8 us, 4 183.8, 6 181.5).
+    static constexpr int kPieceUnits = 6;
     static constexpr int kQBoxBytes = kRB * 128;   // Q box: 128 rows x 128 bytes
     static constexpr int kQBytes = kBoxes * kQBoxBytes;
     static constexpr int kThreads = 224;
