@@ -170,14 +170,15 @@ def test_paged_bad_page_is_flagged_and_contained():
         assert _same_bits(kpd[page3], kp[page3])
 
 
-@pytest.mark.parametrize("ps", [64, 256])
-def test_paged_tensor_core_bad_page(ps):
-    """A bad block-table entry on the tensor-core kernel (4 rows per KV head): flagged,
-    contained to its sequence, no write into the pool for it."""
-    w = wl.Workload(0, "badm", L=1, B=3, H_q=16, H_kv=4, D=128, N=1, dtype="bf16", T_max=1024, P=0)
-    assert kvd.kvd_decode_plan(3, 16, 4, 128, 1, 700, "bf16")["tensor_cores"] == 1
+@pytest.mark.parametrize("ps,N,tc", [(64, 1, 1), (256, 1, 1), (64, 5, 2)],
+                         ids=["mma_ps64", "mma_ps256", "tcgen05_ps64"])
+def test_paged_tensor_core_bad_page(ps, N, tc):
+    """A bad block-table entry on the tensor-core kernels (4 rows per KV head: mma.sync;
+    20 rows: tcgen05): flagged, contained to its sequence, no write into the pool for it."""
+    w = wl.Workload(0, "badm", L=1, B=3, H_q=16, H_kv=4, D=128, N=N, dtype="bf16", T_max=1024, P=0)
+    assert kvd.kvd_decode_plan(3, 16, 4, 128, N, 700, "bf16")["tensor_cores"] == tc
     past = torch.tensor([700, 300, 64], dtype=torch.int32)
-    _, t, kp, vp, table = _inputs(w, past, ps, seed=8900 + ps)
+    _, t, kp, vp, table = _inputs(w, past, ps, seed=8900 + ps + N)
     good, kpd_good, _, err = _run(w, past, t, kp, vp, table, fused=True)
     assert err == 0
     bad_table = table.clone()
