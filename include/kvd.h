@@ -122,7 +122,7 @@ size_t kvd_decode_workspace_bytes(int B, int H_q, int H_kv, int D, int N, int ma
  *                     it again after a call that reported KVD_DEVERR_TIMEOUT.
  *                     Calls that run concurrently need distinct workspaces.
  * Supported: D in {64, 128}; dtype fp32, bf16 or fp16; H_q % H_kv == 0;
- * (H_q / H_kv) * N <= 128.
+ * (H_q / H_kv) * N <= 1024 (query rows per KV head; chunked prefill).
  * Returns KVD_OK or the first argument error found (see kvd_status).
  * The workspace size does not depend on the cache layout: the paged calls
  * below use the same kvd_decode_workspace_bytes.
@@ -176,7 +176,7 @@ typedef struct kvd_plan_info {
     int rows_per_block;  /* query rows of a (b, h) handled together */
     int tensor_cores;    /* 2: the tcgen05 kernel (bf16 / fp16 caches, contiguous or paged,
                             with (H_q / H_kv) * N >= 17 query rows per KV head: blocks of
-                            128 rows, each K/V tile read once per block);
+                            128 rows, each K/V tile read once per block of rows);
                             1: the mma.sync tensor-core kernel (bf16 / fp16 caches with
                             4 .. 16 rows for D = 128, 8 .. 16 for D = 64; E4M3 caches
                             with D = 128); 0: the CUDA-core kernel */

@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(256) append_e4m3_kernel(const AppendE4m3Args a
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxRows = 128;  // (H_q / H_kv) * N supported per (b, h)
+constexpr int kMaxRows = 1024;  // (H_q / H_kv) * N supported per (b, h): 8 tcgen05 row blocks
 
 std::mutex g_mu;
 int g_sm_count[kMaxDevices];

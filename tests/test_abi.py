@@ -87,7 +87,7 @@ def test_attention_argument_errors(lib):
     assert _attn(lib, max_past=-1) == 1
     assert _attn(lib, D=96) == 3
     assert _attn(lib, dtype=7) == 3
-    assert _attn(lib, H_q=16, H_kv=1, N=9) == 3      # 144 query rows per KV head
+    assert _attn(lib, H_q=16, H_kv=1, N=65) == 3     # 1040 query rows per KV head
     assert _attn(lib, q=A + 8) == 1                   # misaligned
     assert _attn(lib, out=A + 4) == 1
     assert _attn(lib, max_past=64, N=1, T_max=64) == 2  # P + N > T_max

@@ -89,6 +89,7 @@ STEP_EDGES = [
     (1, 32, 4, 128, 16, 600, [583], "bf16"),
     (2, 6, 2, 64, 7, 1100, [1000, 60], "bf16"),
     (1, 2, 2, 128, 1, 1, [0], "f32"),
+    (1, 4, 4, 64, 144, 300, [100], "f32"),           # chunked prefill on the CUDA cores: 144 rows, 18 row blocks
 ]
 
 

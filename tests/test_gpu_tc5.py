@@ -33,6 +33,8 @@ TC5_CASES = [
     (1, 4, 4, 128, 128, 400, [200], "bf16"),                 # chunked prefill: 128 new keys, 3 tiles
     (2, 16, 1, 64, 8, 520, [512, 1], "bf16"),                # D=64, 128 rows
     (2, 8, 2, 128, 5, 69, [0, 64], "f16"),                   # 20 rows, whole history in the masked tile
+    (1, 8, 2, 128, 64, 400, [300], "bf16"),                  # chunked prefill: 256 rows, two row blocks
+    (2, 10, 2, 64, 32, 300, [200, 17], "f16"),               # 160 rows (GQA 5), D=64: a full and a partial block
 ]
 
 
@@ -62,6 +64,7 @@ def test_tc5_merge_modes(orc, case):
 TC5_PAGED_CASES = [
     (2, 8, 1, 128, 4, 1000, [999 - 4, 130], "bf16", 64),     # 32 rows, 64-token pages
     (2, 12, 12, 64, 24, 1024, [1000, 333], "f16", 128),      # 24 rows (MHA chunk), fp16
+    (1, 8, 2, 128, 64, 512, [400], "bf16", 64),              # 256 rows: two row blocks
 ]
 
 
