@@ -266,15 +266,34 @@ __device__ __forceinline__ void tc5_fix_tile(const AttnArgs &a, uint32_t Ks, uin
         if (lo < hi) {
             const unsigned char *kn = static_cast<const unsigned char *>(a.k_new) + (size_t)mt.bh * a.N * S::kRowBytes;
             const unsigned char *vn = static_cast<const unsigned char *>(a.v_new) + (size_t)mt.bh * a.N * S::kRowBytes;
-            for (int idx = lane; idx < (hi - lo) * kChunks; idx += 32) {
-                const int r = lo + idx / kChunks, c = idx % kChunks;
-                const size_t nrow = (size_t)(mt.tile_k0 + r - mt.P) * S::kRowBytes + c * 16;
-                const uint4 kv = ldg128_nc(kn + nrow), vv = ldg128_nc(vn + nrow);
-                sts128(tc5_chunk_addr<S>(Ks, r, c), kv);
-                sts128(tc5_chunk_addr<S>(Vs, r, c), vv);
-                if (kc != nullptr) {
-                    stg128(kc + (size_t)r * S::kRowBytes + c * 16, kv);
-                    stg128(vc + (size_t)r * S::kRowBytes + c * 16, vv);
+            const int n = (hi - lo) * kChunks;
+            // batches of 8 chunks per lane: all loads of a batch in flight
+            // before its stores (a chunk at a time would wait a full load
+            // latency per chunk)
+            for (int base = 0; base < n; base += 8 * 32) {
+                uint4 kv[8], vv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int idx = base + u * 32 + lane;
+                    if (idx < n) {
+                        const int r = lo + idx / kChunks, c = idx % kChunks;
+                        const size_t nrow = (size_t)(mt.tile_k0 + r - mt.P) * S::kRowBytes + c * 16;
+                        kv[u] = ldg128_nc(kn + nrow);
+                        vv[u] = ldg128_nc(vn + nrow);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int idx = base + u * 32 + lane;
+                    if (idx < n) {
+                        const int r = lo + idx / kChunks, c = idx % kChunks;
+                        sts128(tc5_chunk_addr<S>(Ks, r, c), kv[u]);
+                        sts128(tc5_chunk_addr<S>(Vs, r, c), vv[u]);
+                        if (kc != nullptr) {
+                            stg128(kc + (size_t)r * S::kRowBytes + c * 16, kv[u]);
+                            stg128(vc + (size_t)r * S::kRowBytes + c * 16, vv[u]);
+                        }
+                    }
                 }
             }
         }
