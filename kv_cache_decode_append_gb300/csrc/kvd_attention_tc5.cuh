@@ -8,25 +8,27 @@
 // their split, tile ring, partial layout and merges, for blocks of up to 128
 // query rows.  It serves chunked decode and chunked prefill with g * N > 16
 // rows per KV head, where the 16-row mma.sync blocks would read every K/V
-// tile once per block.  One CTA per SM, six warps:
+// tile once per block.  One CTA per SM, seven warps:
 //   * warp 4, the producer: the unit prefix over past_len and the range walk
 //     (RangeWalk); K/V tiles by 2-D TMA into a ring of kStages stages, and the
 //     Q block of each piece (128 rows x D, through a third tensor map) into
 //     one Q buffer;
-//   * warp 5, the MMA warp: allocates the tensor memory; writes the new rows
-//     of a fused step into the tile (and the cache) and zeroes value rows past
+//   * warp 5, the S warp: allocates the tensor memory; writes the new rows of
+//     a fused step into the tile (and the cache) and zeroes value rows past
 //     the sequence end; one thread issues S_j = Q . K_j^T (M = 128 rows,
-//     N = 64 keys, into one of two score buffers in tensor memory) ahead of
-//     O += P_{j-1} . V_{j-1} (M = 128, N = D, O in tensor memory), each group
-//     completed by tcgen05.commit on an mbarrier;
+//     N = 64 keys) into score buffer j % 2 as soon as the tile and the buffer
+//     are free;
+//   * warp 6, the P . V warp: one thread issues O += P_j . V_j (M = 128,
+//     N = D, O in tensor memory) as soon as P_j is written, which also
+//     releases the ring slot; both issuers signal completion by
+//     tcgen05.commit on mbarriers;
 //   * warps 0-3, the softmax warps: thread r owns query row r (tensor-memory
 //     lane r).  It loads the row's 64 scores, masks them, keeps the running
 //     max and sum in registers (a row is one thread: no shuffles), writes the
 //     weights P (bf16 / fp16) into its tensor-memory lane as the A operand of
-//     the next P . V (no shared-memory round trip), rescales its O row in
-//     tensor memory when the max grows by more than 2^8, and at the end of a
-//     piece reads O back and writes the output row or the piece's partial
-//     (o, m, l).
+//     P . V (no shared-memory round trip), rescales its O row in tensor
+//     memory when the max grows by more than 2^8, and at the end of a piece
+//     reads O back and writes the output row or the piece's partial (o, m, l).
 // Shared-memory operands are 128-byte swizzled: Q and K K-major (the head
 // dimension contiguous), V MN-major (D contiguous), each described to the
 // tensor core by a shared-memory matrix descriptor.
