@@ -970,38 +970,51 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
     const int h = hr / a.n_rowblocks, rb = hr % a.n_rowblocks;
     const int rg = rb * RB + r;
     if (rg >= a.rows) return;
+    // (both loads issued before either is used)
     const int P = __ldg(a.past_len + b);
-    if (!past_len_ok(P, a.N, a.T_max, a.max_past_len)) return;  // reported by the split pass
     const int2 seg = static_cast<const int2 *>(a.merge_state)[u];
+    if (!past_len_ok(P, a.N, a.T_max, a.max_past_len)) return;  // reported by the split pass
     if (seg.y <= 1) return;  // the split pass wrote this row directly
 
-    float M = kNegInf;
-    for (int k = lane; k < seg.y; k += 32) {
-        const int c = seg.x + k;
-        M = fmaxf(M, a.part[(((size_t)c * 2 + (k == 0)) * part_rows<RB>(a.rows) + r) * (D + 4) + D]);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off /= 2) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
+    // One pass over the pieces, merged online (running max M, weighted sums);
+    // the loads of up to four pieces are issued before their updates.
+    float M = kNegInf, den = 0.f;
     float acc[kDpl];
 #pragma unroll
     for (int k = 0; k < kDpl; ++k) acc[k] = 0.f;
-    float den = 0.f;
-    for (int k = 0; k < seg.y; ++k) {
-        const size_t pidx = ((size_t)(seg.x + k) * 2 + (k == 0)) * part_rows<RB>(a.rows) + r;
-        const float *pr = a.part + pidx * (D + 4);
-        const float w = safe_weight(pr[D], M);
-        den = fmaf(w, pr[D + 1], den);
-        const float *po = pr + lane * kDpl;
-        if constexpr (kDpl == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(po);
-            acc[0] = fmaf(w, v.x, acc[0]);
-            acc[1] = fmaf(w, v.y, acc[1]);
-            acc[2] = fmaf(w, v.z, acc[2]);
-            acc[3] = fmaf(w, v.w, acc[3]);
-        } else {
+    for (int k0 = 0; k0 < seg.y; k0 += 4) {
+        float2 ml[4];
+        float ov[4][kDpl];
 #pragma unroll
-            for (int k2 = 0; k2 < kDpl; ++k2) acc[k2] = fmaf(w, po[k2], acc[k2]);
+        for (int i = 0; i < 4; ++i) {
+            const int k = k0 + i;
+            if (k < seg.y) {
+                const size_t pidx = ((size_t)(seg.x + k) * 2 + (k == 0)) * part_rows<RB>(a.rows) + r;
+                const float *pr = a.part + pidx * (D + 4);
+                ml[i] = *reinterpret_cast<const float2 *>(pr + D);
+                const float *po = pr + lane * kDpl;
+                if constexpr (kDpl == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(po);
+                    ov[i][0] = v.x;
+                    ov[i][1] = v.y;
+                    ov[i][2] = v.z;
+                    ov[i][3] = v.w;
+                } else {
+#pragma unroll
+                    for (int k2 = 0; k2 < kDpl; ++k2) ov[i][k2] = po[k2];
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (k0 + i < seg.y) {
+                const float Mn = fmaxf(M, ml[i].x);
+                const float wa = safe_weight(M, Mn), wb = safe_weight(ml[i].x, Mn);
+                den = den * wa + ml[i].y * wb;
+#pragma unroll
+                for (int k2 = 0; k2 < kDpl; ++k2) acc[k2] = acc[k2] * wa + ov[i][k2] * wb;
+                M = Mn;
+            }
         }
     }
     const int bh = b * a.H_kv + h;
