@@ -195,7 +195,11 @@ def kvd_decode_workspace_bytes(B: int, H_q: int, H_kv: int, D: int, N: int, max_
 
 
 def kvd_decode_plan(B: int, H_q: int, H_kv: int, D: int, N: int, max_past_len: int, dtype) -> dict:
-    """The split-T plan kvd_decode_attention uses for these shapes on the current device."""
+    """The split-T plan kvd_decode_attention uses for these shapes on the current device.
+
+    ``tensor_cores``: 0 the CUDA-core kernel, 1 the mma.sync tensor-core kernel (16-row
+    blocks), 2 the tcgen05 kernel (128-row blocks, for more than 16 query rows per KV
+    head); ``launches`` 2 when split heads are merged by the separate merge pass."""
     code = _NAME_DTYPE[dtype] if isinstance(dtype, str) else _TORCH_DTYPE[dtype]
     info = PlanInfo()
     _check("kvd_decode_plan", raw.kvd_decode_plan(B, H_q, H_kv, D, N, int(max_past_len), code,
