@@ -101,11 +101,17 @@ def _code_only(text: str) -> str:
     return " ".join("".join(out).split())
 
 
+# Device sources the dominant kernel of the default workload (the bf16 mma.sync
+# decode step and its merge pass, described by PROFILE_SUMMARY) is compiled from.
+PROFILED_KERNEL_SOURCES = ("kvd_device.cuh", "kvd_attention.cuh", "kvd_attention_mma.cuh", "kvd_mma_bf16.cu",
+                           "kvd_mma_bf16_tk.cu")
+
+
 def kernel_source_hash() -> str:
-    """Hash of the kernel sources (code only, see _code_only)."""
+    """Hash of the profiled kernel's sources (code only, see _code_only)."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "kv_cache_decode_append_gb300", "csrc", "*"))):
-        with open(p, encoding="utf-8") as f:
+    for name in PROFILED_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "kv_cache_decode_append_gb300", "csrc", name), encoding="utf-8") as f:
             h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
