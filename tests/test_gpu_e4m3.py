@@ -129,6 +129,110 @@ def test_e4m3_merge_modes(orc, case):
     _check(orc, w, past, seed=9810 + launches)
 
 
+# From 17 query rows per KV head the tcgen05 kernel runs (E4M3 tiles widened to bf16
+# in shared memory): (B, H_q, H_kv, D, N, T_max, past)
+E4M3_TC5_CASES = [
+    (2, 32, 8, 128, 8, 1100, [1000, 63]),                             # 32 rows, ragged tails
+    (3, 32, 2, 128, 10, 800, [700, 0, 129]),                          # 160 rows: two row blocks
+    (1, 32, 8, 128, 32, 300, [200]),                                  # 128 rows, a chunk of 32 across tiles
+]
+
+
+@pytest.mark.parametrize("case", E4M3_TC5_CASES, ids=[f"e4m3_tc5_{i}" for i in range(len(E4M3_TC5_CASES))])
+def test_e4m3_tc5_parity(orc, case):
+    B, H_q, H_kv, D, N, T_max, past = case
+    assert kvd.kvd_decode_plan(B, H_q, H_kv, D, N, max(past), "e4m3")["tensor_cores"] == 2
+    w = wl.Workload(0, "e4m3t", L=1, B=B, H_q=H_q, H_kv=H_kv, D=D, N=N, dtype="bf16", T_max=T_max, P=0)
+    _check(orc, w, past, seed=9650 + N)
+
+
+@pytest.mark.parametrize("case", [(16, 32, 8, 128, 9300, 9200, 2), (16, 32, 8, 128, 1100, 1000, 1)],
+                         ids=["merge_pass", "in_kernel"])
+def test_e4m3_tc5_merge_modes(orc, case):
+    B, H_q, H_kv, D, T_max, max_past, launches = case
+    plan = kvd.kvd_decode_plan(B, H_q, H_kv, D, 8, max_past, "e4m3")
+    assert plan["tensor_cores"] == 2 and plan["launches"] == launches
+    gen = torch.Generator().manual_seed(9830 + launches)
+    past = torch.randint(0, max_past + 1, (B,), generator=gen, dtype=torch.int32)
+    past[5] = max_past
+    w = wl.Workload(0, "e4m3tm", L=1, B=B, H_q=H_q, H_kv=H_kv, D=D, N=8, dtype="bf16", T_max=T_max, P=0)
+    _check(orc, w, past, seed=9840 + launches)
+
+
+def _gpu_attention(w, past, t):
+    """kvd_decode_attention_e4m3 alone over the given caches (no append)."""
+    g = {k: v.to(DEV) for k, v in t.items()}
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, int(past.max()), "e4m3", DEV)
+    out = torch.full_like(g["q"], float("nan"))
+    kvd.kvd_decode_attention_e4m3(g["q"], g["k_cache"], g["v_cache"], out, past.to(DEV), int(past.max()), K_SCALE,
+                                  V_SCALE, 0.0, ws, err)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), int(err.item())
+
+
+def _oracle_attention(orc, t, past):
+    h = {k: (v.cpu().numpy().copy() if v.dtype == torch.uint8 else to_np(v)) for k, v in t.items()}
+    ref, st = orc.decode_attention_e4m3(h["q"], h["k_cache"], h["v_cache"], past.numpy(), "bf16", K_SCALE, V_SCALE)
+    assert st == 0
+    return ref
+
+
+def test_e4m3_tc5_subnormal_codes(orc):
+    """Caches of zero and subnormal codes only (|x| = m * 2^-9): the tcgen05 kernel's widening
+    keeps them exactly (a flush to zero would zero the output)."""
+    w = wl.Workload(0, "e4m3s", L=1, B=2, H_q=32, H_kv=8, D=128, N=8, dtype="bf16", T_max=400, P=0)
+    past = torch.tensor([300, 57], dtype=torch.int32)
+    t = wl.layer_inputs(w, 0, past, device="cpu", seed_base=9870)
+    gen = torch.Generator().manual_seed(9871)
+    for key in ("k_cache", "v_cache"):
+        mag = torch.randint(0, 8, t[key].shape, generator=gen, dtype=torch.int32)
+        sign = torch.randint(0, 2, t[key].shape, generator=gen, dtype=torch.int32) * 0x80
+        t[key] = (mag | sign).to(torch.uint8)
+    # (every slot holds a code: the chunk's rows P .. P+N-1 included)
+    out, err = _gpu_attention(w, past, t)
+    assert err == 0
+    ref = _oracle_attention(orc, t, past)
+    assert np.abs(ref).max() > 0
+    assert row_rel_err(out, ref) <= TOL["bf16"]
+
+
+def test_e4m3_tc5_nan_codes(orc):
+    """A NaN code among the keys makes exactly the rows that see it NaN, as in the oracle (a
+    masked key's score is replaced, not multiplied); a NaN value code seen by every row of its
+    head makes that column NaN.  (A non-finite value at a key masked for some rows of the
+    chunk reaches them too: the zero weight times NaN in the P . V product is NaN.)"""
+    w = wl.Workload(0, "e4m3n", L=1, B=2, H_q=32, H_kv=8, D=128, N=8, dtype="bf16", T_max=400, P=0)
+    past = torch.tensor([300, 120], dtype=torch.int32)
+    _, t = _inputs(w, past + w.N, 9880)      # valid codes up to P + N (the chunk's rows), NaN codes after
+    t["k_cache"][0, 1, 200, 5] = 0x7F        # every row of (b 0, h 1) sees key 200
+    t["k_cache"][1, 5, 121, 7] = 0xFF        # rows of (b 1, h 5) from the second new token on see key P + 1
+    t["v_cache"][1, 3, 100, 64] = 0x7F       # every row of (b 1, h 3) sees value row 100
+    out, err = _gpu_attention(w, past, t)
+    assert err == 0
+    ref = _oracle_attention(orc, t, past)
+    assert np.array_equal(np.isnan(out), np.isnan(ref))
+    rows = np.isnan(ref).any(axis=-1)
+    assert rows[0, 4:8].all() and rows[1, 12:16].all()
+    assert rows[1, 20:24].sum() == 28 and not rows[1, 20:24, 0].any()  # (row i of the chunk: key P + i)
+    fin = ~np.isnan(ref).any(axis=-1)
+    assert row_rel_err(out[fin], ref[fin]) <= TOL["bf16"]
+
+
+def test_e4m3_kernel_choice():
+    assert kvd.kvd_decode_plan(4, 32, 8, 128, 4, 1000, "e4m3")["tensor_cores"] == 1   # 16 rows: mma.sync
+    assert kvd.kvd_decode_plan(4, 17, 1, 128, 1, 1000, "e4m3")["tensor_cores"] == 2   # 17 rows: tcgen05
+    assert kvd.kvd_decode_plan(4, 32, 1, 64, 1, 1000, "e4m3")["tensor_cores"] == 0    # D = 64: CUDA cores
+
+
+def test_e4m3_tc5_gqa_longctx_chunk8_full_size(orc):
+    """The long-context workload at full size with an E4M3 cache and 8 new tokens (32 rows per
+    KV head: the tcgen05 kernel), in the launch configuration bench.py --cache e4m3 --n-new 8 times."""
+    w = wl.with_n(wl.WORKLOADS["gqa_longctx_b32_bf16"], 8)
+    assert kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max(wl.past_lens(w).tolist()), "e4m3")["tensor_cores"] == 2
+    _check(orc, w, wl.past_lens(w), seed=9910, device=DEV)
+
+
 def test_e4m3_gqa_longctx_full_size(orc):
     """The long-context workload's shapes and lengths at full size with an E4M3 cache."""
     w = wl.WORKLOADS["gqa_longctx_b32_bf16"]
