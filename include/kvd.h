@@ -175,12 +175,11 @@ typedef struct kvd_plan_info {
     size_t workspace_bytes;
     int rows_per_block;  /* query rows of a (b, h) handled together */
     int tensor_cores;    /* 2: the tcgen05 kernel (bf16 / fp16 caches, contiguous or paged,
-                            and E4M3 caches with D = 128, with (H_q / H_kv) * N >= 17
-                            query rows per KV head: blocks of 128 rows, each K/V tile
-                            read once per block of rows);
+                            with (H_q / H_kv) * N >= 17 query rows per KV head: blocks of
+                            128 rows, each K/V tile read once per block of rows);
                             1: the mma.sync tensor-core kernel (bf16 / fp16 caches with
                             4 .. 16 rows for D = 128, 8 .. 16 for D = 64; E4M3 caches
-                            with D = 128 and up to 16 rows); 0: the CUDA-core kernel */
+                            with D = 128); 0: the CUDA-core kernel */
 } kvd_plan_info;
 
 kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len,
@@ -284,10 +283,8 @@ kvd_status kvd_paged_decode_step(const void *q, void *k_pages, void *v_pages, co
  * kvd_decode_step_e4m3 are kvd_decode_attention / kvd_decode_step over such a
  * cache (the fused step quantizes the new rows exactly as kvd_append_e4m3
  * does).  Workspace: kvd_decode_workspace_bytes(..., KVD_E4M3).  Query rows
- * per KV head are processed in blocks of 4 (D = 64), 16 (D = 128, up to 16
- * rows) or 128 (D = 128, from 17 rows; kvd_plan_info.tensor_cores = 2: the
- * codes are widened to bf16 in shared memory, exactly, and multiplied on the
- * tcgen05 tensor cores).  Other arguments, errors
+ * per KV head are processed in blocks of 4 (D = 64) or 16 (D = 128, on the
+ * tensor cores: kvd_plan_info.tensor_cores = 1).  Other arguments, errors
  * and device-side checks as for the bf16 calls; any other entry point given
  * KVD_E4M3 returns KVD_ERR_UNSUPPORTED, except kvd_append / kvd_paged_append,
  * which copy already-quantized rows bit for bit.

@@ -9,11 +9,6 @@
 
 namespace kvd {
 
-// tcgen05 kernels over E4M3 caches (kvd_tc5_e4m3.cu): bf16 q / out, D = 128,
-// contiguous caches; the separate merge pass, or split heads merged in-kernel
-bool attn_variant_tc5_e4m3(int D, AttnVariant *v);
-bool attn_variant_tc5_e4m3_tk(int D, AttnVariant *v);
-
 // ---------------------------------------------------------------------------
 // kv_append: cache[b, h, P_b + i, :] = new[b, h, i, :] for i < N, K and V.
 // The cache is updated in place in its preallocated slots, as production
@@ -351,22 +346,17 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     if (st != KVD_OK) return st;
     pl->rows = (H_q / H_kv) * N;
     // Many query rows per KV head (chunked decode with GQA): the tensor cores,
-    // in blocks of 16 rows (mma.sync) or, from kTc5MinRows rows, of 128 rows
-    // (tcgen05: 16-bit caches, and E4M3 caches at D = 128).  The choice does
-    // not depend on the cache layout, so paged and contiguous calls give the
-    // same bits.
+    // in blocks of 16 rows (mma.sync) or, for 16-bit caches from kTc5MinRows
+    // rows, of 128 rows (tcgen05).  The choice does not depend on the cache
+    // layout, so paged and contiguous calls give the same bits.
     const bool f16_family = dtype == KVD_BF16 || dtype == KVD_F16;
-    pl->tc5 = (f16_family || (dtype == KVD_E4M3 && D == 128)) && pl->rows >= kTc5MinRows;
+    pl->tc5 = f16_family && pl->rows >= kTc5MinRows;
     pl->mma = !pl->tc5 && ((pl->rows >= (D == 128 ? kMmaMinRows128 : kMmaMinRows64) && f16_family) ||
                            (dtype == KVD_E4M3 && D == 128 && pl->rows >= kMmaMinRowsE4m3));
     pl->rb = pl->tc5 ? 128 : pl->mma ? 16 : pl->rows <= 1 ? 1 : pl->rows <= 2 ? 2 : (pl->rows <= 4 || dtype == KVD_E4M3) ? 4 : 8;
     pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
     AttnVariant vp, vt, op, ot;  // this layout's builds, and the other layout's
-    if (pl->tc5 && dtype == KVD_E4M3) {  // (contiguous only: no other layout)
-        if (!attn_variant_tc5_e4m3(D, &vp) || !attn_variant_tc5_e4m3_tk(D, &vt)) return KVD_ERR_UNSUPPORTED;
-        op = vp;
-        ot = vt;
-    } else if (pl->tc5) {
+    if (pl->tc5) {
         const auto builds = [&](bool pg, AttnVariant *p, AttnVariant *t) {
             return dtype == KVD_BF16 ? attn_variant_tc5_bf16(D, pg, p) && attn_variant_tc5_bf16_tk(D, pg, t)
                                      : attn_variant_tc5_f16(D, pg, p) && attn_variant_tc5_f16_tk(D, pg, t);
@@ -627,8 +617,7 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
         if (pl.v.q_map) {  // q viewed as [B * H_q * N, D], 128-row boxes (one row block)
             const long long q_rows = (long long)B * H_kv * pl.rows;
             if (q_rows + pl.rb > 0x7fffffffLL) return KVD_ERR_UNSUPPORTED;
-            const kvd_dtype qt = dtype == KVD_E4M3 ? KVD_BF16 : dtype;  // (E4M3 caches: bf16 q)
-            if ((st = encode_cache_map(&tmq, q, q_rows, D, qt, pl.rb)) != KVD_OK) return st;
+            if ((st = encode_cache_map(&tmq, q, q_rows, D, dtype, pl.rb)) != KVD_OK) return st;
         }
         if (cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.fused_fn : pl.v.fn, targs) != cudaSuccess)
             return KVD_ERR_CUDA;

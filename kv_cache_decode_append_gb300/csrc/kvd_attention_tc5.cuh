@@ -182,48 +182,34 @@ __device__ __forceinline__ void tc5_st32(uint32_t taddr, const uint32_t (&r)[32]
 
 // 128-row blocks, 64-key tiles, 16-bit caches, D = 64 or 128.  Member names
 // match AttnShape where RangeWalk uses them.
-// 128-row blocks, 64-key tiles, D = 64 or 128; C is the cache element: T
-// (bf16 / fp16), or E4M3 codes with bf16 q and out (D = 128), widened to bf16
-// tiles in shared memory before the MMAs.  Member names match AttnShape where
-// RangeWalk uses them (kRowBytes, kTileBytes, kBoxes, ... describe the cache
-// tiles the producer loads).
-template <typename T, int D, typename C = T> struct Tc5Shape {
-    static constexpr bool k8 = sizeof(C) == 1;     // E4M3 cache
+template <typename T, int D> struct Tc5Shape {
     static constexpr bool kTma = true;
     static constexpr bool kQInRing = false;        // Q has its own buffer and tensor map
     static constexpr int kRB = 128;
-    static constexpr int kRowBytes = D * (int)sizeof(C);
+    static constexpr int kRowBytes = D * 2;
     static constexpr int kQRowBytes = D * 2;
     static constexpr int kTK = 64;
-    static constexpr int kBoxCols = 128 / (int)sizeof(C);  // elements per 128-byte box row
-    static constexpr int kBoxes = D / kBoxCols;
+    static constexpr int kBoxCols = 64;            // elements per 128-byte box row
+    static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = kTK * 128;    // K / V box: 64 keys x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;
-    // (a ring slot is released by its tile's P . V -- E4M3: once both halves
-    // are widened -- so the stages beyond the two being computed are the
-    // copies in flight)
-    static constexpr int kStages = k8 ? 6 : (D == 128 ? 5 : 8);
+    // (a ring slot is released by its tile's P . V: the stages beyond the
+    // two being computed are the copies in flight)
+    static constexpr int kStages = D == 128 ? 5 : 8;
     // Cost of a piece boundary in tile units for the static split: a piece
     // ends with its 128-row epilogue and starts with a Q load (measured on
     // GB300 at 128 rows per KV head: 2 units 191.8 us, 4 183.8, 6 181.5).
     static constexpr int kPieceUnits = 6;
-    static constexpr int kQBoxes = D / 64;         // Q is 16-bit: 64 elements per 128-byte box row
     static constexpr int kQBoxBytes = kRB * 128;   // Q box: 128 rows x 128 bytes
-    static constexpr int kQBytes = kQBoxes * kQBoxBytes;
+    static constexpr int kQBytes = kBoxes * kQBoxBytes;
     static constexpr int kThreads = 224;
     static constexpr int kTmemCols = 512;
     static constexpr int kTmemS = 0;               // two score buffers of 64 columns
     static constexpr int kTmemO = 128;             // O: D columns
     static constexpr int kTmemP = 256;             // two P buffers of 32 columns (64 keys, 16-bit pairs)
-    // MMA operand tiles: the cache tiles themselves, or (E4M3) two bf16 K and
-    // two bf16 V tiles widened from them, in the bf16 tile layout
-    static constexpr int kOpBoxBytes = kTK * 128;  // bf16 tile box: 64 keys x 64 elements
-    static constexpr int kOpTileBytes = (D / 64) * kOpBoxBytes;
 
     static constexpr int kRingOff = 0;
-    static constexpr int kCvOff = kRingOff + kStages * 2 * kTileBytes;  // (E4M3) K bf16 [2], V bf16 [2]
-    static constexpr int kCvBytes = k8 ? 4 * kOpTileBytes : 0;
-    static constexpr int kQOff = kCvOff + kCvBytes;  // the Q buffer
+    static constexpr int kQOff = kRingOff + kStages * 2 * kTileBytes;  // the Q buffer
     static constexpr int kQSlotBytes = 0;          // (no q in the ring stages)
     static constexpr int kMetaOff = kQOff + kQBytes;
     static constexpr int kBarOff = kMetaOff + kStages * (int)sizeof(TileMeta);
@@ -236,8 +222,7 @@ template <typename T, int D, typename C = T> struct Tc5Shape {
     static constexpr int kFixedBytes = kMiscOff + 16;
 
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(!k8 || D == 128, "E4M3 tiles: one 128-byte box per row");
-    static_assert(kQOff % 1024 == 0 && kCvOff % 1024 == 0 && kTileBytes % 1024 == 0, "swizzle atoms");
+    static_assert(kQOff % 1024 == 0 && kTileBytes % 1024 == 0, "swizzle atoms");
     static_assert(kTmemO + D <= kTmemP && kTmemP + 2 * (kTK / 2) <= kTmemCols, "tensor memory columns");
     static_assert(kFixedBytes + 4096 <= 227 * 1024, "shared memory");
 };
@@ -321,165 +306,10 @@ __device__ __forceinline__ void tc5_fix_tile(const AttnArgs &a, uint32_t Ks, uin
     }
 }
 
-// ---- E4M3 caches ----
-
-__device__ __forceinline__ uint4 lds128_addr(uint32_t a)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-
-// 128-byte swizzle of the 16-byte chunk c (0 .. 7) of row r of a box at the
-// 1024-byte-aligned shared address box.
-__device__ __forceinline__ uint32_t tc5_swz(uint32_t box, int r, int c)
-{
-    const uint32_t lin = box + r * 128 + (c << 4);
-    return lin ^ ((lin >> 3) & 0x70u);
-}
-
-// A 16-byte chunk of E4M3 codes (16 elements) as two 16-byte chunks of bf16
-// by the hardware conversion (every E4M3 value is a bf16 value: exact; NaN
-// codes give NaN).
-__device__ __forceinline__ void tc5_widen_e4m3_cvt(const uint4 &c, uint4 &lo, uint4 &hi)
-{
-    auto w2 = [](uint32_t two) {
-        const float2 f = Elem<__nv_fp8_e4m3>::pair(two);
-        return pack_pair<__nv_bfloat16>(f.x, f.y);
-    };
-    lo = make_uint4(w2(c.x & 0xffffu), w2(c.x >> 16), w2(c.y & 0xffffu), w2(c.y >> 16));
-    hi = make_uint4(w2(c.z & 0xffffu), w2(c.z >> 16), w2(c.w & 0xffffu), w2(c.w >> 16));
-}
-
-// Four E4M3 codes (a 32-bit word, code 0 in the low byte) as two bf16 pairs,
-// exactly, without the conversion unit: the code s.eeee.mmm laid out as the
-// bf16 bits s.0000eeee.mmm0000 (exponent bias 127 for 7) is its value times
-// 2^-120 -- zero and subnormal codes included -- and one bf16 multiply by
-// 2^120, a power-of-two scaling into the normal range, restores it.  Only the
-// NaN codes (s.1111.111) come out wrong (+-480).
-__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w)
-{
-    const uint32_t kTwo120 = 0x7b807b80u;   // bf16 2^120, both halves
-    const uint32_t kNegZero = 0x80008000u;  // (-0 + -0 keeps a code's negative zero)
-    const uint32_t t0 = __byte_perm(w, 0u, 0x1404);  // [c1, 0, c0, 0]: each code the high byte of a half
-    const uint32_t t1 = __byte_perm(w, 0u, 0x3424);  // [c3, 0, c2, 0]
-    const uint32_t b0 = ((t0 & 0x7f007f00u) >> 4) | (t0 & 0x80008000u);
-    const uint32_t b1 = ((t1 & 0x7f007f00u) >> 4) | (t1 & 0x80008000u);
-    uint2 r;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r.x) : "r"(b0), "r"(kTwo120), "r"(kNegZero));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r.y) : "r"(b1), "r"(kTwo120), "r"(kNegZero));
-    return r;
-}
-
-// Whether a 16-byte chunk of E4M3 codes holds a NaN code (low seven bits all
-// set): adding 1 to the seven low bits of a byte carries into its top bit only then.
-__device__ __forceinline__ bool e4m3_chunk_has_nan(const uint4 &c)
-{
-    const uint32_t m = 0x7f7f7f7fu, one = 0x01010101u;
-    return ((((c.x & m) + one) | ((c.y & m) + one) | ((c.z & m) + one) | ((c.w & m) + one)) & 0x80808080u) != 0u;
-}
-
-// One K or V tile of E4M3 codes (64 rows x 128 codes: one swizzled box at
-// src) widened by the 32 lanes of a warp into a bf16 operand tile (two
-// swizzled boxes at dst); rows at or past zero_from become zeros (value rows
-// past a sequence's end: a zero weight times a stale NaN is NaN in the MMA).
-// Lane l keeps one chunk column k and takes rows r0 + 4u: each group of 8
-// lanes covers two rows, chunks 0-3 of one and 4-7 of the other, so its
-// 16-byte loads and stores hit eight different bank groups.  A batch of 8
-// chunks is tested for NaN codes once and converted without branches (one
-// warp widens a whole tile: its latency is hidden by the batch's ILP).
-template <typename S>
-__device__ __forceinline__ void tc5_widen_tile(uint32_t src, uint32_t dst, int zero_from, int lane)
-{
-    const int l = lane & 7;
-    const int r0 = 2 * (lane >> 4) + (l >> 2);
-    const int k = (l & 3) + 4 * ((l >> 2) ^ ((lane >> 3) & 1));
-    // bf16 chunks 2k, 2k + 1 of a row: box (2k) / 8, chunk (2k) % 8 (and + 1)
-    const uint32_t dbox = dst + ((2 * k) >> 3) * S::kOpBoxBytes;
-    const int dc = (2 * k) & 7;
-#pragma unroll
-    for (int pass = 0; pass < S::kTK / 32; ++pass) {
-        uint4 c[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) c[u] = lds128_addr(tc5_swz(src, 32 * pass + 4 * u + r0, k));
-        bool nan = false;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) nan |= e4m3_chunk_has_nan(c[u]);
-        if (!nan) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int r = 32 * pass + 4 * u + r0;
-                const uint2 a = e4m3x4_to_bf16x4(c[u].x), b = e4m3x4_to_bf16x4(c[u].y);
-                const uint2 d = e4m3x4_to_bf16x4(c[u].z), e = e4m3x4_to_bf16x4(c[u].w);
-                const bool z = r >= zero_from;
-                sts128(tc5_swz(dbox, r, dc), z ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(a.x, a.y, b.x, b.y));
-                sts128(tc5_swz(dbox, r, dc + 1), z ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(d.x, d.y, e.x, e.y));
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int r = 32 * pass + 4 * u + r0;
-                uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                if (r < zero_from) tc5_widen_e4m3_cvt(c[u], lo, hi);
-                sts128(tc5_swz(dbox, r, dc), lo);
-                sts128(tc5_swz(dbox, r, dc + 1), hi);
-            }
-        }
-    }
-}
-
-// In a fused step with an E4M3 cache, the new K (or V) rows P .. P+N-1 that
-// the tile at shared address tile8 holds, quantized as kvd_append_e4m3 stores
-// them (each element divided by the scale, rounded to E4M3, saturating) into
-// the tile, and into the cache when cache_row0 (the cache row of the tile's
-// first key) is given.  nn: the new rows of this (b, h), T elements.
-template <typename T, typename S>
-__device__ __forceinline__ void tc5_insert_e4m3(uint32_t tile8, const TileMeta &mt, const unsigned char *nn,
-                                                float scale, unsigned char *cache_row0, int lane)
-{
-    constexpr int kIn = 16 / Elem<T>::kPerChunk;  // input chunks of T per 16 codes
-    const int lo = max(0, mt.P - mt.tile_k0), hi = mt.nk;
-    const int n = (hi - lo) * 8;
-    for (int base = 0; base < n; base += 4 * 32) {
-        uint4 raw[4][kIn];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = base + u * 32 + lane;
-            if (idx < n) {
-                const int r = lo + (idx >> 3), k = idx & 7;
-                const unsigned char *src = nn + (size_t)(mt.tile_k0 + r - mt.P) * S::kQRowBytes + k * 32;
-#pragma unroll
-                for (int i = 0; i < kIn; ++i) raw[u][i] = ldg128_nc(src + i * 16);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = base + u * 32 + lane;
-            if (idx < n) {
-                const int r = lo + (idx >> 3), k = idx & 7;
-                float x[16];
-#pragma unroll
-                for (int i = 0; i < kIn; ++i) Elem<T>::widen(raw[u][i], x + i * Elem<T>::kPerChunk);
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t lo2 = e4m3x2_from_f32(__fdiv_rn(x[4 * q], scale), __fdiv_rn(x[4 * q + 1], scale));
-                    const uint32_t hi2 = e4m3x2_from_f32(__fdiv_rn(x[4 * q + 2], scale), __fdiv_rn(x[4 * q + 3], scale));
-                    w[q] = lo2 | (hi2 << 16);
-                }
-                const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
-                sts128(tc5_swz(tile8, r, k), codes);
-                if (cache_row0 != nullptr) stg128(cache_row0 + (size_t)r * S::kRowBytes + k * 16, codes);
-            }
-        }
-    }
-}
-
 // Log-sum-exp merge of a split head's pieces, one warp per query row (the
 // four softmax warps share the rows): the pieces' partials were written by the
 // CTAs c_first .. c_first + n_chunks - 1 (slot 1 of the first, else slot 0).
-// kScaleV: the result times v_scale (E4M3 cache).
-template <typename T, int D, bool kScaleV>
+template <typename T, int D>
 __device__ __forceinline__ void tc5_merge_rows(const AttnArgs &a, const MergeJob &job, int warp, int lane)
 {
     using Tq = Elem<T>;
@@ -507,26 +337,20 @@ __device__ __forceinline__ void tc5_merge_rows(const AttnArgs &a, const MergeJob
             for (int i = 0; i < kDpl; ++i) acc[i] = fmaf(w, __ldcg(pr + lane * kDpl + i), acc[i]);
         }
         T *dst = static_cast<T *>(a.out) + ((size_t)job.bh * a.rows + job.rb * kRB + r) * D + lane * kDpl;
-        const float vs = kScaleV ? a.kv_scale.y : 1.f;
 #pragma unroll
-        for (int i = 0; i < kDpl; ++i) Tq::store(dst + i, acc[i] / den * vs);
+        for (int i = 0; i < kDpl; ++i) Tq::store(dst + i, acc[i] / den);
     }
 }
 
 // The kernel.  kFused: append + attention (kvd_decode_step); kTicketMerge:
 // split heads merged at the end of the kernel by the CTA that completes them,
-// else by the separate merge pass; kPaged: tiles from a page pool.  C: the
-// cache element (T, or E4M3 codes with bf16 T: contiguous caches, D = 128;
-// the S warp widens K and the P . V warp widens V into bf16 operand tiles,
-// and each releases its half of the ring slot once widened).
-template <typename T, int D, bool kFused, bool kTicketMerge, bool kPaged, typename C = T>
+// else by the separate merge pass; kPaged: tiles from a page pool.
+template <typename T, int D, bool kFused, bool kTicketMerge, bool kPaged>
 __global__ void __launch_bounds__(224, 1)
     attn_tc5_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q)
 {
-    using S = Tc5Shape<T, D, C>;
-    constexpr bool k8 = S::k8;
-    static_assert(!(k8 && kPaged), "E4M3 caches are contiguous");
+    using S = Tc5Shape<T, D>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr float kRescaleThreshold = 8.0f;
     const float kNegInf = __int_as_float(0xff800000);
@@ -557,7 +381,7 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
         for (int s = 0; s < S::kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], k8 ? 2 : 1);  // (E4M3: the S and the P . V warp each release their half)
+            mbar_init(&empty[s], 1);
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
@@ -641,8 +465,8 @@ __global__ void __launch_bounds__(224, 1)
                     }
                     mbar_arrive_expect_tx(q_full, (uint32_t)S::kQBytes);
 #pragma unroll
-                    for (int bx = 0; bx < S::kQBoxes; ++bx)
-                        tma_load_2d(smem + S::kQOff + bx * S::kQBoxBytes, &tm_q, bx * 64, qy, q_full,
+                    for (int bx = 0; bx < S::kBoxes; ++bx)
+                        tma_load_2d(smem + S::kQOff + bx * S::kQBoxBytes, &tm_q, bx * S::kBoxCols, qy, q_full,
                                     walk.policy);
                     ++q_loads;
                 }
@@ -681,31 +505,7 @@ __global__ void __launch_bounds__(224, 1)
             const bool first = (mt.flags & kMetaFirst) != 0;
             if (first) ++n_pieces;
             const uint32_t kt = ring + st * 2 * S::kTileBytes;
-            uint32_t kop = kt;  // the K operand of S_pos
-            if constexpr (k8) {
-                // operand buffer pos & 1 was last read by S_{pos-2}: complete
-                // once its softmax has released the score buffer
-                if (lane == 0 && pos >= 2 && !tc5_wait(&s_free[pos & 1], (uint32_t)((pos >> 1) - 1) & 1u, abort))
-                    ok = 0;
-                __syncwarp();  // (orders the other lanes' accesses after lane 0's waits)
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    dead = true;
-                    break;
-                }
-                if (kFused && mt.tile_k0 + S::kTK > mt.P) {
-                    const unsigned char *kn = static_cast<const unsigned char *>(a.k_new) + (size_t)mt.bh * a.N * S::kQRowBytes;
-                    unsigned char *kc = mt.rb == 0 ? static_cast<unsigned char *>(const_cast<void *>(a.k_cache)) +
-                                                         ((size_t)mt.bh * a.T_max + mt.tile_k0) * S::kRowBytes
-                                                   : nullptr;
-                    tc5_insert_e4m3<T, S>(kt, mt, kn, a.kv_scale.x, kc, lane);
-                    __syncwarp();
-                }
-                kop = smem_addr(smem + S::kCvOff) + (pos & 1) * S::kOpTileBytes;
-                tc5_widen_tile<S>(kt, kop, S::kTK, lane);  // (keys past the end are masked by the softmax)
-                fence_proxy_async_shared();  // generic writes before the tensor core / the next copy
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[st]);  // the K half of the ring slot is free
-            } else if ((kFused && mt.tile_k0 + S::kTK > mt.P) || mt.nk < S::kTK) {
+            if ((kFused && mt.tile_k0 + S::kTK > mt.P) || mt.nk < S::kTK) {
                 unsigned char *kc = nullptr, *vc = nullptr;
                 if constexpr (kFused) {
                     size_t crow = 0;  // cache row of the tile's first key
@@ -730,15 +530,14 @@ __global__ void __launch_bounds__(224, 1)
             if (lane == 0) {
                 if (first && !tc5_wait(q_full, (uint32_t)(n_pieces - 1) & 1u, abort)) ok = 0;
                 // the score buffer was last read by the softmax of tile pos - 2
-                if (!k8 && ok && pos >= 2 && !tc5_wait(&s_free[pos & 1], (uint32_t)((pos >> 1) - 1) & 1u, abort))
-                    ok = 0;
+                if (ok && pos >= 2 && !tc5_wait(&s_free[pos & 1], (uint32_t)((pos >> 1) - 1) & 1u, abort)) ok = 0;
                 if (ok) {
                     tc5_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
                         tc5_mma_f16(tmem + S::kTmemS + (pos & 1) * S::kTK,
                                     tc5_desc(qbuf + (ks >> 2) * S::kQBoxBytes + (ks & 3) * 32, 0u, 1024u),
-                                    tc5_desc(kop + (ks >> 2) * S::kOpBoxBytes + (ks & 3) * 32, 0u, 1024u), kIdescS,
+                                    tc5_desc(kt + (ks >> 2) * S::kBoxBytes + (ks & 3) * 32, 0u, 1024u), kIdescS,
                                     ks > 0 ? 1u : 0u);
                     tc5_commit(&s_full[pos & 1]);
                     if (mt.flags & kMetaLast) tc5_commit(q_empty);
@@ -756,68 +555,6 @@ __global__ void __launch_bounds__(224, 1)
             }
             tc5_commit(&mma_done[0]);  // this thread's MMAs complete before the tensor memory is freed
             mbar_wait_bounded(&mma_done[0], 0u);
-        }
-        __syncwarp();
-    } else if (warp == 6 && k8) {
-        // ---- P . V warp (E4M3): the warp widens V_j, one thread issues O += P_j . V_j ----
-        constexpr uint32_t kIdescO = tc5_idesc<kBf16>(128, D, false, true);
-        const uint32_t vop0 = smem_addr(smem + S::kCvOff) + 2 * S::kOpTileBytes;
-        bool dead = false;
-        for (int j = 0;; ++j) {
-            const int st = j % S::kStages;
-            int ok = 1;
-            if (lane == 0) {
-                ok = tc5_wait(&full[st], (uint32_t)(j / S::kStages) & 1u, abort) ? 1 : 0;
-                // operand buffer j & 1 was last read by P . V_{j-2}
-                if (ok && j >= 2 && !tc5_wait(&p_empty[j & 1], (uint32_t)((j >> 1) - 1) & 1u, abort)) ok = 0;
-            }
-            __syncwarp();  // (orders the other lanes' accesses after lane 0's waits)
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                dead = true;
-                break;
-            }
-            const TileMeta mt = meta[st];
-            if (mt.flags & kMetaEnd) break;
-            const uint32_t vt = ring + st * 2 * S::kTileBytes + S::kTileBytes;
-            if (kFused && mt.tile_k0 + S::kTK > mt.P) {
-                const unsigned char *vn = static_cast<const unsigned char *>(a.v_new) + (size_t)mt.bh * a.N * S::kQRowBytes;
-                unsigned char *vc = mt.rb == 0 ? static_cast<unsigned char *>(const_cast<void *>(a.v_cache)) +
-                                                     ((size_t)mt.bh * a.T_max + mt.tile_k0) * S::kRowBytes
-                                               : nullptr;
-                tc5_insert_e4m3<T, S>(vt, mt, vn, a.kv_scale.y, vc, lane);
-                __syncwarp();
-            }
-            const uint32_t vop = vop0 + (j & 1) * S::kOpTileBytes;
-            tc5_widen_tile<S>(vt, vop, mt.nk, lane);  // value rows past the end: zeros
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&empty[st]);  // the V half of the ring slot is free
-                if (!tc5_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u, abort)) ok = 0;
-                if (ok) {
-                    tc5_fence_after();
-                    const uint32_t pt = tmem + S::kTmemP + (j & 1) * (S::kTK / 2);
-                    const bool first = (mt.flags & kMetaFirst) != 0;
-#pragma unroll
-                    for (int ks = 0; ks < S::kTK / 16; ++ks)
-                        tc5_mma_f16_ts(tmem + S::kTmemO, pt + ks * 8,
-                                       tc5_desc(vop + ks * 16 * 128, (uint32_t)S::kOpBoxBytes, 1024u), kIdescO,
-                                       (ks > 0 || !first) ? 1u : 0u);
-                    tc5_commit(&p_empty[j & 1]);  // P buffer and operand buffer j & 1 free, O final
-                }
-            }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                dead = true;
-                break;
-            }
-        }
-        if (lane == 0) {
-            if (dead) {
-                *abort = 1u;
-                raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
-            }
-            tc5_commit(&mma_done[1]);
-            mbar_wait_bounded(&mma_done[1], 0u);
         }
         __syncwarp();
     } else if (warp == 6) {
@@ -985,7 +722,7 @@ __global__ void __launch_bounds__(224, 1)
             const int rg = mt.rb * S::kRB + r;
             const bool real = rg < a.rows;  // (every lane loads: the loads are warp-collective)
             {
-                const float inv = (k8 ? a.kv_scale.y : 1.f) / l_run;  // (E4M3: values are stored / v_scale)
+                const float inv = 1.f / l_run;
                 float *pr = nullptr;
                 T *orow = static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D;
                 if (!single) {
@@ -1051,7 +788,7 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const MergeJob job = jobs[i];
-                if (i < n_split && job.n_chunks) tc5_merge_rows<T, D, k8>(a, job, warp, lane);
+                if (i < n_split && job.n_chunks) tc5_merge_rows<T, D>(a, job, warp, lane);
             }
         }
     }
@@ -1064,14 +801,14 @@ __global__ void __launch_bounds__(224, 1)
     }
 }
 
-template <typename T, int D, bool kTicketMerge, bool kPaged, typename C = T> AttnVariant make_tc5_variant()
+template <typename T, int D, bool kTicketMerge, bool kPaged> AttnVariant make_tc5_variant()
 {
-    using S = Tc5Shape<T, D, C>;
+    using S = Tc5Shape<T, D>;
     AttnVariant v;
-    v.fn = reinterpret_cast<const void *>(&attn_tc5_kernel<T, D, false, kTicketMerge, kPaged, C>);
-    v.fused_fn = reinterpret_cast<const void *>(&attn_tc5_kernel<T, D, true, kTicketMerge, kPaged, C>);
+    v.fn = reinterpret_cast<const void *>(&attn_tc5_kernel<T, D, false, kTicketMerge, kPaged>);
+    v.fused_fn = reinterpret_cast<const void *>(&attn_tc5_kernel<T, D, true, kTicketMerge, kPaged>);
     if constexpr (kTicketMerge) v.merge_fn = nullptr;
-    else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, S::kRB, S::k8>);
+    else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, S::kRB, false>);
     v.threads = S::kThreads;
     v.fixed_smem_bytes = S::kFixedBytes;
     v.tile_keys = S::kTK;
@@ -1094,14 +831,6 @@ template <typename T, bool kTicketMerge> bool pick_tc5_variant(int D, bool paged
         return true;
     default: return false;
     }
-}
-
-// The tcgen05 builds for E4M3 caches (bf16 q / out, D = 128, contiguous).
-template <bool kTicketMerge> bool pick_tc5_e4m3_variant(int D, AttnVariant *v)
-{
-    if (D != 128) return false;
-    *v = make_tc5_variant<__nv_bfloat16, 128, kTicketMerge, false, __nv_fp8_e4m3>();
-    return true;
 }
 
 }  // namespace kvd

@@ -129,29 +129,29 @@ def test_e4m3_merge_modes(orc, case):
     _check(orc, w, past, seed=9810 + launches)
 
 
-# From 17 query rows per KV head the tcgen05 kernel runs (E4M3 tiles widened to bf16
-# in shared memory): (B, H_q, H_kv, D, N, T_max, past)
-E4M3_TC5_CASES = [
+# More than 16 query rows per KV head: several 16-row tensor-core blocks per head.
+# (B, H_q, H_kv, D, N, T_max, past)
+E4M3_MANY_ROWS_CASES = [
     (2, 32, 8, 128, 8, 1100, [1000, 63]),                             # 32 rows, ragged tails
     (3, 32, 2, 128, 10, 800, [700, 0, 129]),                          # 160 rows: two row blocks
     (1, 32, 8, 128, 32, 300, [200]),                                  # 128 rows, a chunk of 32 across tiles
 ]
 
 
-@pytest.mark.parametrize("case", E4M3_TC5_CASES, ids=[f"e4m3_tc5_{i}" for i in range(len(E4M3_TC5_CASES))])
-def test_e4m3_tc5_parity(orc, case):
+@pytest.mark.parametrize("case", E4M3_MANY_ROWS_CASES, ids=[f"e4m3_rows_{i}" for i in range(len(E4M3_MANY_ROWS_CASES))])
+def test_e4m3_many_rows_parity(orc, case):
     B, H_q, H_kv, D, N, T_max, past = case
-    assert kvd.kvd_decode_plan(B, H_q, H_kv, D, N, max(past), "e4m3")["tensor_cores"] == 2
+    assert kvd.kvd_decode_plan(B, H_q, H_kv, D, N, max(past), "e4m3")["tensor_cores"] == 1
     w = wl.Workload(0, "e4m3t", L=1, B=B, H_q=H_q, H_kv=H_kv, D=D, N=N, dtype="bf16", T_max=T_max, P=0)
     _check(orc, w, past, seed=9650 + N)
 
 
 @pytest.mark.parametrize("case", [(16, 32, 8, 128, 9300, 9200, 2), (16, 32, 8, 128, 1100, 1000, 1)],
                          ids=["merge_pass", "in_kernel"])
-def test_e4m3_tc5_merge_modes(orc, case):
+def test_e4m3_many_rows_merge_modes(orc, case):
     B, H_q, H_kv, D, T_max, max_past, launches = case
     plan = kvd.kvd_decode_plan(B, H_q, H_kv, D, 8, max_past, "e4m3")
-    assert plan["tensor_cores"] == 2 and plan["launches"] == launches
+    assert plan["tensor_cores"] == 1 and plan["launches"] == launches
     gen = torch.Generator().manual_seed(9830 + launches)
     past = torch.randint(0, max_past + 1, (B,), generator=gen, dtype=torch.int32)
     past[5] = max_past
@@ -178,9 +178,9 @@ def _oracle_attention(orc, t, past):
     return ref
 
 
-def test_e4m3_tc5_subnormal_codes(orc):
-    """Caches of zero and subnormal codes only (|x| = m * 2^-9): the tcgen05 kernel's widening
-    keeps them exactly (a flush to zero would zero the output)."""
+def test_e4m3_subnormal_codes(orc):
+    """Caches of zero and subnormal codes only (|x| = m * 2^-9), 32 rows per KV head: the
+    widening keeps them exactly (a flush to zero would zero the output)."""
     w = wl.Workload(0, "e4m3s", L=1, B=2, H_q=32, H_kv=8, D=128, N=8, dtype="bf16", T_max=400, P=0)
     past = torch.tensor([300, 57], dtype=torch.int32)
     t = wl.layer_inputs(w, 0, past, device="cpu", seed_base=9870)
@@ -197,7 +197,7 @@ def test_e4m3_tc5_subnormal_codes(orc):
     assert row_rel_err(out, ref) <= TOL["bf16"]
 
 
-def test_e4m3_tc5_nan_codes(orc):
+def test_e4m3_nan_codes(orc):
     """A NaN code among the keys makes exactly the rows that see it NaN, as in the oracle (a
     masked key's score is replaced, not multiplied); a NaN value code seen by every row of its
     head makes that column NaN.  (A non-finite value at a key masked for some rows of the
@@ -220,16 +220,17 @@ def test_e4m3_tc5_nan_codes(orc):
 
 
 def test_e4m3_kernel_choice():
-    assert kvd.kvd_decode_plan(4, 32, 8, 128, 4, 1000, "e4m3")["tensor_cores"] == 1   # 16 rows: mma.sync
-    assert kvd.kvd_decode_plan(4, 17, 1, 128, 1, 1000, "e4m3")["tensor_cores"] == 2   # 17 rows: tcgen05
-    assert kvd.kvd_decode_plan(4, 32, 1, 64, 1, 1000, "e4m3")["tensor_cores"] == 0    # D = 64: CUDA cores
+    """E4M3 caches stay on mma.sync at every row count (D = 128), CUDA cores at D = 64."""
+    assert kvd.kvd_decode_plan(4, 32, 8, 128, 4, 1000, "e4m3")["tensor_cores"] == 1   # 16 rows
+    assert kvd.kvd_decode_plan(4, 17, 1, 128, 1, 1000, "e4m3")["tensor_cores"] == 1   # 17 rows
+    assert kvd.kvd_decode_plan(4, 32, 1, 64, 1, 1000, "e4m3")["tensor_cores"] == 0    # D = 64
 
 
-def test_e4m3_tc5_gqa_longctx_chunk8_full_size(orc):
+def test_e4m3_gqa_longctx_chunk8_full_size(orc):
     """The long-context workload at full size with an E4M3 cache and 8 new tokens (32 rows per
-    KV head: the tcgen05 kernel), in the launch configuration bench.py --cache e4m3 --n-new 8 times."""
+    KV head), in the launch configuration bench.py --cache e4m3 --n-new 8 times."""
     w = wl.with_n(wl.WORKLOADS["gqa_longctx_b32_bf16"], 8)
-    assert kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max(wl.past_lens(w).tolist()), "e4m3")["tensor_cores"] == 2
+    assert kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max(wl.past_lens(w).tolist()), "e4m3")["tensor_cores"] == 1
     _check(orc, w, wl.past_lens(w), seed=9910, device=DEV)
 
 
