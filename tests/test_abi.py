@@ -138,3 +138,55 @@ def test_paged_argument_errors(lib):
     assert _paged_attn(lib, H_q=3) == 1
     assert lib.kvd_paged_decode_step(A, A, A, 0, A, A, A, A, 1, 4, 2, 64, 1, 64, 4, 8, 10, 0.0, 1,
                                      None, 0, None, None) == 1   # k_new missing
+
+
+def _append8(lib, k=A, v=A, kn=A, vn=A, past=A, B=1, H_kv=2, T_max=64, D=64, N=1, max_past=10, new_dtype=1,
+             k_scale=0.5, v_scale=0.5):
+    return lib.kvd_append_e4m3(k, v, kn, vn, past, B, H_kv, T_max, D, N, max_past, new_dtype, k_scale, v_scale,
+                               None, None)
+
+
+def _attn8(lib, q=A, k=A, v=A, out=A, past=A, B=1, H_q=4, H_kv=2, T_max=64, D=128, N=1, max_past=10,
+           k_scale=0.5, v_scale=0.5):
+    return lib.kvd_decode_attention_e4m3(q, k, v, out, past, B, H_q, H_kv, T_max, D, N, max_past, 0.0, k_scale,
+                                         v_scale, None, 0, None, None)
+
+
+def test_e4m3_argument_errors(lib):
+    assert _append8(lib, new_dtype=3) == 3              # new rows are fp32 / bf16 / fp16, not codes
+    assert _append8(lib, k=0) == 1
+    assert _append8(lib, k_scale=0.0) == 1              # scales: finite and positive
+    assert _append8(lib, v_scale=float("inf")) == 1
+    assert _append8(lib, k_scale=float("nan")) == 1
+    assert _append8(lib, D=8) == 3                      # 8 codes are not a whole 16-byte chunk
+    assert _append8(lib, kn=A + 4) == 1                 # misaligned
+    assert _append8(lib, max_past=60, N=5, T_max=64) == 2
+    assert _append8(lib, B=0) == 0
+    assert _attn8(lib, k_scale=-1.0) == 1
+    assert _attn8(lib, v_scale=float("nan")) == 1
+    assert _attn8(lib, q=A + 8) == 1
+    assert _attn8(lib, D=96) == 3
+    assert _attn8(lib, H_q=16, H_kv=1, N=65) == 3       # 1040 query rows per KV head
+    assert _attn8(lib, max_past=64, T_max=64) == 2
+    assert _attn8(lib, B=0) == 0
+    assert _attn(lib, dtype=3) == 3                     # an E4M3 cache only through the _e4m3 calls (scales)
+    assert lib.kvd_decode_step_e4m3(A, A, A, 0, A, A, A, 1, 4, 2, 64, 128, 1, 10, 0.0, 0.5, 0.5,
+                                    None, 0, None, None) == 1   # k_new missing
+    assert lib.kvd_decode_step_e4m3(A, A, A, A, A + 8, A, A, 1, 4, 2, 64, 128, 1, 10, 0.0, 0.5, 0.5,
+                                    None, 0, None, None) == 1   # v_new misaligned
+
+
+def test_decode_step_argument_errors(lib):
+    def step(kn=A, vn=A, **kw):
+        args = dict(q=A, k=A, v=A, out=A, past=A, B=1, H_q=4, H_kv=2, T_max=64, D=64, N=1, max_past=10, dtype=1)
+        args.update(kw)
+        return lib.kvd_decode_step(args["q"], args["k"], args["v"], kn, vn, args["out"], args["past"], args["B"],
+                                   args["H_q"], args["H_kv"], args["T_max"], args["D"], args["N"],
+                                   args["max_past"], 0.0, args["dtype"], None, 0, None, None)
+    assert step(kn=0) == 1
+    assert step(vn=A + 2) == 1
+    assert step(q=0) == 1
+    assert step(H_q=6, H_kv=4) == 1
+    assert step(D=80) == 3
+    assert step(max_past=60, N=5, T_max=64) == 2
+    assert step(B=0) == 0
