@@ -283,8 +283,8 @@ kvd_status kvd_paged_decode_step(const void *q, void *k_pages, void *v_pages, co
  * kvd_decode_step_e4m3 are kvd_decode_attention / kvd_decode_step over such a
  * cache (the fused step quantizes the new rows exactly as kvd_append_e4m3
  * does).  Workspace: kvd_decode_workspace_bytes(..., KVD_E4M3).  Query rows
- * per KV head are processed in blocks of 4 (D = 64) or 16 (D = 128, on the
- * tensor cores: kvd_plan_info.tensor_cores = 1).  Other arguments, errors
+ * per KV head are processed in blocks of at most 4 (D = 64) or of 16 (D = 128,
+ * on the tensor cores: kvd_plan_info.tensor_cores = 1).  Other arguments, errors
  * and device-side checks as for the bf16 calls; any other entry point given
  * KVD_E4M3 returns KVD_ERR_UNSUPPORTED, except kvd_append / kvd_paged_append,
  * which copy already-quantized rows bit for bit.
