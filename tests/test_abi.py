@@ -190,3 +190,14 @@ def test_decode_step_argument_errors(lib):
     assert step(D=80) == 3
     assert step(max_past=60, N=5, T_max=64) == 2
     assert step(B=0) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built CUDA library every entry point raises: there is no fallback path."""
+    from kv_cache_decode_append_gb300 import kvd
+    monkeypatch.setattr(kvd, "_loaded", None)
+    monkeypatch.setattr(kvd._build, "LIB_PATH", str(tmp_path / "libkvd.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        kvd.load()
+    with pytest.raises(RuntimeError, match="missing"):
+        kvd.raw.kvd_cache_bytes(1, 1, 1, 64, 1, 0)
