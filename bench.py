@@ -12,7 +12,15 @@ L2 size between timed steps, outside the per-step events.
 
 Metric: achieved HBM GB/s of algorithmic bytes (K/V read over P+N keys, Q
 read, O written, append read+write; workspace traffic excluded) and
-microseconds per layer-step.  Prints ONE JSON line on rank 0.
+microseconds per layer-step.  Prints ONE JSON line on rank 0.  Each timed step
+replays the step graph R times, R chosen so that the timed region spans at
+least --min-seconds (R = 1 when the L2 is flushed between steps), which gives
+the clock sampler tens of samples.  A single-GPU default run also times the
+other workloads (``per_config``: the GPT-2 Small cases, the chunked sweep
+N = 2, 4, 8, 16, the long-context caches with N = 8 and with an E4M3 cache),
+each with its own end-to-end time and the oracle's time on all host cores and
+on one; ``memory`` puts the allocator's counters next to the cache size
+formula.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -294,6 +302,21 @@ def time_oracle(w, host, past, budget_s: float = 10.0, max_reps: int = 64):
 
 
 # ---------------------------------------------------------------------------------
+def config_block(w: wl.Workload, past, world: int, layout: str = "contiguous", page_size: int = 64,
+                 page_order: str = "shuffled", cache: str = "same") -> dict:
+    """The workload keys shared by both arms' ``config`` (shapes, layout, cache type)."""
+    return {
+        "workload": w.name, "describe": w.describe(), "layers": w.L, "B": w.B, "H_q": w.H_q,
+        "H_kv": w.H_kv, "D": w.D, "N": w.N, "T_max": w.T_max,
+        "P": (w.P if w.P is not None else f"U[{w.P_range[0]},{w.P_range[1]}] seeded, sum {int(sum(past))}"),
+        "parallelism": f"replicas x{world}",
+        "cache_layout": (f"paged: {page_size}-token pages, {page_order} pool, block table"
+                         if layout == "paged" else "contiguous [B, H_kv, T_max, D]"),
+        "cache_dtype": (f"e4m3 (k_scale {E4M3_SCALES[0]}, v_scale {E4M3_SCALES[1]}; q, new K/V, out bf16)"
+                        if cache == "e4m3" else w.dtype),
+    }
+
+
 def run_reference(args, w, rank, world):
     """The reference arm: the CPU oracle, as it stands, one layer-step per step."""
     if rank != 0:
@@ -312,13 +335,18 @@ def run_reference(args, w, rank, world):
     el = time.perf_counter() - t0
     per_step = el / args.steps
     gbs = layer_bytes(w, past.tolist()) / per_step / 1e9
+    config = config_block(w, past.tolist(), world)
+    config["step"] = (f"one layer-step (append + decode attention, fp64) of the {w.L}-layer workload per "
+                      f"step, as a bounded sample; GB/s (algorithmic bytes / time) is the unit comparable "
+                      f"with the GPU arm, whose step is the whole layer stack")
+    config["l2"] = "host memory (CPU oracle)"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "describe": w.describe(),
-                   "step": "one layer-step (append + decode attention) of the workload"},
+        "config": config,
+        "us_per_layer_step": round(per_step * 1e6, 1),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": orc.max_threads(),
                          "kind": "oracle",
                          "sample": f"one layer of {w.name} (all {w.B} sequences) per step"},
@@ -327,204 +355,339 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_gpu(args, w, rank, world, local):
-    import kv_cache_decode_append_gb300 as kvd
+# ---------------------------------------------------------------------------------
+class Case:
+    """One workload on the device: every layer's inputs, caches, outputs and the
+    calls of one decode step, as the library's public API takes them."""
 
+    def __init__(self, w, dev, *, path="fused", layout="contiguous", cache="same", page_size=64,
+                 page_order="shuffled", reuse=None):
+        import kv_cache_decode_append_gb300 as kvd
+        self.kvd = kvd
+        self.w, self.dev = w, dev
+        self.fused = path == "fused"
+        self.paged = layout == "paged"
+        self.e4m3 = cache == "e4m3"
+        if self.e4m3 and (self.paged or w.dtype != "bf16"):
+            raise SystemExit("an E4M3 cache needs a bf16 workload and the contiguous layout")
+        self.cache_elem = 1 if self.e4m3 else 0
+        self.past = wl.past_lens(w)
+        self.max_past = int(self.past.max())
+        self.past_d = self.past.to(dev)
+        self.layers = []
+        for l in range(w.L):
+            if reuse is not None:  # another chunk size N over the same caches
+                x = wl.new_rows(w, l, device=dev)
+                for key in ("k_cache", "v_cache", "k_pages", "v_pages", "table"):
+                    if key in reuse.layers[l]:
+                        x[key] = reuse.layers[l][key]
+            else:
+                x = wl.layer_inputs(w, l, self.past, device=dev, tail_fill="zero")
+                if self.e4m3:  # the same data as E4M3 codes (torch's float8 cast of value / scale)
+                    for key, sc in zip(("k_cache", "v_cache"), E4M3_SCALES):
+                        x[key] = (x[key].float() / sc).to(torch.float8_e4m3fn).view(torch.uint8)
+                if self.paged:  # the same data as a page pool with a block table
+                    x["k_pages"], x["v_pages"], x["table"] = wl.to_paged(
+                        x.pop("k_cache"), x.pop("v_cache"), page_size, seed=l, fill=0.0,
+                        shuffle=page_order == "shuffled")
+            self.layers.append(x)
+        self.outs = [torch.empty_like(x["q"]) for x in self.layers]
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        plan_dtype = "e4m3" if self.e4m3 else w.torch_dtype
+        self.ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, self.max_past, plan_dtype, dev)
+        self.plan = kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, self.max_past, plan_dtype)
+        self.launches_per_layer = self.plan["launches"] + (0 if self.fused else 1)
+        self.step_bytes = w.L * layer_bytes(w, self.past.tolist(), self.cache_elem)
+
+    def layer_call(self, l, attention_only=False):
+        kvd, x, out, past_d, mp = self.kvd, self.layers[l], self.outs[l], self.past_d, self.max_past
+        ws, err = self.ws, self.err
+        if self.e4m3 and self.fused:
+            kvd.kvd_decode_step_e4m3(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], out, past_d,
+                                     mp, *E4M3_SCALES, 0.0, ws, err)
+        elif self.e4m3:
+            if not attention_only:
+                kvd.kvd_append_e4m3(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, mp,
+                                    *E4M3_SCALES, err)
+            kvd.kvd_decode_attention_e4m3(x["q"], x["k_cache"], x["v_cache"], out, past_d, mp, *E4M3_SCALES,
+                                          0.0, ws, err)
+        elif self.paged and self.fused:
+            kvd.kvd_paged_decode_step(x["q"], x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], out,
+                                      x["table"], past_d, mp, 0.0, ws, err)
+        elif self.paged:
+            if not attention_only:
+                kvd.kvd_paged_append(x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], x["table"], past_d,
+                                     mp, err)
+            kvd.kvd_paged_decode_attention(x["q"], x["k_pages"], x["v_pages"], out, x["table"], past_d, mp,
+                                           0.0, ws, err)
+        elif self.fused:
+            kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], out, past_d, mp,
+                                0.0, ws, err)
+        else:
+            if not attention_only:
+                kvd.kvd_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, mp, err)
+            kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], out, past_d, mp, 0.0, ws, err)
+
+    def step(self, attention_only=False):
+        for l in range(self.w.L):
+            self.layer_call(l, attention_only)
+
+    def check_err(self):
+        torch.cuda.synchronize()
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"{self.w.name}: device error word {int(self.err.item())}")
+
+    def graph(self, attention_only=False):
+        """The L calls of one step captured as one CUDA graph (launch overhead off the
+        critical path; programmatic launches keep their early start inside it)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(attention_only)
+        return g
+
+    def e2e(self, steps, warmup, world):
+        """The same step through the public API with its inputs copied in from pinned
+        host memory and every layer's output read back, every step (eager calls)."""
+        w, stream = self.w, torch.cuda.current_stream()
+        host_in = [{k: self.layers[l][k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
+                   for l in range(w.L)]
+        host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.outs]
+        past_h = self.past.pin_memory()
+        h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values()) + past_h.numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def one():
+            self.past_d.copy_(past_h, non_blocking=True)
+            for l in range(w.L):
+                for key in ("q", "k_new", "v_new"):
+                    self.layers[l][key].copy_(host_in[l][key], non_blocking=True)
+                self.layer_call(l)
+                host_out[l].copy_(self.outs[l], non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(max(1, warmup)):
+            one()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        el = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+        return {"value": round(whole_job_gbs(self.step_bytes, steps, el, world), 2), "unit": "GB/s",
+                "ms_per_step": round(el / steps * 1e3, 4), "us_per_layer_step": round(el / steps / w.L * 1e6, 3),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "timing": f"{steps} eager steps, CUDA events on the stream"}
+
+
+class Timer:
+    """CUDA-event timing of graph replays on the capturing stream.  A workload whose
+    step reads less than twice the L2 gets a write of twice the L2 size before each
+    timed step, outside its events, so every step starts from a cold L2."""
+
+    def __init__(self, dev):
+        self.stream = torch.cuda.current_stream()
+        self.l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_FALLBACK_BYTES)
+        self.scratch = torch.empty(2 * self.l2_bytes // 4, dtype=torch.int32, device=dev)
+
+    def needs_flush(self, step_bytes):
+        return step_bytes <= 2 * self.l2_bytes
+
+    def time(self, graph, steps, replays, flush):
+        """Seconds of steps x replays graph replays (the sum over per-step windows
+        when flushing; then replays is 1)."""
+        if not flush:
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(self.stream)
+            for _ in range(steps * replays):
+                graph.replay()
+            t1.record(self.stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / 1e3
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i, (t0, t1) in enumerate(evs):
+            self.scratch.fill_(i)
+            t0.record(self.stream)
+            graph.replay()
+            t1.record(self.stream)
+        torch.cuda.synchronize()
+        return sum(t0.elapsed_time(t1) for t0, t1 in evs) / 1e3
+
+
+def oracle_times(case, cores_all: int, reps_all: int = 1, reps_one: int = 1):
+    """The oracle on layer 0 of a case: ms per layer-step on all host cores and on one."""
+    import oracle
+    orc = oracle.load()
+    host = {k: to_host_np(v) for k, v in case.layers[0].items()}
+    past_np = case.past.numpy()
+    out = {}
+    for label, cores, reps in (("all_cores", cores_all, reps_all), ("one_core", 1, reps_one)):
+        if reps < 1:
+            continue
+        orc.set_threads(cores)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle_layer_step(orc, host, past_np, case.w.dtype)
+        out[label] = {"ms_per_layer_step": round((time.perf_counter() - t0) / reps * 1e3, 3), "cores": cores,
+                      "reps": reps}
+    orc.set_threads(cores_all)
+    return out
+
+
+def per_config_line(case, timer, steps, world, label, cores_all, with_oracle=True):
+    """Throughput of one more workload (a graph of its L-layer step, timed like the
+    headline), its end-to-end time and the oracle's time on its layer 0."""
+    w = case.w
+    for _ in range(3):
+        case.step()
+    case.check_err()
+    g = case.graph()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    flush = timer.needs_flush(case.step_bytes)
+    n = max(steps, 20)
+    el = max_over_ranks(timer.time(g, n, 1, flush), world)
+    case.check_err()
+    peak, _ = measured_peak()
+    gbs = whole_job_gbs(case.step_bytes, n, el, world)
+    line = {
+        "workload": w.name, "N": w.N, "label": label, "path": "fused" if case.fused else "separate",
+        "us_per_layer_step": round(el / n / w.L * 1e6, 3), "gbs": round(gbs, 2),
+        "frac": round(gbs / world / peak, 4), "step_bytes": case.step_bytes,
+        "l2": "flushed before each step" if flush else "not flushed (step larger than twice the L2)",
+        "steps": n,
+        "plan": {k: case.plan[k] for k in ("grid", "tensor_cores", "launches", "l2_prefetch", "rows_per_block")},
+        "e2e": case.e2e(max(3, steps // 4), 2, world),
+    }
+    if with_oracle:
+        line["oracle"] = oracle_times(case, cores_all)
+    del g
+    return line
+
+
+def memory_report(case, ws_bytes):
+    w = case.w
+    s = 1 if case.e4m3 else w.elem_bytes
+    return {
+        "kv_cache_bytes_preallocated": case.kvd.kvd_cache_bytes(w.L, w.B, w.H_kv, w.D, w.T_max,
+                                                                 "e4m3" if case.e4m3 else w.torch_dtype),
+        "kv_cache_bytes_in_use": 2 * w.L * w.H_kv * w.D * s * sum(int(p) + w.N for p in case.past.tolist()),
+        "workspace_bytes": ws_bytes,
+        "torch_memory_allocated": torch.cuda.memory_allocated(),
+        "torch_memory_reserved": torch.cuda.memory_reserved(),
+        "torch_max_memory_allocated": torch.cuda.max_memory_allocated(),
+        "note": "torch counters taken after the timed region (peak since the caches were allocated)",
+    }
+
+
+def run_gpu(args, w, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
-    past = wl.past_lens(w)
-    max_past = int(past.max())
-    past_d = past.to(dev)
-    paged = args.layout == "paged"
-    e4m3 = args.cache == "e4m3"
-    if e4m3 and (paged or w.dtype != "bf16"):
-        raise SystemExit("--cache e4m3 needs a bf16 workload and the contiguous layout")
-    cache_elem = 1 if e4m3 else 0
-    layers = []
-    for l in range(w.L):
-        x = wl.layer_inputs(w, l, past, device=dev, tail_fill="zero")
-        if e4m3:  # the same data as E4M3 codes (torch's float8 cast of value / scale)
-            for key, sc in zip(("k_cache", "v_cache"), E4M3_SCALES):
-                x[key] = (x[key].float() / sc).to(torch.float8_e4m3fn).view(torch.uint8)
-        if paged:  # the same data as a shuffled page pool with a block table
-            x["k_pages"], x["v_pages"], x["table"] = wl.to_paged(
-                x.pop("k_cache"), x.pop("v_cache"), args.page_size, seed=l, fill=0.0,
-                shuffle=args.page_order == "shuffled")
-        layers.append(x)
-    outs = [torch.empty_like(x["q"]) for x in layers]
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    plan_dtype = "e4m3" if e4m3 else w.torch_dtype
-    ws = kvd.alloc_workspace(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, plan_dtype, dev)
-    plan = kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max_past, plan_dtype)
-    merge = plan["launches"] == 2
-    launches_per_layer = plan["launches"] + (0 if args.path == "fused" else 1)
-
-    fused = args.path == "fused"
-
-    def layer_step(l):
-        x = layers[l]
-        # the current stream: the capture stream inside torch.cuda.graph
-        if e4m3 and fused:
-            kvd.kvd_decode_step_e4m3(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l], past_d,
-                                     max_past, *E4M3_SCALES, 0.0, ws, err)
-        elif e4m3:
-            kvd.kvd_append_e4m3(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past,
-                                *E4M3_SCALES, err)
-            kvd.kvd_decode_attention_e4m3(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past,
-                                          *E4M3_SCALES, 0.0, ws, err)
-        elif paged and fused:
-            kvd.kvd_paged_decode_step(x["q"], x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], outs[l],
-                                      x["table"], past_d, max_past, 0.0, ws, err)
-        elif paged:
-            kvd.kvd_paged_append(x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], x["table"], past_d,
-                                 max_past, err)
-            kvd.kvd_paged_decode_attention(x["q"], x["k_pages"], x["v_pages"], outs[l], x["table"], past_d,
-                                           max_past, 0.0, ws, err)
-        elif fused:
-            kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l], past_d,
-                                max_past, 0.0, ws, err)
-        else:
-            kvd.kvd_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, max_past, err)
-            kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past, 0.0, ws,
-                                     err)
-
-    def step():
-        for l in range(w.L):
-            layer_step(l)
-
-    # warm-up (also builds nothing: the library is loaded on the first call)
+    torch.cuda.reset_peak_memory_stats(dev)
+    case = Case(w, dev, path=args.path, layout=args.layout, cache=args.cache, page_size=args.page_size,
+                page_order=args.page_order)
     for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item())}")
+        case.step()
+    case.check_err()
 
     sampler = ClockSampler(gpu_smi_id(dev))
     if rank == 0:
         sampler.start()
         time.sleep(0.2)
 
-    # The step is captured once as a CUDA graph (launch overhead off the
-    # critical path); a second graph holds only the L attention calls, for
-    # the roofline of the attention kernel.
-    step_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(step_graph):
-        step()
-    attn_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(attn_graph):
-        for l in range(w.L):
-            x = layers[l]
-            if e4m3 and fused:
-                kvd.kvd_decode_step_e4m3(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l],
-                                         past_d, max_past, *E4M3_SCALES, 0.0, ws, err)
-            elif e4m3:
-                kvd.kvd_decode_attention_e4m3(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past,
-                                              *E4M3_SCALES, 0.0, ws, err)
-            elif paged and fused:
-                kvd.kvd_paged_decode_step(x["q"], x["k_pages"], x["v_pages"], x["k_new"], x["v_new"], outs[l],
-                                          x["table"], past_d, max_past, 0.0, ws, err)
-            elif paged:
-                kvd.kvd_paged_decode_attention(x["q"], x["k_pages"], x["v_pages"], outs[l], x["table"], past_d,
-                                               max_past, 0.0, ws, err)
-            elif fused:  # the dominant kernel is the fused step itself
-                kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], outs[l],
-                                    past_d, max_past, 0.0, ws, err)
-            else:
-                kvd.kvd_decode_attention(x["q"], x["k_cache"], x["v_cache"], outs[l], past_d, max_past, 0.0,
-                                         ws, err)
-    graph_stream = torch.cuda.current_stream()
+    # The step is captured once as a CUDA graph; a second graph holds only the
+    # attention calls (the fused step itself when fused), for the roofline.
+    step_graph = case.graph()
+    attn_graph = case.graph(attention_only=True)
     for _ in range(2):
         step_graph.replay()
         attn_graph.replay()
     torch.cuda.synchronize()
+    timer = Timer(dev)
+    flush = timer.needs_flush(case.step_bytes)
 
-    # A step that reads less than twice the L2 would find its inputs there on
-    # the next step: then every timed step gets its own events, with a write
-    # of twice the L2 size between steps (outside the events).
-    step_bytes = w.L * layer_bytes(w, past.tolist(), cache_elem)
-    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_FALLBACK_BYTES)
-    flush = step_bytes <= 2 * l2_bytes
-    scratch = torch.empty(2 * l2_bytes // 4, dtype=torch.int32, device=dev) if flush else None
+    # Each timed step replays the step graph R times (R = 1 with an L2 flush), R
+    # chosen so that the timed region spans at least --min-seconds.
+    replays = 1
+    if not flush:
+        probe = timer.time(step_graph, 3, 1, False) / 3
+        replays = max(1, int(-(-args.min_seconds // max(probe * args.steps, 1e-9))))
 
-    def replay_timed(graph) -> float:
-        """Seconds of args.steps replays of graph, on its stream."""
-        if not flush:
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0.record(graph_stream)
-            for _ in range(args.steps):
-                graph.replay()
-            t1.record(graph_stream)
-            torch.cuda.synchronize()
-            return t0.elapsed_time(t1) / 1e3
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for i, (t0, t1) in enumerate(evs):
-            scratch.fill_(i)
-            t0.record(graph_stream)
-            graph.replay()
-            t1.record(graph_stream)
-        torch.cuda.synchronize()
-        return sum(t0.elapsed_time(t1) for t0, t1 in evs) / 1e3
-
-    # timed region: K steps
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    elapsed = replay_timed(step_graph)
+    elapsed = timer.time(step_graph, args.steps, replays, flush)
     t_wall1 = time.time()
     barrier(world)
     elapsed_max = max_over_ranks(elapsed, world)
+    passes = args.steps * replays
+    attn_per_launch = timer.time(attn_graph, args.steps, replays, flush) / (passes * w.L)
+    case.check_err()
+    mem = memory_report(case, case.ws.numel() if case.ws is not None else 0)
+    e2e = case.e2e(max(1, args.steps // 2), max(1, args.warmup // 2), world)
+    clocks = sampler.summary(t_wall0, t_wall1)
 
-    # attention kernel alone, same number of launches
-    attn_per_launch = replay_timed(attn_graph) / (args.steps * w.L)
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item())}")
-
-    # end to end: inputs from pinned host memory each step, result read back each step
-    host_in = [{k: layers[l][k].cpu().pin_memory() for k in ("q", "k_new", "v_new")} for l in range(w.L)]
-    host_out = [torch.empty(outs[l].shape, dtype=outs[l].dtype).pin_memory() for l in range(w.L)]
-    past_h = past.pin_memory()
-    h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values()) + past_h.numel() * 4
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
-
-    def e2e_step():
-        past_d.copy_(past_h, non_blocking=True)
-        for l in range(w.L):
-            for key in ("q", "k_new", "v_new"):
-                layers[l][key].copy_(host_in[l][key], non_blocking=True)
-            layer_step(l)
-            host_out[l].copy_(outs[l], non_blocking=True)
-        stream.synchronize()
-
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
-    barrier(world)
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_steps = max(1, args.steps // 2)
-    e_start.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e_end.record(stream)
-    torch.cuda.synchronize()
-    e2e_el = max_over_ranks(e_start.elapsed_time(e_end) / 1e3, world)
+    # More workloads on the same device: the other configurations, the chunked
+    # sweep and the long-context variants (rank 0 of a single-GPU run only).
+    per_config = []
+    cores_all = None
+    if rank == 0:
+        import oracle
+        cores_all = oracle.load().max_threads()
+    if args.per_config == "on" or (args.per_config == "auto" and world == 1 and w.name == DEFAULT_WORKLOAD
+                                   and args.n_new is None and args.layout == "contiguous" and args.cache == "same"):
+        del step_graph, attn_graph
+        torch.cuda.synchronize()
+        specs = [("gpt2s_1layer_p16_f32", None, {}), ("gpt2s_12layer_p1000_f32", None, {})]
+        specs += [("gpt2s_chunked_p512_f32", n, {}) for n in wl.CHUNKED_N]
+        specs += [("gpt2s_b8_p1023_bf16", None, {}), ("gpt2s_b8_p1023_bf16", None, {"layout": "paged"})]
+        for name, n, opts in specs:
+            wc = wl.WORKLOADS[name] if n is None else wl.with_n(wl.WORKLOADS[name], n)
+            c = Case(wc, dev, **opts)
+            label = wc.describe() + (" (paged)" if opts else "")
+            per_config.append(per_config_line(c, timer, args.steps, world, label, cores_all,
+                                              with_oracle=rank == 0 and not opts))
+            del c
+            torch.cuda.empty_cache()
+        for n in (8,):  # the chunked decode over the long-context caches: tcgen05, 32 rows per KV head
+            c = Case(wl.with_n(w, n), dev, reuse=case)
+            per_config.append(per_config_line(c, timer, args.steps, world, f"{w.name} N={n} (same caches)",
+                                              cores_all, with_oracle=False))
+            del c
+        c = Case(w, dev, cache="e4m3")
+        per_config.append(per_config_line(c, timer, args.steps, world, f"{w.name} with an E4M3 cache",
+                                          cores_all, with_oracle=False))
+        del c
+        torch.cuda.empty_cache()
+    t_wall2 = time.time()
     if rank == 0:
         sampler.stop()
-
     if rank != 0:
         return
-    bytes_step = w.L * layer_bytes(w, past.tolist(), cache_elem)
-    gbs = whole_job_gbs(bytes_step, args.steps, elapsed_max, world)
-    ms_step = elapsed_max / args.steps * 1e3
+
     peak, peak_kind = measured_peak()
-    a_bytes = layer_bytes(w, past.tolist(), cache_elem) if fused else attn_bytes(w, past.tolist(), cache_elem)
+    gbs = whole_job_gbs(case.step_bytes, passes, elapsed_max, world)
+    ms_step = elapsed_max / args.steps * 1e3
+    lb = layer_bytes(w, case.past.tolist(), case.cache_elem)
+    a_bytes = lb if case.fused else attn_bytes(w, case.past.tolist(), case.cache_elem)
     achieved = a_bytes / attn_per_launch / 1e9
 
-    # CPU baseline: the oracle on layer 0's data, all host cores, ~10 s
-    host = {k: to_host_np(v) for k, v in layers[0].items()}
-    reps, cpu_el, cores = time_oracle(w, host, past, budget_s=args.cpu_seconds)
-    cpu_gbs = reps * layer_bytes(w, past.tolist(), cache_elem) / cpu_el / 1e9
+    # CPU baseline: the oracle on layer 0's data, all host cores (~cpu_seconds), and once on one core
+    host = {k: to_host_np(v) for k, v in case.layers[0].items()}
+    reps, cpu_el, cores = time_oracle(w, host, case.past, budget_s=args.cpu_seconds)
+    cpu_gbs = reps * lb / cpu_el / 1e9
+    one = oracle_times(case, cores, reps_all=0, reps_one=1)["one_core"] if args.cpu_one_core else None
 
+    config = config_block(w, case.past.tolist(), world, args.layout, args.page_size, args.page_order, args.cache)
+    config["step"] = ((f"{replays} replay(s) of one CUDA graph of " if replays > 1 else "one CUDA graph of ") +
+                      (f"{w.L} x kvd_decode_step (append + attention in one launch)" if case.fused else
+                       f"{w.L} x (kvd_append + kvd_decode_attention)") + " on one stream")
+    config["l2"] = ((f"flushed: {2 * timer.l2_bytes / 1e6:.0f} MB written before each timed step, outside its "
+                     f"events ({case.step_bytes / 1e6:.1f} MB per step; e2e not flushed)") if flush else
+                    f"no flush: inputs larger than L2 ({case.step_bytes / 1e9:.1f} GB per pass of the layers)")
     line = {
         "metric": METRIC,
         "value": round(gbs, 2),
@@ -538,51 +701,40 @@ def run_gpu(args, w, rank, world, local):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic",
-        "config": {
-            "workload": w.name, "describe": w.describe(), "layers": w.L, "B": w.B, "H_q": w.H_q,
-            "H_kv": w.H_kv, "D": w.D, "N": w.N, "T_max": w.T_max,
-            "P": (w.P if w.P is not None else f"U[{w.P_range[0]},{w.P_range[1]}] seeded, sum {int(past.sum())}"),
-            "step": (f"{w.L} x kvd_decode_step (append + attention in one launch)" if fused else
-                     f"{w.L} x (kvd_append + kvd_decode_attention)") + " on one stream, one CUDA graph per step",
-            "l2": (f"flushed: {2 * l2_bytes / 1e6:.0f} MB written between timed steps, outside their events "
-                   f"({bytes_step / 1e6:.1f} MB per step; e2e not flushed)") if flush else
-                  f"no flush: inputs larger than L2 ({bytes_step / 1e9:.1f} GB per step)",
-            "parallelism": f"replicas x{world}",
-            "cache_layout": (f"paged: {args.page_size}-token pages, {args.page_order} pool, block table"
-                             if paged else "contiguous [B, H_kv, T_max, D]"),
-            "cache_dtype": (f"e4m3 (k_scale {E4M3_SCALES[0]}, v_scale {E4M3_SCALES[1]}; q, new K/V, out bf16)"
-                            if e4m3 else w.dtype),
-        },
-        "us_per_layer_step": round(ms_step * 1e3 / w.L, 3),
+        "config": config,
+        "replays_per_step": replays,
+        "timed_seconds": round(elapsed_max, 3),
+        "us_per_layer_step": round(elapsed_max / passes / w.L * 1e6, 3),
         "frac_of_peak": round(gbs / world / peak, 4),
         "attn_us_per_layer": round(attn_per_launch * 1e6, 3),
         "path": args.path,
         "roofline": {
             "bound": "hbm",
-            "kernel": ("kvd_decode_step (fused append + split-T attention" if fused else
-                       "kvd_decode_attention (split-T attention") + (" + LSE merge)" if merge else ")"),
-            "timing": "graph of the L calls replayed K times, CUDA events on its stream",
+            "kernel": ("kvd_decode_step (fused append + split-T attention" if case.fused else
+                       "kvd_decode_attention (split-T attention") + (" + LSE merge)" if case.plan["launches"] == 2 else ")"),
+            "timing": "graph of the L calls replayed, CUDA events on its stream",
             "achieved": round(achieved, 2),
             "peak": peak,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy burst)" if peak_kind == "measured" else "fallback",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "algorithmic_bytes_per_launch": a_bytes,
-            "plan": plan,
-            "traffic": None if (paged or e4m3) else profiled_traffic(),
+            "plan": case.plan,
+            "traffic": None if (case.paged or case.e4m3) else profiled_traffic(),
         },
         "cpu_baseline": {
             "value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"layer 0 of {w.name} (all {w.B} sequences, append + attention, fp64), "
                       f"repeated {reps}x in {cpu_el:.1f} s",
+            "ms_per_layer_step": round(cpu_el / reps * 1e3, 3),
+            "one_core": one,
         },
-        "e2e": {
-            "value": round(whole_job_gbs(bytes_step, e_steps, e2e_el, world), 2), "unit": "GB/s",
-            "ms_per_step": round(e2e_el / e_steps * 1e3, 4),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-        },
-        "gpu_launches": args.steps * w.L * launches_per_layer,
-        "clocks": sampler.summary(t_wall0, t_wall1),
+        "e2e": e2e,
+        "memory": mem,
+        "gpu_launches": passes * w.L * case.launches_per_layer,
+        "clocks": clocks,
+        "clocks_whole_run": sampler.summary(t_wall0, t_wall2),
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
 
@@ -605,6 +757,13 @@ def main():
                     help="cache element type: the workload's, or E4M3 codes (bf16 workloads)")
     ap.add_argument("--page-order", default="shuffled", choices=["shuffled", "sequential"],
                     help="physical page order of the pool for --layout paged")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="each timed step replays the step graph often enough that the timed region "
+                         "spans at least this long (workloads larger than twice the L2)")
+    ap.add_argument("--per-config", default="auto", choices=["auto", "on", "off"],
+                    help="also time the other workloads (auto: single-GPU default runs)")
+    ap.add_argument("--no-cpu-one-core", dest="cpu_one_core", action="store_false",
+                    help="skip the one-core oracle time")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -155,6 +155,35 @@ kvd_status kvd_decode_step(const void *q, void *k_cache, void *v_cache, const vo
                            uint32_t *err_word, void *stream);
 
 /*
+ * kvd_decode_step_flags -- kvd_decode_step with caller guarantees that let
+ * the kernel start its reads before the work queued ahead of it on `stream`
+ * has finished.  No counterpart in the source pages: the pages time the
+ * cached decode step and name launch and scheduling overhead as what remains
+ * of its cost ("GPT-2缓存实测：千倍计算只快6倍", section
+ * "千倍计算量为何只换来6倍速度"; "7.1 自回归生成过程", section "Decode 阶段");
+ * this call lets a layer's cache reads overlap that overhead.
+ *
+ * flags (bitwise OR; any other bit returns KVD_ERR_INVALID_ARG):
+ *   KVD_STEP_HISTORY_STABLE -- no work queued on `stream` before this call
+ *     writes past_len or the cache rows below past_len[b] (the history).
+ *     Typical in a model: the kernels ahead of a layer's step write q, k_new
+ *     and v_new (and other layers' caches), and past_len advances once per
+ *     token after the last layer.  For a small layer (kvd_plan_info.l2_prefetch
+ *     = 1) on a contiguous cache the kernel then reads past_len and loads its
+ *     first K/V tiles before it waits for the previous kernel; q, k_new,
+ *     v_new, the workspace and every write still wait.  Elsewhere the flag is
+ *     accepted and changes nothing.  Breaking the guarantee gives wrong results
+ *     (the history may be read before it is written); nothing is checked.
+ * Everything else, including the result bit for bit, is kvd_decode_step's.
+ */
+#define KVD_STEP_HISTORY_STABLE 1u
+kvd_status kvd_decode_step_flags(const void *q, void *k_cache, void *v_cache, const void *k_new,
+                                 const void *v_new, void *out, const int32_t *past_len, int B, int H_q,
+                                 int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                                 kvd_dtype dtype, uint32_t flags, void *workspace, size_t workspace_bytes,
+                                 uint32_t *err_word, void *stream);
+
+/*
  * kvd_decode_plan -- how kvd_decode_attention would run these shapes on the
  * current device, without launching anything: keys per tile, the most tiles
  * one sequence-head can have (from max_past_len + N), the persistent grid
@@ -180,6 +209,16 @@ typedef struct kvd_plan_info {
                             1: the mma.sync tensor-core kernel (bf16 / fp16 caches with
                             4 .. 16 rows for D = 128, 8 .. 16 for D = 64; E4M3 caches
                             with D = 128); 0: the CUDA-core kernel */
+    int l2_prefetch;     /* 1: a small layer (K/V of at most 26 MiB at max_past_len, on the
+                            CUDA-core kernel): one CTA per SM, and each CTA prefetches its
+                            rows into L2 and lets the next kernel on the stream launch
+                            before it waits for the previous one, so consecutive calls
+                            overlap their HBM reads with each other's prologue and tail */
+    int cluster;         /* > 0: of those, a contiguous layer whose longest head fits in a few
+                            ring fills runs as one thread-block cluster of `cluster` CTAs per
+                            (b, h_kv, row block): each CTA loads its equal share of the head's
+                            keys at once and the shares merge through distributed shared
+                            memory (the workspace is then unused) */
 } kvd_plan_info;
 
 kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len,
@@ -199,15 +238,18 @@ kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_
  * until the process exits).  The function allocates nothing and calls no
  * allocating routine.
  *
- *   - Shapes whose kvd_decode_workspace_bytes exceeds 4 MiB are rejected with
- *     KVD_ERR_WORKSPACE before anything is launched.
+ *   - Invalid arguments return their status, and shapes whose
+ *     kvd_decode_workspace_bytes exceeds 4 MiB return KVD_ERR_WORKSPACE,
+ *     before anything is queued on `stream`.
  *   - The first call on each device looks up that device's scratch address
- *     (cudaGetSymbolAddress, with the device current); make that first call
- *     before any stream capture on the device.
+ *     (cudaGetSymbolAddress, with the device current) and keeps it; make that
+ *     first call before any stream capture on the device, and do not use this
+ *     entry point on a device after cudaDeviceReset.
  *   - All calls on a device share the one scratch array: calls whose GPU work
  *     can overlap (unordered streams) race and give undefined results.
  *   - The scratch keeps the previous call's contents; each call clears the
- *     part that must start at zero (its merge counters) before it launches.
+ *     part that must start at zero (its merge counters, a few bytes per
+ *     sequence-head) with cudaMemsetAsync on `stream` before it launches.
  */
 kvd_status kvd_decode_attention_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                         void *out, const int32_t *past_len, int B, int H_q,

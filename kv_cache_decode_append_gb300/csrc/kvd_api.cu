@@ -175,6 +175,30 @@ constexpr int kMmaMinRowsE4m3 = 1;
 // kernel (128-row blocks: every K/V tile read once for all rows), where the
 // 16-row mma.sync blocks would read each tile once per block.
 constexpr int kTc5MinRows = 17;
+// Small layers (K/V bytes of one call, counted at max_past_len, at most
+// kL2PrefetchMaxBytes, a fifth of GB300's L2) run on the CUDA-core kernel with
+// kArgL2Prefetch and kL2PrefetchCtasPerSm CTAs per SM: each layer then
+// occupies part of every SM, so the next calls' CTAs become resident early,
+// prefetch their rows into L2 and wait, and the stream of consecutive layers
+// keeps HBM busy through each layer's prologue and merge tail.
+#ifndef KVD_L2_PREFETCH_CTAS_PER_SM
+#define KVD_L2_PREFETCH_CTAS_PER_SM 2
+#endif
+constexpr int kL2PrefetchCtasPerSm = KVD_L2_PREFETCH_CTAS_PER_SM;
+#ifndef KVD_L2_PREFETCH_MAX_BYTES
+#define KVD_L2_PREFETCH_MAX_BYTES (26LL << 20)
+#endif
+constexpr long long kL2PrefetchMaxBytes = KVD_L2_PREFETCH_MAX_BYTES;
+// Small contiguous layers whose longest head needs at most kMaxCluster ring
+// fills run in cluster mode: one thread-block cluster of C CTAs per
+// sequence-head, C = tiles of the longest head / ring stages (rounded up), so
+// that every CTA loads its whole share of the head at once (before the wait,
+// with a stable history) and the pieces merge through distributed shared
+// memory.  (8: the portable cluster size.)
+#ifndef KVD_MAX_CLUSTER
+#define KVD_MAX_CLUSTER 8
+#endif
+constexpr int kMaxCluster = KVD_MAX_CLUSTER;
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link to the
 // driver library).
@@ -268,6 +292,50 @@ kvd_status occupancy(int dev, const void *fn, int threads, int smem, int *ctas_p
     return KVD_OK;
 }
 
+// Whether clusters of `c` CTAs of `fn` (threads, smem) can be resident at
+// all (cudaOccupancyMaxActiveClusters > 0), cached per device.
+struct ClusterEntry {
+    int device;
+    const void *fn;
+    int smem, c;
+    bool ok;
+};
+ClusterEntry g_cl[64];
+int g_cl_n = 0;
+
+kvd_status cluster_fits(int dev, const void *fn, int threads, int smem, int c, bool *ok)
+{
+    int dummy = 0;
+    kvd_status st = occupancy(dev, fn, threads, smem, &dummy);  // (opts the kernel into large shared memory)
+    if (st != KVD_OK) return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int k = 0; k < g_cl_n; ++k) {
+        if (g_cl[k].device == dev && g_cl[k].fn == fn && g_cl[k].smem == smem && g_cl[k].c == c) {
+            *ok = g_cl[k].ok;
+            return KVD_OK;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)c);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    if (g_cl_n < 64) g_cl[g_cl_n++] = ClusterEntry{dev, fn, smem, c, n > 0};
+    *ok = n > 0;
+    return KVD_OK;
+}
+
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int elem_bytes(kvd_dtype dt)
@@ -291,6 +359,8 @@ struct Plan {
     bool merge_pass;  // split heads merged by a second launch (else inside the kernel)
     bool mma;         // tensor-core kernel (16-row blocks, tiles by tensor map)
     bool tc5;         // tcgen05 kernel (128-row blocks, tiles and q by tensor map)
+    bool l2_prefetch; // small layer: kArgL2Prefetch, fewer CTAs per SM
+    int cluster;      // > 0: cluster mode with this many CTAs per sequence-head
     size_t part_off, tickets_off, seg_off, ws_bytes;
 };
 
@@ -398,7 +468,11 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     if ((st = min_occupancy(dev, op, ot, pl->smem, &occ_other)) != KVD_OK) return st;
 
     // One CTA per resident slot; each takes an equal share of all tiles.
-    pl->grid = sms * occ;
+    // Small layers leave room on every SM for the calls that follow.
+    const long long kv_bytes_hint =
+        2LL * B * H_kv * ((long long)max_past_len + N) * D * elem_bytes(dtype);
+    pl->l2_prefetch = !pl->mma && !pl->tc5 && kv_bytes_hint <= kL2PrefetchMaxBytes;
+    pl->grid = sms * (pl->l2_prefetch && occ > kL2PrefetchCtasPerSm ? kL2PrefetchCtasPerSm : occ);
     const long long t_hint = (long long)max_past_len + N;
     pl->max_tiles = (int)((t_hint + pl->v.tile_keys - 1) / pl->v.tile_keys);
     // Heads split across CTAs: merged inside the kernel by the CTA that
@@ -408,9 +482,26 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     // tail of the last CTA.
     const long long units_hint =
         (long long)B * H_kv * pl->n_rowblocks * (pl->max_tiles + pl->v.piece_units);
-    pl->merge_pass = units_hint > (long long)kLongRangeUnits * pl->grid;
+    pl->merge_pass = !pl->l2_prefetch && units_hint > (long long)kLongRangeUnits * pl->grid;
     pl->launches = pl->merge_pass ? 2 : 1;
     if (!pl->merge_pass) pl->v = vt;
+    pl->cluster = 0;
+    if (pl->l2_prefetch && !paged && pl->v.cluster_fn != nullptr && pl->v.stages > 0) {
+        const int c = (pl->max_tiles + pl->v.stages - 1) / pl->v.stages;
+        const long long ctas = (long long)B * H_kv * pl->n_rowblocks * c;
+        bool fits = false;
+        if (c >= 2 && c <= kMaxCluster && ctas <= 8LL * sms) {
+            if ((st = cluster_fits(dev, pl->v.cluster_fn, pl->v.threads, pl->smem, c, &fits)) != KVD_OK) return st;
+            bool fits2 = false;
+            if (fits && (st = cluster_fits(dev, pl->v.cluster_fused_fn, pl->v.threads, pl->smem, c, &fits2)) != KVD_OK)
+                return st;
+            fits = fits && fits2;
+        }
+        if (fits) {
+            pl->cluster = c;
+            pl->grid = (int)ctas;
+        }
+    }
 
     // (partial slots of the tensor-core kernels hold only a block's real rows)
     const int part_rows = (pl->mma || pl->tc5) && pl->rows < pl->rb ? pl->rows : pl->rb;
@@ -500,6 +591,8 @@ kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_
     info->workspace_bytes = pl.ws_bytes;
     info->rows_per_block = pl.rb;
     info->tensor_cores = pl.tc5 ? 2 : pl.mma ? 1 : 0;
+    info->l2_prefetch = pl.l2_prefetch ? 1 : 0;
+    info->cluster = pl.cluster;
     return KVD_OK;
 }
 
@@ -529,11 +622,46 @@ kvd_status check_paged(const PagedCache &pc, int *T_max, int *page_shift)
     return KVD_OK;
 }
 
+}  // namespace
+
+// Host checks of a kvd_decode_attention call (contiguous cache, no E4M3) and
+// the workspace it needs, without launching anything: the bytes, and the
+// region [*zero_off, *zero_off + *zero_bytes) that must be zero when the
+// kernel starts (the merge counters; every complete call leaves them zero).
+// For the entry point whose workspace is built into the library.
+namespace kvd {
+kvd_status decode_attention_prepare(const void *q, const void *k_cache, const void *v_cache, const void *out,
+                                    const int32_t *past_len, int B, int H_q, int H_kv, int T_max, int D, int N,
+                                    int max_past_len, kvd_dtype dtype, size_t *ws_bytes, size_t *zero_off,
+                                    size_t *zero_bytes)
+{
+    *ws_bytes = *zero_off = *zero_bytes = 0;
+    if (!q || !k_cache || !v_cache || !out || !past_len) return KVD_ERR_INVALID_ARG;
+    kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
+    if (st != KVD_OK) return st;
+    if (dtype == KVD_E4M3) return KVD_ERR_UNSUPPORTED;
+    if (T_max < 1) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return KVD_ERR_INVALID_ARG;
+    if ((long long)max_past_len + N > T_max) return KVD_ERR_CAPACITY;
+    if (B == 0) return KVD_OK;
+    Plan pl;
+    if ((st = make_plan(B, H_q, H_kv, D, N, max_past_len, dtype, &pl)) != KVD_OK) return st;
+    *ws_bytes = pl.ws_bytes;
+    *zero_off = pl.tickets_off;
+    *zero_bytes = pl.seg_off - pl.tickets_off;
+    return KVD_OK;
+}
+}  // namespace kvd
+
+namespace {
+
 kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache, const void *k_new,
                          const void *v_new, void *out, const int32_t *past_len, int B, int H_q, int H_kv,
                          int T_max, int D, int N, int max_past_len, float scale, kvd_dtype dtype,
                          void *workspace, size_t workspace_bytes, uint32_t *err_word, void *stream,
-                         const PagedCache *paged = nullptr, const float *e4m3_scales = nullptr)
+                         const PagedCache *paged = nullptr, const float *e4m3_scales = nullptr,
+                         uint32_t step_flags = 0u)
 {
     if (!q || !k_cache || !v_cache || !out || !past_len) return KVD_ERR_INVALID_ARG;
     kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
@@ -575,7 +703,12 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     else
         a.block_table = paged != nullptr ? paged->block_table : nullptr;
     a.num_pages = paged != nullptr ? paged->num_pages : 0;
-    a.page_shift = page_shift;
+    a.page_shift = (short)page_shift;
+    a.flags = pl.l2_prefetch ? kArgL2Prefetch : 0;
+    // (a promise about the history only helps the fused step of a small
+    // contiguous layer: its K/V tiles then load before the wait)
+    if (pl.l2_prefetch && k_new != nullptr && paged == nullptr && (step_flags & KVD_STEP_HISTORY_STABLE))
+        a.flags |= kArgHistoryStable;
     a.err_word = err_word;
     a.B = B;
     a.H_kv = H_kv;
@@ -591,7 +724,7 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     // Both kernels are programmatic dependents of whatever precedes them on
     // the stream: they start early and wait (griddepcontrol.wait) before
     // touching any input, which hides their launch latency.
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
@@ -599,6 +732,20 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     void *args[] = {&a};
+    if (pl.cluster > 0) {  // one cluster of pl.cluster CTAs per sequence-head
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)pl.cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+        cfg.gridDim = dim3((unsigned)pl.grid);
+        cfg.blockDim = dim3(pl.v.threads);
+        cfg.dynamicSmemBytes = (size_t)pl.smem;
+        return cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.cluster_fused_fn : pl.v.cluster_fn, args) ==
+                       cudaSuccess
+                   ? KVD_OK
+                   : KVD_ERR_CUDA;
+    }
 
     cfg.gridDim = dim3((unsigned)pl.grid);
     cfg.blockDim = dim3(pl.v.threads);
@@ -658,6 +805,20 @@ kvd_status kvd_decode_step(const void *q, void *k_cache, void *v_cache, const vo
     if (!aligned16(k_new) || !aligned16(v_new)) return KVD_ERR_INVALID_ARG;
     return decode_launch(q, k_cache, v_cache, k_new, v_new, out, past_len, B, H_q, H_kv, T_max, D, N,
                          max_past_len, scale, dtype, workspace, workspace_bytes, err_word, stream);
+}
+
+kvd_status kvd_decode_step_flags(const void *q, void *k_cache, void *v_cache, const void *k_new,
+                                 const void *v_new, void *out, const int32_t *past_len, int B, int H_q,
+                                 int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                                 kvd_dtype dtype, uint32_t flags, void *workspace, size_t workspace_bytes,
+                                 uint32_t *err_word, void *stream)
+{
+    if ((flags & ~(uint32_t)KVD_STEP_HISTORY_STABLE) != 0u) return KVD_ERR_INVALID_ARG;
+    if (!k_new || !v_new) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return KVD_ERR_INVALID_ARG;
+    return decode_launch(q, k_cache, v_cache, k_new, v_new, out, past_len, B, H_q, H_kv, T_max, D, N,
+                         max_past_len, scale, dtype, workspace, workspace_bytes, err_word, stream, nullptr,
+                         nullptr, flags);
 }
 
 kvd_status kvd_paged_append(void *k_pages, void *v_pages, const void *k_new, const void *v_new,

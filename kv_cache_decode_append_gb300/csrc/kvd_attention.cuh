@@ -91,7 +91,27 @@ struct AttnArgs {
     int n_rowblocks;  // ceil(rows / RB)
     float qscale;     // softmax scale * log2(e)
     int num_pages;    // paged only: pages in the pool
-    int page_shift;   // paged only: log2(page_size); page_size is a multiple of the tile keys
+    short page_shift; // paged only: log2(page_size); page_size is a multiple of the tile keys
+    short flags;      // kArgL2Prefetch
+};
+// AttnArgs::flags: before its griddepcontrol.wait, each CTA reads past_len as
+// a hint (clamped to [0, max_past_len]), prefetches the K/V rows, q rows and
+// new rows of its expected range into L2, and lets the next kernel on the
+// stream launch; after the wait it reads past_len again and works from that.
+// Chosen for layers small enough that several fit in L2 at once.
+constexpr short kArgL2Prefetch = 1;
+// AttnArgs::flags (with kArgL2Prefetch): the caller guarantees that no work
+// queued before this call on the stream writes past_len or the cache rows
+// below past_len.  The CTAs then read past_len and fill their ring with K/V
+// tiles before griddepcontrol.wait; the q rows (second arrival on each full
+// barrier), the new rows of a fused step and every write wait for it.
+constexpr short kArgHistoryStable = 2;
+
+// How RangeWalk::fill arms a stage's full barrier.
+enum FillMode {
+    kFillOne = 0,     // one arrival: K/V (+ q) bytes
+    kFillKvOnly = 1,  // first of two arrivals, K/V bytes only; the q rows are issued by issue_pending
+    kFillTwo = 2,     // both arrivals at once: K/V (+ q) bytes, then a plain arrival
 };
 static_assert(sizeof(AttnArgs) == 128, "keep the kernel parameter block at 128 bytes");
 
@@ -362,6 +382,8 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
     const unsigned char *kg, *vg, *qg;
     uint64_t policy;
     int page_next;          // paged: physical page of the next tile (loaded one tile ahead)
+    const unsigned char *pend_q[S::kStages];  // kFillKvOnly: the q rows each stage still has to load
+    uint32_t pend_qb[S::kStages];
     const int32_t *bt_row;  // paged: block-table row of the current sequence
     const void *tm_k, *tm_v;  // tensor-map tiles (S::kTma): the K and V tensor maps
 
@@ -377,17 +399,23 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
 
     __device__ __forceinline__ void enter_head(const AttnArgs &a, const int *pl)
     {
-        const int h = hr / a.n_rowblocks;
-        rb = hr % a.n_rowblocks;
-        bh = b * a.H_kv + h;
-        P = pl[b];
-        T_b = P + a.N;
         const long long ts = t - tin;  // unit of the head's first tile
         c_first = owner_cta(ts, n, G);
         n_chunks = owner_cta(ts + tb - 1, n, G) - c_first + 1;
         if constexpr (kWriteSeg) {  // the split's shape, for the merge pass
             if (tin == 0) static_cast<int2 *>(a.merge_state)[(size_t)b * HR + hr] = make_int2(c_first, n_chunks);
         }
+        set_head(a, pl[b]);
+    }
+
+    // Per-head fields of (b, hr) with history P_: row block, addresses, q rows.
+    __device__ __forceinline__ void set_head(const AttnArgs &a, int P_)
+    {
+        const int h = hr / a.n_rowblocks;
+        rb = hr % a.n_rowblocks;
+        bh = b * a.H_kv + h;
+        P = P_;
+        T_b = P + a.N;
         if constexpr (kPaged) {
             const size_t hoff = ((size_t)h << a.page_shift) * S::kRowBytes;
             kg = static_cast<const unsigned char *>(a.k_cache) + hoff;
@@ -400,6 +428,30 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
         }
         qg = static_cast<const unsigned char *>(a.q) + ((size_t)bh * a.rows + rb * S::kRB) * S::kQRowBytes;
         q_bytes = min(S::kRB, a.rows - rb * S::kRB) * S::kQRowBytes;
+    }
+
+    // Cluster mode: the walk covers tiles [tin0, tin1) of the one
+    // sequence-head (b_, hr_) with history P_ and tb_ tiles; t counts the
+    // piece's tiles and HR is set so that the walk never moves to a next head.
+    __device__ __forceinline__ void start_piece(const AttnArgs &a, int b_, int hr_, int P_, int tb_, int tin0,
+                                                int tin1, int n_chunks_)
+    {
+        policy = l2_evict_first_policy();
+        HR = 0x7fffffff;
+        b = b_;
+        hr = hr_;
+        tb = tb_;
+        tin = tin0;
+        t = 0;
+        hi = tin1 - tin0;
+        n = hi;
+        G = 1;
+        ended = false;
+        piece_start = true;
+        c_first = 0;
+        n_chunks = n_chunks_;
+        if (t < hi) set_head(a, P_);
+        prefetch_page(a);
     }
 
     // pre[b] = units of sequences 0..b-1 per head (a head of sequence b has
@@ -437,7 +489,8 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
 
     // Describe and load the next tile into slot s, or mark the end of work.
     __device__ __forceinline__ void fill(const AttnArgs &a, const int *pre, const int *pl,
-                                         unsigned char *smem, TileMeta *meta, uint64_t *full, int s)
+                                         unsigned char *smem, TileMeta *meta, uint64_t *full, int s,
+                                         FillMode mode = kFillOne)
     {
         // (paged) page of the tile: a tile never straddles a page
         int page = 0;
@@ -445,6 +498,8 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
         if (t >= hi) {
             meta[s].flags = kMetaEnd;
             mbar_arrive(&full[s]);
+            if (mode == kFillTwo) mbar_arrive(&full[s]);
+            if (mode == kFillKvOnly) pend_qb[s] = 0u;
             ended = true;
             return;
         }
@@ -460,7 +515,12 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
         meta[s] = mt;
 
         const uint32_t bytes = (uint32_t)mt.nk * S::kRowBytes;
-        const uint32_t qbytes = (S::kQInRing && piece_start) ? (uint32_t)q_bytes : 0u;
+        uint32_t qbytes = (S::kQInRing && piece_start) ? (uint32_t)q_bytes : 0u;
+        if (mode == kFillKvOnly) {
+            pend_q[s] = qg;
+            pend_qb[s] = qbytes;
+            qbytes = 0u;
+        }
         size_t off;
         if constexpr (kPaged) {
             page = page_next;
@@ -503,6 +563,7 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
             bulk_load_g2s(dst + S::kTileBytes, vg + off, bytes, &full[s], policy);
         }
         if (qbytes) bulk_load_g2s(smem + S::kQOff + s * S::kQSlotBytes, qg, qbytes, &full[s], policy);
+        if (mode == kFillTwo) mbar_arrive(&full[s]);
 
         // advance to the next tile of the flattened list (skipping the next
         // head's overhead units)
@@ -522,6 +583,17 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
             if (t < hi) enter_head(a, pl);
         }
         prefetch_page(a);
+    }
+
+    // The second arrival of stage s filled with kFillKvOnly: its q rows, if any.
+    __device__ __forceinline__ void issue_pending(unsigned char *smem, uint64_t *full, int s)
+    {
+        if (pend_qb[s]) {
+            mbar_arrive_expect_tx(&full[s], pend_qb[s]);
+            bulk_load_g2s(smem + S::kQOff + s * S::kQSlotBytes, pend_q[s], pend_qb[s], &full[s], policy);
+        } else {
+            mbar_arrive(&full[s]);
+        }
     }
 };
 
@@ -623,10 +695,156 @@ __device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &
     }
 }
 
+// Units per sequence-head, prefix-summed over sequences by warp 0's scan:
+// pre[b] = units of sequences 0..b-1 per head, pl[b] = P_b.  A hint
+// (kArgL2Prefetch, before the wait) clamps P_b into [0, max_past_len] and
+// reads it through L2 only; otherwise a sequence with an invalid P_b gets no
+// units and CTA 0 reports it.
+template <typename S>
+__device__ __forceinline__ bool unit_prefix(const AttnArgs &a, int *pre, int *pl, int lane, bool hint,
+                                           bool defer_error = false)
+{
+    bool bad = false;  // (defer_error: an invalid P_b, for the caller to report)
+    int carry = 0;
+    if (lane == 0) pre[0] = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int b = b0 + lane;
+        int units = 0;
+        if (b < a.B) {
+            int P;
+            bool ok = true;
+            if (hint) {
+                P = min(max(__ldcg(a.past_len + b), 0), a.max_past_len);
+            } else {
+                P = __ldg(a.past_len + b);
+                ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
+                if (!ok && blockIdx.x == 0) {
+                    if (defer_error) bad = true;
+                    else raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
+                }
+            }
+            units = ok ? (P + a.N + S::kTK - 1) / S::kTK + S::kPieceUnits : 0;
+            pl[b] = P;
+        }
+        int v = units;  // inclusive scan over the warp
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += n;
+        }
+        if (b < a.B) pre[b + 1] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    __syncwarp();
+    return __any_sync(0xffffffffu, bad);
+}
+
+// This CTA's range [lo, hi) of the flattened unit list (see RangeWalk).
+__device__ __forceinline__ void cta_range(const AttnArgs &a, const int *pre, long long *n_total, long long *G,
+                                          long long *lo, long long *hi)
+{
+    const int HR = a.H_kv * a.n_rowblocks;
+    *n_total = (long long)pre[a.B] * HR;
+    *G = min((long long)gridDim.x, *n_total);  // CTAs that get work
+    *lo = blockIdx.x < *G ? *n_total * blockIdx.x / *G : 0;
+    *hi = blockIdx.x < *G ? *n_total * (blockIdx.x + 1) / *G : 0;
+}
+
+// Warp 0, before griddepcontrol.wait (kArgL2Prefetch): bulk-prefetch into L2
+// what the CTA's range [lo, hi) will read -- the K and V rows of its tiles
+// (one tile per lane at a time), the q rows of each head it touches and, in a
+// fused step, the new K/V rows of the heads whose last tile it holds.  pre /
+// pl are the hinted prefix; every address stays inside its buffer whatever
+// the hint (P_b <= max_past_len, and max_past_len + N <= T_max is checked on
+// the host), so a stale hint only costs useless prefetches.
+template <typename S, bool kFused, bool kPaged>
+__device__ __forceinline__ void l2_prefetch_range(const AttnArgs &a, const int *pre, const int *pl, int lane,
+                                                  long long lo, long long hi)
+{
+    if (lo >= hi) return;
+    const int HR = a.H_kv * a.n_rowblocks;
+    int b = 0, hb = a.B - 1;  // last b with pre[b] * HR <= lo
+    while (b < hb) {
+        const int mid = (b + hb + 1) / 2;
+        if ((long long)pre[mid] * HR <= lo) b = mid; else hb = mid - 1;
+    }
+    long long t = lo;
+    for (; b < a.B && t < hi; ++b) {
+        const int ub = pre[b + 1] - pre[b];
+        if (ub == 0) continue;
+        const long long sb = (long long)pre[b] * HR;
+        const int tb = ub - S::kPieceUnits;
+        const int T_b = pl[b] + a.N;
+        for (int hr = (int)((t - sb) / ub); hr < HR && t < hi; ++hr) {
+            const long long base = sb + (long long)hr * ub + S::kPieceUnits;  // unit of the head's tile 0
+            const int tin0 = (int)max(0LL, t - base);
+            const int tin1 = (int)min((long long)tb, hi - base);
+            t = base + tb;
+            if (tin1 <= tin0) continue;
+            const int h = hr / a.n_rowblocks, rb = hr % a.n_rowblocks;
+            const int bh = b * a.H_kv + h;
+            for (int tin = tin0 + lane; tin < tin1; tin += 32) {
+                const int k0 = tin * S::kTK;
+                const uint32_t bytes = (uint32_t)(min(S::kTK, T_b - k0) * S::kRowBytes);
+                size_t off;
+                if constexpr (kPaged) {
+                    const int pages = a.T_max >> a.page_shift;
+                    int page = __ldcg(a.block_table + (size_t)b * pages + (k0 >> a.page_shift));
+                    if ((unsigned)page >= (unsigned)a.num_pages) page = 0;
+                    off = ((((size_t)page * a.H_kv + h) << a.page_shift) + (k0 & ((1 << a.page_shift) - 1))) *
+                          S::kRowBytes;
+                } else {
+                    off = ((size_t)bh * a.T_max + k0) * S::kRowBytes;
+                }
+                prefetch_l2(static_cast<const unsigned char *>(a.k_cache) + off, bytes);
+                prefetch_l2(static_cast<const unsigned char *>(a.v_cache) + off, bytes);
+            }
+            if (lane == 0) {
+                const int q_rows = min(S::kRB, a.rows - rb * S::kRB);
+                prefetch_l2(static_cast<const unsigned char *>(a.q) + ((size_t)bh * a.rows + rb * S::kRB) * S::kQRowBytes,
+                            (uint32_t)(q_rows * S::kQRowBytes));
+                if constexpr (kFused) {
+                    if (tin1 == tb) {
+                        const size_t nrow = (size_t)bh * a.N * S::kQRowBytes;
+                        prefetch_l2(static_cast<const unsigned char *>(a.k_new) + nrow, (uint32_t)(a.N * S::kQRowBytes));
+                        prefetch_l2(static_cast<const unsigned char *>(a.v_new) + nrow, (uint32_t)(a.N * S::kQRowBytes));
+                    }
+                }
+            }
+        }
+        t = max(t, (long long)pre[b + 1] * HR);
+    }
+}
+
+// Cluster mode, thread 0: the CTA's piece of its cluster's sequence-head (an
+// equal share of the head's tiles by cluster rank) and its first ring fills.
+// Returns whether past_len of the head's sequence is valid (else the range is
+// empty and the sequence is skipped).
+template <typename S, typename Walk>
+__device__ __forceinline__ bool cluster_start(const AttnArgs &a, Walk &walk, unsigned char *smem, TileMeta *meta,
+                                              uint64_t *full, int &issued, FillMode mode)
+{
+    const int csize = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
+    const int HR = a.H_kv * a.n_rowblocks;
+    const int u = (int)blockIdx.x / csize;  // the cluster's sequence-head (b, hr)
+    const int b = u / HR, hr = u % HR;
+    const int P = __ldg(a.past_len + b);
+    const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
+    const int tb = ok ? (P + a.N + S::kTK - 1) / S::kTK : 0;
+    walk.start_piece(a, b, hr, P, tb, tb * crank / csize, tb * (crank + 1) / csize, csize);
+    for (; issued < S::kStages && !walk.ended; ++issued) walk.fill(a, nullptr, nullptr, smem, meta, full, issued, mode);
+    return ok;
+}
+
 // kFused: append inside (kvd_decode_step).  kTicketMerge: split heads are
 // merged at the end of this kernel (else by attn_merge_kernel).  kPaged: the
 // cache is paged (block table), else contiguous [B, H_kv, T_max, D].
-template <typename T, int D, int RB, bool kFused, bool kTicketMerge, bool kPaged, typename C = T>
+// kCluster (small layers, contiguous cache): the grid is one thread-block
+// cluster per sequence-head; the cluster's CTAs split the head's tiles in equal
+// shares by rank, each loads its whole share into its ring, and rank 0 merges
+// the pieces from the other CTAs' shared memory (no workspace, no atomics).
+template <typename T, int D, int RB, bool kFused, bool kTicketMerge, bool kPaged, typename C = T,
+          bool kCluster = false>
 __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     attn_balanced_kernel(const AttnArgs a)
 {
@@ -648,62 +866,94 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     const int warp = tid / 32, lane = tid % 32;
     const int grp = lane / S::kL, j = lane % S::kL;
 
+    const bool early = (a.flags & kArgL2Prefetch) != 0;
+    const bool stable = early && (a.flags & kArgHistoryStable) != 0;
+    const FillMode refill = stable ? kFillTwo : kFillOne;
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < S::kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], stable ? 2 : 1);  // (stable: K/V before the wait, q after)
             mbar_init(&empty[s], S::kNW);
         }
         fence_mbar_init();
     }
-    // Every input may come from the previous kernel on the stream.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // The next kernel on the stream may launch now: its CTAs take the SM
-    // slots this grid frees and run up to their own griddepcontrol.wait,
-    // which still waits for this whole grid to finish and flush.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __syncthreads();  // barrier initialisation visible to every thread
-
     // Warp 0 forms the unit prefix over sequences and thread 0 starts the ring
     // (slot s of ring position p is free again once every warp has released
     // position p - STAGES on empty[s]); the other warps go straight to
     // waiting for the first tile.
     RangeWalk<S, !kTicketMerge, kPaged> walk;  // used by thread 0 only
     int issued = 0;     // ring positions filled so far (thread 0)
-    if (warp == 0) {
-        // ---- units per sequence-head, prefix-summed over sequences by a warp scan ----
-        int carry = 0;
-        if (lane == 0) pre[0] = 0;
-        for (int b0 = 0; b0 < a.B; b0 += 32) {
-            const int b = b0 + lane;
-            int units = 0;
-            if (b < a.B) {
-                const int P = __ldg(a.past_len + b);
-                const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
-                if (!ok && blockIdx.x == 0) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
-                units = ok ? (P + a.N + S::kTK - 1) / S::kTK + S::kPieceUnits : 0;
-                pl[b] = P;
+    bool bad_past = false;
+    int *cl_ok = reinterpret_cast<int *>(jobs);  // cluster mode: the head's sequence is valid
+    if constexpr (kCluster) {
+        static_assert(!kPaged, "cluster mode serves contiguous caches");
+        // (planned for small layers only: the next kernel may launch now)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (stable && tid == 0) bad_past = !cluster_start<S>(a, walk, smem, meta, full, issued, kFillKvOnly);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (tid == 0) {
+            if (stable) {
+                for (int p = 0; p < issued; ++p) walk.issue_pending(smem, full, p);  // the q rows
+            } else {
+                bad_past = !cluster_start<S>(a, walk, smem, meta, full, issued, kFillOne);
             }
-            int v = units;  // inclusive scan over the warp
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, v, off);
-                if (lane >= off) v += n;
-            }
-            if (b < a.B) pre[b + 1] = carry + v;
-            carry += __shfl_sync(0xffffffffu, v, 31);
+            *cl_ok = bad_past ? 0 : 1;
+            // (one report per sequence: the first rank of its first head's cluster)
+            if (bad_past && cluster_ctarank() == 0 && ((int)blockIdx.x / (int)cluster_nctarank()) % (a.H_kv * a.n_rowblocks) == 0)
+                raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
         }
-        __syncwarp();
-        if (lane == 0) {
-            const int HR = a.H_kv * a.n_rowblocks;
-            const long long n_total = (long long)pre[a.B] * HR;
-            const long long G = min((long long)gridDim.x, n_total);  // CTAs that get work
-            const long long lo = blockIdx.x < G ? n_total * blockIdx.x / G : 0;
-            const long long hi = blockIdx.x < G ? n_total * (blockIdx.x + 1) / G : 0;
-            walk.start(a, pre, pl, lo, hi, n_total, G);
-            for (; issued < S::kStages; ++issued) walk.fill(a, pre, pl, smem, meta, full, issued);
+        __syncthreads();
+    } else {
+    if (early) {
+        // Small layers: let the next kernel launch now, so that its CTAs
+        // prefetch their own rows while this grid runs, and prefetch this
+        // CTA's rows into L2 before waiting: from the hinted split, or with
+        // a stable history from the exact one, whose first K/V tiles then go
+        // straight into the ring.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (warp == 0) {
+            bad_past = unit_prefix<S>(a, pre, pl, lane, !stable, true);
+            long long n_total, G, lo, hi;
+            cta_range(a, pre, &n_total, &G, &lo, &hi);
+            if (stable && lane == 0) {
+                walk.start(a, pre, pl, lo, hi, n_total, G);
+                for (; issued < S::kStages && !walk.ended; ++issued)
+                    walk.fill(a, pre, pl, smem, meta, full, issued, kFillKvOnly);
+            }
+            // CTAs below the SM count are the first to find a free slot (the
+            // grid is dispatched in order): they also prefetch the ranges of
+            // CTAs c + SMs, c + 2 SMs, ..., which become resident only as the
+            // previous grid's CTAs exit.
+            uint32_t nsm;
+            asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+            for (long long c = blockIdx.x; c < G; c += nsm) {
+                l2_prefetch_range<S, kFused, kPaged>(a, pre, pl, lane, n_total * c / G, n_total * (c + 1) / G);
+                if (blockIdx.x >= nsm) break;
+            }
         }
     }
+    // Every input may come from the previous kernel on the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The next kernel on the stream may launch now: its CTAs take the SM
+    // slots this grid frees and run up to their own griddepcontrol.wait,
+    // which still waits for this whole grid to finish and flush.
+    if (!early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (stable && warp == 0 && lane == 0) {
+        if (bad_past) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
+        for (int p = 0; p < issued; ++p) walk.issue_pending(smem, full, p);  // the q rows
+    }
+    __syncthreads();  // barrier initialisation visible to every thread
+
+    if (warp == 0 && !stable) {
+        unit_prefix<S>(a, pre, pl, lane, false);
+        if (lane == 0) {
+            long long n_total, G, lo, hi;
+            cta_range(a, pre, &n_total, &G, &lo, &hi);
+            walk.start(a, pre, pl, lo, hi, n_total, G);
+            for (; issued < S::kStages && !walk.ended; ++issued) walk.fill(a, pre, pl, smem, meta, full, issued);
+        }
+    }
+    }  // (not kCluster)
 
     f32x2 qv[RB][S::kE / 2];
     f32x2 o[RB][S::kE / 2];
@@ -726,7 +976,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
                     timed_out = true;
                     raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
                 }
-                walk.fill(a, pre, pl, smem, meta, full, fs);
+                walk.fill(a, pre, pl, smem, meta, full, fs, refill);
                 ++issued;
             }
         }
@@ -811,7 +1061,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
             const int fs = issued % S::kStages;
             const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
             if (mbar_test_wait(&empty[fs], fph)) {
-                walk.fill(a, pre, pl, smem, meta, full, fs);
+                walk.fill(a, pre, pl, smem, meta, full, fs, refill);
                 ++issued;
             }
         }
@@ -866,7 +1116,11 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
             }
         }
         __syncthreads();
-        const bool single = (mt.n_chunks == 1);
+        const bool single = !kCluster && (mt.n_chunks == 1);
+        // Cluster mode: the CTA's one piece goes to the start of its own ring
+        // (every tile of the range has been consumed and no copy is in flight:
+        // the walk has ended), for rank 0 to read after the cluster barrier.
+        float *cl_part = reinterpret_cast<float *>(smem + S::kRingOff);
         // A CTA holds at most two partial pieces: slot 1 for the head it starts
         // (it is that head's first CTA), slot 0 for the head it continues.
         const size_t pbase = ((size_t)blockIdx.x * 2 + ((int)blockIdx.x == mt.c_first ? 1 : 0)) * RB;
@@ -890,6 +1144,13 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
                               num / den * a.kv_scale.y);
                 else
                     Tq::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
+            } else if constexpr (kCluster) {
+                float *pr = cl_part + r * (D + 2);
+                pr[d] = num;
+                if (d == 0) {
+                    pr[D] = M;
+                    pr[D + 1] = den;
+                }
             } else {
                 float *pr = a.part + (pbase + r) * (D + 4);
                 pr[d] = num;
@@ -899,7 +1160,8 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
                 }
             }
         }
-        if constexpr (kTicketMerge) {
+        if constexpr (kCluster) ++n_pieces;
+        if constexpr (kTicketMerge && !kCluster) {
             if (!single) {  // (a range holds at most two split pieces: the head it continues, the head it starts)
                 if (tid == 0 && n_pieces < 2) jobs[n_pieces] = MergeJob{mt.bh, mt.rb, mt.c_first, mt.n_chunks};
                 ++n_pieces;
@@ -907,7 +1169,43 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
         }
     }
 
-    if constexpr (kTicketMerge) {
+    if constexpr (kCluster) {
+        // ---- merge the cluster's pieces in rank 0, from each CTA's shared memory ----
+        float *cl_part = reinterpret_cast<float *>(smem + S::kRingOff);
+        if (n_pieces == 0) {  // an empty share: a piece of weight zero
+            for (int idx = tid; idx < RB * (D + 2); idx += S::kThreads) {
+                const int r = idx / (D + 2), d = idx % (D + 2);
+                cl_part[idx] = (d == D) ? kNegInf : 0.f;
+                (void)r;
+            }
+        }
+        cluster_sync_all();  // every piece written
+        if (cluster_ctarank() == 0 && *cl_ok) {
+            const int csize = (int)cluster_nctarank();
+            const int HR = a.H_kv * a.n_rowblocks;
+            const int u = (int)blockIdx.x / csize;
+            const int bh = (u / HR) * a.H_kv + (u % HR) / a.n_rowblocks, rb = (u % HR) % a.n_rowblocks;
+            for (int idx = tid; idx < RB * D; idx += S::kThreads) {
+                const int r = idx / D, d = idx % D;
+                const int rg = rb * RB + r;
+                if (rg >= a.rows) continue;
+                const float *pr = cl_part + r * (D + 2);
+                float M = kNegInf;
+                for (int k = 0; k < csize; ++k) M = fmaxf(M, ld_cluster_f32(pr + D, (uint32_t)k));
+                float num = 0.f, den = 0.f;
+                for (int k = 0; k < csize; ++k) {
+                    const float wt = safe_weight(ld_cluster_f32(pr + D, (uint32_t)k), M);
+                    num = fmaf(wt, ld_cluster_f32(pr + d, (uint32_t)k), num);
+                    den = fmaf(wt, ld_cluster_f32(pr + D + 1, (uint32_t)k), den);
+                }
+                if constexpr (kQuant)  // values are stored / v_scale
+                    Tq::store(static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + d, num / den * a.kv_scale.y);
+                else
+                    Tq::store(static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + d, num / den);
+            }
+        }
+        cluster_sync_all();  // rank 0 is done reading the others' shared memory
+    } else if constexpr (kTicketMerge) {
         // ---- count this CTA's split pieces; merge the heads they complete ----
         n_pieces = min(n_pieces, 2);
         __syncthreads();  // every thread's share of the partials is written
@@ -1040,6 +1338,9 @@ struct AttnVariant {
     int piece_units;       // cost of a piece boundary in tile units
     bool tma = false;      // tensor-core kernel: takes the K and V tensor maps
     bool q_map = false;    // tcgen05 kernel: also a Q tensor map (128-row boxes)
+    int stages = 0;        // ring stages
+    const void *cluster_fn = nullptr;        // cluster mode (contiguous, small layers), attention
+    const void *cluster_fused_fn = nullptr;  // cluster mode, fused step
 };
 
 template <typename T, int D, int RB, bool kTicketMerge, bool kPaged, typename C = T> AttnVariant make_variant()
@@ -1051,11 +1352,16 @@ template <typename T, int D, int RB, bool kTicketMerge, bool kPaged, typename C 
     v.fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, kTicketMerge, kPaged, C>);
     if constexpr (kTicketMerge) v.merge_fn = nullptr;
     else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, RB, kQuant>);
+    if constexpr (kTicketMerge && !kPaged) {  // (built with the in-kernel-merge, contiguous variants)
+        v.cluster_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false, true, false, C, true>);
+        v.cluster_fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, true, false, C, true>);
+    }
     v.threads = S::kThreads;
     v.fixed_smem_bytes = S::kFixedBytes;
     v.tile_keys = S::kTK;
     v.rows_per_block = RB;
     v.piece_units = S::kPieceUnits;
+    v.stages = S::kStages;
     return v;
 }
 

@@ -124,6 +124,14 @@ __device__ __forceinline__ void bulk_load_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes a
+// multiple of 16).  A hint only: nothing completes, nothing is written, and
+// later writes by other grids still reach the line in L2 (the coherence point).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tiled bulk (TMA) load of one box of a tensor map (a kernel parameter)
 // at element coordinates (x, y) into shared memory, completing on bar.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar,
@@ -428,6 +436,37 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v)
     int old;
     asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
+}
+
+// ---- thread-block clusters ----
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// fp32 load from the shared memory of CTA `rank` of this cluster, at the
+// offset that p has in this CTA's shared memory.
+__device__ __forceinline__ float ld_cluster_f32(const void *p, uint32_t rank)
+{
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+// Every thread of every CTA of the cluster: arrive (releasing this thread's
+// shared-memory writes) and wait for all (acquiring theirs).
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void raise_error(uint32_t *err_word, uint32_t bit)

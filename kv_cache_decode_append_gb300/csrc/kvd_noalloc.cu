@@ -15,9 +15,14 @@
 //     overlap (different streams without ordering between them) race on it;
 //   * the array keeps whatever the previous call left in it; the part of it
 //     that must start at zero (the counters the kernel uses to merge heads
-//     split across CTAs) is cleared with cudaMemsetAsync before each launch;
+//     split across CTAs, a few bytes per sequence-head) is cleared with
+//     cudaMemsetAsync before each launch, once the host checks have passed;
+//     the rest (partial results) is always written before it is read;
 //   * shapes needing more than kNoAllocScratchBytes are rejected with
-//     KVD_ERR_WORKSPACE before anything is launched.
+//     KVD_ERR_WORKSPACE, and invalid arguments with their status, before
+//     anything is queued on the stream;
+//   * the scratch's device address is looked up once per device and kept:
+//     the entry point must not be used on a device after cudaDeviceReset.
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -55,6 +60,13 @@ kvd_status noalloc_scratch(void **ptr)
 
 }  // namespace
 
+namespace kvd {
+kvd_status decode_attention_prepare(const void *q, const void *k_cache, const void *v_cache, const void *out,
+                                    const int32_t *past_len, int B, int H_q, int H_kv, int T_max, int D, int N,
+                                    int max_past_len, kvd_dtype dtype, size_t *ws_bytes, size_t *zero_off,
+                                    size_t *zero_bytes);
+}
+
 extern "C" kvd_status kvd_decode_attention_noalloc(const void *q, const void *k_cache,
                                                    const void *v_cache, void *out,
                                                    const int32_t *past_len, int B, int H_q,
@@ -62,19 +74,20 @@ extern "C" kvd_status kvd_decode_attention_noalloc(const void *q, const void *k_
                                                    int max_past_len, float scale, kvd_dtype dtype,
                                                    uint32_t *err_word, void *stream)
 {
-    const size_t need = kvd_decode_workspace_bytes(B, H_q, H_kv, D, N, max_past_len, dtype);
-    if (need == 0) {
-        // Invalid shapes: let the regular entry point report which argument is wrong.
-        return kvd_decode_attention(q, k_cache, v_cache, out, past_len, B, H_q, H_kv, T_max, D, N,
-                                    max_past_len, scale, dtype, nullptr, 0, err_word, stream);
-    }
+    // Every host check first: an invalid call returns without queuing anything.
+    size_t need = 0, zero_off = 0, zero_bytes = 0;
+    kvd_status st = kvd::decode_attention_prepare(q, k_cache, v_cache, out, past_len, B, H_q, H_kv, T_max, D, N,
+                                                  max_past_len, dtype, &need, &zero_off, &zero_bytes);
+    if (st != KVD_OK) return st;
+    if (B == 0) return KVD_OK;
     if (need > kNoAllocScratchBytes) return KVD_ERR_WORKSPACE;
     void *scratch = nullptr;
-    const kvd_status st = noalloc_scratch(&scratch);
-    if (st != KVD_OK) return st;
-    // Clear the used part (the kernel needs its merge counters at zero); a
-    // memset allocates nothing.
-    if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if ((st = noalloc_scratch(&scratch)) != KVD_OK) return st;
+    // The merge counters must start at zero (a call that gave up on a
+    // timeout may have left some set); a memset allocates nothing.
+    if (zero_bytes != 0 &&
+        cudaMemsetAsync(static_cast<unsigned char *>(scratch) + zero_off, 0, zero_bytes,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return KVD_ERR_CUDA;
     return kvd_decode_attention(q, k_cache, v_cache, out, past_len, B, H_q, H_kv, T_max, D, N,
                                 max_past_len, scale, dtype, scratch, kNoAllocScratchBytes, err_word,

@@ -40,6 +40,8 @@ KVD_DEVERR_TIMEOUT = 2
 KVD_DEVERR_PAGE = 4
 KVD_DEVERR_INTERNAL = 8
 
+KVD_STEP_HISTORY_STABLE = 1  # kvd_decode_step_flags: no earlier work writes past_len or the history
+
 _TORCH_DTYPE = {torch.float32: KVD_F32, torch.bfloat16: KVD_BF16, torch.float16: KVD_F16}
 _NAME_DTYPE = {"f32": KVD_F32, "bf16": KVD_BF16, "f16": KVD_F16, "e4m3": KVD_E4M3}
 
@@ -54,7 +56,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("tile_keys", ctypes.c_int), ("max_tiles", ctypes.c_int), ("grid", ctypes.c_int),
                 ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("launches", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_size_t), ("rows_per_block", ctypes.c_int),
-                ("tensor_cores", ctypes.c_int)]
+                ("tensor_cores", ctypes.c_int), ("l2_prefetch", ctypes.c_int),
+                ("cluster", ctypes.c_int)]
 
 
 class _Lib:
@@ -73,6 +76,9 @@ class _Lib:
         lib.kvd_decode_step.restype = ci
         lib.kvd_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
                                         vp, sz, u32p, vp]
+        lib.kvd_decode_step_flags.restype = ci
+        lib.kvd_decode_step_flags.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
+                                              ctypes.c_uint32, vp, sz, u32p, vp]
         lib.kvd_paged_append.restype = ci
         lib.kvd_paged_append.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, u32p, vp]
         lib.kvd_paged_decode_attention.restype = ci
@@ -199,7 +205,10 @@ def kvd_decode_plan(B: int, H_q: int, H_kv: int, D: int, N: int, max_past_len: i
 
     ``tensor_cores``: 0 the CUDA-core kernel, 1 the mma.sync tensor-core kernel (16-row
     blocks), 2 the tcgen05 kernel (128-row blocks, for more than 16 query rows per KV
-    head); ``launches`` 2 when split heads are merged by the separate merge pass."""
+    head); ``launches`` 2 when split heads are merged by the separate merge pass;
+    ``l2_prefetch`` 1 for small layers (the next kernel on the stream may start early);
+    ``cluster`` > 0 when such a layer runs as one thread-block cluster of that many CTAs
+    per KV head."""
     code = _NAME_DTYPE[dtype] if isinstance(dtype, str) else _TORCH_DTYPE[dtype]
     info = PlanInfo()
     _check("kvd_decode_plan", raw.kvd_decode_plan(B, H_q, H_kv, D, N, int(max_past_len), code,
@@ -246,8 +255,11 @@ def kvd_decode_attention(q, k_cache, v_cache, out, past_len, max_past_len: int, 
 
 def kvd_decode_step(q, k_cache, v_cache, k_new, v_new, out, past_len, max_past_len: int,
                     scale: float = 0.0, workspace: Optional[torch.Tensor] = None, err_word=None,
-                    stream=None) -> None:
-    """Append ``k_new``/``v_new`` and attend the new rows of ``q`` in one launch."""
+                    stream=None, flags: Optional[int] = None) -> None:
+    """Append ``k_new``/``v_new`` and attend the new rows of ``q`` in one launch.
+
+    ``flags`` (e.g. ``KVD_STEP_HISTORY_STABLE``) calls ``kvd_decode_step_flags``
+    with the caller's guarantees instead."""
     for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new),
                  ("v_new", v_new), ("out", out)):
         _need_cuda(n, t, q.dtype)
@@ -262,6 +274,13 @@ def kvd_decode_step(q, k_cache, v_cache, k_new, v_new, out, past_len, max_past_l
     if past_len.numel() != B:
         raise ValueError("past_len must hold B entries")
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    if flags is not None:
+        st = raw.kvd_decode_step_flags(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
+                                       v_new.data_ptr(), out.data_ptr(), past_len.data_ptr(), B, H_q, H_kv,
+                                       T_max, D, N, int(max_past_len), float(scale), _dtype_code(q), int(flags),
+                                       ws_ptr, ws_bytes, _ptr(err_word), _stream_handle(stream))
+        _check("kvd_decode_step_flags", st)
+        return
     st = raw.kvd_decode_step(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
                              v_new.data_ptr(), out.data_ptr(), past_len.data_ptr(), B, H_q, H_kv, T_max, D,
                              N, int(max_past_len), float(scale), _dtype_code(q), ws_ptr, ws_bytes,

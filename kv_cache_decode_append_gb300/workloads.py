@@ -156,3 +156,13 @@ def to_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, page_size: int, extra
         out.append(pages)
     table = perm.to(torch.int32).view(B, max_pages).to(dev)
     return out[0], out[1], table
+
+
+def new_rows(w: Workload, layer: int, device="cpu") -> dict:
+    """Q, K_new and V_new of one layer, drawn exactly as ``layer_inputs`` draws them
+    (for a chunk size N set on an existing cache)."""
+    dt = w.torch_dtype
+    base = 10 * (1000 * w.wid + layer)
+    return {"q": _randn((w.B, w.H_q, w.N, w.D), base + 0, device, dt),
+            "k_new": _randn((w.B, w.H_kv, w.N, w.D), base + 1, device, dt),
+            "v_new": _randn((w.B, w.H_kv, w.N, w.D), base + 2, device, dt)}

@@ -9,8 +9,9 @@ The file is named to be collected last, so that a run stopping at its first
 failure has already run every other test.  Each case calls the new entry point
 through the C ABI twice in a row (different shapes, so the second call finds
 the first call's leftovers in the shared scratch) and compares both outputs
-with the workspace entry point's, within the parity tolerance of the other
-tests.
+with the workspace entry point's: within the parity tolerance of the other
+tests, and bit for bit, since both run the same plan and kernels on the same
+inputs (the split heads' pieces are merged in a fixed order).
 """
 import ctypes
 
@@ -66,17 +67,24 @@ def _noalloc(c_entry, w, g, past_d, max_past, err):
     return out
 
 
+def _same_bits(a, b):
+    return np.array_equal(a.contiguous().cpu().view(torch.uint8).numpy(), b.contiguous().cpu().view(torch.uint8).numpy())
+
+
 def test_noalloc_matches_workspace_entry_point_twice_in_a_row(c_entry):
     cases = [
-        # long GQA heads spread over many CTAs: the merge pass reads the scratch
-        (wl.Workload(0, "gqa", L=1, B=6, H_q=32, H_kv=8, D=128, N=1, dtype="bf16", T_max=4200, P=0),
-         [4100, 37, 2048, 1500, 3999, 700], 8101),
-        # chunked fp32 decode with several row blocks per KV head
+        # 32 long GQA sequences: ranges long enough for the separate merge
+        # pass, which reads the split heads' partials from the scratch
+        (wl.Workload(0, "gqa", L=1, B=32, H_q=32, H_kv=8, D=128, N=1, dtype="bf16", T_max=4200, P=0),
+         [4100 - 97 * i for i in range(32)], 8101, 2),
+        # chunked fp32 decode with several row blocks per KV head: split heads
+        # merged inside the kernel through counters in the scratch
         (wl.Workload(0, "chunk", L=1, B=2, H_q=12, H_kv=4, D=64, N=4, dtype="f32", T_max=1500, P=0),
-         [1200, 513], 8102),
+         [1200, 513], 8102, 1),
     ]
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    for w, past, seed in cases:
+    for w, past, seed, launches in cases:
+        assert kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max(past), w.torch_dtype)["launches"] == launches
         g, past_d, max_past = _case(w, past, seed)
         got = _noalloc(c_entry, w, g, past_d, max_past, err)
         ref = _reference(w, g, past_d, max_past)
@@ -85,6 +93,21 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row(c_entry):
         got_np, ref_np = got.double().cpu().numpy(), ref.double().cpu().numpy()
         assert np.isfinite(got_np).all()
         assert row_rel_err(got_np, ref_np) <= TOL[w.dtype]
+        # the same plan and kernels on the same inputs: the same bits
+        assert _same_bits(got, ref)
+
+
+def test_noalloc_python_binding(c_entry):
+    """The binding's wrapper calls the same entry point (bf16, split heads)."""
+    w = wl.Workload(0, "py", L=1, B=4, H_q=16, H_kv=4, D=64, N=2, dtype="bf16", T_max=900, P=0)
+    g, past_d, max_past = _case(w, [850, 3, 400, 777], 8103)
+    out = torch.full_like(g["q"], float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvd.kvd_decode_attention_noalloc(g["q"], g["k_cache"], g["v_cache"], out, past_d, max_past, err_word=err)
+    ref = _reference(w, g, past_d, max_past)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _same_bits(out, ref)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(c_entry):
