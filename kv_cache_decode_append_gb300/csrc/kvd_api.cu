@@ -489,17 +489,24 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     if (pl->l2_prefetch && !paged && pl->v.cluster_fn != nullptr && pl->v.stages > 0) {
         const int c = (pl->max_tiles + pl->v.stages - 1) / pl->v.stages;
         const long long ctas = (long long)B * H_kv * pl->n_rowblocks * c;
+        // (the pieces, c x RB rows of D + 2 floats, take the place of the tables)
+        const size_t pieces = round_up((size_t)c * pl->rb * (D + 2) * sizeof(float), 16);
+        const size_t smem_cl = (size_t)pl->v.fixed_smem_bytes +
+                               (pieces > smem - pl->v.fixed_smem_bytes ? pieces : smem - pl->v.fixed_smem_bytes);
         bool fits = false;
-        if (c >= 2 && c <= kMaxCluster && ctas <= 8LL * sms) {
-            if ((st = cluster_fits(dev, pl->v.cluster_fn, pl->v.threads, pl->smem, c, &fits)) != KVD_OK) return st;
+        if (c >= 2 && c <= kMaxCluster && ctas <= 8LL * sms && smem_cl <= (size_t)kMaxSmemPerCta) {
+            if ((st = cluster_fits(dev, pl->v.cluster_fn, pl->v.threads, (int)smem_cl, c, &fits)) != KVD_OK)
+                return st;
             bool fits2 = false;
-            if (fits && (st = cluster_fits(dev, pl->v.cluster_fused_fn, pl->v.threads, pl->smem, c, &fits2)) != KVD_OK)
+            if (fits &&
+                (st = cluster_fits(dev, pl->v.cluster_fused_fn, pl->v.threads, (int)smem_cl, c, &fits2)) != KVD_OK)
                 return st;
             fits = fits && fits2;
         }
         if (fits) {
             pl->cluster = c;
             pl->grid = (int)ctas;
+            pl->smem = (int)smem_cl;
         }
     }
 

@@ -841,8 +841,10 @@ __device__ __forceinline__ bool cluster_start(const AttnArgs &a, Walk &walk, uns
 // cache is paged (block table), else contiguous [B, H_kv, T_max, D].
 // kCluster (small layers, contiguous cache): the grid is one thread-block
 // cluster per sequence-head; the cluster's CTAs split the head's tiles in equal
-// shares by rank, each loads its whole share into its ring, and rank 0 merges
-// the pieces from the other CTAs' shared memory (no workspace, no atomics).
+// shares by rank, each loads its whole share into its ring and stores its
+// piece into rank 0's shared memory, and rank 0 merges them (no workspace, no
+// atomics, one cluster barrier).  The pieces live after the fixed layout, in
+// place of the per-sequence tables: cluster size x RB rows of (o[D], m, l).
 template <typename T, int D, int RB, bool kFused, bool kTicketMerge, bool kPaged, typename C = T,
           bool kCluster = false>
 __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
@@ -1117,10 +1119,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
         }
         __syncthreads();
         const bool single = !kCluster && (mt.n_chunks == 1);
-        // Cluster mode: the CTA's one piece goes to the start of its own ring
-        // (every tile of the range has been consumed and no copy is in flight:
-        // the walk has ended), for rank 0 to read after the cluster barrier.
-        float *cl_part = reinterpret_cast<float *>(smem + S::kRingOff);
+        // Cluster mode: the CTA's one piece goes to its slot in rank 0's
+        // shared memory, for rank 0 to merge after the cluster barrier.
+        float *cl_part = reinterpret_cast<float *>(smem + S::kFixedBytes) +
+                         (kCluster ? cluster_ctarank() * RB * (D + 2) : 0);
         // A CTA holds at most two partial pieces: slot 1 for the head it starts
         // (it is that head's first CTA), slot 0 for the head it continues.
         const size_t pbase = ((size_t)blockIdx.x * 2 + ((int)blockIdx.x == mt.c_first ? 1 : 0)) * RB;
@@ -1146,10 +1148,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
                     Tq::store(static_cast<T *>(a.out) + ((size_t)mt.bh * a.rows + rg) * D + d, num / den);
             } else if constexpr (kCluster) {
                 float *pr = cl_part + r * (D + 2);
-                pr[d] = num;
+                st_cluster_f32(pr + d, 0u, num);
                 if (d == 0) {
-                    pr[D] = M;
-                    pr[D + 1] = den;
+                    st_cluster_f32(pr + D, 0u, M);
+                    st_cluster_f32(pr + D + 1, 0u, den);
                 }
             } else {
                 float *pr = a.part + (pbase + r) * (D + 4);
@@ -1170,41 +1172,44 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     }
 
     if constexpr (kCluster) {
-        // ---- merge the cluster's pieces in rank 0, from each CTA's shared memory ----
-        float *cl_part = reinterpret_cast<float *>(smem + S::kRingOff);
+        // ---- merge the cluster's pieces in rank 0 ----
+        const uint32_t crank = cluster_ctarank();
+        float *cl_base = reinterpret_cast<float *>(smem + S::kFixedBytes);
         if (n_pieces == 0) {  // an empty share: a piece of weight zero
-            for (int idx = tid; idx < RB * (D + 2); idx += S::kThreads) {
-                const int r = idx / (D + 2), d = idx % (D + 2);
-                cl_part[idx] = (d == D) ? kNegInf : 0.f;
-                (void)r;
-            }
+            float *pr = cl_base + crank * RB * (D + 2);
+            for (int idx = tid; idx < RB * (D + 2); idx += S::kThreads)
+                st_cluster_f32(pr + idx, 0u, (idx % (D + 2) == D) ? kNegInf : 0.f);
         }
-        cluster_sync_all();  // every piece written
-        if (cluster_ctarank() == 0 && *cl_ok) {
-            const int csize = (int)cluster_nctarank();
-            const int HR = a.H_kv * a.n_rowblocks;
-            const int u = (int)blockIdx.x / csize;
-            const int bh = (u / HR) * a.H_kv + (u % HR) / a.n_rowblocks, rb = (u % HR) % a.n_rowblocks;
-            for (int idx = tid; idx < RB * D; idx += S::kThreads) {
-                const int r = idx / D, d = idx % D;
-                const int rg = rb * RB + r;
-                if (rg >= a.rows) continue;
-                const float *pr = cl_part + r * (D + 2);
-                float M = kNegInf;
-                for (int k = 0; k < csize; ++k) M = fmaxf(M, ld_cluster_f32(pr + D, (uint32_t)k));
-                float num = 0.f, den = 0.f;
-                for (int k = 0; k < csize; ++k) {
-                    const float wt = safe_weight(ld_cluster_f32(pr + D, (uint32_t)k), M);
-                    num = fmaf(wt, ld_cluster_f32(pr + d, (uint32_t)k), num);
-                    den = fmaf(wt, ld_cluster_f32(pr + D + 1, (uint32_t)k), den);
+        cluster_arrive_release();  // this CTA's piece is in rank 0
+        if (crank == 0) {
+            cluster_wait_acquire();  // every piece is in
+            if (*cl_ok) {
+                const int csize = (int)cluster_nctarank();
+                const int HR = a.H_kv * a.n_rowblocks;
+                const int u = (int)blockIdx.x / csize;
+                const int bh = (u / HR) * a.H_kv + (u % HR) / a.n_rowblocks, rb = (u % HR) % a.n_rowblocks;
+                for (int idx = tid; idx < RB * D; idx += S::kThreads) {
+                    const int r = idx / D, d = idx % D;
+                    const int rg = rb * RB + r;
+                    if (rg >= a.rows) continue;
+                    float M = kNegInf;
+                    for (int k = 0; k < csize; ++k) M = fmaxf(M, cl_base[(k * RB + r) * (D + 2) + D]);
+                    float num = 0.f, den = 0.f;
+                    for (int k = 0; k < csize; ++k) {
+                        const float *pr = cl_base + (k * RB + r) * (D + 2);
+                        const float wt = safe_weight(pr[D], M);
+                        num = fmaf(wt, pr[d], num);
+                        den = fmaf(wt, pr[D + 1], den);
+                    }
+                    if constexpr (kQuant)  // values are stored / v_scale
+                        Tq::store(static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + d,
+                                  num / den * a.kv_scale.y);
+                    else
+                        Tq::store(static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + d, num / den);
                 }
-                if constexpr (kQuant)  // values are stored / v_scale
-                    Tq::store(static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + d, num / den * a.kv_scale.y);
-                else
-                    Tq::store(static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + d, num / den);
             }
         }
-        cluster_sync_all();  // rank 0 is done reading the others' shared memory
+        // (the other CTAs may exit now: no one reads their shared memory)
     } else if constexpr (kTicketMerge) {
         // ---- count this CTA's split pieces; merge the heads they complete ----
         n_pieces = min(n_pieces, 2);

@@ -451,22 +451,25 @@ __device__ __forceinline__ uint32_t cluster_nctarank()
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
     return r;
 }
-// fp32 load from the shared memory of CTA `rank` of this cluster, at the
+// fp32 store into the shared memory of CTA `rank` of this cluster, at the
 // offset that p has in this CTA's shared memory.
-__device__ __forceinline__ float ld_cluster_f32(const void *p, uint32_t rank)
+__device__ __forceinline__ void st_cluster_f32(void *p, uint32_t rank, float v)
 {
     uint32_t remote;
-    float v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
-// Every thread of every CTA of the cluster: arrive (releasing this thread's
-// shared-memory writes) and wait for all (acquiring theirs).
-__device__ __forceinline__ void cluster_sync_all()
+// Cluster barrier, all threads of the CTA: arrive, releasing this thread's
+// earlier shared-memory writes (local and remote) ...
+__device__ __forceinline__ void cluster_arrive_release()
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// ... and wait until every thread of the cluster that has not exited has
+// arrived, acquiring their writes.
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void raise_error(uint32_t *err_word, uint32_t bit)
