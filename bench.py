@@ -361,13 +361,14 @@ class Case:
     calls of one decode step, as the library's public API takes them."""
 
     def __init__(self, w, dev, *, path="fused", layout="contiguous", cache="same", page_size=64,
-                 page_order="shuffled", reuse=None):
+                 page_order="shuffled", reuse=None, flags=None):
         import kv_cache_decode_append_gb300 as kvd
         self.kvd = kvd
         self.w, self.dev = w, dev
         self.fused = path == "fused"
         self.paged = layout == "paged"
         self.e4m3 = cache == "e4m3"
+        self.flags = flags  # kvd_decode_step_flags (contiguous fused step): the caller's guarantees
         if self.e4m3 and (self.paged or w.dtype != "bf16"):
             raise SystemExit("an E4M3 cache needs a bf16 workload and the contiguous layout")
         self.cache_elem = 1 if self.e4m3 else 0
@@ -422,7 +423,7 @@ class Case:
                                            0.0, ws, err)
         elif self.fused:
             kvd.kvd_decode_step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], out, past_d, mp,
-                                0.0, ws, err)
+                                0.0, ws, err, flags=self.flags)
         else:
             if not attention_only:
                 kvd.kvd_append(x["k_cache"], x["v_cache"], x["k_new"], x["v_new"], past_d, mp, err)
@@ -555,17 +556,23 @@ def per_config_line(case, timer, steps, world, label, cores_all, with_oracle=Tru
     gbs = whole_job_gbs(case.step_bytes, n, el, world)
     line = {
         "workload": w.name, "N": w.N, "label": label, "path": "fused" if case.fused else "separate",
+        "flags": case.flags or 0,
         "us_per_layer_step": round(el / n / w.L * 1e6, 3), "gbs": round(gbs, 2),
         "frac": round(gbs / world / peak, 4), "step_bytes": case.step_bytes,
         "l2": "flushed before each step" if flush else "not flushed (step larger than twice the L2)",
         "steps": n,
-        "plan": {k: case.plan[k] for k in ("grid", "tensor_cores", "launches", "l2_prefetch", "rows_per_block")},
+        "plan": {k: case.plan[k] for k in ("grid", "tensor_cores", "launches", "early_start", "cluster", "rows_per_block")},
         "e2e": case.e2e(max(3, steps // 4), 2, world),
     }
     if with_oracle:
         line["oracle"] = oracle_times(case, cores_all)
     del g
     return line
+
+
+def kvd_stable_flag() -> int:
+    import kv_cache_decode_append_gb300 as kvd
+    return kvd.KVD_STEP_HISTORY_STABLE
 
 
 def memory_report(case, ws_bytes):
@@ -644,10 +651,16 @@ def run_gpu(args, w, rank, world, local):
         specs = [("gpt2s_1layer_p16_f32", None, {}), ("gpt2s_12layer_p1000_f32", None, {})]
         specs += [("gpt2s_chunked_p512_f32", n, {}) for n in wl.CHUNKED_N]
         specs += [("gpt2s_b8_p1023_bf16", None, {}), ("gpt2s_b8_p1023_bf16", None, {"layout": "paged"})]
+        # The same steps through kvd_decode_step_flags(KVD_STEP_HISTORY_STABLE): in this
+        # step nothing writes past_len or a layer's history between the layers' calls.
+        stable = {"flags": kvd_stable_flag()}
+        specs += [("gpt2s_12layer_p1000_f32", None, stable), ("gpt2s_chunked_p512_f32", 16, stable),
+                  ("gpt2s_b8_p1023_bf16", None, stable)]
         for name, n, opts in specs:
             wc = wl.WORKLOADS[name] if n is None else wl.with_n(wl.WORKLOADS[name], n)
             c = Case(wc, dev, **opts)
-            label = wc.describe() + (" (paged)" if opts else "")
+            label = wc.describe() + (" (paged)" if "layout" in opts else "") + \
+                (" (kvd_decode_step_flags: history stable)" if "flags" in opts else "")
             per_config.append(per_config_line(c, timer, args.steps, world, label, cores_all,
                                               with_oracle=rank == 0 and not opts))
             del c

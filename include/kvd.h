@@ -168,7 +168,7 @@ kvd_status kvd_decode_step(const void *q, void *k_cache, void *v_cache, const vo
  *     writes past_len or the cache rows below past_len[b] (the history).
  *     Typical in a model: the kernels ahead of a layer's step write q, k_new
  *     and v_new (and other layers' caches), and past_len advances once per
- *     token after the last layer.  For a small layer (kvd_plan_info.l2_prefetch
+ *     token after the last layer.  For a small layer (kvd_plan_info.early_start
  *     = 1) on a contiguous cache the kernel then reads past_len and loads its
  *     first K/V tiles before it waits for the previous kernel; q, k_new,
  *     v_new, the workspace and every write still wait.  Elsewhere the flag is
@@ -209,16 +209,15 @@ typedef struct kvd_plan_info {
                             1: the mma.sync tensor-core kernel (bf16 / fp16 caches with
                             4 .. 16 rows for D = 128, 8 .. 16 for D = 64; E4M3 caches
                             with D = 128); 0: the CUDA-core kernel */
-    int l2_prefetch;     /* 1: a small layer (K/V of at most 26 MiB at max_past_len, on the
-                            CUDA-core kernel): one CTA per SM, and each CTA prefetches its
-                            rows into L2 and lets the next kernel on the stream launch
-                            before it waits for the previous one, so consecutive calls
-                            overlap their HBM reads with each other's prologue and tail */
-    int cluster;         /* > 0: of those, a contiguous layer whose longest head fits in a few
-                            ring fills runs as one thread-block cluster of `cluster` CTAs per
-                            (b, h_kv, row block): each CTA loads its equal share of the head's
-                            keys at once and the shares merge through distributed shared
-                            memory (the workspace is then unused) */
+    int early_start;     /* 1: a small layer (K/V of at most 26 MiB at max_past_len, on the
+                            CUDA-core kernel): the next kernel on the stream may launch as
+                            soon as this one starts, so its CTAs take free SM slots and,
+                            with KVD_STEP_HISTORY_STABLE, start loading before this one ends */
+    int cluster;         /* > 0: such a layer whose longest head fits in a few ring fills
+                            runs as one thread-block cluster of `cluster` CTAs per
+                            (b, h_kv, row block): each CTA loads its equal share of the
+                            head's keys at once and the shares merge through distributed
+                            shared memory (the workspace is then unused) */
 } kvd_plan_info;
 
 kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len,

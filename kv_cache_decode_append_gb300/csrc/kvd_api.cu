@@ -176,20 +176,18 @@ constexpr int kMmaMinRowsE4m3 = 1;
 // 16-row mma.sync blocks would read each tile once per block.
 constexpr int kTc5MinRows = 17;
 // Small layers (K/V bytes of one call, counted at max_past_len, at most
-// kL2PrefetchMaxBytes, a fifth of GB300's L2) run on the CUDA-core kernel with
-// kArgL2Prefetch and kL2PrefetchCtasPerSm CTAs per SM: each layer then
-// occupies part of every SM, so the next calls' CTAs become resident early,
-// prefetch their rows into L2 and wait, and the stream of consecutive layers
-// keeps HBM busy through each layer's prologue and merge tail.
-#ifndef KVD_L2_PREFETCH_CTAS_PER_SM
-#define KVD_L2_PREFETCH_CTAS_PER_SM 2
+// kEarlyMaxBytes, a fifth of GB300's L2) run on the CUDA-core kernel with
+// kArgEarly: the next kernel on the stream may launch as soon as this one
+// starts, and kEarlyCtasPerSm CTAs per SM leave room for its CTAs.
+#ifndef KVD_EARLY_CTAS_PER_SM
+#define KVD_EARLY_CTAS_PER_SM 2
 #endif
-constexpr int kL2PrefetchCtasPerSm = KVD_L2_PREFETCH_CTAS_PER_SM;
-#ifndef KVD_L2_PREFETCH_MAX_BYTES
-#define KVD_L2_PREFETCH_MAX_BYTES (26LL << 20)
+constexpr int kEarlyCtasPerSm = KVD_EARLY_CTAS_PER_SM;
+#ifndef KVD_EARLY_MAX_BYTES
+#define KVD_EARLY_MAX_BYTES (26LL << 20)
 #endif
-constexpr long long kL2PrefetchMaxBytes = KVD_L2_PREFETCH_MAX_BYTES;
-// Small contiguous layers whose longest head needs at most kMaxCluster ring
+constexpr long long kEarlyMaxBytes = KVD_EARLY_MAX_BYTES;
+// Small layers whose longest head needs at most kMaxCluster ring
 // fills run in cluster mode: one thread-block cluster of C CTAs per
 // sequence-head, C = tiles of the longest head / ring stages (rounded up), so
 // that every CTA loads its whole share of the head at once (before the wait,
@@ -359,7 +357,7 @@ struct Plan {
     bool merge_pass;  // split heads merged by a second launch (else inside the kernel)
     bool mma;         // tensor-core kernel (16-row blocks, tiles by tensor map)
     bool tc5;         // tcgen05 kernel (128-row blocks, tiles and q by tensor map)
-    bool l2_prefetch; // small layer: kArgL2Prefetch, fewer CTAs per SM
+    bool early;       // small layer: kArgEarly, fewer CTAs per SM
     int cluster;      // > 0: cluster mode with this many CTAs per sequence-head
     size_t part_off, tickets_off, seg_off, ws_bytes;
 };
@@ -471,8 +469,8 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     // Small layers leave room on every SM for the calls that follow.
     const long long kv_bytes_hint =
         2LL * B * H_kv * ((long long)max_past_len + N) * D * elem_bytes(dtype);
-    pl->l2_prefetch = !pl->mma && !pl->tc5 && kv_bytes_hint <= kL2PrefetchMaxBytes;
-    pl->grid = sms * (pl->l2_prefetch && occ > kL2PrefetchCtasPerSm ? kL2PrefetchCtasPerSm : occ);
+    pl->early = !pl->mma && !pl->tc5 && kv_bytes_hint <= kEarlyMaxBytes;
+    pl->grid = sms * (pl->early && occ > kEarlyCtasPerSm ? kEarlyCtasPerSm : occ);
     const long long t_hint = (long long)max_past_len + N;
     pl->max_tiles = (int)((t_hint + pl->v.tile_keys - 1) / pl->v.tile_keys);
     // Heads split across CTAs: merged inside the kernel by the CTA that
@@ -482,11 +480,11 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     // tail of the last CTA.
     const long long units_hint =
         (long long)B * H_kv * pl->n_rowblocks * (pl->max_tiles + pl->v.piece_units);
-    pl->merge_pass = !pl->l2_prefetch && units_hint > (long long)kLongRangeUnits * pl->grid;
+    pl->merge_pass = !pl->early && units_hint > (long long)kLongRangeUnits * pl->grid;
     pl->launches = pl->merge_pass ? 2 : 1;
     if (!pl->merge_pass) pl->v = vt;
     pl->cluster = 0;
-    if (pl->l2_prefetch && !paged && pl->v.cluster_fn != nullptr && pl->v.stages > 0) {
+    if (pl->early && pl->v.cluster_fn != nullptr && pl->v.stages > 0) {
         const int c = (pl->max_tiles + pl->v.stages - 1) / pl->v.stages;
         const long long ctas = (long long)B * H_kv * pl->n_rowblocks * c;
         // (the pieces, c x RB rows of D + 2 floats, take the place of the tables)
@@ -598,7 +596,7 @@ kvd_status kvd_decode_plan(int B, int H_q, int H_kv, int D, int N, int max_past_
     info->workspace_bytes = pl.ws_bytes;
     info->rows_per_block = pl.rb;
     info->tensor_cores = pl.tc5 ? 2 : pl.mma ? 1 : 0;
-    info->l2_prefetch = pl.l2_prefetch ? 1 : 0;
+    info->early_start = pl.early ? 1 : 0;
     info->cluster = pl.cluster;
     return KVD_OK;
 }
@@ -711,10 +709,10 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
         a.block_table = paged != nullptr ? paged->block_table : nullptr;
     a.num_pages = paged != nullptr ? paged->num_pages : 0;
     a.page_shift = (short)page_shift;
-    a.flags = pl.l2_prefetch ? kArgL2Prefetch : 0;
+    a.flags = pl.early ? kArgEarly : 0;
     // (a promise about the history only helps the fused step of a small
     // contiguous layer: its K/V tiles then load before the wait)
-    if (pl.l2_prefetch && k_new != nullptr && paged == nullptr && (step_flags & KVD_STEP_HISTORY_STABLE))
+    if (pl.early && k_new != nullptr && paged == nullptr && (step_flags & KVD_STEP_HISTORY_STABLE))
         a.flags |= kArgHistoryStable;
     a.err_word = err_word;
     a.B = B;

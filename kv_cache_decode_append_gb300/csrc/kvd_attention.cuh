@@ -92,15 +92,14 @@ struct AttnArgs {
     float qscale;     // softmax scale * log2(e)
     int num_pages;    // paged only: pages in the pool
     short page_shift; // paged only: log2(page_size); page_size is a multiple of the tile keys
-    short flags;      // kArgL2Prefetch
+    short flags;      // kArgEarly, kArgHistoryStable
 };
-// AttnArgs::flags: before its griddepcontrol.wait, each CTA reads past_len as
-// a hint (clamped to [0, max_past_len]), prefetches the K/V rows, q rows and
-// new rows of its expected range into L2, and lets the next kernel on the
-// stream launch; after the wait it reads past_len again and works from that.
-// Chosen for layers small enough that several fit in L2 at once.
-constexpr short kArgL2Prefetch = 1;
-// AttnArgs::flags (with kArgL2Prefetch): the caller guarantees that no work
+// AttnArgs::flags: the CTAs let the next kernel on the stream launch as soon
+// as they start (before their own griddepcontrol.wait), so that its CTAs take
+// free SM slots early and, with a stable history, start their loads.  Chosen
+// for small layers, where a launch's fixed latencies are a large part of it.
+constexpr short kArgEarly = 1;
+// AttnArgs::flags (with kArgEarly): the caller guarantees that no work
 // queued before this call on the stream writes past_len or the cache rows
 // below past_len.  The CTAs then read past_len and fill their ring with K/V
 // tiles before griddepcontrol.wait; the q rows (second arrival on each full
@@ -186,6 +185,7 @@ struct TileMeta {
 constexpr int kMetaFirst = 1;  // first tile of a piece: the stage also carries the q rows
 constexpr int kMetaLast = 2;   // last tile of a piece
 constexpr int kMetaEnd = 4;    // no more work
+constexpr int kMetaSkip = 8;   // a speculative tile that turned out not to be needed: release it
 
 // One tile for one warp: keys warp*kKpw .. +kKpw of the tile, RB query rows.
 // q, K, V and the accumulators are held as fp32 pairs (E/2 per row) and
@@ -585,6 +585,21 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
         prefetch_page(a);
     }
 
+    // The history of the current head, once known (cluster mode fills with
+    // the host's bound first).
+    __device__ __forceinline__ void set_history(const AttnArgs &a, int P_)
+    {
+        P = P_;
+        T_b = P + a.N;
+    }
+
+    // Stage s (filled, not yet consumed) becomes a tile to skip.
+    __device__ __forceinline__ void skip_stage(TileMeta *meta, int s)
+    {
+        meta[s].flags = kMetaSkip;
+        pend_qb[s] = 0u;
+    }
+
     // The second arrival of stage s filled with kFillKvOnly: its q rows, if any.
     __device__ __forceinline__ void issue_pending(unsigned char *smem, uint64_t *full, int s)
     {
@@ -696,32 +711,24 @@ __device__ __forceinline__ void merge_pieces(const AttnArgs &a, const MergeJob &
 }
 
 // Units per sequence-head, prefix-summed over sequences by warp 0's scan:
-// pre[b] = units of sequences 0..b-1 per head, pl[b] = P_b.  A hint
-// (kArgL2Prefetch, before the wait) clamps P_b into [0, max_past_len] and
-// reads it through L2 only; otherwise a sequence with an invalid P_b gets no
-// units and CTA 0 reports it.
+// pre[b] = units of sequences 0..b-1 per head, pl[b] = P_b.  A sequence with
+// an invalid P_b gets no units; CTA 0 reports it, or (defer_error) returns
+// true for the caller to report later.
 template <typename S>
-__device__ __forceinline__ bool unit_prefix(const AttnArgs &a, int *pre, int *pl, int lane, bool hint,
-                                           bool defer_error = false)
+__device__ __forceinline__ bool unit_prefix(const AttnArgs &a, int *pre, int *pl, int lane, bool defer_error = false)
 {
-    bool bad = false;  // (defer_error: an invalid P_b, for the caller to report)
+    bool bad = false;
     int carry = 0;
     if (lane == 0) pre[0] = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
         const int b = b0 + lane;
         int units = 0;
         if (b < a.B) {
-            int P;
-            bool ok = true;
-            if (hint) {
-                P = min(max(__ldcg(a.past_len + b), 0), a.max_past_len);
-            } else {
-                P = __ldg(a.past_len + b);
-                ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
-                if (!ok && blockIdx.x == 0) {
-                    if (defer_error) bad = true;
-                    else raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
-                }
+            const int P = __ldg(a.past_len + b);
+            const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
+            if (!ok && blockIdx.x == 0) {
+                if (defer_error) bad = true;
+                else raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
             }
             units = ok ? (P + a.N + S::kTK - 1) / S::kTK + S::kPieceUnits : 0;
             pl[b] = P;
@@ -750,77 +757,15 @@ __device__ __forceinline__ void cta_range(const AttnArgs &a, const int *pre, lon
     *hi = blockIdx.x < *G ? *n_total * (blockIdx.x + 1) / *G : 0;
 }
 
-// Warp 0, before griddepcontrol.wait (kArgL2Prefetch): bulk-prefetch into L2
-// what the CTA's range [lo, hi) will read -- the K and V rows of its tiles
-// (one tile per lane at a time), the q rows of each head it touches and, in a
-// fused step, the new K/V rows of the heads whose last tile it holds.  pre /
-// pl are the hinted prefix; every address stays inside its buffer whatever
-// the hint (P_b <= max_past_len, and max_past_len + N <= T_max is checked on
-// the host), so a stale hint only costs useless prefetches.
-template <typename S, bool kFused, bool kPaged>
-__device__ __forceinline__ void l2_prefetch_range(const AttnArgs &a, const int *pre, const int *pl, int lane,
-                                                  long long lo, long long hi)
-{
-    if (lo >= hi) return;
-    const int HR = a.H_kv * a.n_rowblocks;
-    int b = 0, hb = a.B - 1;  // last b with pre[b] * HR <= lo
-    while (b < hb) {
-        const int mid = (b + hb + 1) / 2;
-        if ((long long)pre[mid] * HR <= lo) b = mid; else hb = mid - 1;
-    }
-    long long t = lo;
-    for (; b < a.B && t < hi; ++b) {
-        const int ub = pre[b + 1] - pre[b];
-        if (ub == 0) continue;
-        const long long sb = (long long)pre[b] * HR;
-        const int tb = ub - S::kPieceUnits;
-        const int T_b = pl[b] + a.N;
-        for (int hr = (int)((t - sb) / ub); hr < HR && t < hi; ++hr) {
-            const long long base = sb + (long long)hr * ub + S::kPieceUnits;  // unit of the head's tile 0
-            const int tin0 = (int)max(0LL, t - base);
-            const int tin1 = (int)min((long long)tb, hi - base);
-            t = base + tb;
-            if (tin1 <= tin0) continue;
-            const int h = hr / a.n_rowblocks, rb = hr % a.n_rowblocks;
-            const int bh = b * a.H_kv + h;
-            for (int tin = tin0 + lane; tin < tin1; tin += 32) {
-                const int k0 = tin * S::kTK;
-                const uint32_t bytes = (uint32_t)(min(S::kTK, T_b - k0) * S::kRowBytes);
-                size_t off;
-                if constexpr (kPaged) {
-                    const int pages = a.T_max >> a.page_shift;
-                    int page = __ldcg(a.block_table + (size_t)b * pages + (k0 >> a.page_shift));
-                    if ((unsigned)page >= (unsigned)a.num_pages) page = 0;
-                    off = ((((size_t)page * a.H_kv + h) << a.page_shift) + (k0 & ((1 << a.page_shift) - 1))) *
-                          S::kRowBytes;
-                } else {
-                    off = ((size_t)bh * a.T_max + k0) * S::kRowBytes;
-                }
-                prefetch_l2(static_cast<const unsigned char *>(a.k_cache) + off, bytes);
-                prefetch_l2(static_cast<const unsigned char *>(a.v_cache) + off, bytes);
-            }
-            if (lane == 0) {
-                const int q_rows = min(S::kRB, a.rows - rb * S::kRB);
-                prefetch_l2(static_cast<const unsigned char *>(a.q) + ((size_t)bh * a.rows + rb * S::kRB) * S::kQRowBytes,
-                            (uint32_t)(q_rows * S::kQRowBytes));
-                if constexpr (kFused) {
-                    if (tin1 == tb) {
-                        const size_t nrow = (size_t)bh * a.N * S::kQRowBytes;
-                        prefetch_l2(static_cast<const unsigned char *>(a.k_new) + nrow, (uint32_t)(a.N * S::kQRowBytes));
-                        prefetch_l2(static_cast<const unsigned char *>(a.v_new) + nrow, (uint32_t)(a.N * S::kQRowBytes));
-                    }
-                }
-            }
-        }
-        t = max(t, (long long)pre[b + 1] * HR);
-    }
-}
-
 // Cluster mode, thread 0: the CTA's piece of its cluster's sequence-head (an
 // equal share of the head's tiles by cluster rank) and its first ring fills.
-// Returns whether past_len of the head's sequence is valid (else the range is
-// empty and the sequence is skipped).
-template <typename S, typename Walk>
+// For a contiguous cache the share is first taken with the history at
+// max_past_len (the host's bound) while past_len is being read; if the real tile count is the same the
+// filled stages only get their history and row count corrected, else they are
+// marked to be skipped and the walk starts again.  Returns whether past_len
+// of the head's sequence is valid (else the range is empty and the sequence
+// is skipped).
+template <typename S, bool kPaged, typename Walk>
 __device__ __forceinline__ bool cluster_start(const AttnArgs &a, Walk &walk, unsigned char *smem, TileMeta *meta,
                                               uint64_t *full, int &issued, FillMode mode)
 {
@@ -828,18 +773,41 @@ __device__ __forceinline__ bool cluster_start(const AttnArgs &a, Walk &walk, uns
     const int HR = a.H_kv * a.n_rowblocks;
     const int u = (int)blockIdx.x / csize;  // the cluster's sequence-head (b, hr)
     const int b = u / HR, hr = u % HR;
-    const int P = __ldg(a.past_len + b);
+    const int P = __ldg(a.past_len + b);  // (in flight during the fills below)
+    if constexpr (kPaged) {
+        // (no speculation: block-table entries past a sequence's end need not
+        // name valid pages)
+        const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
+        const int tb = ok ? (P + a.N + S::kTK - 1) / S::kTK : 0;
+        walk.start_piece(a, b, hr, P, tb, tb * crank / csize, tb * (crank + 1) / csize, csize);
+        for (; issued < S::kStages && !walk.ended; ++issued)
+            walk.fill(a, nullptr, nullptr, smem, meta, full, issued, mode);
+        return ok;
+    }
+    const int tb_bound = (a.max_past_len + a.N + S::kTK - 1) / S::kTK;
+    walk.start_piece(a, b, hr, a.max_past_len, tb_bound, tb_bound * crank / csize, tb_bound * (crank + 1) / csize,
+                     csize);
+    for (; issued < S::kStages && !walk.ended; ++issued) walk.fill(a, nullptr, nullptr, smem, meta, full, issued, mode);
     const bool ok = past_len_ok(P, a.N, a.T_max, a.max_past_len);
     const int tb = ok ? (P + a.N + S::kTK - 1) / S::kTK : 0;
-    walk.start_piece(a, b, hr, P, tb, tb * crank / csize, tb * (crank + 1) / csize, csize);
-    for (; issued < S::kStages && !walk.ended; ++issued) walk.fill(a, nullptr, nullptr, smem, meta, full, issued, mode);
+    if (tb == tb_bound) {  // the same tiles: correct the history and the rows of each filled tile
+        walk.set_history(a, P);
+        for (int s = 0; s < issued; ++s)
+            if (!(meta[s].flags & kMetaEnd)) {
+                meta[s].P = P;
+                meta[s].nk = min(S::kTK, P + a.N - meta[s].tile_k0);
+            }
+    } else {
+        for (int s = 0; s < issued; ++s) walk.skip_stage(meta, s);
+        walk.start_piece(a, b, hr, P, tb, tb * crank / csize, tb * (crank + 1) / csize, csize);
+    }
     return ok;
 }
 
 // kFused: append inside (kvd_decode_step).  kTicketMerge: split heads are
 // merged at the end of this kernel (else by attn_merge_kernel).  kPaged: the
 // cache is paged (block table), else contiguous [B, H_kv, T_max, D].
-// kCluster (small layers, contiguous cache): the grid is one thread-block
+// kCluster (small layers): the grid is one thread-block
 // cluster per sequence-head; the cluster's CTAs split the head's tiles in equal
 // shares by rank, each loads its whole share into its ring and stores its
 // piece into rank 0's shared memory, and rank 0 merges them (no workspace, no
@@ -868,7 +836,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     const int warp = tid / 32, lane = tid % 32;
     const int grp = lane / S::kL, j = lane % S::kL;
 
-    const bool early = (a.flags & kArgL2Prefetch) != 0;
+    const bool early = (a.flags & kArgEarly) != 0;
     const bool stable = early && (a.flags & kArgHistoryStable) != 0;
     const FillMode refill = stable ? kFillTwo : kFillOne;
     if (tid == 0) {
@@ -888,16 +856,15 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     bool bad_past = false;
     int *cl_ok = reinterpret_cast<int *>(jobs);  // cluster mode: the head's sequence is valid
     if constexpr (kCluster) {
-        static_assert(!kPaged, "cluster mode serves contiguous caches");
         // (planned for small layers only: the next kernel may launch now)
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        if (stable && tid == 0) bad_past = !cluster_start<S>(a, walk, smem, meta, full, issued, kFillKvOnly);
+        if (stable && tid == 0) bad_past = !cluster_start<S, kPaged>(a, walk, smem, meta, full, issued, kFillKvOnly);
         asm volatile("griddepcontrol.wait;" ::: "memory");
         if (tid == 0) {
             if (stable) {
                 for (int p = 0; p < issued; ++p) walk.issue_pending(smem, full, p);  // the q rows
             } else {
-                bad_past = !cluster_start<S>(a, walk, smem, meta, full, issued, kFillOne);
+                bad_past = !cluster_start<S, kPaged>(a, walk, smem, meta, full, issued, kFillOne);
             }
             *cl_ok = bad_past ? 0 : 1;
             // (one report per sequence: the first rank of its first head's cluster)
@@ -907,30 +874,19 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
         __syncthreads();
     } else {
     if (early) {
-        // Small layers: let the next kernel launch now, so that its CTAs
-        // prefetch their own rows while this grid runs, and prefetch this
-        // CTA's rows into L2 before waiting: from the hinted split, or with
-        // a stable history from the exact one, whose first K/V tiles then go
-        // straight into the ring.
+        // Small layers: the next kernel may launch now (its CTAs take the SM
+        // slots that are free and wait in their turn).  With a stable
+        // history, the split and the first K/V tiles need nothing from the
+        // previous kernel: start them before waiting.
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        if (warp == 0) {
-            bad_past = unit_prefix<S>(a, pre, pl, lane, !stable, true);
-            long long n_total, G, lo, hi;
-            cta_range(a, pre, &n_total, &G, &lo, &hi);
-            if (stable && lane == 0) {
+        if (stable && warp == 0) {
+            bad_past = unit_prefix<S>(a, pre, pl, lane, true);
+            if (lane == 0) {
+                long long n_total, G, lo, hi;
+                cta_range(a, pre, &n_total, &G, &lo, &hi);
                 walk.start(a, pre, pl, lo, hi, n_total, G);
                 for (; issued < S::kStages && !walk.ended; ++issued)
                     walk.fill(a, pre, pl, smem, meta, full, issued, kFillKvOnly);
-            }
-            // CTAs below the SM count are the first to find a free slot (the
-            // grid is dispatched in order): they also prefetch the ranges of
-            // CTAs c + SMs, c + 2 SMs, ..., which become resident only as the
-            // previous grid's CTAs exit.
-            uint32_t nsm;
-            asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
-            for (long long c = blockIdx.x; c < G; c += nsm) {
-                l2_prefetch_range<S, kFused, kPaged>(a, pre, pl, lane, n_total * c / G, n_total * (c + 1) / G);
-                if (blockIdx.x >= nsm) break;
             }
         }
     }
@@ -947,7 +903,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     __syncthreads();  // barrier initialisation visible to every thread
 
     if (warp == 0 && !stable) {
-        unit_prefix<S>(a, pre, pl, lane, false);
+        unit_prefix<S>(a, pre, pl, lane);
         if (lane == 0) {
             long long n_total, G, lo, hi;
             cta_range(a, pre, &n_total, &G, &lo, &hi);
@@ -991,6 +947,11 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
         }
         const TileMeta mt = meta[s];
         if (mt.flags & kMetaEnd) break;
+        if (mt.flags & kMetaSkip) {  // (cluster mode: a speculative tile, not needed)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            continue;
+        }
         const unsigned char *Ks = smem + S::kRingOff + s * 2 * S::kTileBytes;
         const unsigned char *Vs = Ks + S::kTileBytes;
 
@@ -1357,9 +1318,9 @@ template <typename T, int D, int RB, bool kTicketMerge, bool kPaged, typename C 
     v.fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, kTicketMerge, kPaged, C>);
     if constexpr (kTicketMerge) v.merge_fn = nullptr;
     else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, RB, kQuant>);
-    if constexpr (kTicketMerge && !kPaged) {  // (built with the in-kernel-merge, contiguous variants)
-        v.cluster_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false, true, false, C, true>);
-        v.cluster_fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, true, false, C, true>);
+    if constexpr (kTicketMerge) {  // (built with the in-kernel-merge variants)
+        v.cluster_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, false, true, kPaged, C, true>);
+        v.cluster_fused_fn = reinterpret_cast<const void *>(&attn_balanced_kernel<T, D, RB, true, true, kPaged, C, true>);
     }
     v.threads = S::kThreads;
     v.fixed_smem_bytes = S::kFixedBytes;

@@ -124,14 +124,6 @@ __device__ __forceinline__ void bulk_load_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
-// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes a
-// multiple of 16).  A hint only: nothing completes, nothing is written, and
-// later writes by other grids still reach the line in L2 (the coherence point).
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // 2-D tiled bulk (TMA) load of one box of a tensor map (a kernel parameter)
 // at element coordinates (x, y) into shared memory, completing on bar.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar,

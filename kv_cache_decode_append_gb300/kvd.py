@@ -56,7 +56,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("tile_keys", ctypes.c_int), ("max_tiles", ctypes.c_int), ("grid", ctypes.c_int),
                 ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("launches", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_size_t), ("rows_per_block", ctypes.c_int),
-                ("tensor_cores", ctypes.c_int), ("l2_prefetch", ctypes.c_int),
+                ("tensor_cores", ctypes.c_int), ("early_start", ctypes.c_int),
                 ("cluster", ctypes.c_int)]
 
 
@@ -206,7 +206,7 @@ def kvd_decode_plan(B: int, H_q: int, H_kv: int, D: int, N: int, max_past_len: i
     ``tensor_cores``: 0 the CUDA-core kernel, 1 the mma.sync tensor-core kernel (16-row
     blocks), 2 the tcgen05 kernel (128-row blocks, for more than 16 query rows per KV
     head); ``launches`` 2 when split heads are merged by the separate merge pass;
-    ``l2_prefetch`` 1 for small layers (the next kernel on the stream may start early);
+    ``early_start`` 1 for small layers (the next kernel on the stream may start early);
     ``cluster`` > 0 when such a layer runs as one thread-block cluster of that many CTAs
     per KV head."""
     code = _NAME_DTYPE[dtype] if isinstance(dtype, str) else _TORCH_DTYPE[dtype]

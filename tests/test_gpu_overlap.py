@@ -1,9 +1,8 @@
 """Consecutive decode steps that start before the previous kernel finishes.
 
-Small layers (kvd_plan_info.l2_prefetch) let the next kernel on the stream
-launch early: its CTAs prefetch their rows into L2 and, with
-KVD_STEP_HISTORY_STABLE, load their first K/V tiles before they wait for the
-previous kernel.  Only what the previous kernel may write has to wait: q, the
+Small layers (kvd_plan_info.early_start) let the next kernel on the stream
+launch early: with KVD_STEP_HISTORY_STABLE its CTAs read past_len and load
+their first K/V tiles before they wait for the previous kernel.  Only what the previous kernel may write has to wait: q, the
 new rows, the workspace.  These tests chain layers whose q, k_new and v_new
 are the previous layer's output, so a read issued before the wait would see
 stale data, and require the chained results to be bit-identical to layers run
@@ -81,7 +80,7 @@ CASES = [  # (B, H, D, N, T_max, past, dtype)
 def test_chained_layers_match_serial(case, flags, graph):
     B, H, D, N, T_max, past, dtype = case
     w = wl.Workload(0, "chain", L=1, B=B, H_q=H, H_kv=H, D=D, N=N, dtype=dtype, T_max=T_max, P=0)
-    assert kvd.kvd_decode_plan(B, H, H, D, N, max(past), w.torch_dtype)["l2_prefetch"] == 1
+    assert kvd.kvd_decode_plan(B, H, H, D, N, max(past), w.torch_dtype)["early_start"] == 1
     layers = 6
     ins_ref, ref = _chain(w, past, layers, None)
     ins, got = _chain(w, past, layers, flags, graph=graph)
@@ -97,7 +96,7 @@ def test_small_workloads_run_in_cluster_mode(name):
     CTAs per KV head, shares merged in distributed shared memory)."""
     w = wl.WORKLOADS[name]
     plan = kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, int(wl.past_lens(w).max()), w.torch_dtype)
-    assert plan["l2_prefetch"] == 1 and plan["cluster"] >= 2
+    assert plan["early_start"] == 1 and plan["cluster"] >= 2
     assert plan["grid"] == w.B * w.H_kv * -(-w.group * w.N // plan["rows_per_block"]) * plan["cluster"]
 
 
