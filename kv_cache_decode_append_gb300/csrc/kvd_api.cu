@@ -336,6 +336,10 @@ kvd_status cluster_fits(int dev, const void *fn, int threads, int smem, int c, b
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+#ifdef KVD_TIMEOUT_TEST
+int g_test_stall = 0;  // test builds: plant kArgTestStall in the next launches
+#endif
+
 int elem_bytes(kvd_dtype dt)
 {
     switch (dt) {
@@ -714,6 +718,9 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     // contiguous layer: its K/V tiles then load before the wait)
     if (pl.early && k_new != nullptr && paged == nullptr && (step_flags & KVD_STEP_HISTORY_STABLE))
         a.flags |= kArgHistoryStable;
+#ifdef KVD_TIMEOUT_TEST
+    if (g_test_stall) a.flags |= kArgTestStall;
+#endif
     a.err_word = err_word;
     a.B = B;
     a.H_kv = H_kv;
@@ -991,6 +998,12 @@ size_t kvd_cache_bytes(int L, int B, int H_kv, int D, int T, kvd_dtype dtype)
     if (s == 0 || L < 0 || B < 0 || H_kv < 0 || D < 0 || T < 0) return 0;
     return (size_t)2 * (size_t)L * (size_t)H_kv * (size_t)D * (size_t)T * (size_t)B * (size_t)s;
 }
+
+#ifdef KVD_TIMEOUT_TEST
+// Test builds only (not part of include/kvd.h): make the next launches stall
+// the first pipeline stage of every CTA so that the bounded waits run out.
+void kvd_test_inject_stall(int on) { g_test_stall = on; }
+#endif
 
 const char *kvd_status_string(kvd_status status)
 {

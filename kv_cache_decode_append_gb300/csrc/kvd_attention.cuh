@@ -105,6 +105,12 @@ constexpr short kArgEarly = 1;
 // tiles before griddepcontrol.wait; the q rows (second arrival on each full
 // barrier), the new rows of a fused step and every write wait for it.
 constexpr short kArgHistoryStable = 2;
+#ifdef KVD_TIMEOUT_TEST
+// Test builds only: the first tile fill of every CTA expects 16 bytes more
+// than its copies bring, so that stage never completes and every wait for it
+// runs out (kWaitLimitNs is 2 ms in those builds).  Nothing is left in flight.
+constexpr short kArgTestStall = 4;
+#endif
 
 // How RangeWalk::fill arms a stage's full barrier.
 enum FillMode {
@@ -158,7 +164,8 @@ template <typename T, int D, int RB, typename C = T> struct AttnShape {
     static constexpr int kBarOff = kMetaOff + kStages * 32;
     static constexpr int kJobOff = kBarOff + 2 * kStages * 8;     // after the full and empty barriers
     static constexpr int kPageOff = kJobOff + 32;                   // two pieces to count (4 ints each)
-    static constexpr int kFixedBytes = kPageOff + 16;               // physical page of each stage (paged)
+    static constexpr int kCtlOff = kPageOff + 16;                   // physical page of each stage (paged)
+    static constexpr int kFixedBytes = kCtlOff + 16;                // AbortCtl words
 
     static_assert(kRowBytes % 16 == 0, "rows must be whole 16-byte chunks");
     static_assert(kQChunks >= 1, "q chunks per cache chunk");
@@ -356,6 +363,48 @@ __device__ __forceinline__ float safe_weight(float m, float M)
     return (m == __int_as_float(0xff800000)) ? 0.f : exp2f(m - M);
 }
 
+// Giving up on a wait (the CUDA-core and mma.sync kernels).  A wait that runs
+// out of time -- which a healthy GPU never sees -- must not leave the CTA's
+// threads on different paths: the piece epilogues contain CTA barriers, so
+// every thread has to step through the same ring positions.  Thread 0
+// publishes how many positions it has described (their TileMeta written)
+// before it can block at a CTA barrier, and once its own warp gives up it
+// describes no more and publishes that count as the last; a warp that has
+// given up steps on through described positions without waiting for their
+// data (its results are garbage, flagged by KVD_DEVERR_TIMEOUT) and stops
+// where the walk stops.  A stage is refilled only after every warp released
+// it, which a warp that gave up never does, so no barrier is ever armed while
+// its previous phase is open; thread 0 waits (kDrainLimitNs) for its copies
+// still in flight before the CTA exits.
+struct AbortCtl {
+    volatile int *w;  // [0] abort, [1] positions described, [2] final count + 1 (0: not yet)
+
+    __device__ __forceinline__ void init() const
+    {
+        w[0] = 0;
+        w[1] = 0;
+        w[2] = 0;
+    }
+    __device__ __forceinline__ const volatile int *flag() const { return w; }
+    __device__ __forceinline__ void set_abort() const { w[0] = 1; }
+    __device__ __forceinline__ bool aborted() const { return w[0] != 0; }
+    // thread 0, after writing the TileMeta of positions < n
+    __device__ __forceinline__ void described(int n) const { st_release_cta(w + 1, n); }
+    __device__ __forceinline__ void final_count(int n) const { st_release_cta(w + 2, n + 1); }
+    // A thread that gave up, at position pos: whether pos is described (its
+    // TileMeta may be read), else the walk stops before it.  Bounded.
+    __device__ __forceinline__ bool describable(int pos) const
+    {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t it = 0;; ++it) {
+            if (pos < ld_acquire_cta(w + 1)) return true;
+            const int f = ld_acquire_cta(w + 2);
+            if (f != 0) return pos < f - 1;
+            if ((it & 63u) == 0u && global_timer_ns() - t0 > 2 * kDrainLimitNs) return false;
+        }
+    }
+};
+
 // CTA whose range [c*n/G, (c+1)*n/G) holds flattened unit t.  With G <= n
 // every range is non-empty, so the CTAs holding a head's tiles are consecutive.
 __device__ __forceinline__ int owner_cta(long long t, long long n, long long G)
@@ -384,6 +433,17 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
     int page_next;          // paged: physical page of the next tile (loaded one tile ahead)
     const unsigned char *pend_q[S::kStages];  // kFillKvOnly: the q rows each stage still has to load
     uint32_t pend_qb[S::kStages];
+#ifdef KVD_TIMEOUT_TEST
+    bool stalled;  // kArgTestStall: the stall has been planted
+    __device__ __forceinline__ uint32_t stall_bytes(const AttnArgs &a)
+    {
+        if (!(a.flags & kArgTestStall) || stalled) return 0u;
+        stalled = true;
+        return 16u;
+    }
+#else
+    __device__ __forceinline__ uint32_t stall_bytes(const AttnArgs &) { return 0u; }
+#endif
     const int32_t *bt_row;  // paged: block-table row of the current sequence
     const void *tm_k, *tm_v;  // tensor-map tiles (S::kTma): the K and V tensor maps
 
@@ -437,6 +497,9 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
                                                 int tin1, int n_chunks_)
     {
         policy = l2_evict_first_policy();
+#ifdef KVD_TIMEOUT_TEST
+        stalled = false;
+#endif
         HR = 0x7fffffff;
         b = b_;
         hr = hr_;
@@ -460,6 +523,9 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
                                           long long hi_, long long n_, long long G_)
     {
         policy = l2_evict_first_policy();
+#ifdef KVD_TIMEOUT_TEST
+        stalled = false;
+#endif
         HR = a.H_kv * a.n_rowblocks;
         hi = hi_;
         n = n_;
@@ -546,7 +612,7 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
             // whole boxes of kTK rows (rows past the head are masked, or zero
             // past the tensor), 128-byte swizzled, kBoxes per K or V tile
             (void)off;
-            mbar_arrive_expect_tx(&full[s], 2u * S::kTileBytes + qbytes);
+            mbar_arrive_expect_tx(&full[s], 2u * S::kTileBytes + qbytes + stall_bytes(a));
             int y;  // first row of the tile in the tensor map's [rows, D] view
             if constexpr (kPaged)
                 y = ((page * a.H_kv + (bh - b * a.H_kv)) << a.page_shift) + (mt.tile_k0 & ((1 << a.page_shift) - 1));
@@ -558,7 +624,7 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
                 tma_load_2d(dst + S::kTileBytes + bx * S::kBoxBytes, tm_v, bx * S::kBoxCols, y, &full[s], policy);
             }
         } else {
-            mbar_arrive_expect_tx(&full[s], 2u * bytes + qbytes);
+            mbar_arrive_expect_tx(&full[s], 2u * bytes + qbytes + stall_bytes(a));
             bulk_load_g2s(dst, kg + off, bytes, &full[s], policy);
             bulk_load_g2s(dst + S::kTileBytes, vg + off, bytes, &full[s], policy);
         }
@@ -831,6 +897,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     MergeJob *jobs = reinterpret_cast<MergeJob *>(smem + S::kJobOff);  // this CTA's split pieces (two at most)
     int *pre = reinterpret_cast<int *>(smem + S::kFixedBytes);  // [B + 1] unit prefix per head
     int *pl = pre + a.B + 1;                                     // [B] history lengths
+    const AbortCtl ctl{reinterpret_cast<volatile int *>(smem + S::kCtlOff)};
 
     const int tid = threadIdx.x;
     const int warp = tid / 32, lane = tid % 32;
@@ -845,6 +912,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
             mbar_init(&full[s], stable ? 2 : 1);  // (stable: K/V before the wait, q after)
             mbar_init(&empty[s], S::kNW);
         }
+        ctl.init();
         fence_mbar_init();
     }
     // Warp 0 forms the unit prefix over sequences and thread 0 starts the ring
@@ -867,6 +935,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
                 bad_past = !cluster_start<S, kPaged>(a, walk, smem, meta, full, issued, kFillOne);
             }
             *cl_ok = bad_past ? 0 : 1;
+            ctl.described(issued);
             // (one report per sequence: the first rank of its first head's cluster)
             if (bad_past && cluster_ctarank() == 0 && ((int)blockIdx.x / (int)cluster_nctarank()) % (a.H_kv * a.n_rowblocks) == 0)
                 raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
@@ -899,6 +968,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     if (stable && warp == 0 && lane == 0) {
         if (bad_past) raise_error(a.err_word, KVD_DEVERR_PAST_LEN);
         for (int p = 0; p < issued; ++p) walk.issue_pending(smem, full, p);  // the q rows
+        ctl.described(issued);
     }
     __syncthreads();  // barrier initialisation visible to every thread
 
@@ -909,6 +979,7 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
             cta_range(a, pre, &n_total, &G, &lo, &hi);
             walk.start(a, pre, pl, lo, hi, n_total, G);
             for (; issued < S::kStages && !walk.ended; ++issued) walk.fill(a, pre, pl, smem, meta, full, issued);
+            ctl.described(issued);
         }
     }
     }  // (not kCluster)
@@ -917,39 +988,49 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     f32x2 o[RB][S::kE / 2];
     float m_run[RB], l_run[RB];
     int lim[RB];
-    bool timed_out = false;
-    int first_unwaited = -1;  // first ring position this thread gave up waiting for
+    bool gave_up = false;     // this warp no longer waits for data (see AbortCtl)
+    int first_unwaited = -1;  // thread 0: first ring position whose copies it did not see land
     int n_pieces = 0;         // split pieces computed so far (two at most)
 
     for (int pos = 0;; ++pos) {  // until the end marker
         const int s = pos % S::kStages;
         const uint32_t ph = (uint32_t)(pos / S::kStages) & 1u;
-        if (tid == 0) {
-            // Position pos must have been issued before anyone waits for it; its
-            // slot frees as soon as the slower warps release pos - STAGES.
-            while (issued <= pos && !walk.ended) {
-                const int fs = issued % S::kStages;
-                const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
-                if (!timed_out && !mbar_wait_bounded(&empty[fs], fph)) {
-                    timed_out = true;
-                    raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+        if (!gave_up) {
+            if (tid == 0) {
+                // Position pos must have been issued before anyone waits for it; its
+                // slot frees as soon as the slower warps release pos - STAGES.
+                while (issued <= pos && !walk.ended) {
+                    const int fs = issued % S::kStages;
+                    const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
+                    const int r = mbar_wait_or_abort(&empty[fs], fph, ctl.flag());
+                    if (r != 0) {
+                        if (r == 1) {
+                            ctl.set_abort();
+                            raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+                        }
+                        break;
+                    }
+                    walk.fill(a, pre, pl, smem, meta, full, fs, refill);
+                    ++issued;
                 }
-                walk.fill(a, pre, pl, smem, meta, full, fs, refill);
-                ++issued;
             }
+            const int r = mbar_wait_or_abort(&full[s], ph, ctl.flag());
+            if (r == 1) {
+                ctl.set_abort();
+                raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+            }
+            gave_up = __any_sync(0xffffffffu, r != 0);  // (warp-uniform: the tile code shuffles)
+            if (gave_up && tid == 0) first_unwaited = pos;
         }
-        if (!timed_out && !mbar_wait_bounded(&full[s], ph)) {
-            // Keep the same control flow as every other thread (the metadata is
-            // valid even if the data never landed); the result is flagged.
-            timed_out = true;
-            first_unwaited = pos;
-            raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+        if (gave_up) {
+            if (tid == 0) ctl.final_count(issued);
+            if (!ctl.describable(pos)) break;
         }
         const TileMeta mt = meta[s];
         if (mt.flags & kMetaEnd) break;
         if (mt.flags & kMetaSkip) {  // (cluster mode: a speculative tile, not needed)
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (lane == 0 && !gave_up) mbar_arrive(&empty[s]);
             continue;
         }
         const unsigned char *Ks = smem + S::kRingOff + s * 2 * S::kTileBytes;
@@ -985,8 +1066,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
 
         const int k_end = mt.tile_k0 + mt.nk;
         // Tiles below every row's limit (and, in a fused step, below the new
-        // keys) take the unmasked path; the rest the masked one.
-        if (mt.tile_k0 + S::kTK <= mt.P + (kFused ? 0 : 1)) {
+        // keys) take the unmasked path; the rest the masked one.  (A warp that
+        // gave up computes nothing and writes nothing.)
+        if (gave_up) {
+        } else if (mt.tile_k0 + S::kTK <= mt.P + (kFused ? 0 : 1)) {
             attn_tile<T, D, RB, false, kFused, false, C>(Ks, Vs, qv, o, m_run, l_run, warp, grp, j, mt.tile_k0,
                                                          lim, k_end, mt.P, nullptr, nullptr, nullptr, nullptr);
         } else {
@@ -1017,10 +1100,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
                                                          lim, k_end, mt.P, kn, vn, kc, vc, kvs);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with slot s
+        if (lane == 0 && !gave_up) mbar_arrive(&empty[s]);  // this warp is done with slot s
 
         // Opportunistic refill: if every warp has released the slot, issue now.
-        if (tid == 0 && !walk.ended && issued < pos + 1 + S::kStages) {
+        if (tid == 0 && !gave_up && !walk.ended && issued < pos + 1 + S::kStages) {
             const int fs = issued % S::kStages;
             const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
             if (mbar_test_wait(&empty[fs], fph)) {
@@ -1056,6 +1139,9 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
                 m_run[r] = M;
             }
         }
+        // (thread 0 may now block at a CTA barrier: what it has described must
+        // be known to warps that gave up, so that they can reach it too)
+        if (tid == 0) ctl.described(issued);
         __syncthreads();  // the previous piece's readers are done with the shared area
         if (grp == 0) {
 #pragma unroll
@@ -1132,6 +1218,10 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
         }
     }
 
+    if (tid == 0) {  // (as above: the barriers below need every thread)
+        ctl.described(issued);
+        ctl.final_count(issued);
+    }
     if constexpr (kCluster) {
         // ---- merge the cluster's pieces in rank 0 ----
         const uint32_t crank = cluster_ctarank();
@@ -1201,13 +1291,13 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
         }
     }
 
-    if (tid == 0 && timed_out && first_unwaited >= 0) {
+    if (tid == 0 && gave_up && first_unwaited >= 0) {
         // Copies that may still be in flight must land before the CTA exits:
         // wait for every issued position from the first abandoned one, one deadline.
         const uint64_t t0 = global_timer_ns();
         for (int p = first_unwaited; p < issued; ++p) {
             const uint32_t ph = (uint32_t)(p / S::kStages) & 1u;
-            while (!mbar_try_wait(&full[p % S::kStages], ph) && global_timer_ns() - t0 < kWaitLimitNs) {
+            while (!mbar_try_wait(&full[p % S::kStages], ph) && global_timer_ns() - t0 < kDrainLimitNs) {
             }
         }
     }

@@ -74,7 +74,8 @@ template <typename T, int D, typename C = T> struct MmaShape {
     static constexpr int kBarOff = kMetaOff + kStages * 32;
     static constexpr int kJobOff = kBarOff + 2 * kStages * 8;
     static constexpr int kPageOff = kJobOff + 32;
-    static constexpr int kFixedBytes = kPageOff + 16;
+    static constexpr int kCtlOff = kPageOff + 16;    // AbortCtl words
+    static constexpr int kFixedBytes = kCtlOff + 16;
 
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(kBoxBytes % 1024 == 0 && kQOff % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
@@ -425,12 +426,14 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         return;
     }
 
+    const AbortCtl ctl{reinterpret_cast<volatile int *>(smem + S::kCtlOff)};
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < S::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], S::kNW);
         }
+        ctl.init();
         fence_mbar_init();
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -470,7 +473,8 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
             walk.tm_k = &tm_k;
             walk.tm_v = &tm_v;
             walk.start(a, pre, pl, lo, hi, n_total, G);
-            for (; issued < S::kStages; ++issued) walk.fill(a, pre, pl, smem, meta, full, issued);
+            for (; issued < S::kStages && !walk.ended; ++issued) walk.fill(a, pre, pl, smem, meta, full, issued);
+            ctl.described(issued);
         }
     }
 
@@ -479,29 +483,41 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
     float m_run[2], l_run[2];
     float sfac[2];  // E4M3: per-row score factor (see mma_tile_e4m3)
     int lim[2];
-    bool timed_out = false;
+    bool gave_up = false;  // this warp no longer waits for data (AbortCtl)
     int first_unwaited = -1;
     int n_pieces = 0;
 
     for (int pos = 0;; ++pos) {
         const int s = pos % S::kStages;
         const uint32_t ph = (uint32_t)(pos / S::kStages) & 1u;
-        if (tid == 0) {
-            while (issued <= pos && !walk.ended) {
-                const int fs = issued % S::kStages;
-                const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
-                if (!timed_out && !mbar_wait_bounded(&empty[fs], fph)) {
-                    timed_out = true;
-                    raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+        if (!gave_up) {
+            if (tid == 0) {
+                while (issued <= pos && !walk.ended) {
+                    const int fs = issued % S::kStages;
+                    const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
+                    const int r = mbar_wait_or_abort(&empty[fs], fph, ctl.flag());
+                    if (r != 0) {
+                        if (r == 1) {
+                            ctl.set_abort();
+                            raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+                        }
+                        break;
+                    }
+                    walk.fill(a, pre, pl, smem, meta, full, fs);
+                    ++issued;
                 }
-                walk.fill(a, pre, pl, smem, meta, full, fs);
-                ++issued;
             }
+            const int r = mbar_wait_or_abort(&full[s], ph, ctl.flag());
+            if (r == 1) {
+                ctl.set_abort();
+                raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+            }
+            gave_up = __any_sync(0xffffffffu, r != 0);  // (warp-uniform: the MMAs are warp-wide)
+            if (gave_up && tid == 0) first_unwaited = pos;
         }
-        if (!timed_out && !mbar_wait_bounded(&full[s], ph)) {
-            timed_out = true;
-            first_unwaited = pos;
-            raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
+        if (gave_up) {
+            if (tid == 0) ctl.final_count(issued);
+            if (!ctl.describable(pos)) break;
         }
         const TileMeta mt = meta[s];
         if (mt.flags & kMetaEnd) break;
@@ -577,7 +593,8 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         }
 
         const int k_end = mt.tile_k0 + mt.nk;
-        if (mt.tile_k0 + S::kTK <= mt.P + (kFused ? 0 : 1)) {
+        if (gave_up) {  // (computes nothing, writes nothing)
+        } else if (mt.tile_k0 + S::kTK <= mt.P + (kFused ? 0 : 1)) {
             if constexpr (k8)
                 mma_tile_e4m3<D, false>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, sfac);
             else
@@ -614,10 +631,10 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         // (a piece's last tile keeps its slot for the merge below)
         if (!(mt.flags & kMetaLast)) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (lane == 0 && !gave_up) mbar_arrive(&empty[s]);
         }
 
-        if (tid == 0 && !walk.ended && issued < pos + 1 + S::kStages) {
+        if (tid == 0 && !gave_up && !walk.ended && issued < pos + 1 + S::kStages) {
             const int fs = issued % S::kStages;
             const uint32_t fph = ((uint32_t)(issued / S::kStages) & 1u) ^ 1u;
             if (mbar_test_wait(&empty[fs], fph)) {
@@ -695,6 +712,9 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
                 }
             }
         };
+        // (thread 0 may now block at a CTA barrier: what it has described must
+        // be known to warps that gave up, so that they can reach it too)
+        if (tid == 0) ctl.described(issued);
         __syncthreads();  // every warp is done with the slot's K, V and q (or the previous merge)
         if constexpr (S::kMergePhases == 2) {
             if (warp >= S::kMergeWarps) exchange(warp - S::kMergeWarps, false);
@@ -738,7 +758,7 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         // the slot is free again (its generic writes ordered before the next bulk copy)
         fence_proxy_async_shared();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0 && !gave_up) mbar_arrive(&empty[s]);
         if constexpr (kTicketMerge) {
             if (!single) {
                 if (tid == 0 && n_pieces < 2) jobs[n_pieces] = MergeJob{mt.bh, mt.rb, mt.c_first, mt.n_chunks};
@@ -747,6 +767,10 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         }
     }
 
+    if (tid == 0) {  // (as above: the barriers below need every thread)
+        ctl.described(issued);
+        ctl.final_count(issued);
+    }
     if constexpr (kTicketMerge) {
         n_pieces = min(n_pieces, 2);
         __syncthreads();
@@ -773,11 +797,11 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         }
     }
 
-    if (tid == 0 && timed_out && first_unwaited >= 0) {
+    if (tid == 0 && gave_up && first_unwaited >= 0) {
         const uint64_t t0 = global_timer_ns();
         for (int p = first_unwaited; p < issued; ++p) {
             const uint32_t ph2 = (uint32_t)(p / S::kStages) & 1u;
-            while (!mbar_try_wait(&full[p % S::kStages], ph2) && global_timer_ns() - t0 < kWaitLimitNs) {
+            while (!mbar_try_wait(&full[p % S::kStages], ph2) && global_timer_ns() - t0 < kDrainLimitNs) {
             }
         }
     }

@@ -479,10 +479,10 @@ __global__ void __launch_bounds__(224, 1)
                 const uint64_t t0 = global_timer_ns();
                 for (int p = max(0, issued - S::kStages); p < issued; ++p)
                     while (!mbar_try_wait(&full[p % S::kStages], (uint32_t)(p / S::kStages) & 1u) &&
-                           global_timer_ns() - t0 < kWaitLimitNs) {
+                           global_timer_ns() - t0 < kDrainLimitNs) {
                     }
                 if (q_loads > 0)
-                    while (!mbar_try_wait(q_full, (uint32_t)(q_loads - 1) & 1u) && global_timer_ns() - t0 < kWaitLimitNs) {
+                    while (!mbar_try_wait(q_full, (uint32_t)(q_loads - 1) & 1u) && global_timer_ns() - t0 < kDrainLimitNs) {
                     }
             }
         }
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(224, 1)
                 raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
             }
             tc5_commit(&mma_done[0]);  // this thread's MMAs complete before the tensor memory is freed
-            mbar_wait_bounded(&mma_done[0], 0u);
+            mbar_wait_drain(&mma_done[0], 0u);
         }
         __syncwarp();
     } else if (warp == 6) {
@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(224, 1)
                 raise_error(a.err_word, KVD_DEVERR_TIMEOUT);
             }
             tc5_commit(&mma_done[1]);
-            mbar_wait_bounded(&mma_done[1], 0u);
+            mbar_wait_drain(&mma_done[1], 0u);
         }
         __syncwarp();
     } else {

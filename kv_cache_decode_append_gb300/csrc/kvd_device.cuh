@@ -20,7 +20,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 // A pipeline wait gives up after this long (ns of %globaltimer), sets
 // KVD_DEVERR_TIMEOUT and lets the kernel wind down.  A healthy wait ends in
 // microseconds; the bound only exists so that no kernel can spin forever.
+// (A test build, KVD_TIMEOUT_TEST, shortens it so that a test can make a
+// pipeline wait run out.)  The waits of the wind-down itself -- for copies and
+// MMAs still in flight before the CTA exits -- keep the long bound.
+#ifdef KVD_TIMEOUT_TEST
+constexpr uint64_t kWaitLimitNs = 2000000ull;
+#else
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+#endif
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
@@ -94,6 +102,44 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
+}
+
+// The wind-down's wait for work still in flight: bounded by kDrainLimitNs.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > kDrainLimitNs) return false;
+    return true;
+}
+
+// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs or when
+// *abort_flag is set by another thread: 0 the phase completed, 1 this wait
+// timed out, 2 another thread gave up.
+__device__ __forceinline__ int mbar_wait_or_abort(uint64_t *bar, uint32_t parity, const volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return 0;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return 0;
+        if ((it & 63u) == 0u) {
+            if (*abort_flag != 0) return 2;
+            if (global_timer_ns() - t0 > kWaitLimitNs) return 1;
+        }
+    }
+}
+
+// Shared-memory int with release (store) / acquire (load) semantics at CTA
+// scope: what the writer stored before is visible to the reader after.
+__device__ __forceinline__ void st_release_cta(volatile int *p, int v)
+{
+    asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_addr((const void *)p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const volatile int *p)
+{
+    int v;
+    asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr((const void *)p)) : "memory");
+    return v;
 }
 
 // 2^x with the hardware approximation (ex2.approx.ftz.f32, one MUFU op).
