@@ -3,6 +3,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kvd_attention.cuh"
@@ -160,6 +161,8 @@ int g_occ_n = 0;
 constexpr int kMaxSmemPerCta = 227 * 1024;
 // Ranges longer than this many tile units per CTA use the separate merge pass.
 constexpr int kLongRangeUnits = 32;
+// The merge pass: at most this many four-warp CTAs per SM.
+constexpr int kMergeCtasPerSm = 8;
 // Query rows per KV head from which the tensor-core kernel (16-row blocks) is
 // used, by head dim.  Measured on GB300 (bench.py, bf16): D=128 with 4 rows
 // (the long-context workload) 106.4 us per layer against 113.6 on the CUDA
@@ -358,6 +361,7 @@ struct Plan {
     AttnVariant v;
     int rows, rb, n_rowblocks;
     int grid, smem, launches, max_tiles;
+    int sms;          // SMs of the device
     bool merge_pass;  // split heads merged by a second launch (else inside the kernel)
     bool mma;         // tensor-core kernel (16-row blocks, tiles by tensor map)
     bool tc5;         // tcgen05 kernel (128-row blocks, tiles and q by tensor map)
@@ -462,6 +466,7 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     int dev = 0, sms = 0, occ = 0, occ_other = 0;
     if ((st = current_device(&dev)) != KVD_OK) return st;
     if ((st = sm_count(dev, &sms)) != KVD_OK) return st;
+    pl->sms = sms;
     // The attention and the fused-step kernels of both builds share the plan:
     // size the grid for the one with the lowest occupancy.  The workspace is
     // sized for the larger grid of the two cache layouts, so that one size
@@ -783,9 +788,15 @@ kvd_status decode_launch(const void *q, const void *k_cache, const void *v_cache
     } else if (cudaLaunchKernelExC(&cfg, k_new != nullptr ? pl.v.fused_fn : pl.v.fn, args) != cudaSuccess) {
         return KVD_ERR_CUDA;
     }
-    if (pl.merge_pass) {  // one warp per query row of the split heads
-        const long long warps = (long long)B * H_kv * pl.n_rowblocks * pl.rb;
-        cfg.gridDim = dim3((unsigned)((warps * 32 + 127) / 128));
+    if (pl.merge_pass) {
+        // four-warp CTAs striding over the real query rows, a warp per row
+        // up to kMergeCtasPerSm CTAs per SM (then kMergeRows rows per warp at
+        // a time), so that the whole grid is resident soon after the
+        // attention kernel's CTAs leave (a warp per padded row slot, most of
+        // them empty, cost several microseconds per layer)
+        const long long rows_total = (long long)B * H_kv * pl.rows;
+        const long long ctas = std::min<long long>((rows_total + 3) / 4, (long long)pl.sms * kMergeCtasPerSm);
+        cfg.gridDim = dim3((unsigned)std::max<long long>(ctas, 1));
         cfg.blockDim = dim3(128);
         cfg.dynamicSmemBytes = 0;
         if (cudaLaunchKernelExC(&cfg, pl.v.merge_fn, args) != cudaSuccess) return KVD_ERR_CUDA;

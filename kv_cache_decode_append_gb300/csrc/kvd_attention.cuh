@@ -1303,82 +1303,121 @@ __global__ void __launch_bounds__(AttnShape<T, D, RB, C>::kThreads)
     }
 }
 
-// Second pass: log-sum-exp merge of the pieces of one query row per warp.
+// Second pass: log-sum-exp merge of the pieces of a query row.
 //   M = max_c m_c;  w_c = 2^(m_c - M);  out = sum_c w_c o_c / sum_c w_c l_c
-// (times v_scale with an E4M3 cache: kScaleV).
+// (times v_scale with an E4M3 cache: kScaleV).  The warps stride over the
+// heads' real rows (B * H_kv * rows; a row block's padding rows have none),
+// so the host may launch fewer warps than rows.  A warp takes one row at a
+// time when the grid has a warp per row, else kMergeRows consecutive rows of
+// one head with the loads of all of them in flight together (a row alone is
+// two dependent memory round trips).  Measured on GB300 (long-context layer):
+// one row per warp is best at 1024 rows, two at 8192 and 32768 rows.
+constexpr int kMergeRows = 2;
+
 template <typename T, int D, int RB, bool kScaleV = false>
 __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a)
 {
     using Ty = Elem<T>;
     const float kNegInf = __int_as_float(0xff800000);
     constexpr int kDpl = D / 32;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    constexpr int kR = kMergeRows;
+    // The next kernel may launch at once: like every kernel here it waits for
+    // this grid's completion before it touches anything this grid writes,
+    // and launching early lets its CTAs take the SMs as these warps finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x % 32;
     const int HR = a.H_kv * a.n_rowblocks;
-    if (gw >= (long long)a.B * HR * RB) return;
-    const int r = (int)(gw % RB);
-    const int u = (int)(gw / RB);
-    const int b = u / HR, hr = u % HR;
-    const int h = hr / a.n_rowblocks, rb = hr % a.n_rowblocks;
-    const int rg = rb * RB + r;
-    if (rg >= a.rows) return;
-    // (both loads issued before either is used)
-    const int P = __ldg(a.past_len + b);
-    const int2 seg = static_cast<const int2 *>(a.merge_state)[u];
-    if (!past_len_ok(P, a.N, a.T_max, a.max_past_len)) return;  // reported by the split pass
-    if (seg.y <= 1) return;  // the split pass wrote this row directly
+    const long long stride = (long long)gridDim.x * (blockDim.x / 32);
+    const int kr = (long long)a.B * a.H_kv * a.rows > stride ? kR : 1;  // rows per warp at a time
+    const int gph = (a.rows + kr - 1) / kr;  // row groups per head
+    const long long n_groups = (long long)a.B * a.H_kv * gph;
+    const int prow = part_rows<RB>(a.rows);
+    for (long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32; gw < n_groups; gw += stride) {
+        const int bh = (int)(gw / gph);
+        const int rg0 = (int)(gw % gph) * kr;
+        const int b = bh / a.H_kv, h = bh % a.H_kv;
+        // (all loads issued before any is used)
+        const int P = __ldg(a.past_len + b);
+        int2 seg[kR];
+#pragma unroll
+        for (int i = 0; i < kR; ++i)
+            seg[i] = i < kr && rg0 + i < a.rows
+                         ? static_cast<const int2 *>(a.merge_state)[(size_t)b * HR + h * a.n_rowblocks + (rg0 + i) / RB]
+                         : make_int2(0, 0);
+        if (!past_len_ok(P, a.N, a.T_max, a.max_past_len)) continue;  // reported by the split pass
+        // pieces to merge per row (0: the split pass wrote the row directly)
+        int cnt[kR], kmax = 0;
+#pragma unroll
+        for (int i = 0; i < kR; ++i) {
+            cnt[i] = seg[i].y > 1 ? seg[i].y : 0;
+            kmax = max(kmax, cnt[i]);
+        }
+        if (kmax == 0) continue;
 
-    // One pass over the pieces, merged online (running max M, weighted sums);
-    // the loads of up to four pieces are issued before their updates.
-    float M = kNegInf, den = 0.f;
-    float acc[kDpl];
+        // One pass over the pieces, merged online (running max M, weighted
+        // sums); two pieces of every row loaded before their updates.
+        float M[kR], den[kR], acc[kR][kDpl];
 #pragma unroll
-    for (int k = 0; k < kDpl; ++k) acc[k] = 0.f;
-    for (int k0 = 0; k0 < seg.y; k0 += 4) {
-        float2 ml[4];
-        float ov[4][kDpl];
+        for (int i = 0; i < kR; ++i) {
+            M[i] = kNegInf;
+            den[i] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int k = k0 + i;
-            if (k < seg.y) {
-                const size_t pidx = ((size_t)(seg.x + k) * 2 + (k == 0)) * part_rows<RB>(a.rows) + r;
-                const float *pr = a.part + pidx * (D + 4);
-                ml[i] = *reinterpret_cast<const float2 *>(pr + D);
-                const float *po = pr + lane * kDpl;
-                if constexpr (kDpl == 4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(po);
-                    ov[i][0] = v.x;
-                    ov[i][1] = v.y;
-                    ov[i][2] = v.z;
-                    ov[i][3] = v.w;
-                } else {
+            for (int k = 0; k < kDpl; ++k) acc[i][k] = 0.f;
+        }
+        for (int k0 = 0; k0 < kmax; k0 += 2) {
+            float2 ml[kR][2];
+            float ov[kR][2][kDpl];
 #pragma unroll
-                    for (int k2 = 0; k2 < kDpl; ++k2) ov[i][k2] = po[k2];
+            for (int i = 0; i < kR; ++i) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int k = k0 + j;
+                    if (k < cnt[i]) {
+                        const size_t pidx = ((size_t)(seg[i].x + k) * 2 + (k == 0)) * prow + (rg0 + i) % RB;
+                        const float *pr = a.part + pidx * (D + 4);
+                        ml[i][j] = *reinterpret_cast<const float2 *>(pr + D);
+                        const float *po = pr + lane * kDpl;
+                        if constexpr (kDpl == 4) {
+                            const float4 v = *reinterpret_cast<const float4 *>(po);
+                            ov[i][j][0] = v.x;
+                            ov[i][j][1] = v.y;
+                            ov[i][j][2] = v.z;
+                            ov[i][j][3] = v.w;
+                        } else {
+#pragma unroll
+                            for (int k2 = 0; k2 < kDpl; ++k2) ov[i][j][k2] = po[k2];
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kR; ++i) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (k0 + j < cnt[i]) {
+                        const float Mn = fmaxf(M[i], ml[i][j].x);
+                        const float wa = safe_weight(M[i], Mn), wb = safe_weight(ml[i][j].x, Mn);
+                        den[i] = den[i] * wa + ml[i][j].y * wb;
+#pragma unroll
+                        for (int k2 = 0; k2 < kDpl; ++k2) acc[i][k2] = acc[i][k2] * wa + ov[i][j][k2] * wb;
+                        M[i] = Mn;
+                    }
                 }
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (k0 + i < seg.y) {
-                const float Mn = fmaxf(M, ml[i].x);
-                const float wa = safe_weight(M, Mn), wb = safe_weight(ml[i].x, Mn);
-                den = den * wa + ml[i].y * wb;
+        for (int i = 0; i < kR; ++i) {
+            if (cnt[i] == 0) continue;
+            T *out = static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg0 + i) * D + lane * kDpl;
 #pragma unroll
-                for (int k2 = 0; k2 < kDpl; ++k2) acc[k2] = acc[k2] * wa + ov[i][k2] * wb;
-                M = Mn;
+            for (int k = 0; k < kDpl; ++k) {
+                if constexpr (kScaleV)
+                    Ty::store(out + k, acc[i][k] / den[i] * a.kv_scale.y);
+                else
+                    Ty::store(out + k, acc[i][k] / den[i]);
             }
         }
-    }
-    const int bh = b * a.H_kv + h;
-    T *out = static_cast<T *>(a.out) + ((size_t)bh * a.rows + rg) * D + lane * kDpl;
-#pragma unroll
-    for (int k = 0; k < kDpl; ++k) {
-        if constexpr (kScaleV)
-            Ty::store(out + k, acc[k] / den * a.kv_scale.y);
-        else
-            Ty::store(out + k, acc[k] / den);
     }
 }
 
