@@ -43,8 +43,12 @@ def test_mma_parity(orc, case):
     test_gpu_step._check(orc, w, past, seed=9400 + D + N)
 
 
-@pytest.mark.parametrize("case", [(32, 64, 4, 128, 6200, 6100, 2), (16, 32, 2, 128, 1100, 1000, 1)],
-                         ids=["merge_pass", "in_kernel"])
+# The last: 128 x 8 heads x 5 rows = 5120 real rows, more than the merge pass's
+# capped grid has warps (4864 on 152 SMs): two rows per warp at a time, the last
+# group of each head holding one.
+@pytest.mark.parametrize("case", [(32, 64, 4, 128, 6200, 6100, 2), (16, 32, 2, 128, 1100, 1000, 1),
+                                  (128, 40, 8, 128, 1100, 1000, 2)],
+                         ids=["merge_pass", "in_kernel", "merge_pass_two_rows_per_warp"])
 def test_mma_merge_modes(orc, case):
     B, H_q, H_kv, D, T_max, max_past, launches = case
     plan = kvd.kvd_decode_plan(B, H_q, H_kv, D, 1, max_past, "bf16")

@@ -47,8 +47,13 @@ def test_tc5_parity(orc, case):
     test_gpu_step._check(orc, w, past, seed=9600 + D + N)
 
 
-@pytest.mark.parametrize("case", [(32, 64, 4, 128, 2, 6200, 6100, 2), (4, 32, 2, 128, 2, 1100, 1000, 1)],
-                         ids=["merge_pass", "in_kernel"])
+# The last two: 64 x 8 heads x 17 rows = 8704 real rows, more than the merge
+# pass's capped grid has warps (8 four-warp CTAs per SM: 4864 on 152 SMs), so
+# its warps take two rows at a time and the last group of each head holds one.
+@pytest.mark.parametrize("case", [(32, 64, 4, 128, 2, 6200, 6100, 2), (4, 32, 2, 128, 2, 1100, 1000, 1),
+                                  (64, 8, 8, 128, 17, 560, 540, 2), (64, 8, 8, 64, 17, 560, 540, 2)],
+                         ids=["merge_pass", "in_kernel", "merge_pass_two_rows_per_warp",
+                              "merge_pass_two_rows_per_warp_d64"])
 def test_tc5_merge_modes(orc, case):
     B, H_q, H_kv, D, N, T_max, max_past, launches = case
     plan = kvd.kvd_decode_plan(B, H_q, H_kv, D, N, max_past, "bf16")
