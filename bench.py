@@ -447,24 +447,41 @@ class Case:
         return g
 
     def e2e(self, steps, warmup, world):
-        """The same step through the public API with its inputs copied in from pinned
-        host memory and every layer's output read back, every step (eager calls)."""
+        """The same step through the public API with its inputs in page-locked host
+        memory and every layer's output read back, every step (eager calls).  A
+        contiguous fused step goes through kvd_decode_step_host (the library copies
+        q, k_new, v_new and past_len in and out back, on the stream); the other
+        paths copy with torch around their device-pointer calls."""
         w, stream = self.w, torch.cuda.current_stream()
         host_in = [{k: self.layers[l][k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
                    for l in range(w.L)]
         host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.outs]
         past_h = self.past.pin_memory()
-        h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values()) + past_h.numel() * 4
+        in_bytes = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out)
+        host_call = self.fused and not self.paged and not self.e4m3 and not self.flags
+        if host_call:
+            kvd = self.kvd
+            staging = kvd.alloc_host_staging(w.B, w.H_q, w.H_kv, w.D, w.N, w.torch_dtype, self.dev)
+            h2d = in_bytes + w.L * past_h.numel() * 4
 
-        def one():
-            self.past_d.copy_(past_h, non_blocking=True)
-            for l in range(w.L):
-                for key in ("q", "k_new", "v_new"):
-                    self.layers[l][key].copy_(host_in[l][key], non_blocking=True)
-                self.layer_call(l)
-                host_out[l].copy_(self.outs[l], non_blocking=True)
-            stream.synchronize()
+            def one():
+                for l in range(w.L):
+                    x, hx = self.layers[l], host_in[l]
+                    kvd.kvd_decode_step_host(hx["q"], x["k_cache"], x["v_cache"], hx["k_new"], hx["v_new"],
+                                             host_out[l], past_h, self.max_past, staging, 0.0, self.ws, self.err)
+                stream.synchronize()
+        else:
+            h2d = in_bytes + past_h.numel() * 4
+
+            def one():
+                self.past_d.copy_(past_h, non_blocking=True)
+                for l in range(w.L):
+                    for key in ("q", "k_new", "v_new"):
+                        self.layers[l][key].copy_(host_in[l][key], non_blocking=True)
+                    self.layer_call(l)
+                    host_out[l].copy_(self.outs[l], non_blocking=True)
+                stream.synchronize()
 
         for _ in range(max(1, warmup)):
             one()
@@ -479,6 +496,8 @@ class Case:
         return {"value": round(whole_job_gbs(self.step_bytes, steps, el, world), 2), "unit": "GB/s",
                 "ms_per_step": round(el / steps * 1e3, 4), "us_per_layer_step": round(el / steps / w.L * 1e6, 3),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "kvd_decode_step_host (host buffers, library copies)" if host_call else
+                       "device-pointer calls, torch copies from / to page-locked host memory",
                 "timing": f"{steps} eager steps, CUDA events on the stream"}
 
 

@@ -184,6 +184,53 @@ kvd_status kvd_decode_step_flags(const void *q, void *k_cache, void *v_cache, co
                                  uint32_t *err_word, void *stream);
 
 /*
+ * kvd_decode_step_host -- kvd_decode_step with the call's own inputs and its
+ * output in host memory: the whole step as the pages time it per token, the
+ * new token's q, K and V coming from the host side and the attention result
+ * going back ("GPT-2缓存实测：千倍计算只快6倍", section "实验到底测了什么";
+ * the decode step itself: "7.1 自回归生成过程", section "Decode 阶段").
+ *
+ *   q_host, k_new_host, v_new_host   page-locked host memory, read; layouts as
+ *                                    for kvd_decode_step
+ *   past_len_host                    page-locked host int32[B], read
+ *   out_host                         page-locked host memory, written
+ *   k_cache, v_cache                 device, as for kvd_decode_step (updated in
+ *                                    place)
+ *   staging                          device scratch of at least
+ *                                    kvd_host_staging_bytes(B, H_q, H_kv, D, N,
+ *                                    dtype) bytes, 256-byte aligned, owned by
+ *                                    the caller; it holds the device copies of
+ *                                    q, k_new, v_new, past_len and out
+ *   workspace, workspace_bytes       as for kvd_decode_step
+ *
+ * Enqueues on `stream`, in order: copies of q, k_new, v_new and past_len from
+ * the host into `staging` (cudaMemcpyAsync), kvd_decode_step on the staged
+ * copies, and the copy of out back to out_host.  Like every call here it
+ * returns at once: out_host holds the result once `stream` has passed the
+ * call, and the host buffers must stay valid and unchanged until then.  The
+ * result is kvd_decode_step's, bit for bit.
+ *
+ * Errors, all found before anything is queued: every argument error of
+ * kvd_decode_step (E4M3 caches are not taken: KVD_ERR_UNSUPPORTED); a host
+ * buffer that is not page-locked (cudaHostAlloc / cudaHostRegister), so that
+ * no copy can block the host: KVD_ERR_INVALID_ARG; staging null, misaligned
+ * or too small: KVD_ERR_WORKSPACE.  A failed copy or launch: KVD_ERR_CUDA.
+ */
+kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache, const void *k_new_host,
+                                const void *v_new_host, void *out_host, const int32_t *past_len_host, int B,
+                                int H_q, int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                                kvd_dtype dtype, void *staging, size_t staging_bytes, void *workspace,
+                                size_t workspace_bytes, uint32_t *err_word, void *stream);
+
+/*
+ * kvd_host_staging_bytes -- device bytes of kvd_decode_step_host's staging
+ * buffer for these shapes: q and out (B * H_q * N * D elements each), k_new and
+ * v_new (B * H_kv * N * D each) and past_len (B int32), each region starting
+ * on a 256-byte boundary.  0 for invalid shapes or dtypes (E4M3 included).
+ */
+size_t kvd_host_staging_bytes(int B, int H_q, int H_kv, int D, int N, kvd_dtype dtype);
+
+/*
  * kvd_decode_plan -- how kvd_decode_attention would run these shapes on the
  * current device, without launching anything: keys per tile, the most tiles
  * one sequence-head can have (from max_past_len + N), the persistent grid

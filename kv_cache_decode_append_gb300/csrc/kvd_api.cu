@@ -1016,6 +1016,78 @@ size_t kvd_cache_bytes(int L, int B, int H_kv, int D, int T, kvd_dtype dtype)
 void kvd_test_inject_stall(int on) { g_test_stall = on; }
 #endif
 
+// Staging layout of kvd_decode_step_host: q, k_new, v_new, out, past_len,
+// each region 256-byte aligned.
+size_t kvd_host_staging_bytes(int B, int H_q, int H_kv, int D, int N, kvd_dtype dtype)
+{
+    if (dtype == KVD_E4M3 || check_shapes(B, H_q, H_kv, D, N, 0, dtype) != KVD_OK) return 0;
+    const size_t s = (size_t)elem_bytes(dtype);
+    const size_t qb = (size_t)B * H_q * N * D * s, nb = (size_t)B * H_kv * N * D * s;
+    return round_up(qb, 256) * 2 + round_up(nb, 256) * 2 + round_up((size_t)B * 4, 256);
+}
+
+namespace {
+// Page-locked host memory (cudaHostAlloc / cudaHostRegister): a copy from or
+// to it never blocks the host.
+bool page_locked(const void *p)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+}
+}  // namespace
+
+kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache, const void *k_new_host,
+                                const void *v_new_host, void *out_host, const int32_t *past_len_host, int B,
+                                int H_q, int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                                kvd_dtype dtype, void *staging, size_t staging_bytes, void *workspace,
+                                size_t workspace_bytes, uint32_t *err_word, void *stream)
+{
+    // Every check before anything is queued.
+    if (!q_host || !k_new_host || !v_new_host || !out_host || !past_len_host || !k_cache || !v_cache)
+        return KVD_ERR_INVALID_ARG;
+    kvd_status st = check_shapes(B, H_q, H_kv, D, N, max_past_len, dtype);
+    if (st != KVD_OK) return st;
+    if (dtype == KVD_E4M3) return KVD_ERR_UNSUPPORTED;
+    if (T_max < 1) return KVD_ERR_INVALID_ARG;
+    if ((long long)max_past_len + N > T_max) return KVD_ERR_CAPACITY;
+    if (B == 0) return KVD_OK;  // (nothing to copy or compute)
+    const size_t need = kvd_host_staging_bytes(B, H_q, H_kv, D, N, dtype);
+    if (staging == nullptr || (reinterpret_cast<uintptr_t>(staging) & 255u) != 0 || staging_bytes < need)
+        return KVD_ERR_WORKSPACE;
+    const size_t s = (size_t)elem_bytes(dtype);
+    const size_t qb = (size_t)B * H_q * N * D * s, nb = (size_t)B * H_kv * N * D * s, pb = (size_t)B * 4;
+    char *st_base = static_cast<char *>(staging);
+    char *q_d = st_base;
+    char *kn_d = q_d + round_up(qb, 256);
+    char *vn_d = kn_d + round_up(nb, 256);
+    char *out_d = vn_d + round_up(nb, 256);
+    int32_t *pl_d = reinterpret_cast<int32_t *>(out_d + round_up(qb, 256));
+    size_t ws_need = 0, zero_off = 0, zero_bytes = 0;
+    st = kvd::decode_attention_prepare(q_d, k_cache, v_cache, out_d, pl_d, B, H_q, H_kv, T_max, D, N,
+                                       max_past_len, dtype, &ws_need, &zero_off, &zero_bytes);
+    if (st != KVD_OK) return st;
+    if (workspace == nullptr || workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KVD_ERR_WORKSPACE;
+    if (!page_locked(q_host) || !page_locked(k_new_host) || !page_locked(v_new_host) || !page_locked(out_host) ||
+        !page_locked(past_len_host))
+        return KVD_ERR_INVALID_ARG;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(q_d, q_host, qb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(kn_d, k_new_host, nb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(vn_d, v_new_host, nb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(pl_d, past_len_host, pb, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return KVD_ERR_CUDA;
+    st = kvd_decode_step(q_d, k_cache, v_cache, kn_d, vn_d, out_d, pl_d, B, H_q, H_kv, T_max, D, N, max_past_len,
+                         scale, dtype, workspace, workspace_bytes, err_word, stream);
+    if (st != KVD_OK) return st;
+    return cudaMemcpyAsync(out_host, out_d, qb, cudaMemcpyDeviceToHost, cs) == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
 const char *kvd_status_string(kvd_status status)
 {
     switch (status) {

@@ -79,6 +79,11 @@ class _Lib:
         lib.kvd_decode_step_flags.restype = ci
         lib.kvd_decode_step_flags.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
                                               ctypes.c_uint32, vp, sz, u32p, vp]
+        lib.kvd_decode_step_host.restype = ci
+        lib.kvd_decode_step_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
+                                             vp, sz, vp, sz, u32p, vp]
+        lib.kvd_host_staging_bytes.restype = sz
+        lib.kvd_host_staging_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
         lib.kvd_paged_append.restype = ci
         lib.kvd_paged_append.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, u32p, vp]
         lib.kvd_paged_decode_attention.restype = ci
@@ -286,6 +291,57 @@ def kvd_decode_step(q, k_cache, v_cache, k_new, v_new, out, past_len, max_past_l
                              N, int(max_past_len), float(scale), _dtype_code(q), ws_ptr, ws_bytes,
                              _ptr(err_word), _stream_handle(stream))
     _check("kvd_decode_step", st)
+
+
+def kvd_host_staging_bytes(B, H_q, H_kv, D, N, dtype) -> int:
+    return int(raw.kvd_host_staging_bytes(B, H_q, H_kv, D, N, _NAME_DTYPE[dtype] if isinstance(dtype, str)
+                                          else _TORCH_DTYPE[dtype]))
+
+
+def alloc_host_staging(B, H_q, H_kv, D, N, dtype, device=None) -> torch.Tensor:
+    """A device staging buffer for ``kvd_decode_step_host`` with these shapes."""
+    n = kvd_host_staging_bytes(B, H_q, H_kv, D, N, dtype)
+    if n == 0:
+        raise ValueError("no staging layout for these shapes / dtype")
+    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def _need_pinned(name, t, dtype):
+    if t.is_cuda or not t.is_pinned() or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous page-locked host tensor of dtype {dtype}")
+
+
+def kvd_decode_step_host(q_host, k_cache, v_cache, k_new_host, v_new_host, out_host, past_len_host,
+                         max_past_len: int, staging: torch.Tensor, scale: float = 0.0,
+                         workspace: Optional[torch.Tensor] = None, err_word=None, stream=None) -> None:
+    """``kvd_decode_step`` with q, k_new, v_new, past_len and out in page-locked host memory:
+    the library copies them through ``staging`` (device) on the stream."""
+    dt = q_host.dtype
+    for n, t in (("q_host", q_host), ("k_new_host", k_new_host), ("v_new_host", v_new_host),
+                 ("out_host", out_host)):
+        _need_pinned(n, t, dt)
+    _need_pinned("past_len_host", past_len_host, torch.int32)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, dt)
+    if staging.device.type != "cuda" or not staging.is_contiguous():
+        raise ValueError("staging must be a contiguous CUDA tensor")
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_q, N, D = q_host.shape
+    _, H_kv, T_max, _ = k_cache.shape
+    if (out_host.shape != q_host.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B
+            or k_cache.shape[3] != D or tuple(k_new_host.shape) != (B, H_kv, N, D)
+            or v_new_host.shape != k_new_host.shape):
+        raise ValueError("shape mismatch between q, out, the caches and the new K/V")
+    if past_len_host.numel() != B:
+        raise ValueError("past_len must hold B entries")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = raw.kvd_decode_step_host(q_host.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_new_host.data_ptr(),
+                                  v_new_host.data_ptr(), out_host.data_ptr(), past_len_host.data_ptr(), B, H_q,
+                                  H_kv, T_max, D, N, int(max_past_len), float(scale), _TORCH_DTYPE[dt],
+                                  staging.data_ptr(), staging.numel() * staging.element_size(), ws_ptr, ws_bytes,
+                                  _ptr(err_word), _stream_handle(stream))
+    _check("kvd_decode_step_host", st)
 
 
 # ---------------------------------------------------------------------------------

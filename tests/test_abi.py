@@ -192,6 +192,35 @@ def test_decode_step_argument_errors(lib):
     assert step(B=0) == 0
 
 
+def test_decode_step_host_argument_errors(lib):
+    def step(staging=A, staging_bytes=1 << 20, **kw):
+        args = dict(q=A, k=A, v=A, kn=A, vn=A, out=A, past=A, B=1, H_q=4, H_kv=2, T_max=64, D=64, N=1,
+                    max_past=10, dtype=1)
+        args.update(kw)
+        return lib.kvd_decode_step_host(args["q"], args["k"], args["v"], args["kn"], args["vn"], args["out"],
+                                        args["past"], args["B"], args["H_q"], args["H_kv"], args["T_max"], args["D"],
+                                        args["N"], args["max_past"], 0.0, args["dtype"], staging, staging_bytes, None,
+                                        0, None, None)
+    assert step(q=0) == 1
+    assert step(past=0) == 1
+    assert step(H_q=6, H_kv=4) == 1
+    assert step(D=80) == 3
+    assert step(dtype=3) == 3                      # E4M3 caches: not through this entry point
+    assert step(max_past=60, N=5, T_max=64) == 2
+    assert step(staging=None) == 4
+    assert step(staging=A + 16) == 4               # staging must be 256-byte aligned
+    assert step(staging_bytes=1791) == 4           # one byte short (next test)
+    assert step(B=0, staging=None) == 0
+
+
+def test_host_staging_bytes(lib):
+    # q and out: 1*4*1*64 bf16 = 512 B each; k_new, v_new: 256 B each; past_len: 4 B -> 256
+    assert lib.kvd_host_staging_bytes(1, 4, 2, 64, 1, 1) == 512 + 512 + 256 + 256 + 256
+    assert lib.kvd_host_staging_bytes(3, 8, 2, 128, 5, 0) == 2 * (3 * 8 * 5 * 128 * 4) + 2 * (3 * 2 * 5 * 128 * 4) + 256
+    assert lib.kvd_host_staging_bytes(1, 4, 2, 64, 1, 3) == 0   # E4M3
+    assert lib.kvd_host_staging_bytes(1, 6, 4, 64, 1, 1) == 0   # H_q % H_kv != 0
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """Without the built CUDA library every entry point raises: there is no fallback path."""
     from kv_cache_decode_append_gb300 import kvd

@@ -118,3 +118,59 @@ def test_step_skips_bad_sequences():
     assert bool((out[1] == 7.0).all())
     assert _same_bits(g["k_cache"][0, :, 100:102], g["k_new"][0])
     assert bool(torch.isfinite(out[0]).all() and torch.isfinite(out[2]).all())
+
+
+# (B, H_q, H_kv, D, N, T_max, past, dtype): a 4-row tensor-core step and an fp32
+# CUDA-core step with a split head
+HOST_CASES = [(4, 8, 2, 128, 1, 300, [100, 0, 297, 50], "bf16"),
+              (2, 12, 12, 64, 3, 1100, [1000, 7], "f32")]
+
+
+@pytest.mark.parametrize("case", HOST_CASES, ids=["bf16_tensor_cores", "f32"])
+def test_step_host_buffers(orc, case):
+    """kvd_decode_step_host: inputs and output in page-locked host memory, copied by
+    the library through its staging buffer; bit-identical to kvd_decode_step."""
+    B, H_q, H_kv, D, N, T_max, past, dtype = case
+    w = wl.Workload(0, "host", L=1, B=B, H_q=H_q, H_kv=H_kv, D=D, N=N, dtype=dtype, T_max=T_max, P=0)
+    past = torch.as_tensor(past, dtype=torch.int32)
+    t = wl.layer_inputs(w, 0, past, device="cpu", seed_base=9900 + N)
+    max_past = int(past.max())
+    ws = kvd.alloc_workspace(B, H_q, H_kv, D, N, max_past, w.torch_dtype, DEV)
+    # device path
+    g1 = {k: v.to(DEV).clone() for k, v in t.items()}
+    out1 = torch.full_like(g1["q"], float("nan"))
+    kvd.kvd_decode_step(g1["q"], g1["k_cache"], g1["v_cache"], g1["k_new"], g1["v_new"], out1, past.to(DEV),
+                        max_past, 0.0, ws)
+    # host path (its own caches and workspace)
+    kc, vc = t["k_cache"].to(DEV).clone(), t["v_cache"].to(DEV).clone()
+    host = {k: t[k].pin_memory() for k in ("q", "k_new", "v_new")}
+    past_h = past.pin_memory()
+    out_h = torch.full(t["q"].shape, float("nan"), dtype=t["q"].dtype).pin_memory()
+    staging = kvd.alloc_host_staging(B, H_q, H_kv, D, N, w.torch_dtype, DEV)
+    ws2 = kvd.alloc_workspace(B, H_q, H_kv, D, N, max_past, w.torch_dtype, DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvd.kvd_decode_step_host(host["q"], kc, vc, host["k_new"], host["v_new"], out_h, past_h, max_past, staging,
+                             0.0, ws2, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _same_bits(out_h, out1)
+    assert _same_bits(kc, g1["k_cache"]) and _same_bits(vc, g1["v_cache"])
+    ref, st = orc.decode_attention(to_np(t["q"]), to_np(g1["k_cache"]), to_np(g1["v_cache"]), past.numpy(), dtype)
+    assert st == 0 and row_rel_err(out_h.double().numpy(), ref) <= TOL[dtype]
+
+    # errors return before anything is queued: out_h keeps its bits
+    before = out_h.clone()
+    raw = kvd.raw
+    code = {torch.bfloat16: kvd.KVD_BF16, torch.float32: kvd.KVD_F32}[t["q"].dtype]
+
+    def call(q_ptr, staging_bytes, ws_bytes):
+        return raw.kvd_decode_step_host(q_ptr, kc.data_ptr(), vc.data_ptr(), host["k_new"].data_ptr(),
+                                        host["v_new"].data_ptr(), out_h.data_ptr(), past_h.data_ptr(), B, H_q, H_kv,
+                                        T_max, D, N, max_past, 0.0, code, staging.data_ptr(), staging_bytes,
+                                        ws2.data_ptr(), ws_bytes, None, None)
+    pageable = t["q"].clone()
+    assert call(pageable.data_ptr(), staging.numel(), ws2.numel()) == kvd.KVD_ERR_INVALID_ARG
+    assert call(host["q"].data_ptr(), staging.numel() - 1, ws2.numel()) == kvd.KVD_ERR_WORKSPACE
+    assert call(host["q"].data_ptr(), staging.numel(), 16) == kvd.KVD_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert _same_bits(out_h, before)
