@@ -461,15 +461,25 @@ class Case:
         d2h = sum(t.numel() * t.element_size() for t in host_out)
         host_call = self.fused and not self.paged and not self.e4m3 and not self.flags
         if host_call:
+            # each layer's inputs in one page-locked block laid out as the
+            # staging buffer's inputs: one host-to-device copy per call
             kvd = self.kvd
             staging = kvd.alloc_host_staging(w.B, w.H_q, w.H_kv, w.D, w.N, w.torch_dtype, self.dev)
+            packed = []
+            for l in range(w.L):
+                hp = kvd.alloc_host_inputs(w.B, w.H_q, w.H_kv, w.D, w.N, w.torch_dtype)
+                for key in ("q", "k_new", "v_new"):
+                    hp[key].copy_(host_in[l][key])
+                hp["past_len"].copy_(self.past)
+                packed.append(hp)
             h2d = in_bytes + w.L * past_h.numel() * 4
 
             def one():
                 for l in range(w.L):
-                    x, hx = self.layers[l], host_in[l]
-                    kvd.kvd_decode_step_host(hx["q"], x["k_cache"], x["v_cache"], hx["k_new"], hx["v_new"],
-                                             host_out[l], past_h, self.max_past, staging, 0.0, self.ws, self.err)
+                    x, hp = self.layers[l], packed[l]
+                    kvd.kvd_decode_step_host(hp["q"], x["k_cache"], x["v_cache"], hp["k_new"], hp["v_new"],
+                                             host_out[l], hp["past_len"], self.max_past, staging, 0.0, self.ws,
+                                             self.err)
                 stream.synchronize()
         else:
             h2d = in_bytes + past_h.numel() * 4
@@ -496,7 +506,7 @@ class Case:
         return {"value": round(whole_job_gbs(self.step_bytes, steps, el, world), 2), "unit": "GB/s",
                 "ms_per_step": round(el / steps * 1e3, 4), "us_per_layer_step": round(el / steps / w.L * 1e6, 3),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "kvd_decode_step_host (host buffers, library copies)" if host_call else
+                "api": "kvd_decode_step_host (host buffers, one copy in and one out per call)" if host_call else
                        "device-pointer calls, torch copies from / to page-locked host memory",
                 "timing": f"{steps} eager steps, CUDA events on the stream"}
 

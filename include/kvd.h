@@ -205,7 +205,10 @@ kvd_status kvd_decode_step_flags(const void *q, void *k_cache, void *v_cache, co
  *
  * Enqueues on `stream`, in order: copies of q, k_new, v_new and past_len from
  * the host into `staging` (cudaMemcpyAsync), kvd_decode_step on the staged
- * copies, and the copy of out back to out_host.  Like every call here it
+ * copies, and the copy of out back to out_host.  When k_new_host, v_new_host
+ * and past_len_host sit at their staging offsets from q_host (one host block
+ * laid out as the first kvd_host_staging_inputs_bytes bytes of the staging
+ * buffer), the four inputs go in one copy.  Like every call here it
  * returns at once: out_host holds the result once `stream` has passed the
  * call, and the host buffers must stay valid and unchanged until then.  The
  * result is kvd_decode_step's, bit for bit.
@@ -224,11 +227,16 @@ kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache
 
 /*
  * kvd_host_staging_bytes -- device bytes of kvd_decode_step_host's staging
- * buffer for these shapes: q and out (B * H_q * N * D elements each), k_new and
- * v_new (B * H_kv * N * D each) and past_len (B int32), each region starting
- * on a 256-byte boundary.  0 for invalid shapes or dtypes (E4M3 included).
+ * buffer for these shapes: in this order q (B * H_q * N * D elements), k_new
+ * and v_new (B * H_kv * N * D each), past_len (B int32) and out (as q), each
+ * region starting on a 256-byte boundary.  0 for invalid shapes or dtypes
+ * (E4M3 included).
+ *
+ * kvd_host_staging_inputs_bytes -- the bytes of that layout up to the end of
+ * past_len (the four inputs), for a host block that mirrors it.
  */
 size_t kvd_host_staging_bytes(int B, int H_q, int H_kv, int D, int N, kvd_dtype dtype);
+size_t kvd_host_staging_inputs_bytes(int B, int H_q, int H_kv, int D, int N, kvd_dtype dtype);
 
 /*
  * kvd_decode_plan -- how kvd_decode_attention would run these shapes on the

@@ -1016,7 +1016,7 @@ size_t kvd_cache_bytes(int L, int B, int H_kv, int D, int T, kvd_dtype dtype)
 void kvd_test_inject_stall(int on) { g_test_stall = on; }
 #endif
 
-// Staging layout of kvd_decode_step_host: q, k_new, v_new, out, past_len,
+// Staging layout of kvd_decode_step_host: q, k_new, v_new, past_len, out,
 // each region 256-byte aligned.
 size_t kvd_host_staging_bytes(int B, int H_q, int H_kv, int D, int N, kvd_dtype dtype)
 {
@@ -1024,6 +1024,14 @@ size_t kvd_host_staging_bytes(int B, int H_q, int H_kv, int D, int N, kvd_dtype 
     const size_t s = (size_t)elem_bytes(dtype);
     const size_t qb = (size_t)B * H_q * N * D * s, nb = (size_t)B * H_kv * N * D * s;
     return round_up(qb, 256) * 2 + round_up(nb, 256) * 2 + round_up((size_t)B * 4, 256);
+}
+
+size_t kvd_host_staging_inputs_bytes(int B, int H_q, int H_kv, int D, int N, kvd_dtype dtype)
+{
+    if (dtype == KVD_E4M3 || check_shapes(B, H_q, H_kv, D, N, 0, dtype) != KVD_OK) return 0;
+    const size_t s = (size_t)elem_bytes(dtype);
+    const size_t qb = (size_t)B * H_q * N * D * s, nb = (size_t)B * H_kv * N * D * s;
+    return round_up(qb, 256) + round_up(nb, 256) * 2 + (size_t)B * 4;
 }
 
 namespace {
@@ -1064,8 +1072,8 @@ kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache
     char *q_d = st_base;
     char *kn_d = q_d + round_up(qb, 256);
     char *vn_d = kn_d + round_up(nb, 256);
-    char *out_d = vn_d + round_up(nb, 256);
-    int32_t *pl_d = reinterpret_cast<int32_t *>(out_d + round_up(qb, 256));
+    int32_t *pl_d = reinterpret_cast<int32_t *>(vn_d + round_up(nb, 256));
+    char *out_d = reinterpret_cast<char *>(pl_d) + round_up(pb, 256);
     size_t ws_need = 0, zero_off = 0, zero_bytes = 0;
     st = kvd::decode_attention_prepare(q_d, k_cache, v_cache, out_d, pl_d, B, H_q, H_kv, T_max, D, N,
                                        max_past_len, dtype, &ws_need, &zero_off, &zero_bytes);
@@ -1077,11 +1085,23 @@ kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache
         return KVD_ERR_INVALID_ARG;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(q_d, q_host, qb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-        cudaMemcpyAsync(kn_d, k_new_host, nb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-        cudaMemcpyAsync(vn_d, v_new_host, nb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-        cudaMemcpyAsync(pl_d, past_len_host, pb, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    // Inputs laid out in one host block exactly as in the staging buffer
+    // (k_new, v_new and past_len at the staging offsets from q): one copy,
+    // else one per input.
+    const char *qh = static_cast<const char *>(q_host);
+    const bool packed = static_cast<const char *>(k_new_host) == qh + (kn_d - q_d) &&
+                        static_cast<const char *>(v_new_host) == qh + (vn_d - q_d) &&
+                        reinterpret_cast<const char *>(past_len_host) == qh + (reinterpret_cast<char *>(pl_d) - q_d);
+    if (packed) {
+        if (cudaMemcpyAsync(q_d, q_host, (size_t)(reinterpret_cast<char *>(pl_d) - q_d) + pb, cudaMemcpyHostToDevice,
+                            cs) != cudaSuccess)
+            return KVD_ERR_CUDA;
+    } else if (cudaMemcpyAsync(q_d, q_host, qb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+               cudaMemcpyAsync(kn_d, k_new_host, nb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+               cudaMemcpyAsync(vn_d, v_new_host, nb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+               cudaMemcpyAsync(pl_d, past_len_host, pb, cudaMemcpyHostToDevice, cs) != cudaSuccess) {
         return KVD_ERR_CUDA;
+    }
     st = kvd_decode_step(q_d, k_cache, v_cache, kn_d, vn_d, out_d, pl_d, B, H_q, H_kv, T_max, D, N, max_past_len,
                          scale, dtype, workspace, workspace_bytes, err_word, stream);
     if (st != KVD_OK) return st;

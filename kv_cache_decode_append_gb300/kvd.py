@@ -84,6 +84,8 @@ class _Lib:
                                              vp, sz, vp, sz, u32p, vp]
         lib.kvd_host_staging_bytes.restype = sz
         lib.kvd_host_staging_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
+        lib.kvd_host_staging_inputs_bytes.restype = sz
+        lib.kvd_host_staging_inputs_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
         lib.kvd_paged_append.restype = ci
         lib.kvd_paged_append.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, ci, u32p, vp]
         lib.kvd_paged_decode_attention.restype = ci
@@ -298,6 +300,29 @@ def kvd_host_staging_bytes(B, H_q, H_kv, D, N, dtype) -> int:
                                           else _TORCH_DTYPE[dtype]))
 
 
+def alloc_host_inputs(B, H_q, H_kv, D, N, dtype) -> dict:
+    """Page-locked host tensors q [B,H_q,N,D], k_new / v_new [B,H_kv,N,D] and past_len [B]
+    (int32), views into one block laid out as the staging buffer's inputs, so that
+    ``kvd_decode_step_host`` moves the four in one copy."""
+    tdt = dtype if isinstance(dtype, torch.dtype) else {"f32": torch.float32, "bf16": torch.bfloat16,
+                                                         "f16": torch.float16}[dtype]
+    code = _TORCH_DTYPE[tdt]
+    n = int(raw.kvd_host_staging_inputs_bytes(B, H_q, H_kv, D, N, code))
+    if n == 0:
+        raise ValueError("no staging layout for these shapes / dtype")
+    block = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    es = torch.tensor([], dtype=tdt).element_size()
+    up = lambda x: (x + 255) // 256 * 256
+    qb, nb = B * H_q * N * D * es, B * H_kv * N * D * es
+    offs = {"q": 0, "k_new": up(qb), "v_new": up(qb) + up(nb), "past_len": up(qb) + 2 * up(nb)}
+    out = {"block": block,
+           "q": block[offs["q"]:offs["q"] + qb].view(tdt).view(B, H_q, N, D),
+           "k_new": block[offs["k_new"]:offs["k_new"] + nb].view(tdt).view(B, H_kv, N, D),
+           "v_new": block[offs["v_new"]:offs["v_new"] + nb].view(tdt).view(B, H_kv, N, D),
+           "past_len": block[offs["past_len"]:offs["past_len"] + 4 * B].view(torch.int32)}
+    return out
+
+
 def alloc_host_staging(B, H_q, H_kv, D, N, dtype, device=None) -> torch.Tensor:
     """A device staging buffer for ``kvd_decode_step_host`` with these shapes."""
     n = kvd_host_staging_bytes(B, H_q, H_kv, D, N, dtype)
@@ -307,7 +332,8 @@ def alloc_host_staging(B, H_q, H_kv, D, N, dtype, device=None) -> torch.Tensor:
 
 
 def _need_pinned(name, t, dtype):
-    if t.is_cuda or not t.is_pinned() or t.dtype != dtype or not t.is_contiguous():
+    if t.is_cuda or not (t.is_pinned() or (t._base is not None and t._base.is_pinned())) or t.dtype != dtype \
+            or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous page-locked host tensor of dtype {dtype}")
 
 

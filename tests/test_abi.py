@@ -219,6 +219,9 @@ def test_host_staging_bytes(lib):
     assert lib.kvd_host_staging_bytes(3, 8, 2, 128, 5, 0) == 2 * (3 * 8 * 5 * 128 * 4) + 2 * (3 * 2 * 5 * 128 * 4) + 256
     assert lib.kvd_host_staging_bytes(1, 4, 2, 64, 1, 3) == 0   # E4M3
     assert lib.kvd_host_staging_bytes(1, 6, 4, 64, 1, 1) == 0   # H_q % H_kv != 0
+    # the inputs alone: q, k_new, v_new from 256-byte boundaries, then past_len unpadded
+    assert lib.kvd_host_staging_inputs_bytes(1, 4, 2, 64, 1, 1) == 512 + 256 + 256 + 4
+    assert lib.kvd_host_staging_inputs_bytes(1, 4, 2, 64, 1, 3) == 0
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

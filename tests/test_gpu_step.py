@@ -158,6 +158,19 @@ def test_step_host_buffers(orc, case):
     ref, st = orc.decode_attention(to_np(t["q"]), to_np(g1["k_cache"]), to_np(g1["v_cache"]), past.numpy(), dtype)
     assert st == 0 and row_rel_err(out_h.double().numpy(), ref) <= TOL[dtype]
 
+    # the four inputs in one block laid out as the staging buffer's: one copy
+    hp = kvd.alloc_host_inputs(B, H_q, H_kv, D, N, t["q"].dtype)
+    for key in ("q", "k_new", "v_new"):
+        hp[key].copy_(t[key])
+    hp["past_len"].copy_(past)
+    kc2, vc2 = t["k_cache"].to(DEV).clone(), t["v_cache"].to(DEV).clone()
+    out_p = torch.full(t["q"].shape, float("nan"), dtype=t["q"].dtype).pin_memory()
+    kvd.kvd_decode_step_host(hp["q"], kc2, vc2, hp["k_new"], hp["v_new"], out_p, hp["past_len"], max_past, staging,
+                             0.0, ws2, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _same_bits(out_p, out1) and _same_bits(kc2, g1["k_cache"]) and _same_bits(vc2, g1["v_cache"])
+
     # errors return before anything is queued: out_h keeps its bits
     before = out_h.clone()
     raw = kvd.raw
