@@ -449,7 +449,7 @@ class Case:
     def e2e(self, steps, warmup, world):
         """The same step through the public API with its inputs in page-locked host
         memory and every layer's output read back, every step (eager calls).  A
-        contiguous fused step goes through kvd_decode_step_host (the library copies
+        contiguous fused step goes through kvd_decode_step_host_packed (the library copies
         q, k_new, v_new and past_len in and out back, on the stream); the other
         paths copy with torch around their device-pointer calls."""
         w, stream = self.w, torch.cuda.current_stream()
@@ -477,9 +477,8 @@ class Case:
             def one():
                 for l in range(w.L):
                     x, hp = self.layers[l], packed[l]
-                    kvd.kvd_decode_step_host(hp["q"], x["k_cache"], x["v_cache"], hp["k_new"], hp["v_new"],
-                                             host_out[l], hp["past_len"], self.max_past, staging, 0.0, self.ws,
-                                             self.err)
+                    kvd.kvd_decode_step_host_packed(hp, x["k_cache"], x["v_cache"], host_out[l], self.max_past,
+                                                    staging, 0.0, self.ws, self.err)
                 stream.synchronize()
         else:
             h2d = in_bytes + past_h.numel() * 4
@@ -506,7 +505,7 @@ class Case:
         return {"value": round(whole_job_gbs(self.step_bytes, steps, el, world), 2), "unit": "GB/s",
                 "ms_per_step": round(el / steps * 1e3, 4), "us_per_layer_step": round(el / steps / w.L * 1e6, 3),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "kvd_decode_step_host (host buffers, one copy in and one out per call)" if host_call else
+                "api": "kvd_decode_step_host_packed (host buffers, one copy in and one out per call)" if host_call else
                        "device-pointer calls, torch copies from / to page-locked host memory",
                 "timing": f"{steps} eager steps, CUDA events on the stream"}
 

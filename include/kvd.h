@@ -205,10 +205,8 @@ kvd_status kvd_decode_step_flags(const void *q, void *k_cache, void *v_cache, co
  *
  * Enqueues on `stream`, in order: copies of q, k_new, v_new and past_len from
  * the host into `staging` (cudaMemcpyAsync), kvd_decode_step on the staged
- * copies, and the copy of out back to out_host.  When k_new_host, v_new_host
- * and past_len_host sit at their staging offsets from q_host (one host block
- * laid out as the first kvd_host_staging_inputs_bytes bytes of the staging
- * buffer), the four inputs go in one copy.  Like every call here it
+ * copies, and the copy of out back to out_host (five copies in all; see
+ * kvd_decode_step_host_packed for one copy of the inputs).  Like every call here it
  * returns at once: out_host holds the result once `stream` has passed the
  * call, and the host buffers must stay valid and unchanged until then.  The
  * result is kvd_decode_step's, bit for bit.
@@ -226,6 +224,26 @@ kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache
                                 size_t workspace_bytes, uint32_t *err_word, void *stream);
 
 /*
+ * kvd_decode_step_host_packed -- kvd_decode_step_host with the four inputs in
+ * one page-locked host block, copied to the device in one piece:
+ *
+ *   inputs_host   one page-locked host allocation of at least
+ *                 kvd_host_staging_inputs_bytes(B, H_q, H_kv, D, N, dtype)
+ *                 bytes, laid out as the staging buffer's input part: q at
+ *                 offset 0, then k_new, v_new and past_len (int32[B]), each
+ *                 starting on the next 256-byte boundary after the previous
+ *                 one (kvd_host_staging_bytes gives the full layout)
+ *
+ * Everything else (arguments, result, errors) is kvd_decode_step_host's.  The
+ * block must be a single allocation: a copy may not span two page-locked
+ * allocations, even adjacent ones (the call then fails with KVD_ERR_CUDA).
+ */
+kvd_status kvd_decode_step_host_packed(const void *inputs_host, void *k_cache, void *v_cache, void *out_host, int B,
+                                       int H_q, int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                                       kvd_dtype dtype, void *staging, size_t staging_bytes, void *workspace,
+                                       size_t workspace_bytes, uint32_t *err_word, void *stream);
+
+/*
  * kvd_host_staging_bytes -- device bytes of kvd_decode_step_host's staging
  * buffer for these shapes: in this order q (B * H_q * N * D elements), k_new
  * and v_new (B * H_kv * N * D each), past_len (B int32) and out (as q), each
@@ -233,7 +251,8 @@ kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache
  * (E4M3 included).
  *
  * kvd_host_staging_inputs_bytes -- the bytes of that layout up to the end of
- * past_len (the four inputs), for a host block that mirrors it.
+ * past_len (the four inputs): the size of kvd_decode_step_host_packed's
+ * input block.
  */
 size_t kvd_host_staging_bytes(int B, int H_q, int H_kv, int D, int N, kvd_dtype dtype);
 size_t kvd_host_staging_inputs_bytes(int B, int H_q, int H_kv, int D, int N, kvd_dtype dtype);

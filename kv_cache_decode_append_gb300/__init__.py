@@ -8,7 +8,8 @@ it is missing.
 from .kvd import (  # noqa: F401
     KVD_BF16, KVD_DEVERR_PAGE, KVD_DEVERR_PAST_LEN, KVD_DEVERR_TIMEOUT, KVD_ERR_CAPACITY, KVD_ERR_CUDA,
     KVD_ERR_INVALID_ARG, KVD_ERR_UNSUPPORTED, KVD_ERR_WORKSPACE, KVD_F16, KVD_F32, KVD_OK, KvdError,
-    KVD_STEP_HISTORY_STABLE, alloc_host_inputs, alloc_host_staging, kvd_decode_step_host, kvd_host_staging_bytes,
+    KVD_STEP_HISTORY_STABLE, alloc_host_inputs, alloc_host_staging, kvd_decode_step_host, kvd_decode_step_host_packed,
+    kvd_host_staging_bytes,
     alloc_workspace, kvd_append, kvd_cache_bytes, kvd_decode_attention, kvd_decode_attention_noalloc,
     kvd_decode_plan, kvd_decode_step, kvd_decode_workspace_bytes, kvd_paged_append,
     kvd_paged_decode_attention, kvd_paged_decode_step, KVD_E4M3, kvd_append_e4m3,

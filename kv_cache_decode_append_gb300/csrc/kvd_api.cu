@@ -1048,11 +1048,13 @@ bool page_locked(const void *p)
 }
 }  // namespace
 
-kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache, const void *k_new_host,
-                                const void *v_new_host, void *out_host, const int32_t *past_len_host, int B,
-                                int H_q, int H_kv, int T_max, int D, int N, int max_past_len, float scale,
-                                kvd_dtype dtype, void *staging, size_t staging_bytes, void *workspace,
-                                size_t workspace_bytes, uint32_t *err_word, void *stream)
+namespace {
+// kvd_decode_step_host and _packed: `packed` (one host block in the staging
+// layout's input part, at q_host) or the four inputs at their own addresses.
+kvd_status host_step(const void *q_host, const void *k_new_host, const void *v_new_host, const int32_t *past_len_host,
+                     bool packed, void *k_cache, void *v_cache, void *out_host, int B, int H_q, int H_kv, int T_max,
+                     int D, int N, int max_past_len, float scale, kvd_dtype dtype, void *staging,
+                     size_t staging_bytes, void *workspace, size_t workspace_bytes, uint32_t *err_word, void *stream)
 {
     // Every check before anything is queued.
     if (!q_host || !k_new_host || !v_new_host || !out_host || !past_len_host || !k_cache || !v_cache)
@@ -1068,34 +1070,26 @@ kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache
         return KVD_ERR_WORKSPACE;
     const size_t s = (size_t)elem_bytes(dtype);
     const size_t qb = (size_t)B * H_q * N * D * s, nb = (size_t)B * H_kv * N * D * s, pb = (size_t)B * 4;
-    char *st_base = static_cast<char *>(staging);
-    char *q_d = st_base;
+    char *q_d = static_cast<char *>(staging);
     char *kn_d = q_d + round_up(qb, 256);
     char *vn_d = kn_d + round_up(nb, 256);
     int32_t *pl_d = reinterpret_cast<int32_t *>(vn_d + round_up(nb, 256));
     char *out_d = reinterpret_cast<char *>(pl_d) + round_up(pb, 256);
+    const size_t in_bytes = (size_t)(reinterpret_cast<char *>(pl_d) - q_d) + pb;  // the inputs part
     size_t ws_need = 0, zero_off = 0, zero_bytes = 0;
     st = kvd::decode_attention_prepare(q_d, k_cache, v_cache, out_d, pl_d, B, H_q, H_kv, T_max, D, N,
                                        max_past_len, dtype, &ws_need, &zero_off, &zero_bytes);
     if (st != KVD_OK) return st;
     if (workspace == nullptr || workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return KVD_ERR_WORKSPACE;
-    if (!page_locked(q_host) || !page_locked(k_new_host) || !page_locked(v_new_host) || !page_locked(out_host) ||
-        !page_locked(past_len_host))
+    if (!page_locked(q_host) || !page_locked(out_host) ||
+        (packed ? !page_locked(static_cast<const char *>(q_host) + in_bytes - 1)
+                : (!page_locked(k_new_host) || !page_locked(v_new_host) || !page_locked(past_len_host))))
         return KVD_ERR_INVALID_ARG;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // Inputs laid out in one host block exactly as in the staging buffer
-    // (k_new, v_new and past_len at the staging offsets from q): one copy,
-    // else one per input.
-    const char *qh = static_cast<const char *>(q_host);
-    const bool packed = static_cast<const char *>(k_new_host) == qh + (kn_d - q_d) &&
-                        static_cast<const char *>(v_new_host) == qh + (vn_d - q_d) &&
-                        reinterpret_cast<const char *>(past_len_host) == qh + (reinterpret_cast<char *>(pl_d) - q_d);
     if (packed) {
-        if (cudaMemcpyAsync(q_d, q_host, (size_t)(reinterpret_cast<char *>(pl_d) - q_d) + pb, cudaMemcpyHostToDevice,
-                            cs) != cudaSuccess)
-            return KVD_ERR_CUDA;
+        if (cudaMemcpyAsync(q_d, q_host, in_bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess) return KVD_ERR_CUDA;
     } else if (cudaMemcpyAsync(q_d, q_host, qb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
                cudaMemcpyAsync(kn_d, k_new_host, nb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
                cudaMemcpyAsync(vn_d, v_new_host, nb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
@@ -1106,6 +1100,31 @@ kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache
                          scale, dtype, workspace, workspace_bytes, err_word, stream);
     if (st != KVD_OK) return st;
     return cudaMemcpyAsync(out_host, out_d, qb, cudaMemcpyDeviceToHost, cs) == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+}  // namespace
+
+kvd_status kvd_decode_step_host(const void *q_host, void *k_cache, void *v_cache, const void *k_new_host,
+                                const void *v_new_host, void *out_host, const int32_t *past_len_host, int B,
+                                int H_q, int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                                kvd_dtype dtype, void *staging, size_t staging_bytes, void *workspace,
+                                size_t workspace_bytes, uint32_t *err_word, void *stream)
+{
+    return host_step(q_host, k_new_host, v_new_host, past_len_host, false, k_cache, v_cache, out_host, B, H_q, H_kv,
+                     T_max, D, N, max_past_len, scale, dtype, staging, staging_bytes, workspace, workspace_bytes,
+                     err_word, stream);
+}
+
+kvd_status kvd_decode_step_host_packed(const void *inputs_host, void *k_cache, void *v_cache, void *out_host, int B,
+                                       int H_q, int H_kv, int T_max, int D, int N, int max_past_len, float scale,
+                                       kvd_dtype dtype, void *staging, size_t staging_bytes, void *workspace,
+                                       size_t workspace_bytes, uint32_t *err_word, void *stream)
+{
+    // (the inputs' own addresses inside the block only matter for the null
+    // checks: the block is copied in one piece)
+    const void *p = inputs_host;
+    return host_step(p, p, p, static_cast<const int32_t *>(p), true, k_cache, v_cache, out_host, B, H_q, H_kv, T_max,
+                     D, N, max_past_len, scale, dtype, staging, staging_bytes, workspace, workspace_bytes, err_word,
+                     stream);
 }
 
 const char *kvd_status_string(kvd_status status)

@@ -82,6 +82,9 @@ class _Lib:
         lib.kvd_decode_step_host.restype = ci
         lib.kvd_decode_step_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
                                              vp, sz, vp, sz, u32p, vp]
+        lib.kvd_decode_step_host_packed.restype = ci
+        lib.kvd_decode_step_host_packed.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp, sz, vp, sz,
+                                                    u32p, vp]
         lib.kvd_host_staging_bytes.restype = sz
         lib.kvd_host_staging_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
         lib.kvd_host_staging_inputs_bytes.restype = sz
@@ -301,9 +304,9 @@ def kvd_host_staging_bytes(B, H_q, H_kv, D, N, dtype) -> int:
 
 
 def alloc_host_inputs(B, H_q, H_kv, D, N, dtype) -> dict:
-    """Page-locked host tensors q [B,H_q,N,D], k_new / v_new [B,H_kv,N,D] and past_len [B]
-    (int32), views into one block laid out as the staging buffer's inputs, so that
-    ``kvd_decode_step_host`` moves the four in one copy."""
+    """One page-locked block for ``kvd_decode_step_host_packed`` (key ``block``) and
+    views into it: q [B,H_q,N,D], k_new / v_new [B,H_kv,N,D] and past_len [B] (int32),
+    laid out as the staging buffer's inputs."""
     tdt = dtype if isinstance(dtype, torch.dtype) else {"f32": torch.float32, "bf16": torch.bfloat16,
                                                          "f16": torch.float16}[dtype]
     code = _TORCH_DTYPE[tdt]
@@ -368,6 +371,36 @@ def kvd_decode_step_host(q_host, k_cache, v_cache, k_new_host, v_new_host, out_h
                                   staging.data_ptr(), staging.numel() * staging.element_size(), ws_ptr, ws_bytes,
                                   _ptr(err_word), _stream_handle(stream))
     _check("kvd_decode_step_host", st)
+
+
+def kvd_decode_step_host_packed(host_inputs: dict, k_cache, v_cache, out_host, max_past_len: int,
+                                staging: torch.Tensor, scale: float = 0.0, workspace: Optional[torch.Tensor] = None,
+                                err_word=None, stream=None) -> None:
+    """``kvd_decode_step_host`` with the inputs in the one block of ``alloc_host_inputs``
+    (copied to the device in one piece)."""
+    q = host_inputs["q"]
+    dt = q.dtype
+    block = host_inputs["block"]
+    if block.is_cuda or not block.is_pinned() or block.dtype != torch.uint8:
+        raise ValueError("host_inputs must come from alloc_host_inputs")
+    _need_pinned("out_host", out_host, dt)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, dt)
+    if staging.device.type != "cuda" or not staging.is_contiguous():
+        raise ValueError("staging must be a contiguous CUDA tensor")
+    if err_word is not None:
+        _need_cuda("err_word", err_word, torch.int32)
+    B, H_q, N, D = q.shape
+    _, H_kv, T_max, _ = k_cache.shape
+    if out_host.shape != q.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or k_cache.shape[3] != D \
+            or tuple(host_inputs["k_new"].shape) != (B, H_kv, N, D):
+        raise ValueError("shape mismatch between the inputs, out and the caches")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = raw.kvd_decode_step_host_packed(block.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out_host.data_ptr(),
+                                         B, H_q, H_kv, T_max, D, N, int(max_past_len), float(scale), _TORCH_DTYPE[dt],
+                                         staging.data_ptr(), staging.numel() * staging.element_size(), ws_ptr,
+                                         ws_bytes, _ptr(err_word), _stream_handle(stream))
+    _check("kvd_decode_step_host_packed", st)
 
 
 # ---------------------------------------------------------------------------------

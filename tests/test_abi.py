@@ -213,6 +213,22 @@ def test_decode_step_host_argument_errors(lib):
     assert step(B=0, staging=None) == 0
 
 
+def test_decode_step_host_packed_argument_errors(lib):
+    def step(block=A, staging=A, staging_bytes=1 << 20, **kw):
+        args = dict(k=A, v=A, out=A, B=1, H_q=4, H_kv=2, T_max=64, D=64, N=1, max_past=10, dtype=1)
+        args.update(kw)
+        return lib.kvd_decode_step_host_packed(block, args["k"], args["v"], args["out"], args["B"], args["H_q"],
+                                               args["H_kv"], args["T_max"], args["D"], args["N"], args["max_past"],
+                                               0.0, args["dtype"], staging, staging_bytes, None, 0, None, None)
+    assert step(block=0) == 1
+    assert step(out=0) == 1
+    assert step(D=80) == 3
+    assert step(dtype=3) == 3
+    assert step(staging=None) == 4
+    assert step(staging_bytes=1791) == 4
+    assert step(B=0, staging=None) == 0
+
+
 def test_host_staging_bytes(lib):
     # q and out: 1*4*1*64 bf16 = 512 B each; k_new, v_new: 256 B each; past_len: 4 B -> 256
     assert lib.kvd_host_staging_bytes(1, 4, 2, 64, 1, 1) == 512 + 512 + 256 + 256 + 256

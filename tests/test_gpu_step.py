@@ -165,8 +165,7 @@ def test_step_host_buffers(orc, case):
     hp["past_len"].copy_(past)
     kc2, vc2 = t["k_cache"].to(DEV).clone(), t["v_cache"].to(DEV).clone()
     out_p = torch.full(t["q"].shape, float("nan"), dtype=t["q"].dtype).pin_memory()
-    kvd.kvd_decode_step_host(hp["q"], kc2, vc2, hp["k_new"], hp["v_new"], out_p, hp["past_len"], max_past, staging,
-                             0.0, ws2, err)
+    kvd.kvd_decode_step_host_packed(hp, kc2, vc2, out_p, max_past, staging, 0.0, ws2, err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert _same_bits(out_p, out1) and _same_bits(kc2, g1["k_cache"]) and _same_bits(vc2, g1["v_cache"])
