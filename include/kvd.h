@@ -34,6 +34,15 @@
  *     and never synchronises the host with the device.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     All device work of a call is enqueued on it, in order.
+ *   - The kernels are launched with programmatic stream serialization: each
+ *     waits for the work queued before it (griddepcontrol.wait) before it
+ *     touches anything that work may write, and lets the next kernel on the
+ *     stream launch before it has finished.  A kernel of the caller's, launched
+ *     next on the stream with the programmatic-serialization attribute, must
+ *     itself wait (cudaGridDependencySynchronize) before it reads what these
+ *     calls wrote; kernels launched without that attribute, copies and events
+ *     are ordered as usual.  (KVD_STEP_HISTORY_STABLE, below, lets a call read
+ *     the cached history before that wait.)
  *   - Argument errors are found on the host before anything is launched and are
  *     returned as a status; nothing is written then.  A launch failure returns
  *     KVD_ERR_CUDA.
