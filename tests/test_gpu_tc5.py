@@ -87,3 +87,13 @@ def test_tc5_gqa_longctx_chunk8_full_size(orc):
     w = wl.with_n(wl.WORKLOADS["gqa_longctx_b32_bf16"], 8)
     assert kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max(wl.past_lens(w).tolist()), "bf16")["tensor_cores"] == 2
     test_gpu_step._check(orc, w, wl.past_lens(w), device_inputs=True)
+
+
+@pytest.mark.parametrize("n_new", [16, 32], ids=["n16_64rows", "n32_128rows"])
+def test_tc5_gqa_longctx_chunk_full_size(orc, n_new):
+    """The long-context workload at full size with 16 and 32 new tokens: 64 and 128 rows
+    per KV head (the launch configurations bench.py --n-new 16 / 32 time)."""
+    w = wl.with_n(wl.WORKLOADS["gqa_longctx_b32_bf16"], n_new)
+    plan = kvd.kvd_decode_plan(w.B, w.H_q, w.H_kv, w.D, w.N, max(wl.past_lens(w).tolist()), "bf16")
+    assert plan["tensor_cores"] == 2 and plan["rows_per_block"] == 128
+    test_gpu_step._check(orc, w, wl.past_lens(w), device_inputs=True)
