@@ -340,10 +340,11 @@ __device__ __forceinline__ void mma_tile_e4m3(unsigned char *Ks, unsigned char *
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // chunk c + h
                 const uint32_t v0 = r[c / 2][2 * h], v1 = r[c / 2][2 * h + 1];  // keys kb+2t.., kb+8+2t..
-                mma_16816<__half>(oacc[2 * (c + h)], pa, e4m3x2_to_f16x2(__byte_perm(v0, 0, 0x0020)),
-                                  e4m3x2_to_f16x2(__byte_perm(v1, 0, 0x0020)));
-                mma_16816<__half>(oacc[2 * (c + h) + 1], pa, e4m3x2_to_f16x2(__byte_perm(v0, 0, 0x0031)),
-                                  e4m3x2_to_f16x2(__byte_perm(v1, 0, 0x0031)));
+                // one permute per column parity: the low half holds keys kb+2t, +1,
+                // the high half keys kb+8+2t, +1 (the two B registers)
+                const uint32_t ev = __byte_perm(v0, v1, 0x6420), od = __byte_perm(v0, v1, 0x7531);
+                mma_16816<__half>(oacc[2 * (c + h)], pa, e4m3x2_to_f16x2(ev & 0xffffu), e4m3x2_to_f16x2(ev >> 16));
+                mma_16816<__half>(oacc[2 * (c + h) + 1], pa, e4m3x2_to_f16x2(od & 0xffffu), e4m3x2_to_f16x2(od >> 16));
             }
     }
 }
