@@ -278,22 +278,26 @@ __device__ __forceinline__ void mma_tile_e4m3(unsigned char *Ks, unsigned char *
             for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
     }
 
-    // ---- scale, mask, online softmax (as mma_tile) ----
+    // ---- mask, online softmax (as mma_tile), the row's score factor folded
+    //      into the exponent: the max is taken on the raw scores (sfac > 0, so
+    //      the order is kept and max(s) sfac rounds as max(s sfac) does) and
+    //      each weight is exp2(fma(s, sfac, -m)) -- one instruction less per
+    //      score on this ALU-bound path ----
+    if constexpr (kMasked) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            sacc[nt][e] *= sfac[e >> 1];
-            if constexpr (kMasked) {
+            for (int e = 0; e < 4; ++e) {
                 const int key = tile_k0 + kb + nt * 8 + 2 * t + (e & 1);
                 if (key >= lim[e >> 1]) sacc[nt][e] = kNegInf;
             }
-        }
+    }
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         float mt = fmaxf(fmaxf(sacc[0][2 * rr], sacc[0][2 * rr + 1]), fmaxf(sacc[1][2 * rr], sacc[1][2 * rr + 1]));
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        mt *= sfac[rr];
         if (mt > m[rr] + kRescaleThreshold) {
             const float alpha = fast_exp2(m[rr] - mt);
             l[rr] *= alpha;
@@ -309,7 +313,7 @@ __device__ __forceinline__ void mma_tile_e4m3(unsigned char *Ks, unsigned char *
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 2 * rr; e < 2 * rr + 2; ++e) {
-                const float p = fast_exp2(sacc[nt][e] - mu);
+                const float p = fast_exp2(fmaf(sacc[nt][e], sfac[rr], -mu));
                 l[rr] += p;
                 sacc[nt][e] = p;
             }
