@@ -1,8 +1,10 @@
 """Consecutive decode steps that start before the previous kernel finishes.
 
 Small layers (kvd_plan_info.early_start) let the next kernel on the stream
-launch early: with KVD_STEP_HISTORY_STABLE its CTAs read past_len and load
-their first K/V tiles before they wait for the previous kernel.  Only what the previous kernel may write has to wait: q, the
+launch early: with KVD_STEP_HISTORY_STABLE their CTAs read past_len and load
+their first K/V tiles before they wait for the previous kernel.  The tcgen05
+cases chain layers through the merge pass's early release of the next launch
+(the flag changes nothing there).  Only what the previous kernel may write has to wait: q, the
 new rows, the workspace.  These tests chain layers whose q, k_new and v_new
 are the previous layer's output, so a read issued before the wait would see
 stale data, and require the chained results to be bit-identical to layers run
@@ -71,6 +73,9 @@ CASES = [  # (B, H, D, N, T_max, past, dtype)
     (1, 12, 64, 4, 1024, [512], "f32"),                     # chunked decode
     (3, 4, 128, 2, 700, [31, 697, 300], "bf16"),            # ragged histories, new keys across tiles
     (2, 6, 64, 3, 300, [0, 257], "f16"),                    # empty history
+    (3, 4, 128, 20, 700, [300, 677, 0], "bf16"),            # 20 rows per head: tcgen05, new keys across tiles
+    (2, 2, 64, 40, 900, [860, 1], "f16"),                   # 40 rows, fp16: tcgen05
+    (32, 8, 128, 20, 4100, [4000 - 97 * i for i in range(32)], "bf16"),  # tcgen05, long ranges: merge pass
 ]
 
 
@@ -80,7 +85,8 @@ CASES = [  # (B, H, D, N, T_max, past, dtype)
 def test_chained_layers_match_serial(case, flags, graph):
     B, H, D, N, T_max, past, dtype = case
     w = wl.Workload(0, "chain", L=1, B=B, H_q=H, H_kv=H, D=D, N=N, dtype=dtype, T_max=T_max, P=0)
-    assert kvd.kvd_decode_plan(B, H, H, D, N, max(past), w.torch_dtype)["early_start"] == 1
+    plan = kvd.kvd_decode_plan(B, H, H, D, N, max(past), w.torch_dtype)
+    assert plan["early_start"] == 1 or plan["tensor_cores"] == 2
     layers = 6
     ins_ref, ref = _chain(w, past, layers, None)
     ins, got = _chain(w, past, layers, flags, graph=graph)
