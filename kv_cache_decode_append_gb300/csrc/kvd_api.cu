@@ -422,9 +422,10 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
     if (st != KVD_OK) return st;
     pl->rows = (H_q / H_kv) * N;
     // Many query rows per KV head (chunked decode with GQA): the tensor cores,
-    // in blocks of 16 rows (mma.sync) or, for 16-bit caches from kTc5MinRows
-    // rows, of 128 rows (tcgen05).  The choice does not depend on the cache
-    // layout, so paged and contiguous calls give the same bits.
+    // in blocks of 16 rows (mma.sync; E4M3 heads of at most 8 rows in the
+    // swapped 8-row form) or, for 16-bit caches from kTc5MinRows rows, of 128
+    // rows (tcgen05).  The choice does not depend on the cache layout, so
+    // paged and contiguous calls give the same bits.
     const bool f16_family = dtype == KVD_BF16 || dtype == KVD_F16;
     pl->tc5 = f16_family && pl->rows >= kTc5MinRows;
     pl->mma = !pl->tc5 && ((pl->rows >= (D == 128 ? kMmaMinRows128 : kMmaMinRows64) && f16_family) ||
@@ -439,9 +440,12 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
         };
         if (!builds(paged, &vp, &vt) || !builds(!paged, &op, &ot)) return KVD_ERR_UNSUPPORTED;
     } else if (pl->mma && dtype == KVD_E4M3) {
-        if (!attn_variant_mma_e4m3(D, &vp) || !attn_variant_mma_e4m3_tk(D, &vt)) return KVD_ERR_UNSUPPORTED;
+        if (!attn_variant_mma_e4m3(D, pl->rows, &vp) || !attn_variant_mma_e4m3_tk(D, pl->rows, &vt))
+            return KVD_ERR_UNSUPPORTED;
         op = vp;
         ot = vt;
+        pl->rb = vp.rows_per_block;  // (16, or 8 in the swapped form)
+        pl->n_rowblocks = (pl->rows + pl->rb - 1) / pl->rb;
     } else if (pl->mma) {
         const auto builds = [&](bool pg, AttnVariant *p, AttnVariant *t) {
             return dtype == KVD_BF16 ? attn_variant_mma_bf16(D, pg, p) && attn_variant_mma_bf16_tk(D, pg, t)
@@ -517,8 +521,10 @@ kvd_status make_plan(int B, int H_q, int H_kv, int D, int N, int max_past_len, k
         }
     }
 
-    // (partial slots of the tensor-core kernels hold only a block's real rows)
-    const int part_rows = (pl->mma || pl->tc5) && pl->rows < pl->rb ? pl->rows : pl->rb;
+    // (partial slots of blocks of 16 or more rows -- the tensor-core kernels'
+    // but the 8-row E4M3 form -- hold only a block's real rows: the kernels'
+    // part_rows<RB>)
+    const int part_rows = pl->rb >= 16 && pl->rows < pl->rb ? pl->rows : pl->rb;
     const size_t pieces = (size_t)sms * (occ > occ_other ? occ : occ_other) * 2 * part_rows;
     size_t off = 0;
     pl->part_off = off;  // per piece row: o[D], m, l, 2 floats of padding (16-byte rows)

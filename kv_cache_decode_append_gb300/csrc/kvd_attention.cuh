@@ -678,10 +678,11 @@ template <typename S, bool kWriteSeg, bool kPaged> struct RangeWalk {
     }
 };
 
-// Rows per partial slot.  The CUDA-core kernels' row blocks (RB 1, 2, 4, 8)
-// are sized to their rows; the tensor-core kernels' 16- and 128-row blocks
-// (used by no other kernel) keep only the block's real rows, min(RB, rows),
-// so few-row decodes do not carry padded partials.
+// Rows per partial slot.  Row blocks of fewer than 16 rows (the CUDA-core
+// kernels' RB 1, 2, 4, 8 and the 8-row E4M3 tensor-core form) keep all RB
+// slots; the tensor-core kernels' 16- and 128-row blocks keep only the
+// block's real rows, min(RB, rows), so few-row decodes do not carry padded
+// partials.  The host sizes the workspace by the same rule.
 template <int RB> __device__ __forceinline__ int part_rows(int rows)
 {
     if constexpr (RB >= 16) return rows < RB ? rows : RB;
@@ -1507,8 +1508,8 @@ bool attn_variant_mma_bf16(int D, bool paged, AttnVariant *v);
 bool attn_variant_mma_bf16_tk(int D, bool paged, AttnVariant *v);
 bool attn_variant_mma_f16(int D, bool paged, AttnVariant *v);
 bool attn_variant_mma_f16_tk(int D, bool paged, AttnVariant *v);
-bool attn_variant_mma_e4m3(int D, AttnVariant *v);  // bf16 q / out, E4M3 cache, D = 128
-bool attn_variant_mma_e4m3_tk(int D, AttnVariant *v);
+bool attn_variant_mma_e4m3(int D, int rows, AttnVariant *v);  // bf16 q / out, E4M3 cache, D = 128
+bool attn_variant_mma_e4m3_tk(int D, int rows, AttnVariant *v);
 // tcgen05 kernels (kvd_attention_tc5.cuh): 128-row blocks, contiguous or paged caches
 bool attn_variant_tc5_bf16(int D, bool paged, AttnVariant *v);
 bool attn_variant_tc5_bf16_tk(int D, bool paged, AttnVariant *v);

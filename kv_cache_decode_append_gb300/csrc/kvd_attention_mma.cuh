@@ -35,13 +35,16 @@ namespace kvd {
 
 // Compile-time shape of a tensor-core variant: 16 query rows, 64-key tiles,
 // 4 warps of 16 keys.  Member names match AttnShape where RangeWalk and the
-// epilogue use them.
-template <typename T, int D, typename C = T> struct MmaShape {
+// epilogue use them.  RB = 8 (E4M3 caches only) is the swapped form of
+// mma_tile_e4m3_t: blocks of at most 8 query rows, the rows as the MMA's
+// 8-wide N dimension and keys / output columns as its 16-wide M dimension.
+template <typename T, int D, typename C = T, int RB = 16> struct MmaShape {
     using Tq = Elem<T>;
     static constexpr bool k8 = sizeof(C) == 1;         // E4M3 cache (8-bit codes)
+    static constexpr bool kT8 = RB == 8;               // swapped operands (mma_tile_e4m3_t)
     static constexpr bool kTma = true;
     static constexpr bool kQInRing = true;
-    static constexpr int kRB = 16;
+    static constexpr int kRB = RB;
     static constexpr int kRowBytes = D * (int)sizeof(C);
     static constexpr int kQRowBytes = D * 2;
     static constexpr int kTK = 64;
@@ -55,11 +58,15 @@ template <typename T, int D, typename C = T> struct MmaShape {
     // E4M3: 3 stages, so that three CTAs (12 warps) share an SM; the
     // widening makes its tiles latency-bound with fewer warps
     static constexpr int kStages = (D == 128) ? 3 : 4;
+    // (the swapped form, at four CTAs per SM under 128 registers, spilled in
+    // the fused step and was no faster than the 16-row form: three)
     static constexpr int kMinBlocks = k8 ? 3 : 1;     // CTAs per SM the registers must allow
     static constexpr int kQSlotBytes = kRB * kQRowBytes;
     static constexpr int kPieceUnits = 2;
     static constexpr int kKSteps = D / 16;             // k-steps of S = Q.K^T
     static constexpr int kNTiles = D / 8;              // 8-wide output column tiles of O
+    static constexpr int kQRegs = kT8 ? 2 : 4;         // Q fragment registers per k-step (B or A operand)
+    static constexpr int kOTiles = kT8 ? D / 16 : kNTiles;  // accumulator tiles of O (O^T when kT8)
 
     static constexpr int kRingOff = 0;                 // 1024-aligned boxes (swizzle pattern)
     static constexpr int kQOff = kRingOff + kStages * 2 * kTileBytes;
@@ -82,6 +89,8 @@ template <typename T, int D, typename C = T> struct MmaShape {
     static_assert(2 * kNW * kRB * 4 <= kQSlotBytes, "m and l in the q slot");
     static_assert(kMergeWarps * kRB * D * 4 <= 2 * kTileBytes, "merge in the slot");
     static_assert(!k8 || D == 128, "E4M3 tiles: one 128-byte box per row");
+    static_assert(RB == 16 || (kT8 && k8), "8-row blocks: the swapped E4M3 form only");
+    static_assert(!kT8 || kMergePhases == 1, "8-row blocks merge in one phase");
 };
 
 // Shared-memory address of the 16-byte chunk c (0 .. D/8-1) of tile row r in
@@ -353,6 +362,128 @@ __device__ __forceinline__ void mma_tile_e4m3(unsigned char *Ks, unsigned char *
     }
 }
 
+// The same tile with at most 8 query rows per block (RB = 8), operands
+// swapped: S^T = K . Q^T and O^T = V^T . P^T, so that the MMA's 16-wide M
+// dimension runs over the warp's 16 keys (then over 16 output columns) and
+// its 8-wide N dimension over the query rows.  The 16-row form computes 16
+// rows of which 8 .. 15 would be padding; this one issues half the MMAs and
+// holds half the scores, Q fragments and accumulators.  The widening is the
+// same per code.
+//   * K: ldmatrix.x4 of the 16-bit view gives lane (g, t) the codes
+//     16c + 4t .. 4t+3 of keys kb+g and kb+8+g; the low pair widened is A's
+//     columns 2t, 2t+1, the high pair its columns 2t+8, 2t+9 (rows g, g+8):
+//     the contraction order of mma_tile_e4m3, which qb follows
+//     (qb[c] = query row g's columns 16c + 4t, +1 | 4t+2, 4t+3).
+//   * S^T's accumulators hold keys kb+g (e = 0, 1) and kb+8+g (e = 2, 3) of
+//     query rows 2t + (e & 1); m, l, lim and sfac are per row 2t + j.
+//   * P^T: each 8x8 half of S^T packed to fp16 is in ldmatrix's fragment
+//     layout (row = key); movmatrix transposes it into B's layout (keys 2t,
+//     2t+1 | 2t+8, 2t+9 at query row g).
+//   * V: ldmatrix.x4.trans as in mma_tile_e4m3; the even-column permute
+//     gives A's rows 0 .. 7 (output column 16c + 2g), the odd one its rows
+//     8 .. 15 (column 16c + 2g + 1), so oacc[c][e] is query row 2t + (e & 1)
+//     at output column 16c + 2g + (e >> 1).
+template <int D, bool kMasked>
+__device__ __forceinline__ void mma_tile_e4m3_t(unsigned char *Ks, unsigned char *Vs, const uint32_t (&qb)[D / 16][2],
+                                                float (&oacc)[D / 16][4], float (&m)[2], float (&l)[2], int warp,
+                                                int lane, int tile_k0, const int (&lim)[2], int k_end,
+                                                const float (&sfac)[2])
+{
+    using S = MmaShape<__nv_bfloat16, D, __nv_fp8_e4m3, 8>;
+    const float kNegInf = __int_as_float(0xff800000);
+    constexpr float kRescaleThreshold = 8.0f;
+    const int g = lane >> 2;
+    const int kb = warp * S::kKpw;
+    const uint32_t k_base = smem_addr(Ks), v_base = smem_addr(Vs);
+    // ldmatrix.x4 matrices: (keys kb.., chunk c), (kb+8.., c), (kb.., c+1), (kb+8.., c+1)
+    const int key = kb + (((lane >> 3) & 1) << 3) + (lane & 7);
+    const int csel = lane >> 4;
+
+    // ---- S^T = K . Q^T: even and odd chunks in two dependency chains ----
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sodd[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+        uint32_t r[D / 32][4];
+#pragma unroll
+        for (int c = 0; c < D / 16; c += 2) ldmatrix_x4_addr(r[c / 2], mma_chunk_addr<S>(k_base, key, c + csel));
+#pragma unroll
+        for (int c = 0; c < D / 16; c += 2)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // chunk c + h: keys kb+g (register 2h), kb+8+g (2h+1)
+                const uint32_t k0 = r[c / 2][2 * h], k1 = r[c / 2][2 * h + 1];
+                const uint32_t ka[4] = {e4m3x2_to_f16x2(k0 & 0xffffu), e4m3x2_to_f16x2(k1 & 0xffffu),
+                                        e4m3x2_to_f16x2(k0 >> 16), e4m3x2_to_f16x2(k1 >> 16)};
+                mma_16816<__half>(h ? sodd : sacc, ka, qb[c + h][0], qb[c + h][1]);
+            }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
+    }
+
+    // ---- mask, online softmax per query row 2t + j (max over the keys of
+    //      the 8 lanes g sharing t), the row's score factor in the exponent
+    //      as in mma_tile_e4m3 ----
+    if constexpr (kMasked) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (tile_k0 + kb + g + ((e >> 1) << 3) >= lim[e & 1]) sacc[e] = kNegInf;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        float mt = fmaxf(sacc[j], sacc[j + 2]);
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        mt *= sfac[j];
+        if (mt > m[j] + kRescaleThreshold) {
+            const float alpha = fast_exp2(m[j] - mt);
+            l[j] *= alpha;
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+                oacc[c][j] *= alpha;
+                oacc[c][j + 2] *= alpha;
+            }
+            m[j] = mt;
+        }
+        const float mu = (m[j] == kNegInf) ? 0.f : m[j];
+#pragma unroll
+        for (int e = j; e < 4; e += 2) {
+            const float p = fast_exp2(fmaf(sacc[e], sfac[j], -mu));
+            l[j] += p;
+            sacc[e] = p;
+        }
+    }
+    // P^T as the B fragments of O^T += V^T . P^T
+    const uint32_t pb0 = movmatrix_trans(pack_pair<__half>(sacc[0], sacc[1]));
+    const uint32_t pb1 = movmatrix_trans(pack_pair<__half>(sacc[2], sacc[3]));
+
+    if constexpr (kMasked) {
+        if (tile_k0 + kb + S::kKpw > k_end) {
+            for (int idx = lane; idx < S::kKpw * (D / 16); idx += 32) {
+                const int rr = kb + idx / (D / 16), c = idx % (D / 16);
+                if (tile_k0 + rr >= k_end) sts128(mma_chunk_addr<S>(v_base, rr, c), make_uint4(0u, 0u, 0u, 0u));
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+        }
+    }
+
+    // ---- O^T += V^T . P^T ----
+    {
+        uint32_t r[D / 32][4];
+#pragma unroll
+        for (int c = 0; c < D / 16; c += 2) ldmatrix_x4_trans_addr(r[c / 2], mma_chunk_addr<S>(v_base, key, c + csel));
+#pragma unroll
+        for (int c = 0; c < D / 16; c += 2)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // chunk c + h
+                const uint32_t v0 = r[c / 2][2 * h], v1 = r[c / 2][2 * h + 1];  // keys kb+2t.., kb+8+2t..
+                const uint32_t ev = __byte_perm(v0, v1, 0x6420), od = __byte_perm(v0, v1, 0x7531);
+                const uint32_t va[4] = {e4m3x2_to_f16x2(ev & 0xffffu), e4m3x2_to_f16x2(od & 0xffffu),
+                                        e4m3x2_to_f16x2(ev >> 16), e4m3x2_to_f16x2(od >> 16)};
+                mma_16816<__half>(oacc[c + h], va, pb0, pb1);
+            }
+    }
+}
+
 // In a fused step the tile holding new keys P .. P+N-1 has stale cache rows:
 // the warp copies its new rows from k_new / v_new into the tile (and, when
 // kc / vc are given, into the cache: kc, vc address the cache row of the
@@ -399,14 +530,16 @@ __device__ __forceinline__ void mma_insert_new_rows(unsigned char *Ks, unsigned 
 // the contiguous cache viewed as [B*H_kv*T_max, D], or over the page pool
 // viewed as [num_pages*H_kv*page_size, D] when kPaged).
 // C: the cache element type (T, or E4M3 codes with bf16 T: contiguous only).
-template <typename T, int D, bool kFused, bool kTicketMerge, bool kPaged, typename C = T>
-__global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>::kMinBlocks)
+// kRows: rows per block, 16, or 8 for the swapped E4M3 form (mma_tile_e4m3_t).
+template <typename T, int D, bool kFused, bool kTicketMerge, bool kPaged, typename C = T, int kRows = 16>
+__global__ void __launch_bounds__(MmaShape<T, D, C, kRows>::kThreads, MmaShape<T, D, C, kRows>::kMinBlocks)
     attn_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v)
 {
-    using S = MmaShape<T, D, C>;
+    using S = MmaShape<T, D, C, kRows>;
     using Tq = Elem<T>;
     constexpr bool k8 = S::k8;
+    constexpr bool kT8 = S::kT8;
     static_assert(!(k8 && kPaged), "the E4M3 cache is contiguous only");
     constexpr int RB = S::kRB;
     const float kNegInf = __int_as_float(0xff800000);
@@ -483,8 +616,9 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         }
     }
 
-    uint32_t qa[S::kKSteps][4];
-    float oacc[S::kNTiles][4];
+    uint32_t qa[S::kKSteps][S::kQRegs];
+    float oacc[S::kOTiles][4];
+    // per row: g, g+8 (16-row blocks) or 2t, 2t+1 (8-row blocks)
     float m_run[2], l_run[2];
     float sfac[2];  // E4M3: per-row score factor (see mma_tile_e4m3)
     int lim[2];
@@ -535,16 +669,48 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
             const int q_rows = min(RB, a.rows - mt.rb * RB);
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const int rg = mt.rb * RB + g + 8 * r;
+                const int rg = mt.rb * RB + (kT8 ? 2 * t + r : g + 8 * r);
                 lim[r] = mt.P + 1 + (rg % a.N);
                 m_run[r] = kNegInf;
                 l_run[r] = 0.f;
             }
 #pragma unroll
-            for (int nt = 0; nt < S::kNTiles; ++nt)
+            for (int nt = 0; nt < S::kOTiles; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.f;
-            if constexpr (k8) {
+            if constexpr (kT8) {
+                // B fragments of Q^T: row g, columns 16c + 4t .. 4t+3 (the
+                // permuted order of mma_tile_e4m3_t); the row's power-of-two
+                // range factor as in the 16-row form, its score factor then
+                // fetched by the lanes that hold the row's scores (t = row / 2)
+                const int row = g;
+                float qf[S::kKSteps][4];
+                float amax = 0.f;
+#pragma unroll
+                for (int c = 0; c < S::kKSteps; ++c) {
+                    uint2 raw = make_uint2(0u, 0u);
+                    if (row < q_rows) raw = *reinterpret_cast<const uint2 *>(qs + row * S::kQRowBytes + (16 * c + 4 * t) * 2);
+                    qf[c][0] = __uint_as_float(raw.x << 16);
+                    qf[c][1] = __uint_as_float(raw.x & 0xffff0000u);
+                    qf[c][2] = __uint_as_float(raw.y << 16);
+                    qf[c][3] = __uint_as_float(raw.y & 0xffff0000u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qf[c][e]));
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const int ex = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+                const int shift = ex >= 15 ? ex - 14 : 0;
+                const float down = __uint_as_float((uint32_t)(127 - shift) << 23);  // 2^-shift
+                const float f = a.qscale * __uint_as_float((uint32_t)(127 + shift) << 23);
+#pragma unroll
+                for (int c = 0; c < S::kKSteps; ++c) {
+                    qa[c][0] = pack_pair<__half>(qf[c][0] * down, qf[c][1] * down);
+                    qa[c][1] = pack_pair<__half>(qf[c][2] * down, qf[c][3] * down);
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) sfac[j] = __shfl_sync(0xffffffffu, f, (2 * t + j) * 4);
+            } else if constexpr (k8) {
                 // fp16 fragments with the permuted column order of mma_tile_e4m3
                 // (slots 2t, 2t+1 | 2t+8, 2t+9 hold columns 4t, 4t+1 | 4t+2, 4t+3);
                 // a row whose largest |q| reaches 2^15 is scaled by an exact power
@@ -600,7 +766,9 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         const int k_end = mt.tile_k0 + mt.nk;
         if (gave_up) {  // (computes nothing, writes nothing)
         } else if (mt.tile_k0 + S::kTK <= mt.P + (kFused ? 0 : 1)) {
-            if constexpr (k8)
+            if constexpr (kT8)
+                mma_tile_e4m3_t<D, false>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, sfac);
+            else if constexpr (k8)
                 mma_tile_e4m3<D, false>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, sfac);
             else
                 mma_tile<T, D, false>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
@@ -628,7 +796,9 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
                                              static_cast<const unsigned char *>(a.k_new) + nrow,
                                              static_cast<const unsigned char *>(a.v_new) + nrow, kc, vc, kvs);
             }
-            if constexpr (k8)
+            if constexpr (kT8)
+                mma_tile_e4m3_t<D, true>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, sfac);
+            else if constexpr (k8)
                 mma_tile_e4m3<D, true>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, sfac);
             else
                 mma_tile<T, D, true>(Ks, Vs, qa, oacc, m_run, l_run, warp, lane, mt.tile_k0, lim, k_end, a.qscale);
@@ -658,8 +828,14 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
         float *ep_l = ep_m + S::kNW * RB;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+            if constexpr (kT8) {  // (a row's keys are spread over the 8 lanes g)
+                l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 4);
+                l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 8);
+                l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 16);
+            } else {
+                l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+                l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+            }
         }
         // this warp's (o, m, l) as merge entry w; with fold, entry w is
         // instead read back and merged into the registers
@@ -668,15 +844,31 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
             if (fold) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float mo = ep_m[w * RB + g + 8 * r];
+                    const int row = kT8 ? 2 * t + r : g + 8 * r;
+                    const float mo = ep_m[w * RB + row];
                     const float M = fmaxf(m_run[r], mo);
                     wa[r] = safe_weight(m_run[r], M);
                     wb[r] = safe_weight(mo, M);
-                    l_run[r] = l_run[r] * wa[r] + ep_l[w * RB + g + 8 * r] * wb[r];
+                    l_run[r] = l_run[r] * wa[r] + ep_l[w * RB + row] * wb[r];
                     m_run[r] = M;
                 }
             }
-            if constexpr (k8) {
+            if constexpr (kT8) {
+                // O^T tile c: lane (g, t) holds columns 16c + 2g, +1 of rows 2t, 2t+1
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        float2 *p = reinterpret_cast<float2 *>(ep_o + (w * RB + 2 * t + r) * D + 16 * c + 2 * g);
+                        if (fold) {
+                            const float2 o = *p;
+                            oacc[c][r] = oacc[c][r] * wa[r] + o.x * wb[r];
+                            oacc[c][r + 2] = oacc[c][r + 2] * wa[r] + o.y * wb[r];
+                        } else {
+                            *p = make_float2(oacc[c][r], oacc[c][r + 2]);
+                        }
+                    }
+            } else if constexpr (k8) {
                 // even / odd column tiles of chunk c: lane (g, t) holds columns 16c + 4t .. 4t+3
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c)
@@ -709,11 +901,12 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
                         }
                     }
             }
-            if (!fold && t == 0) {
+            if (!fold && (kT8 ? g : t) == 0) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    ep_m[w * RB + g + 8 * r] = m_run[r];
-                    ep_l[w * RB + g + 8 * r] = l_run[r];
+                    const int row = kT8 ? 2 * t + r : g + 8 * r;
+                    ep_m[w * RB + row] = m_run[r];
+                    ep_l[w * RB + row] = l_run[r];
                 }
             }
         };
@@ -816,12 +1009,13 @@ __global__ void __launch_bounds__(MmaShape<T, D, C>::kThreads, MmaShape<T, D, C>
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <typename T, int D, bool kTicketMerge, bool kPaged, typename C = T> AttnVariant make_mma_variant()
+template <typename T, int D, bool kTicketMerge, bool kPaged, typename C = T, int kRows = 16>
+AttnVariant make_mma_variant()
 {
-    using S = MmaShape<T, D, C>;
+    using S = MmaShape<T, D, C, kRows>;
     AttnVariant v;
-    v.fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, false, kTicketMerge, kPaged, C>);
-    v.fused_fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, true, kTicketMerge, kPaged, C>);
+    v.fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, false, kTicketMerge, kPaged, C, kRows>);
+    v.fused_fn = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, true, kTicketMerge, kPaged, C, kRows>);
     if constexpr (kTicketMerge) v.merge_fn = nullptr;
     else v.merge_fn = reinterpret_cast<const void *>(&attn_merge_kernel<T, D, S::kRB, S::k8>);
     v.threads = S::kThreads;
@@ -833,11 +1027,13 @@ template <typename T, int D, bool kTicketMerge, bool kPaged, typename C = T> Att
     return v;
 }
 
-// bf16 q / out over an E4M3 cache: D = 128, contiguous.
-template <bool kTicketMerge> bool pick_mma_e4m3_variant(int D, AttnVariant *v)
+// bf16 q / out over an E4M3 cache: D = 128, contiguous; heads of at most 8
+// query rows in the swapped 8-row form.
+template <bool kTicketMerge> bool pick_mma_e4m3_variant(int D, int rows, AttnVariant *v)
 {
     if (D != 128) return false;
-    *v = make_mma_variant<__nv_bfloat16, 128, kTicketMerge, false, __nv_fp8_e4m3>();
+    *v = rows <= 8 ? make_mma_variant<__nv_bfloat16, 128, kTicketMerge, false, __nv_fp8_e4m3, 8>()
+                   : make_mma_variant<__nv_bfloat16, 128, kTicketMerge, false, __nv_fp8_e4m3, 16>();
     return true;
 }
 

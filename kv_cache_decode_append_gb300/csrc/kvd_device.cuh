@@ -216,6 +216,15 @@ __device__ __forceinline__ void ldmatrix_x4_trans_addr(uint32_t (&r)[4], uint32_
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(a));
 }
+// The 8x8 matrix of 16-bit elements held in ldmatrix's fragment layout (lane
+// (g, t): row g, columns 2t, 2t+1), transposed across the warp: the result
+// is lane (g, t)'s pair of rows 2t, 2t+1 at column g.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t r;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
 // 16-byte store to a shared-space address
 __device__ __forceinline__ void sts128(uint32_t a, const uint4 &v)
 {

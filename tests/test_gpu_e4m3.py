@@ -94,6 +94,9 @@ E4M3_CASES = [
     (3, 16, 2, 128, 1, 900, [899, 450, 0]),                           # 8 rows: two row blocks of 4
     (2, 8, 2, 64, 5, 700, [63, 600]),                                 # chunk of 5 across a tile
     (1, 4, 4, 128, 3, 3, [0]),                                        # empty history, P + N = T_max
+    (2, 14, 2, 128, 1, 1500, [1499, 700]),                            # 7 rows (8-row form, one padding row)
+    (3, 8, 4, 128, 3, 700, [650, 64, 0]),                             # 6 rows: chunk of 3, per-row limits
+    (2, 8, 8, 128, 1, 1000, [999, 500]),                              # 1 row per KV head
 ]
 
 
@@ -117,11 +120,14 @@ def test_e4m3_append_other_input_types(orc, new_dtype):
     assert (h["k_cache"][:, :, 17:20] & 0x7F == 0x7E).any()  # saturated codes were exercised
 
 
-@pytest.mark.parametrize("case", [(16, 32, 8, 128, 9300, 9200, 2), (16, 32, 8, 128, 1100, 1000, 1)],
-                         ids=["merge_pass", "in_kernel"])
+# (4 and 8 rows per KV head: the 8-row form)
+@pytest.mark.parametrize("case", [(16, 32, 8, 128, 12300, 12200, 2), (16, 32, 8, 128, 1100, 1000, 1),
+                                  (16, 64, 8, 128, 12300, 12200, 2)],
+                         ids=["merge_pass", "in_kernel", "merge_pass_8rows"])
 def test_e4m3_merge_modes(orc, case):
     B, H_q, H_kv, D, T_max, max_past, launches = case
-    assert kvd.kvd_decode_plan(B, H_q, H_kv, D, 1, max_past, "e4m3")["launches"] == launches
+    plan = kvd.kvd_decode_plan(B, H_q, H_kv, D, 1, max_past, "e4m3")
+    assert plan["launches"] == launches and plan["rows_per_block"] == 8
     gen = torch.Generator().manual_seed(9800 + launches)
     past = torch.randint(0, max_past + 1, (B,), generator=gen, dtype=torch.int32)
     past[2] = max_past
@@ -178,10 +184,16 @@ def _oracle_attention(orc, t, past):
     return ref
 
 
-def test_e4m3_subnormal_codes(orc):
-    """Caches of zero and subnormal codes only (|x| = m * 2^-9), 32 rows per KV head: the
-    widening keeps them exactly (a flush to zero would zero the output)."""
-    w = wl.Workload(0, "e4m3s", L=1, B=2, H_q=32, H_kv=8, D=128, N=8, dtype="bf16", T_max=400, P=0)
+# (H_q, N): 32 rows per KV head (16-row blocks), 8 rows (the 8-row form)
+TWO_FORMS = [(32, 8), (16, 4)]
+
+
+@pytest.mark.parametrize("hq_n", TWO_FORMS, ids=["rows32", "rows8"])
+def test_e4m3_subnormal_codes(orc, hq_n):
+    """Caches of zero and subnormal codes only (|x| = m * 2^-9): the widening keeps them
+    exactly (a flush to zero would zero the output)."""
+    H_q, N = hq_n
+    w = wl.Workload(0, "e4m3s", L=1, B=2, H_q=H_q, H_kv=8, D=128, N=N, dtype="bf16", T_max=400, P=0)
     past = torch.tensor([300, 57], dtype=torch.int32)
     t = wl.layer_inputs(w, 0, past, device="cpu", seed_base=9870)
     gen = torch.Generator().manual_seed(9871)
@@ -197,12 +209,15 @@ def test_e4m3_subnormal_codes(orc):
     assert row_rel_err(out, ref) <= TOL["bf16"]
 
 
-def test_e4m3_nan_codes(orc):
+@pytest.mark.parametrize("hq_n", TWO_FORMS, ids=["rows32", "rows8"])
+def test_e4m3_nan_codes(orc, hq_n):
     """A NaN code among the keys makes exactly the rows that see it NaN, as in the oracle (a
     masked key's score is replaced, not multiplied); a NaN value code seen by every row of its
     head makes that column NaN.  (A non-finite value at a key masked for some rows of the
     chunk reaches them too: the zero weight times NaN in the P . V product is NaN.)"""
-    w = wl.Workload(0, "e4m3n", L=1, B=2, H_q=32, H_kv=8, D=128, N=8, dtype="bf16", T_max=400, P=0)
+    H_q, N = hq_n
+    g = H_q // 8
+    w = wl.Workload(0, "e4m3n", L=1, B=2, H_q=H_q, H_kv=8, D=128, N=N, dtype="bf16", T_max=400, P=0)
     past = torch.tensor([300, 120], dtype=torch.int32)
     _, t = _inputs(w, past + w.N, 9880)      # valid codes up to P + N (the chunk's rows), NaN codes after
     t["k_cache"][0, 1, 200, 5] = 0x7F        # every row of (b 0, h 1) sees key 200
@@ -213,17 +228,26 @@ def test_e4m3_nan_codes(orc):
     ref = _oracle_attention(orc, t, past)
     assert np.array_equal(np.isnan(out), np.isnan(ref))
     rows = np.isnan(ref).any(axis=-1)
-    assert rows[0, 4:8].all() and rows[1, 12:16].all()
-    assert rows[1, 20:24].sum() == 28 and not rows[1, 20:24, 0].any()  # (row i of the chunk: key P + i)
+    assert rows[0, g:2 * g].all() and rows[1, 3 * g:4 * g].all()
+    # (row i of the chunk sees key P + i)
+    assert rows[1, 5 * g:6 * g].sum() == g * (N - 1) and not rows[1, 5 * g:6 * g, 0].any()
     fin = ~np.isnan(ref).any(axis=-1)
     assert row_rel_err(out[fin], ref[fin]) <= TOL["bf16"]
 
 
 def test_e4m3_kernel_choice():
-    """E4M3 caches stay on mma.sync at every row count (D = 128), CUDA cores at D = 64."""
-    assert kvd.kvd_decode_plan(4, 32, 8, 128, 4, 1000, "e4m3")["tensor_cores"] == 1   # 16 rows
-    assert kvd.kvd_decode_plan(4, 17, 1, 128, 1, 1000, "e4m3")["tensor_cores"] == 1   # 17 rows
-    assert kvd.kvd_decode_plan(4, 32, 1, 64, 1, 1000, "e4m3")["tensor_cores"] == 0    # D = 64
+    """E4M3 caches stay on mma.sync at every row count (D = 128), CUDA cores at D = 64; heads
+    of at most 8 rows in the 8-row (swapped) form."""
+    def plan(*a):
+        p = kvd.kvd_decode_plan(*a, 1000, "e4m3")
+        return p["tensor_cores"], p["rows_per_block"]
+    assert plan(4, 32, 8, 128, 4) == (1, 16)   # 16 rows
+    assert plan(4, 17, 1, 128, 1) == (1, 16)   # 17 rows
+    assert plan(4, 9, 1, 128, 1) == (1, 16)    # 9 rows
+    assert plan(4, 32, 8, 128, 2) == (1, 8)    # 8 rows
+    assert plan(4, 32, 8, 128, 1) == (1, 8)    # 4 rows
+    assert plan(4, 8, 8, 128, 1) == (1, 8)     # 1 row
+    assert plan(4, 32, 1, 64, 1)[0] == 0       # D = 64
 
 
 def test_e4m3_gqa_longctx_chunk8_full_size(orc):
