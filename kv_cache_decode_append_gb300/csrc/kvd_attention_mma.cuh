@@ -56,8 +56,10 @@ template <typename T, int D, typename C = T, int RB = 16> struct MmaShape {
     static constexpr int kBoxBytes = kTK * 128;        // one box: 64 rows x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;
     // E4M3: 3 stages, so that three CTAs (12 warps) share an SM; the
-    // widening makes its tiles latency-bound with fewer warps
-    static constexpr int kStages = (D == 128) ? 3 : 4;
+    // widening makes its tiles latency-bound with fewer warps.  The 8-row
+    // form's 2 KB q slots leave room for a fourth stage at three CTAs per SM
+    // (62.7 against 63.4 us per long-context layer).
+    static constexpr int kStages = (D == 128 && !kT8) ? 3 : 4;
     // (the swapped form, at four CTAs per SM under 128 registers, spilled in
     // the fused step and was no faster than the 16-row form: three)
     static constexpr int kMinBlocks = k8 ? 3 : 1;     // CTAs per SM the registers must allow
