@@ -108,3 +108,48 @@ def test_timeout_returns_flagged_and_recovers(tlib, oracle_lib, case):
     ref, st = oracle_lib.decode_attention(h["q"], h["k_cache"], h["v_cache"], past.numpy(), dtype)
     assert st == 0
     assert row_rel_err(out.double().cpu().numpy(), ref) <= TOL[dtype]
+
+
+def test_timeout_e4m3_eight_row_form(tlib, oracle_lib):
+    """The same for the E4M3 fused step in the tensor-core kernel's 8-row (swapped-operand)
+    form: 4 query rows per KV head, four ring stages."""
+    import test_gpu_e4m3 as e8
+    B, H_q, H_kv, D, N, T_max = 2, 16, 4, 128, 1, 900
+    w = wl.Workload(0, "e4m3_timeout", L=1, B=B, H_q=H_q, H_kv=H_kv, D=D, N=N, dtype="bf16", T_max=T_max, P=0)
+    past, t = e8._inputs(w, [850, 200], 9990)
+    max_past = int(past.max())
+    plan = kvd.kvd_decode_plan(B, H_q, H_kv, D, N, max_past, "e4m3")
+    assert plan["tensor_cores"] == 1 and plan["rows_per_block"] == 8
+    past_d = past.to(DEV)
+    nbytes = tlib.kvd_decode_workspace_bytes(B, H_q, H_kv, D, N, max_past, kvd.KVD_E4M3)
+    ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call(g, out):
+        return tlib.kvd_decode_step_e4m3(g["q"].data_ptr(), g["k_cache"].data_ptr(), g["v_cache"].data_ptr(),
+                                         g["k_new"].data_ptr(), g["v_new"].data_ptr(), out.data_ptr(),
+                                         past_d.data_ptr(), B, H_q, H_kv, T_max, D, N, max_past, 0.0, e8.K_SCALE,
+                                         e8.V_SCALE, ws.data_ptr(), ws.numel(), err.data_ptr(), stream)
+
+    g = {k: v.to(DEV) for k, v in t.items()}
+    out = torch.empty_like(g["q"])
+    tlib.kvd_test_inject_stall(1)
+    try:
+        assert call(g, out) == kvd.KVD_OK
+        torch.cuda.synchronize()
+    finally:
+        tlib.kvd_test_inject_stall(0)
+    assert int(err.item()) & kvd.KVD_DEVERR_TIMEOUT
+
+    assert tlib.kvd_workspace_init(ws.data_ptr(), ws.numel(), stream) == kvd.KVD_OK
+    err.zero_()
+    g = {k: v.to(DEV) for k, v in t.items()}
+    out = torch.full_like(g["q"], float("nan"))
+    assert call(g, out) == kvd.KVD_OK
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, h = e8._oracle(oracle_lib, w, past, t)
+    assert np.array_equal(g["k_cache"].cpu().numpy(), h["k_cache"])
+    assert np.array_equal(g["v_cache"].cpu().numpy(), h["v_cache"])
+    assert row_rel_err(out.double().cpu().numpy(), ref) <= TOL["bf16"]
