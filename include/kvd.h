@@ -291,7 +291,8 @@ typedef struct kvd_plan_info {
                             128 rows, each K/V tile read once per block of rows);
                             1: the mma.sync tensor-core kernel (bf16 / fp16 caches with
                             4 .. 16 rows for D = 128, 8 .. 16 for D = 64; E4M3 caches
-                            with D = 128); 0: the CUDA-core kernel */
+                            with D = 128, in blocks of 8 rows when a KV head has at
+                            most 8, else of 16); 0: the CUDA-core kernel */
     int early_start;     /* 1: a small layer (K/V of at most 26 MiB at max_past_len, on the
                             CUDA-core kernel): the next kernel on the stream may launch as
                             soon as this one starts, so its CTAs take free SM slots and,

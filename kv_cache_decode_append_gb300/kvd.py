@@ -214,7 +214,7 @@ def kvd_decode_plan(B: int, H_q: int, H_kv: int, D: int, N: int, max_past_len: i
     """The split-T plan kvd_decode_attention uses for these shapes on the current device.
 
     ``tensor_cores``: 0 the CUDA-core kernel, 1 the mma.sync tensor-core kernel (16-row
-    blocks), 2 the tcgen05 kernel (128-row blocks, for more than 16 query rows per KV
+    blocks; 8-row blocks for E4M3 caches with at most 8 rows per KV head), 2 the tcgen05 kernel (128-row blocks, for more than 16 query rows per KV
     head); ``launches`` 2 when split heads are merged by the separate merge pass;
     ``early_start`` 1 for small layers (the next kernel on the stream may start early);
     ``cluster`` > 0 when such a layer runs as one thread-block cluster of that many CTAs
