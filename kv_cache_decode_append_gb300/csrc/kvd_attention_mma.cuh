@@ -26,7 +26,11 @@
 //   * value rows past the end of a sequence are zeroed in shared memory
 //     before they reach the MMA (a zero weight times a stale NaN would still
 //     be NaN); in a fused step the new rows are written into the tile (and
-//     the cache) before the tile is read.
+//     the cache) before the tile is read;
+//   * E4M3 caches widen their codes to fp16 fragments between ldmatrix and
+//     the MMA; a KV head with at most 8 query rows runs in an 8-row form with
+//     the operands swapped (mma_tile_e4m3_t), so that the MMA's 16-wide
+//     dimension covers keys instead of mostly padding rows.
 #pragma once
 
 #include "kvd_attention.cuh"
